@@ -1,0 +1,289 @@
+/*
+ * moe.h -- C ABI of the batch-invariant MoE layer for NVIDIA GB300 (sm_103a).
+ *
+ * One Mixture-of-Experts layer: E routed SwiGLU experts with top-k routing
+ * plus one sigmoid-gated shared SwiGLU expert (SkyRL PR #2513, section
+ * "What": 512 routed experts, top-10, and a shared expert).  The forward and
+ * backward are deterministic and batch-invariant: a token's output row and
+ * input-gradient row do not depend on the other tokens in the batch, on the
+ * batch size or on the token's position (RL-Kernel PR #557 "EP4 distributed
+ * logprob parity", section "Prior art & reuse decision": batch-invariant
+ * forward and backward; embedded #503 commit message "MoE route/combine
+ * contract with a batch-invariant grouped expert GEMM").
+ *
+ * The layer splits into separate contracts, as the #503 commit message does
+ * (bullets "Routing", "Experts", "Combine", "Backward"):
+ *
+ *   moe_route        router GEMM (FP32 result), softmax, top-k, renormalise,
+ *                    shared-expert gate
+ *   moe_permute      stable counting sort of the routes by expert
+ *   moe_grouped_ffn  per-expert SwiGLU over the expert segments, unweighted
+ *                    rows; the shared expert as one more segment
+ *   moe_combine      ordered FP32 sum of the k weighted rows, plus the gated
+ *                    shared row, one rounding to the output type
+ *   moe_backward     all gradients, reduced in fixed orders
+ *   moe_forward      the four forward calls in sequence, intermediates in the
+ *                    caller's workspace
+ *
+ * Conventions that hold for every entry point:
+ *  - Pointers named as device buffers are CUDA device (or managed) memory of
+ *    the current device; they must be 16-byte aligned.  Matrices are dense
+ *    row-major with the last dimension contiguous.  The caller owns every
+ *    buffer, including the workspace; the library allocates no device memory
+ *    and keeps no state between calls apart from per-device kernel
+ *    attributes set on first use and one device-side status word.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *    call is stream-ordered and asynchronous: it never synchronises and never
+ *    reads device data on the host.
+ *  - Return value: MOE_OK (0) or a negative moe_status.  On a host-detected
+ *    error (bad argument, unsupported shape, small workspace) nothing is
+ *    launched and no output is written.  There is no fallback path.
+ *  - T = 0 is valid: the call succeeds and writes only the fixed-size
+ *    outputs (offsets, weight gradients), which become zero.
+ *  - Element type: `dtype` selects float (MOE_F32) or bfloat16 (MOE_BF16,
+ *    stored as uint16 bit patterns) for x, the expert weights, the shared
+ *    gate weight, the expert rows and the outputs y and dx.  The router
+ *    weight, router bias, routing weights and gate values are always float.
+ *    Every weight gradient is float and is overwritten, not accumulated.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* NULL pointer, negative or zero size, k > E, k > 16, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = -2, /* a shape or dtype the kernels do not cover (see moe_dims_t) */
+  MOE_ERR_WORKSPACE = -3,   /* ws_bytes smaller than moe_workspace_size() */
+  MOE_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed */
+  MOE_ERR_DEVICE = -5       /* (moe_device_status only) a kernel recorded a failed check */
+};
+
+/* Operation selector of moe_workspace_size. */
+enum moe_op {
+  MOE_OP_ROUTE = 0,
+  MOE_OP_PERMUTE = 1,
+  MOE_OP_GROUPED_FFN = 2,
+  MOE_OP_COMBINE = 3,
+  MOE_OP_BACKWARD = 4,
+  MOE_OP_FORWARD = 5
+};
+
+/*
+ * Layer shape.  Limits: T >= 0, T*k < 2^31; 1 <= k <= 16; k <= E <= 1024.
+ * MOE_F32: H, I, Is multiples of 4.
+ * MOE_BF16: H a multiple of 128, I and Is multiples of 64.
+ * Other shapes return MOE_ERR_UNSUPPORTED.
+ */
+typedef struct moe_dims {
+  int32_t T;     /* tokens in this batch */
+  int32_t H;     /* hidden size */
+  int32_t E;     /* routed experts */
+  int32_t k;     /* experts per token */
+  int32_t I;     /* routed-expert intermediate size */
+  int32_t Is;    /* shared-expert intermediate size */
+  int32_t dtype; /* enum moe_dtype */
+} moe_dims_t;
+
+/*
+ * Activations kept by the forward for the backward.  Each pointer may be
+ * NULL (inference); moe_backward needs all four.  Sorted order means the
+ * expert-segment order produced by moe_permute (row j holds route
+ * sorted_route[j]).
+ */
+typedef struct moe_saved {
+  void *gu;        /* [T*k, 2I] dtype, sorted order: gate pre-activation (I) then up (I) */
+  void *h;         /* [T*k, I]  dtype, sorted order: silu(gate) * up, input of the down projection */
+  void *gu_shared; /* [T, 2Is]  dtype, token order */
+  void *h_shared;  /* [T, Is]   dtype, token order */
+} moe_saved_t;
+
+/* Bytes of workspace the operation needs for these dims (0 for an invalid
+ * dims pointer).  The workspace must be 256-byte aligned device memory. */
+size_t moe_workspace_size(const moe_dims_t *d, int op);
+
+/* Static description of a status code. */
+const char *moe_status_string(int status);
+
+/*
+ * moe_route -- router and shared-expert gate.
+ * RL-Kernel PR #557, #503 commit message "Routing": FP32 router GEMM
+ * through a batch-invariant GEMM, fixed-order softmax, stable descending
+ * top-k with ties to the lower expert id, FP32 renormalisation of the k
+ * selected weights.  Shared gate: #503 "TP4 block", a replicated
+ * shared-expert gate, here sigmoid(x . w_shared_gate).
+ *
+ *   x              [T, H]  dtype   input rows
+ *   w_router       [E, H]  float   router weight (nn.Linear layout)
+ *   router_bias    [E]     float   added to the logits, or NULL
+ *   w_shared_gate  [H]     dtype   shared-expert gate weight
+ *   topk_ids       [T, k]  int32   out: expert ids, slot order = descending logit
+ *   topk_w         [T, k]  float   out: softmax over the k selected logits
+ *   shared_sig     [T]     float   out: sigmoid gate of the shared expert
+ *   logits         [T, E]  float   out: router logits (with bias), or NULL
+ *
+ * The logits are FP32 results of an exact bf16 three-way split of the FP32
+ * router weight (MOE_BF16) or FP32 products (MOE_F32), summed in a fixed
+ * order that does not depend on T.  Workspace: moe_workspace_size(ROUTE).
+ */
+int moe_route(const moe_dims_t *d, const void *x, const float *w_router, const float *router_bias,
+              const void *w_shared_gate, int32_t *topk_ids, float *topk_w, float *shared_sig,
+              float *logits, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_permute -- dispatch as a stable counting sort of the routes.
+ * RL-Kernel PR #557 "What": dispatch is a local selection of the routes;
+ * #503 "Experts": one writer per (token, route) row.  Route r = t*k + s.
+ *
+ *   topk_ids        [T, k]  int32  expert ids from moe_route
+ *   expert_offsets  [E+1]   int32  out: first sorted row of each expert; [E] = T*k
+ *   sorted_route    [T*k]   int32  out: route of sorted row j, in (expert, t, s) order
+ *   route_pos       [T*k]   int32  out: sorted row of route r (inverse of sorted_route)
+ *
+ * Integer only, no atomics on positions; the result equals a sequential
+ * counting sort bit for bit.  An id outside [0, E) is skipped and recorded in
+ * the device status word (moe_device_status).  Workspace: PERMUTE.
+ */
+int moe_permute(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_offsets,
+                int32_t *sorted_route, int32_t *route_pos, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_grouped_ffn -- per-expert SwiGLU FFN over the expert segments.
+ * #503 commit message "Experts": per-route gate_up and down projections
+ * through one fixed-configuration grouped GEMM, no routed-weight multiply
+ * and no sum inside the kernel, one writer per row.  The shared expert
+ * (PR #557 "What") runs as one more segment covering all T tokens.
+ *
+ *   x               [T, H]      dtype  input rows
+ *   expert_offsets  [E+1]       int32  from moe_permute
+ *   sorted_route    [T*k]       int32  from moe_permute
+ *   w_gate_up       [E, 2I, H]  dtype  per expert: I gate rows, then I up rows
+ *   w_down          [E, H, I]   dtype
+ *   ws_gate_up      [2Is, H]    dtype  shared expert, same layout
+ *   ws_down         [H, Is]     dtype
+ *   y_routed        [T*k, H]    dtype  out: row t*k+s = expert topk_ids[t,s] applied to x_t, unweighted
+ *   y_shared        [T, H]      dtype  out: shared expert applied to x_t
+ *   saved           may be NULL; non-NULL members are written (moe_saved_t)
+ *
+ * Accumulation in FP32 with a fixed K order; gate/up and h are rounded once
+ * to dtype (h is the down projection's input), rows once to dtype.
+ * Workspace: GROUPED_FFN.
+ */
+int moe_grouped_ffn(const moe_dims_t *d, const void *x, const int32_t *expert_offsets,
+                    const int32_t *sorted_route, const void *w_gate_up, const void *w_down,
+                    const void *ws_gate_up, const void *ws_down, void *y_routed, void *y_shared,
+                    const moe_saved_t *saved, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_combine -- combine_routes.
+ * #503 commit message "Combine": k ordered FP32 multiply-adds and one cast
+ * to the output type, no atomics.  The shared term is added after the k
+ * routed terms in the same FP32 accumulator:
+ *   y[t] = cast( fma(sig[t], Ys[t], fma(w[t,k-1], Yr[t*k+k-1], ... fma(w[t,0], Yr[t*k], 0))) )
+ *
+ *   y_routed [T*k, H] dtype, y_shared [T, H] dtype, topk_w [T, k] float,
+ *   shared_sig [T] float, y [T, H] dtype out.  No workspace.
+ */
+int moe_combine(const moe_dims_t *d, const void *y_routed, const void *y_shared, const float *topk_w,
+                const float *shared_sig, void *y, void *stream);
+
+/* Everything moe_forward reads and writes. */
+typedef struct moe_fwd_args {
+  const void *x;             /* [T, H] dtype */
+  const float *w_router;     /* [E, H] float */
+  const float *router_bias;  /* [E] float or NULL */
+  const void *w_shared_gate; /* [H] dtype */
+  const void *w_gate_up;     /* [E, 2I, H] dtype */
+  const void *w_down;        /* [E, H, I] dtype */
+  const void *ws_gate_up;    /* [2Is, H] dtype */
+  const void *ws_down;       /* [H, Is] dtype */
+  void *y;                   /* out [T, H] dtype */
+  /* Optional outputs (NULL: kept in the workspace).  The backward needs
+   * all of them, plus every member of `saved`. */
+  int32_t *topk_ids;       /* [T, k] */
+  float *topk_w;           /* [T, k] */
+  float *shared_sig;       /* [T] */
+  float *logits;           /* [T, E] (never kept in the workspace) */
+  int32_t *expert_offsets; /* [E+1] */
+  int32_t *sorted_route;   /* [T*k] */
+  int32_t *route_pos;      /* [T*k] */
+  void *y_routed;          /* [T*k, H] dtype */
+  void *y_shared;          /* [T, H] dtype */
+  moe_saved_t saved;
+} moe_fwd_args_t;
+
+/* moe_forward -- moe_route, moe_permute, moe_grouped_ffn, moe_combine on one
+ * stream.  Workspace: FORWARD (covers every optional output left NULL). */
+int moe_forward(const moe_dims_t *d, const moe_fwd_args_t *a, void *ws, size_t ws_bytes, void *stream);
+
+/* Everything moe_backward reads and writes. */
+typedef struct moe_bwd_args {
+  /* forward inputs */
+  const void *x;
+  const float *w_router;
+  const void *w_shared_gate;
+  const void *w_gate_up;
+  const void *w_down;
+  const void *ws_gate_up;
+  const void *ws_down;
+  /* forward results (see moe_fwd_args_t) */
+  const int32_t *topk_ids;
+  const float *topk_w;
+  const float *shared_sig;
+  const int32_t *expert_offsets;
+  const int32_t *sorted_route;
+  const int32_t *route_pos;
+  const void *y_routed;
+  const void *y_shared;
+  moe_saved_t saved;
+  /* upstream gradient */
+  const void *dy; /* [T, H] dtype */
+  /* outputs, all overwritten */
+  void *dx;              /* [T, H] dtype */
+  float *dw_gate_up;     /* [E, 2I, H] */
+  float *dw_down;        /* [E, H, I] */
+  float *dw_router;      /* [E, H] */
+  float *dw_shared_gate; /* [H] */
+  float *dws_gate_up;    /* [2Is, H] */
+  float *dws_down;       /* [H, Is] */
+} moe_bwd_args_t;
+
+/*
+ * moe_backward -- gradients of L = sum(dy * y) with the routes held fixed.
+ * #503 commit message "Backward": per-expert GEMMs write the per-route
+ * input gradients into one dense buffer; dx sums them in ascending expert
+ * order (PR #557 "What").  The route-weight gradient dw[t,s] = dy_t . Yr
+ * is reduced per (t, s) over H in a fixed tree, so the backward stays batch
+ * invariant (PR #557, "Results (4 x H100)", footnote 1: a torch.sum over
+ * hidden there was not batch invariant).
+ *   dx = sum over routes in ascending expert id of the routed input grads
+ *        + shared-expert input grad + dlogit . W_router + dz * w_shared_gate,
+ *   accumulated in FP32 in that order and cast once.  Weight gradients sum
+ *   over their rows in ascending (expert-segment) order in FP32, with no
+ *   split-K atomics.  Workspace: BACKWARD.
+ */
+int moe_backward(const moe_dims_t *d, const moe_bwd_args_t *a, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_device_status -- read (and, if `reset`, clear) the device status word
+ * of the current device.  Synchronises the device.  Returns MOE_OK when no
+ * kernel recorded a failed check since the last reset, MOE_ERR_DEVICE when
+ * one did (`*detail`, if not NULL, receives the first recorded code), or
+ * MOE_ERR_CUDA.  Codes: 1 = expert id out of range in moe_permute,
+ * 2 = a pipeline wait in a tensor-core kernel timed out,
+ * 3 = tensor-memory allocation failed.
+ */
+int moe_device_status(int reset, int32_t *detail);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */
