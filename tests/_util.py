@@ -1,0 +1,117 @@
+"""Shared helpers of the test suite: cached seeded inputs, the near-tie routing
+rule, per-token oracle evaluation at full size, and tolerance checks.
+
+Tolerances (the layer's stated bar): bf16 configurations max |y - y64| <= 2e-2
+and ||y - y64||_2 / ||y64||_2 <= 5e-3 per output tensor; the FP32 tiny
+configuration max |y - y64| <= 1e-4.  Routes and the permutation are compared
+bit for bit, except tokens whose k-th / (k+1)-th logit gap is below 1e-4 in
+either the oracle's FP64 logits or the GPU's FP32 logits: for those the
+oracle selects from the GPU's logits (ties to the lower id) and computes the
+weights in FP64 on that set.
+"""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import torch
+
+import oracle
+from top_routed_grouped_gb300 import inputs as I
+
+TIE_GAP = 1e-4
+BF16_MAX_ABS = 2e-2
+BF16_REL_L2 = 5e-3
+F32_MAX_ABS = 1e-4
+
+
+@functools.lru_cache(maxsize=None)
+def full_weights():
+    """bf16 weights of the 512-expert layer (identical for every bf16 workload)."""
+    cfg = I.CONFIGS["bf16_t1024"]
+    d = I.make_inputs(cfg, T=1)
+    return {k: v for k, v in d.items() if k not in ("x", "dy", "router_bias")}
+
+
+@functools.lru_cache(maxsize=None)
+def full_x(T: int):
+    return I.normal((T, 2048), 0, I._STREAM["x"], 1.0, torch.bfloat16)
+
+
+@functools.lru_cache(maxsize=None)
+def full_dy(T: int):
+    return I.normal((T, 2048), 2, I._STREAM["dy"], 1.0, torch.bfloat16)
+
+
+def to_dev(d: dict, device="cuda") -> dict:
+    return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def kth_gap(logits: np.ndarray, k: int) -> np.ndarray:
+    """logit_(k) - logit_(k+1) of each row (inf when k == E)."""
+    E = logits.shape[1]
+    if k >= E:
+        return np.full(logits.shape[0], np.inf)
+    part = -np.partition(-logits, (k - 1, k), axis=1)
+    return part[:, k - 1] - part[:, k]
+
+
+def oracle_routes(x, w_router, bias, k: int, gpu_logits: np.ndarray):
+    """Oracle routes with the near-tie rule.  Returns (ids, w, near_mask, logits64)."""
+    l64 = oracle.router_logits(x, w_router, bias)
+    ids = oracle.topk_select(l64, k)
+    gl = np.asarray(gpu_logits, dtype=np.float64)
+    near = (kth_gap(l64, k) < TIE_GAP) | (kth_gap(gl, k) < TIE_GAP)
+    if near.any():
+        ids[near] = oracle.topk_select(gl[near], k)
+    w = oracle.topk_weights(l64, ids)
+    return ids, w, near, l64
+
+
+def oracle_rows(x_rows, ids_rows, w_rows, sig_rows, W: dict, want_rows=False):
+    """Oracle forward of a few tokens at full size, one token at a time with
+    only its k experts widened to float64 (the experts are remapped to 0..k-1)."""
+    ys, yrs, yss = [], [], []
+    for t in range(x_rows.shape[0]):
+        e = torch.as_tensor(np.asarray(ids_rows[t], dtype=np.int64))
+        wgu = W["w_gate_up"].index_select(0, e.to(W["w_gate_up"].device)).cpu()
+        wdn = W["w_down"].index_select(0, e.to(W["w_down"].device)).cpu()
+        local = np.arange(len(e), dtype=np.int32)[None, :]
+        r = oracle.moe_forward(x_rows[t:t + 1], local, np.asarray(w_rows[t:t + 1]), np.asarray(sig_rows[t:t + 1]),
+                               wgu, wdn, W["ws_gate_up"].cpu(), W["ws_down"].cpu(), want_rows=want_rows)
+        if want_rows:
+            ys.append(r[0]); yrs.append(r[1]); yss.append(r[2])
+        else:
+            ys.append(r)
+    if want_rows:
+        return np.concatenate(ys), np.concatenate(yrs), np.concatenate(yss)
+    return np.concatenate(ys)
+
+
+def err_stats(got, ref) -> tuple[float, float]:
+    g = got.detach().double().cpu().numpy() if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
+    r = np.asarray(ref, np.float64)
+    max_abs = float(np.max(np.abs(g - r))) if g.size else 0.0
+    den = float(np.linalg.norm(r))
+    rel = float(np.linalg.norm(g - r) / den) if den > 0 else float(np.linalg.norm(g - r))
+    return max_abs, rel
+
+
+def assert_bf16_close(got, ref, what=""):
+    m, r = err_stats(got, ref)
+    assert m <= BF16_MAX_ABS and r <= BF16_REL_L2, f"{what}: max_abs={m:.3e} rel_l2={r:.3e}"
+    return m, r
+
+
+def assert_f32_close(got, ref, what=""):
+    m, r = err_stats(got, ref)
+    assert m <= F32_MAX_ABS, f"{what}: max_abs={m:.3e}"
+    return m, r
+
+
+def bits(t: torch.Tensor) -> torch.Tensor:
+    """Raw bit pattern (signed zeros and NaN payloads compare exactly)."""
+    t = t.detach().contiguous()
+    view = {torch.bfloat16: torch.int16, torch.float16: torch.int16, torch.float32: torch.int32,
+            torch.int32: torch.int32}[t.dtype]
+    return t.view(view).cpu()

@@ -1,0 +1,262 @@
+"""Python binding of ``libmoe_gb300.so``, the batch-invariant MoE layer for GB300.
+
+This module only marshals arguments: torch supplies device memory and the
+stream, every step of the layer runs in the library's CUDA kernels.  The
+functions named ``moe_*`` mirror the C entry points of ``include/moe.h`` one to
+one (pointers in, status out, raising ``MoEError`` on a non-zero status); the
+lower-case helpers (``route``, ``permute``, ``grouped_ffn``, ``combine``,
+``forward``, ``backward``) allocate the outputs with torch and call them.
+
+There is no fallback: if the library is missing, ``lib()`` raises.  Build it
+with ``python -m top_routed_grouped_gb300.build`` (or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+
+MOE_F32, MOE_BF16 = 0, 1
+OP = {"route": 0, "permute": 1, "grouped_ffn": 2, "combine": 3, "backward": 4, "forward": 5}
+STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_WORKSPACE",
+          -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE"}
+EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_permute", "moe_grouped_ffn",
+            "moe_combine", "moe_forward", "moe_backward", "moe_device_status")
+
+_vp = ctypes.c_void_p
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("I", ctypes.c_int32), ("Is", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class Saved(ctypes.Structure):
+    _fields_ = [("gu", _vp), ("h", _vp), ("gu_shared", _vp), ("h_shared", _vp)]
+
+
+class FwdArgs(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("x", "w_router", "router_bias", "w_shared_gate", "w_gate_up", "w_down",
+                                   "ws_gate_up", "ws_down", "y", "topk_ids", "topk_w", "shared_sig", "logits",
+                                   "expert_offsets", "sorted_route", "route_pos", "y_routed", "y_shared")] + \
+              [("saved", Saved)]
+
+
+class BwdArgs(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("x", "w_router", "w_shared_gate", "w_gate_up", "w_down", "ws_gate_up",
+                                   "ws_down", "topk_ids", "topk_w", "shared_sig", "expert_offsets",
+                                   "sorted_route", "route_pos", "y_routed", "y_shared")] + \
+              [("saved", Saved)] + \
+              [(n, _vp) for n in ("dy", "dx", "dw_gate_up", "dw_down", "dw_router", "dw_shared_gate",
+                                  "dws_gate_up", "dws_down")]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library.  Raises if it has not been built (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m top_routed_grouped_gb300.build`; there is no CPU fallback")
+            L = ctypes.CDLL(LIB_PATH)
+            D = ctypes.POINTER(Dims)
+            sigs = {
+                "moe_workspace_size": ([D, ctypes.c_int], ctypes.c_size_t),
+                "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
+                "moe_route": ([D] + [_vp] * 8 + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
+                "moe_permute": ([D] + [_vp] * 4 + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
+                "moe_grouped_ffn": ([D] + [_vp] * 9 + [ctypes.POINTER(Saved), _vp, ctypes.c_size_t, _vp],
+                                    ctypes.c_int),
+                "moe_combine": ([D] + [_vp] * 5 + [_vp], ctypes.c_int),
+                "moe_forward": ([D, ctypes.POINTER(FwdArgs), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
+                "moe_backward": ([D, ctypes.POINTER(BwdArgs), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
+                "moe_device_status": ([ctypes.c_int, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+            }
+            for name, (args, res) in sigs.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != 0:
+        raise MoEError(fn, rc)
+
+
+def _p(t):
+    """Device pointer of a tensor (None -> NULL)."""
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_dims(T, H, E, k, I, Is, dtype) -> Dims:
+    import torch
+    if isinstance(dtype, torch.dtype):
+        dtype = {torch.float32: MOE_F32, torch.bfloat16: MOE_BF16}[dtype]
+    return Dims(int(T), int(H), int(E), int(k), int(I), int(Is), int(dtype))
+
+
+def dims_of(x, w_router, w_gate_up, ws_gate_up, k: int) -> Dims:
+    T, H = x.shape
+    return make_dims(T, H, w_router.shape[0], k, w_gate_up.shape[1] // 2, ws_gate_up.shape[0] // 2, x.dtype)
+
+
+# ---------------------------------------------------------------- raw ABI
+def moe_workspace_size(d: Dims, op) -> int:
+    op = OP[op] if isinstance(op, str) else int(op)
+    return int(lib().moe_workspace_size(ctypes.byref(d), op))
+
+
+def moe_route(d, x, w_router, router_bias, w_shared_gate, topk_ids, topk_w, shared_sig, logits, ws, stream=None):
+    _check("moe_route", lib().moe_route(ctypes.byref(d), _p(x), _p(w_router), _p(router_bias), _p(w_shared_gate),
+                                        _p(topk_ids), _p(topk_w), _p(shared_sig), _p(logits), _p(ws),
+                                        0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_permute(d, topk_ids, expert_offsets, sorted_route, route_pos, ws, stream=None):
+    _check("moe_permute", lib().moe_permute(ctypes.byref(d), _p(topk_ids), _p(expert_offsets), _p(sorted_route),
+                                            _p(route_pos), _p(ws), 0 if ws is None else ws.numel(),
+                                            _stream(stream)))
+
+
+def _saved(saved) -> Saved:
+    saved = saved or {}
+    return Saved(*(_p(saved.get(n)) for n in ("gu", "h", "gu_shared", "h_shared")))
+
+
+def moe_grouped_ffn(d, x, expert_offsets, sorted_route, w_gate_up, w_down, ws_gate_up, ws_down, y_routed,
+                    y_shared, saved, ws, stream=None):
+    s = _saved(saved)
+    _check("moe_grouped_ffn", lib().moe_grouped_ffn(
+        ctypes.byref(d), _p(x), _p(expert_offsets), _p(sorted_route), _p(w_gate_up), _p(w_down), _p(ws_gate_up),
+        _p(ws_down), _p(y_routed), _p(y_shared), ctypes.byref(s), _p(ws), 0 if ws is None else ws.numel(),
+        _stream(stream)))
+
+
+def moe_combine(d, y_routed, y_shared, topk_w, shared_sig, y, stream=None):
+    _check("moe_combine", lib().moe_combine(ctypes.byref(d), _p(y_routed), _p(y_shared), _p(topk_w),
+                                            _p(shared_sig), _p(y), _stream(stream)))
+
+
+def moe_forward(d, args: dict, ws, stream=None):
+    fa = FwdArgs()
+    for name, _ in FwdArgs._fields_:
+        if name != "saved":
+            setattr(fa, name, _p(args.get(name)))
+    fa.saved = _saved(args.get("saved"))
+    _check("moe_forward", lib().moe_forward(ctypes.byref(d), ctypes.byref(fa), _p(ws),
+                                            0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def moe_backward(d, args: dict, ws, stream=None):
+    ba = BwdArgs()
+    for name, _ in BwdArgs._fields_:
+        if name != "saved":
+            setattr(ba, name, _p(args.get(name)))
+    ba.saved = _saved(args.get("saved"))
+    _check("moe_backward", lib().moe_backward(ctypes.byref(d), ctypes.byref(ba), _p(ws),
+                                              0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def moe_device_status(reset: bool = True) -> int:
+    """Synchronise and return the device status code (0 = no failed device check)."""
+    detail = ctypes.c_int32(0)
+    rc = lib().moe_device_status(1 if reset else 0, ctypes.byref(detail))
+    if rc not in (0, -5):
+        raise MoEError("moe_device_status", rc)
+    return int(detail.value)
+
+
+# ---------------------------------------------------------------- helpers
+def workspace(d: Dims, op, device="cuda"):
+    import torch
+    n = moe_workspace_size(d, op)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def route(x, w_router, w_shared_gate, k: int, router_bias=None, E: int | None = None, want_logits=False,
+          stream=None):
+    """Returns dict(topk_ids [T,k] int32, topk_w [T,k] f32, shared_sig [T] f32, logits [T,E] f32 or None)."""
+    import torch
+    T, H = x.shape
+    E = w_router.shape[0]
+    d = make_dims(T, H, E, k, 64, 64, x.dtype)
+    dev = x.device
+    out = {"topk_ids": torch.empty(T, k, dtype=torch.int32, device=dev),
+           "topk_w": torch.empty(T, k, dtype=torch.float32, device=dev),
+           "shared_sig": torch.empty(T, dtype=torch.float32, device=dev),
+           "logits": torch.empty(T, E, dtype=torch.float32, device=dev) if want_logits else None}
+    moe_route(d, x, w_router, router_bias, w_shared_gate, out["topk_ids"], out["topk_w"], out["shared_sig"],
+              out["logits"], workspace(d, "route", dev), stream)
+    return out
+
+
+def permute(topk_ids, E: int, stream=None):
+    """Returns dict(expert_offsets [E+1], sorted_route [T*k], route_pos [T*k]), all int32."""
+    import torch
+    T, k = topk_ids.shape
+    d = make_dims(T, 128, E, k, 64, 64, MOE_BF16)
+    dev = topk_ids.device
+    out = {"expert_offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+           "sorted_route": torch.empty(T * k, dtype=torch.int32, device=dev),
+           "route_pos": torch.empty(T * k, dtype=torch.int32, device=dev)}
+    moe_permute(d, topk_ids, out["expert_offsets"], out["sorted_route"], out["route_pos"],
+                workspace(d, "permute", dev), stream)
+    return out
+
+
+def forward(x, w_router, w_shared_gate, w_gate_up, w_down, ws_gate_up, ws_down, k: int, router_bias=None,
+            save_for_backward: bool = False, want_logits: bool = False, stream=None):
+    """Full layer forward through ``moe_forward``.  Returns a dict with ``y`` and every intermediate."""
+    import torch
+    T, H = x.shape
+    d = dims_of(x, w_router, w_gate_up, ws_gate_up, k)
+    dev, dt = x.device, x.dtype
+    R, E, I, Is = T * k, d.E, d.I, d.Is
+    out = {
+        "y": torch.empty(T, H, dtype=dt, device=dev),
+        "topk_ids": torch.empty(T, k, dtype=torch.int32, device=dev),
+        "topk_w": torch.empty(T, k, dtype=torch.float32, device=dev),
+        "shared_sig": torch.empty(T, dtype=torch.float32, device=dev),
+        "logits": torch.empty(T, E, dtype=torch.float32, device=dev) if want_logits else None,
+        "expert_offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+        "sorted_route": torch.empty(R, dtype=torch.int32, device=dev),
+        "route_pos": torch.empty(R, dtype=torch.int32, device=dev),
+        "y_routed": torch.empty(R, H, dtype=dt, device=dev),
+        "y_shared": torch.empty(T, H, dtype=dt, device=dev),
+    }
+    if save_for_backward:
+        out["saved"] = {"gu": torch.empty(R, 2 * I, dtype=dt, device=dev),
+                        "h": torch.empty(R, I, dtype=dt, device=dev),
+                        "gu_shared": torch.empty(T, 2 * Is, dtype=dt, device=dev),
+                        "h_shared": torch.empty(T, Is, dtype=dt, device=dev)}
+    args = dict(out, x=x, w_router=w_router, router_bias=router_bias, w_shared_gate=w_shared_gate,
+                w_gate_up=w_gate_up, w_down=w_down, ws_gate_up=ws_gate_up, ws_down=ws_down)
+    moe_forward(d, args, workspace(d, "forward", dev), stream)
+    return out

@@ -1,0 +1,279 @@
+// C ABI of the MoE layer (declarations and contracts in include/moe.h):
+// argument validation, workspace carving and the launch sequence of each
+// entry point.  No device memory is allocated here.
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+
+// Device status word: first failed device-side check since the last reset.
+__device__ int g_moe_status;
+
+static int *status_ptr() {
+  static std::mutex mu;
+  static int *cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_moe_status) != cudaSuccess) return nullptr;
+    cache[dev] = (int *)p;
+  }
+  return cache[dev];
+}
+
+// Sequential sub-allocation of the caller's workspace at 256-byte alignment.
+// With base == nullptr it only measures.
+struct Carver {
+  char *base;
+  size_t off = 0;
+  explicit Carver(void *b) : base((char *)b) {}
+  void *take(size_t bytes) {
+    size_t o = (size_t)round_up((int64_t)off, 256);
+    off = o + bytes;
+    return base ? (void *)(base + o) : nullptr;
+  }
+};
+
+static size_t esize(const moe_dims_t *d) { return d->dtype == MOE_F32 ? 4 : 2; }
+
+static int check_dims(const moe_dims_t *d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->H <= 0 || d->E <= 0 || d->k <= 0 || d->I <= 0 || d->Is <= 0) return MOE_ERR_INVALID_ARG;
+  if (d->k > d->E || d->k > 16) return MOE_ERR_INVALID_ARG;
+  if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (d->E > 1024) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)d->T * d->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (d->dtype == MOE_F32) {
+    if (d->H % 4 || d->I % 4 || d->Is % 4) return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (d->H % 128 || d->I % 64 || d->Is % 64) return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+// A buffer of `n` elements: may be NULL only when empty; else 16-byte aligned.
+static bool buf_ok(const void *p, int64_t n) {
+  if (n == 0) return true;
+  return p != nullptr && ((uintptr_t)p & 15) == 0;
+}
+
+static bool opt_ok(const void *p) { return p == nullptr || ((uintptr_t)p & 15) == 0; }
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// ---------------------------------------------------------------- sizes
+static void route_ws(const moe_dims_t *d, Carver &c) {
+  c.take((size_t)d->T * d->E * sizeof(float));  // logits when the caller passes none
+}
+
+static void permute_ws(const moe_dims_t *d, Carver &c) {
+  c.take(permute_scratch_bytes((int64_t)d->T * d->k, d->E));
+}
+
+struct FfnScratch {
+  void *tiles, *h_routed, *h_shared;
+};
+
+static FfnScratch ffn_ws(const moe_dims_t *d, Carver &c) {
+  FfnScratch s;
+  const int64_t R = (int64_t)d->T * d->k;
+  s.tiles = c.take(ffn_simt_scratch_bytes(d->E));
+  s.h_routed = c.take((size_t)R * d->I * esize(d));
+  s.h_shared = c.take((size_t)d->T * d->Is * esize(d));
+  return s;
+}
+
+struct FwdScratch {
+  int32_t *ids;
+  float *w, *sig;
+  int32_t *offsets, *sorted_route, *route_pos;
+  void *y_routed, *y_shared;
+  void *inner;  // scratch shared by the four steps (they run one after another)
+  size_t inner_bytes;
+};
+
+static FwdScratch fwd_ws(const moe_dims_t *d, Carver &c) {
+  FwdScratch s;
+  const int64_t R = (int64_t)d->T * d->k;
+  s.ids = (int32_t *)c.take((size_t)R * 4);
+  s.w = (float *)c.take((size_t)R * 4);
+  s.sig = (float *)c.take((size_t)d->T * 4);
+  s.offsets = (int32_t *)c.take((size_t)(d->E + 1) * 4);
+  s.sorted_route = (int32_t *)c.take((size_t)R * 4);
+  s.route_pos = (int32_t *)c.take((size_t)R * 4);
+  s.y_routed = c.take((size_t)R * d->H * esize(d));
+  s.y_shared = c.take((size_t)d->T * d->H * esize(d));
+  Carver a(nullptr), b(nullptr), f(nullptr);
+  route_ws(d, a);
+  permute_ws(d, b);
+  ffn_ws(d, f);
+  size_t inner = a.off;
+  if (b.off > inner) inner = b.off;
+  if (f.off > inner) inner = f.off;
+  s.inner_bytes = (size_t)round_up((int64_t)inner, 256);
+  s.inner = c.take(s.inner_bytes);
+  return s;
+}
+
+static size_t ws_size(const moe_dims_t *d, int op) {
+  Carver c(nullptr);
+  switch (op) {
+    case MOE_OP_ROUTE: route_ws(d, c); break;
+    case MOE_OP_PERMUTE: permute_ws(d, c); break;
+    case MOE_OP_GROUPED_FFN: ffn_ws(d, c); break;
+    case MOE_OP_COMBINE: break;
+    case MOE_OP_FORWARD: fwd_ws(d, c); break;
+    default: return 0;
+  }
+  return (size_t)round_up((int64_t)c.off, 256);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API size_t moe_workspace_size(const moe_dims_t *d, int op) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return ws_size(d, op);
+}
+
+MOE_API const char *moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size, k > E or k > 16)";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE: return "a kernel recorded a failed device-side check";
+    default: return "unknown status";
+  }
+}
+
+MOE_API int moe_route(const moe_dims_t *d, const void *x, const float *w_router, const float *router_bias,
+                      const void *w_shared_gate, int32_t *topk_ids, float *topk_w, float *shared_sig, float *logits,
+                      void *ws, size_t ws_bytes, void *stream) {
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  const int64_t T = d->T, R = T * d->k;
+  if (!buf_ok(x, T * d->H) || !buf_ok(w_router, 1) || !opt_ok(router_bias) || !buf_ok(w_shared_gate, 1) ||
+      !buf_ok(topk_ids, R) || !buf_ok(topk_w, R) || !buf_ok(shared_sig, T) || !opt_ok(logits) || !opt_ok(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_size(d, MOE_OP_ROUTE)) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  Carver c(ws);
+  float *lg = (float *)c.take((size_t)T * d->E * sizeof(float));
+  if (logits) lg = logits;
+  cudaError_t e = launch_router_logits_simt(d->dtype, d->T, d->H, d->E, x, w_router, router_bias, lg, s);
+  if (e == cudaSuccess)
+    e = launch_topk_gate(d->dtype, d->T, d->H, d->E, d->k, lg, x, w_shared_gate, topk_ids, topk_w, shared_sig, s);
+  return cuda_status(e);
+}
+
+MOE_API int moe_permute(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_offsets,
+                        int32_t *sorted_route, int32_t *route_pos, void *ws, size_t ws_bytes, void *stream) {
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  const int64_t R = (int64_t)d->T * d->k;
+  if (!buf_ok(topk_ids, R) || !buf_ok(expert_offsets, 1) || !buf_ok(sorted_route, R) || !buf_ok(route_pos, R) ||
+      !opt_ok(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_size(d, MOE_OP_PERMUTE)) return MOE_ERR_WORKSPACE;
+  return cuda_status(launch_permute(R, d->E, topk_ids, expert_offsets, sorted_route, route_pos, ws, status_ptr(),
+                                    (cudaStream_t)stream));
+}
+
+MOE_API int moe_grouped_ffn(const moe_dims_t *d, const void *x, const int32_t *expert_offsets,
+                            const int32_t *sorted_route, const void *w_gate_up, const void *w_down,
+                            const void *ws_gate_up, const void *ws_down, void *y_routed, void *y_shared,
+                            const moe_saved_t *saved, void *ws, size_t ws_bytes, void *stream) {
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  const int64_t T = d->T, R = T * d->k;
+  if (!buf_ok(x, T * d->H) || !buf_ok(expert_offsets, 1) || !buf_ok(sorted_route, R) || !buf_ok(w_gate_up, 1) ||
+      !buf_ok(w_down, 1) || !buf_ok(ws_gate_up, 1) || !buf_ok(ws_down, 1) || !buf_ok(y_routed, R * d->H) ||
+      !buf_ok(y_shared, T * d->H) || !opt_ok(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (saved && (!opt_ok(saved->gu) || !opt_ok(saved->h) || !opt_ok(saved->gu_shared) || !opt_ok(saved->h_shared)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_size(d, MOE_OP_GROUPED_FFN)) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  Carver c(ws);
+  FfnScratch sc = ffn_ws(d, c);
+  FfnArgs a;
+  a.T = d->T; a.H = d->H; a.E = d->E; a.k = d->k; a.I = d->I; a.Is = d->Is;
+  a.x = x; a.offsets = expert_offsets; a.sorted_route = sorted_route;
+  a.w_gate_up = w_gate_up; a.w_down = w_down; a.ws_gate_up = ws_gate_up; a.ws_down = ws_down;
+  a.y_routed = y_routed; a.y_shared = y_shared;
+  a.h_routed = (saved && saved->h) ? saved->h : sc.h_routed;
+  a.h_shared = (saved && saved->h_shared) ? saved->h_shared : sc.h_shared;
+  a.gu_routed = saved ? saved->gu : nullptr;
+  a.gu_shared = saved ? saved->gu_shared : nullptr;
+  return cuda_status(launch_ffn_simt(d->dtype, a, sc.tiles, (cudaStream_t)stream));
+}
+
+MOE_API int moe_combine(const moe_dims_t *d, const void *y_routed, const void *y_shared, const float *topk_w,
+                        const float *shared_sig, void *y, void *stream) {
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  const int64_t T = d->T, R = T * d->k;
+  if (!buf_ok(y_routed, R * d->H) || !buf_ok(y_shared, T * d->H) || !buf_ok(topk_w, R) || !buf_ok(shared_sig, T) ||
+      !buf_ok(y, T * d->H))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(d->dtype, d->T, d->H, d->k, y_routed, y_shared, topk_w, shared_sig, y,
+                                    (cudaStream_t)stream));
+}
+
+MOE_API int moe_forward(const moe_dims_t *d, const moe_fwd_args_t *a, void *ws, size_t ws_bytes, void *stream) {
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (!a || !opt_ok(ws)) return MOE_ERR_INVALID_ARG;
+  const int64_t T = d->T;
+  if (!buf_ok(a->x, T * d->H) || !buf_ok(a->y, T * d->H)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_size(d, MOE_OP_FORWARD)) return MOE_ERR_WORKSPACE;
+  Carver c(ws);
+  FwdScratch s = fwd_ws(d, c);
+  int32_t *ids = a->topk_ids ? a->topk_ids : s.ids;
+  float *w = a->topk_w ? a->topk_w : s.w;
+  float *sig = a->shared_sig ? a->shared_sig : s.sig;
+  int32_t *off = a->expert_offsets ? a->expert_offsets : s.offsets;
+  int32_t *srt = a->sorted_route ? a->sorted_route : s.sorted_route;
+  int32_t *pos = a->route_pos ? a->route_pos : s.route_pos;
+  void *yr = a->y_routed ? a->y_routed : s.y_routed;
+  void *ys = a->y_shared ? a->y_shared : s.y_shared;
+  st = moe_route(d, a->x, a->w_router, a->router_bias, a->w_shared_gate, ids, w, sig, a->logits, s.inner,
+                 s.inner_bytes, stream);
+  if (st != MOE_OK) return st;
+  st = moe_permute(d, ids, off, srt, pos, s.inner, s.inner_bytes, stream);
+  if (st != MOE_OK) return st;
+  st = moe_grouped_ffn(d, a->x, off, srt, a->w_gate_up, a->w_down, a->ws_gate_up, a->ws_down, yr, ys, &a->saved,
+                       s.inner, s.inner_bytes, stream);
+  if (st != MOE_OK) return st;
+  return moe_combine(d, yr, ys, w, sig, a->y, stream);
+}
+
+MOE_API int moe_backward(const moe_dims_t *d, const moe_bwd_args_t *a, void *ws, size_t ws_bytes, void *stream) {
+  (void)a; (void)ws; (void)ws_bytes; (void)stream;
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  return MOE_ERR_UNSUPPORTED;
+}
+
+MOE_API int moe_device_status(int reset, int32_t *detail) {
+  int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, g_moe_status, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (reset) {
+    int zero = 0;
+    if (cudaMemcpyToSymbol(g_moe_status, &zero, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (detail) *detail = v;
+  return v == 0 ? MOE_OK : MOE_ERR_DEVICE;
+}

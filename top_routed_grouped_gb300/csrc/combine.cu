@@ -1,0 +1,62 @@
+// combine_routes.
+//
+// RL-Kernel PR #557, embedded #503 commit message, bullet "Combine": the k
+// weighted routed rows are summed with ordered FP32 multiply-adds and cast
+// once to the output type, no atomics; PR #557 "What": every rank applies
+// combine_routes in FP32 route order.  The gated shared-expert row is added
+// after the k routed terms in the same FP32 accumulator:
+//   acc = 0; for s = 0..k-1: acc = fma(w[t,s], Yr[t*k+s], acc);
+//   acc = fma(sig[t], Ys[t], acc);  y = cast(acc)
+// One thread owns 16 bytes of one output row, so the order is the same for
+// every batch.  y_routed is in route order (row t*k + s), so a token's k rows
+// are contiguous.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+template <typename TE>
+__global__ void __launch_bounds__(256)
+combine_kernel(int T, int H, int k, const TE *__restrict__ yr, const TE *__restrict__ ys,
+               const float *__restrict__ w, const float *__restrict__ sig, TE *__restrict__ y) {
+  constexpr int VN = Vec16<TE>::N;
+  const int vec_per_row = H / VN;
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= (int64_t)T * vec_per_row) return;
+  const int64_t t = gid / vec_per_row;
+  const int h = (int)(gid % vec_per_row) * VN;
+  float acc[VN];
+#pragma unroll
+  for (int j = 0; j < VN; ++j) acc[j] = 0.f;
+  for (int s = 0; s < k; ++s) {
+    const float ws = w[t * k + s];
+    float v[VN];
+    Vec16<TE>::load(yr + (t * k + s) * H + h, v);
+#pragma unroll
+    for (int j = 0; j < VN; ++j) acc[j] = fmaf(ws, v[j], acc[j]);
+  }
+  const float g = sig[t];
+  float v[VN];
+  Vec16<TE>::load(ys + t * H + h, v);
+#pragma unroll
+  for (int j = 0; j < VN; ++j) acc[j] = fmaf(g, v[j], acc[j]);
+  Vec16<TE>::store(y + t * H + h, acc);
+}
+
+cudaError_t launch_combine(int dtype, int T, int H, int k, const void *y_routed, const void *y_shared,
+                           const float *w, const float *sig, void *y, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const int VN = dtype == 0 ? 4 : 8;
+  const int64_t n = (int64_t)T * (H / VN);
+  const unsigned blocks = (unsigned)ceil_div(n, 256);
+  if (dtype == 0)
+    combine_kernel<float><<<blocks, 256, 0, stream>>>(T, H, k, (const float *)y_routed, (const float *)y_shared,
+                                                      w, sig, (float *)y);
+  else
+    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(T, H, k, (const __nv_bfloat16 *)y_routed,
+                                                              (const __nv_bfloat16 *)y_shared, w, sig,
+                                                              (__nv_bfloat16 *)y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

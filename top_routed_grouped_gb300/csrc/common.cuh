@@ -1,0 +1,79 @@
+// Shared device helpers of the MoE kernels (element conversion, status word,
+// small integer utilities).  Nothing here is layer arithmetic.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+
+// Device status codes (documented with moe_device_status in moe.h).
+enum : int { STATUS_BAD_EXPERT_ID = 1, STATUS_WAIT_TIMEOUT = 2, STATUS_TMEM_ALLOC = 3 };
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// Record the first failed device-side check; later ones keep the first code.
+__device__ inline void record_status(int *status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// ---- element type conversion (fp32 <-> storage type) ----
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static __device__ inline float load(const float *p) { return *p; }
+  static __device__ inline float to_f32(float v) { return v; }
+  static __device__ inline float from_f32(float v) { return v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static __device__ inline float load(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+  static __device__ inline float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+  static __device__ inline __nv_bfloat16 from_f32(float v) { return __float2bfloat16_rn(v); }
+};
+
+// 16-byte vector of storage elements: 4 floats or 8 bf16.
+template <typename T> struct Vec16;
+template <> struct Vec16<float> {
+  static constexpr int N = 4;
+  static __device__ inline void load(const float *p, float (&o)[4]) {
+    float4 v = *reinterpret_cast<const float4 *>(p);
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
+  static __device__ inline void store(float *p, const float (&o)[4]) {
+    *reinterpret_cast<float4 *>(p) = make_float4(o[0], o[1], o[2], o[3]);
+  }
+};
+template <> struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  static __device__ inline void load(const __nv_bfloat16 *p, float (&o)[8]) {
+    uint4 v = *reinterpret_cast<const uint4 *>(p);
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = __bfloat1622float2(h[i]);
+      o[2 * i] = f.x;
+      o[2 * i + 1] = f.y;
+    }
+  }
+  static __device__ inline void store(__nv_bfloat16 *p, const float (&o)[8]) {
+    uint4 v;
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+    *reinterpret_cast<uint4 *>(p) = v;
+  }
+};
+
+__device__ inline float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+__device__ inline float sigmoid_f32(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+__device__ inline unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+}  // namespace moe

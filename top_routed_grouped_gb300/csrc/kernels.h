@@ -1,0 +1,49 @@
+// Host-side launchers of the MoE kernels (internal; the public surface is
+// include/moe.h).  Every launcher only enqueues work on `stream` and returns
+// the launch status.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---- route.cu ----
+// logits[t,e] = sum_h x[t,h] * wr[e,h] (+ bias[e]) with FP32 products summed
+// sequentially over h (the MOE_F32 router).
+cudaError_t launch_router_logits_simt(int dtype, int T, int H, int E, const void *x, const float *wr,
+                                      const float *bias, float *logits, cudaStream_t stream);
+// Top-k, route weights and shared gate, one warp per token.
+cudaError_t launch_topk_gate(int dtype, int T, int H, int E, int k, const float *logits, const void *x,
+                             const void *w_shared_gate, int32_t *ids, float *w, float *sig,
+                             cudaStream_t stream);
+
+// ---- permute.cu ----
+size_t permute_scratch_bytes(int64_t R, int E);
+cudaError_t launch_permute(int64_t R, int E, const int32_t *ids, int32_t *offsets, int32_t *sorted_route,
+                           int32_t *route_pos, void *scratch, int *status, cudaStream_t stream);
+// tile_start[s] for s in [0, E+1]: prefix of ceil(n_s / bn) over the E routed
+// segments (n_s from offsets) and the shared segment (n_E = T).
+cudaError_t launch_build_tiles(int E, int T, int bn, const int32_t *offsets, int32_t *tile_start,
+                               cudaStream_t stream);
+
+// ---- ffn_simt.cu ----
+struct FfnArgs {
+  int T, H, E, k, I, Is;
+  const void *x;
+  const int32_t *offsets;
+  const int32_t *sorted_route;
+  const void *w_gate_up, *w_down, *ws_gate_up, *ws_down;
+  void *y_routed, *y_shared;
+  void *h_routed, *h_shared;    // intermediate h (required)
+  void *gu_routed, *gu_shared;  // saved pre-activations (nullable)
+};
+size_t ffn_simt_scratch_bytes(int E);
+cudaError_t launch_ffn_simt(int dtype, const FfnArgs &a, void *scratch, cudaStream_t stream);
+
+// ---- combine.cu ----
+cudaError_t launch_combine(int dtype, int T, int H, int k, const void *y_routed, const void *y_shared,
+                           const float *w, const float *sig, void *y, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,212 @@
+// Routing kernels.
+//
+// RL-Kernel PR #557 "EP4 distributed logprob parity", embedded #503 commit
+// message, bullet "Routing": FP32 router through a batch-invariant GEMM, a
+// fixed-order softmax, stable descending top-k (ties to the lower expert id)
+// and FP32 renormalisation of the selected weights.  Shared-expert gate:
+// #503 "TP4 block" (replicated shared-expert gate), a sigmoid of x . w_sg.
+//
+// Batch invariance: every value a token receives is computed by one thread
+// or one warp from that token's row alone, in an order fixed by H and E only.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// FP32 router GEMM on CUDA cores: logits[t,e] = sum_h x[t,h] wr[e,h] (+bias).
+// 64x64 output tile per block, each output accumulated by one thread with
+// fmaf over h = 0, 1, ..., H-1 in that order (zero padding past H adds exact
+// zeros), so the value does not depend on the tile a token falls in.
+// ---------------------------------------------------------------------------
+template <typename TX>
+__global__ void __launch_bounds__(256)
+router_logits_simt_kernel(int T, int H, int E, const TX *__restrict__ x, const float *__restrict__ wr,
+                          const float *__restrict__ bias, float *__restrict__ logits) {
+  __shared__ float xs[32][68];
+  __shared__ float wsm[32][68];
+  const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+  for (int h0 = 0; h0 < H; h0 += 32) {
+    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+      int r = i >> 5, c = i & 31;
+      int t = t0 + r, e = e0 + r, h = h0 + c;
+      xs[c][r] = (t < T && h < H) ? Elem<TX>::load(x + (int64_t)t * H + h) : 0.f;
+      wsm[c][r] = (e < E && h < H) ? wr[(int64_t)e * H + h] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = wsm[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int t = t0 + ty * 4 + i, e = e0 + tx * 4 + j;
+      if (t < T && e < E) {
+        float v = acc[i][j];
+        if (bias) v += bias[e];
+        logits[(int64_t)t * E + e] = v;
+      }
+    }
+}
+
+cudaError_t launch_router_logits_simt(int dtype, int T, int H, int E, const void *x, const float *wr,
+                                      const float *bias, float *logits, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  dim3 grid((unsigned)ceil_div(T, 64), (unsigned)ceil_div(E, 64));
+  if (dtype == 0)
+    router_logits_simt_kernel<float><<<grid, 256, 0, stream>>>(T, H, E, (const float *)x, wr, bias, logits);
+  else
+    router_logits_simt_kernel<__nv_bfloat16>
+        <<<grid, 256, 0, stream>>>(T, H, E, (const __nv_bfloat16 *)x, wr, bias, logits);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Top-k + weights + shared gate, one warp per token.
+//
+// Candidate order: numbers before NaNs before already-taken slots; among
+// numbers the larger logit first; equal keys go to the lower expert id.
+// Each of the k rounds takes the lane-local best, then a butterfly arg-max
+// over the 32 lanes (the comparison is a strict total order, so the winner
+// does not depend on the reduction shape).  Slot s receives the s-th winner,
+// which is the stable descending order of the logits.
+//
+// Weights: w_s = exp(l_s - l_0) / sum_j exp(l_j - l_0) over the k selected
+// logits (l_0 is the largest), the softmax over all experts followed by
+// renormalisation of the selected ones; the sum runs over s = 0..k-1.
+// Shared gate: z = x . w_sg, lane-partial sums in ascending h per lane, then
+// a fixed butterfly; sig = 1 / (1 + exp(-z)).
+// ---------------------------------------------------------------------------
+struct Cand {
+  int cls;  // 2 = number, 1 = NaN, 0 = taken / absent
+  float v;
+  int e;
+};
+
+__device__ inline bool better(const Cand &a, const Cand &b) {
+  if (a.cls != b.cls) return a.cls > b.cls;
+  if (a.v != b.v) return a.v > b.v;
+  return a.e < b.e;
+}
+
+template <typename TX, int EPL>
+__global__ void __launch_bounds__(256)
+topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, const TX *__restrict__ x,
+                 const TX *__restrict__ wsg, int32_t *__restrict__ ids, float *__restrict__ w,
+                 float *__restrict__ sig) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+
+  float v[EPL];
+  int cls[EPL];
+  const float *lrow = logits + t * E;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    int e = lane + 32 * i;
+    if (e < E) {
+      float l = lrow[e];
+      bool nan = l != l;
+      v[i] = nan ? -INFINITY : l;
+      cls[i] = nan ? 1 : 2;
+    } else {
+      v[i] = -INFINITY;
+      cls[i] = 0;
+    }
+  }
+
+  float sel_v = 0.f;  // lane s keeps the logit of slot s
+  int sel_e = 0;
+  for (int s = 0; s < k; ++s) {
+    Cand best{-1, -INFINITY, 0x7fffffff};
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      Cand c{cls[i], v[i], lane + 32 * i};
+      if (better(c, best)) best = c;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      Cand o;
+      o.cls = __shfl_xor_sync(FULL_MASK, best.cls, off);
+      o.v = __shfl_xor_sync(FULL_MASK, best.v, off);
+      o.e = __shfl_xor_sync(FULL_MASK, best.e, off);
+      if (better(o, best)) best = o;
+    }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i == best.e) cls[i] = 0;
+    if (lane == s) {
+      sel_v = best.v;
+      sel_e = best.e;
+    }
+  }
+
+  // Route weights.  Every lane forms the same denominator in slot order.
+  const float m = __shfl_sync(FULL_MASK, sel_v, 0);
+  float z = 0.f;
+  for (int s = 0; s < k; ++s) z += expf(__shfl_sync(FULL_MASK, sel_v, s) - m);
+  if (lane < k) {
+    ids[t * k + lane] = sel_e;
+    w[t * k + lane] = expf(sel_v - m) / z;
+  }
+
+  // Shared-expert gate.
+  constexpr int VN = Vec16<TX>::N;
+  const TX *xr = x + t * (int64_t)H;
+  float part = 0.f;
+  for (int h = lane * VN; h < H; h += 32 * VN) {
+    float xv[VN], gv[VN];
+    Vec16<TX>::load(xr + h, xv);
+    Vec16<TX>::load(wsg + h, gv);
+#pragma unroll
+    for (int j = 0; j < VN; ++j) part = fmaf(xv[j], gv[j], part);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(FULL_MASK, part, off);
+  if (lane == 0) sig[t] = sigmoid_f32(part);
+}
+
+template <typename TX>
+static cudaError_t topk_dispatch(int T, int H, int E, int k, const float *logits, const void *x, const void *wsg,
+                                 int32_t *ids, float *w, float *sig, cudaStream_t stream) {
+  dim3 grid((unsigned)ceil_div(T, 8));
+  const TX *xx = (const TX *)x;
+  const TX *gg = (const TX *)wsg;
+#define MOE_TOPK(EPL) topk_gate_kernel<TX, EPL><<<grid, 256, 0, stream>>>(T, H, E, k, logits, xx, gg, ids, w, sig)
+  if (E <= 32) MOE_TOPK(1);
+  else if (E <= 64) MOE_TOPK(2);
+  else if (E <= 128) MOE_TOPK(4);
+  else if (E <= 256) MOE_TOPK(8);
+  else if (E <= 512) MOE_TOPK(16);
+  else MOE_TOPK(32);
+#undef MOE_TOPK
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_gate(int dtype, int T, int H, int E, int k, const float *logits, const void *x,
+                             const void *w_shared_gate, int32_t *ids, float *w, float *sig, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  if (dtype == 0) return topk_dispatch<float>(T, H, E, k, logits, x, w_shared_gate, ids, w, sig, stream);
+  return topk_dispatch<__nv_bfloat16>(T, H, E, k, logits, x, w_shared_gate, ids, w, sig, stream);
+}
+
+}  // namespace moe
