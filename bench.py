@@ -1,0 +1,344 @@
+"""Benchmark of the batch-invariant MoE layer on GB300.
+
+One step = one forward of the layer over one batch of T tokens (router,
+top-k and gate, dispatch permute, grouped SwiGLU experts with the shared
+expert, ordered combine) through the C ABI, inputs resident in HBM.  The
+default workload is bf16_t8192 (T=8192, H=2048, 512 experts top-10, I=Is=512);
+the expert weights (3.2 GB) exceed L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  Keys beyond the basic contract:
+  e2e          same metric through moe_forward with pinned host buffers and
+               the host<->device copies of x and y inside the timed region
+  roofline     the dominant operation (moe_grouped_ffn) against measured HBM
+  layer_roofline  the whole step against max(bytes/HBM, FLOPs/tensor peak)
+  cpu_baseline the FP64 oracle on the host cores, on a bounded token sample
+  clocks       nvidia-smi samples taken during the timed region
+
+--impl reference times the oracle itself (the reference arm) on the host.
+Multi-GPU (torchrun): every rank runs its own replica of the workload
+(tokens shard with no exchange), value = all ranks' tokens / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "MoE layer tokens/sec (fwd, fwd+bwd) on 1 GB300; % of layer roofline"
+
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def layer_bytes_flops(T, H, E, k, I, Is, active_experts, es=2) -> dict:
+    """Algorithmic bytes and FLOPs of one layer forward.
+
+    FLOPs: 6 H I per route + 6 H Is per token (the router is not counted).
+    Bytes: weights of every expert with >= 1 route, the shared expert, the fp32
+    router weight and the shared gate, x read once and y written once.
+    """
+    weights = active_experts * 3 * H * I * es + 3 * H * Is * es + E * H * 4 + H * es
+    return {"bytes": weights + 2 * T * H * es, "flops": 6 * H * I * T * k + 6 * H * Is * T, "weight_bytes": weights}
+
+
+def ffn_bytes_flops(T, H, k, I, Is, active_experts, es=2) -> dict:
+    """Algorithmic bytes / FLOPs of moe_grouped_ffn: weights of active experts
+    and the shared expert read once, x read once, the unweighted rows written
+    once, and the intermediate h written and read once."""
+    R = T * k
+    w = active_experts * 3 * H * I * es + 3 * H * Is * es
+    b = w + T * H * es + (R + T) * H * es + 2 * (R * I + T * Is) * es
+    return {"bytes": b, "flops": 6 * H * I * R + 6 * H * Is * T}
+
+
+def cpu_oracle_baseline(cfg, x_cpu, W_cpu, bias, budget_s: float = 12.0, max_tokens: int = 4096) -> dict:
+    """Time the FP64 oracle (routing + experts + combine) on the first tokens
+    of the workload, in blocks of 32 tokens until `budget_s` has elapsed."""
+    os.environ.setdefault("OMP_NUM_THREADS", str(host_cores()))
+    import numpy as np
+    import oracle
+    import torch
+
+    f64 = {k: v.to(torch.float64).numpy() for k, v in W_cpu.items()}
+    b64 = None if bias is None else bias.to(torch.float64).numpy()
+    oracle.build()
+    done, elapsed = 0, 0.0
+    while elapsed < budget_s and done < max_tokens:
+        xs = x_cpu[done:done + 32].to(torch.float64).numpy()
+        t0 = time.perf_counter()
+        r = oracle.layer_forward(xs, f64["w_router"], f64["w_shared_gate"], f64["w_gate_up"], f64["w_down"],
+                                 f64["ws_gate_up"], f64["ws_down"], cfg.k, b64)
+        elapsed += time.perf_counter() - t0
+        done += xs.shape[0]
+        assert np.isfinite(r["y"]).all()
+    return {"value": done / elapsed, "unit": "tokens/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
+            "kind": "oracle", "sample": f"first {done} tokens of {cfg.name} (FP64 route + experts + combine), "
+                                        f"{elapsed:.1f} s of oracle time"}
+
+
+def run_reference(args, cfg, rank: int) -> None:
+    """Reference arm: the oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    import torch
+    from top_routed_grouped_gb300 import inputs as I
+    d = I.make_inputs(cfg)
+    W = {k: v for k, v in d.items() if k not in ("x", "dy", "router_bias")}
+    budget = max(2.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_baseline(cfg, d["x"], W, d["router_bias"], budget_s=0.5, max_tokens=32)
+    vals = []
+    cb = None
+    for _ in range(args.steps):
+        cb = cpu_oracle_baseline(cfg, d["x"], W, d["router_bias"], budget_s=budget)
+        vals.append(cb["value"])
+    v = statistics.median(vals)
+    cb["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * cfg.T / v,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I,
+                       "Is": cfg.Is, "step": "forward"},
+            "cpu_baseline": cb, "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="bf16_t8192")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from top_routed_grouped_gb300 import inputs as I
+    cfg = I.CONFIGS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+
+    import torch
+    import top_routed_grouped_gb300 as moe
+    from top_routed_grouped_gb300 import build as B
+    if rank == 0 or not B.up_to_date():
+        B.build()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    # ---- inputs (seeded, made on the host, copied once) ----
+    cpu = I.make_inputs(cfg)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in cpu.items()}
+    T, H, E, k, Iw, Is = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.Is
+    R = T * k
+    dt = cfg.torch_dtype
+    d = moe.make_dims(T, H, E, k, Iw, Is, dt)
+    o = {"ids": torch.empty(T, k, dtype=torch.int32, device="cuda"),
+         "w": torch.empty(T, k, dtype=torch.float32, device="cuda"),
+         "sig": torch.empty(T, dtype=torch.float32, device="cuda"),
+         "off": torch.empty(E + 1, dtype=torch.int32, device="cuda"),
+         "srt": torch.empty(R, dtype=torch.int32, device="cuda"),
+         "pos": torch.empty(R, dtype=torch.int32, device="cuda"),
+         "yr": torch.empty(R, H, dtype=dt, device="cuda"),
+         "ys": torch.empty(T, H, dtype=dt, device="cuda"),
+         "y": torch.empty(T, H, dtype=dt, device="cuda")}
+    ws = torch.empty(max(moe.moe_workspace_size(d, op) for op in ("route", "permute", "grouped_ffn")),
+                     dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        moe.moe_route(d, dev["x"], dev["w_router"], dev["router_bias"], dev["w_shared_gate"], o["ids"], o["w"],
+                      o["sig"], None, ws, stream)
+        moe.moe_permute(d, o["ids"], o["off"], o["srt"], o["pos"], ws, stream)
+        if ev: ev[1].record(stream)
+        moe.moe_grouped_ffn(d, dev["x"], o["off"], o["srt"], dev["w_gate_up"], dev["w_down"], dev["ws_gate_up"],
+                            dev["ws_down"], o["yr"], o["ys"], None, ws, stream)
+        if ev: ev[2].record(stream)
+        moe.moe_combine(d, o["yr"], o["ys"], o["w"], o["sig"], o["y"], stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    moe.moe_device_status(reset=True)
+    active = int((o["off"][1:] - o["off"][:-1] > 0).sum().item())
+
+    # ---- device-timed region ----
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    ms_local = start.elapsed_time(end) / args.steps
+    ffn_ms = statistics.mean(evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps))
+    ms = max_over_ranks(ms_local, world)
+    if moe.moe_device_status(reset=True) != 0:
+        raise RuntimeError("a kernel recorded a failed device-side check during the timed region")
+
+    # ---- end to end: pinned host x -> device, moe_forward, y -> pinned host ----
+    x_host = cpu["x"].pin_memory()
+    y_host = torch.empty(T, H, dtype=dt).pin_memory()
+    x_dev = torch.empty_like(dev["x"])
+    fws = moe.workspace(d, "forward")
+    fargs = {"x": x_dev, "w_router": dev["w_router"], "router_bias": dev["router_bias"],
+             "w_shared_gate": dev["w_shared_gate"], "w_gate_up": dev["w_gate_up"], "w_down": dev["w_down"],
+             "ws_gate_up": dev["ws_gate_up"], "ws_down": dev["ws_down"], "y": o["y"]}
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_forward(d, fargs, fws, stream)
+        y_host.copy_(o["y"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+
+    peaks, peak_src = load_peaks()
+    lb = layer_bytes_flops(T, H, E, k, Iw, Is, active)
+    fb = ffn_bytes_flops(T, H, k, Iw, Is, active)
+    hbm = float(peaks["hbm_gbs"])
+    tf_sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    t_roof_ms = max(lb["bytes"] / (hbm * 1e9), lb["flops"] / (float(peaks["bf16_tflops"]) * 1e12)) * 1e3
+    achieved = fb["bytes"] / (ffn_ms * 1e-3) / 1e9
+    tokens_all = T * world
+    line = {
+        "metric": METRIC, "value": tokens_all / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) weights)",
+        "config": {"workload": cfg.name, "T": T, "H": H, "E": E, "k": k, "I": Iw, "Is": Is, "step": "forward",
+                   "active_experts": active, "l2": "no flush: expert weights (3.2 GB) exceed the 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+                "d2h_bytes_per_step": T * H * 2, "api": "moe_forward"},
+        "gpu_launches": 10 * args.steps,
+        "roofline": {"kernel": "moe_grouped_ffn (gate_up+SwiGLU, down)", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_source": peak_src, "ms_per_launch": ffn_ms,
+                     "algorithmic_bytes": fb["bytes"]},
+        "layer_roofline": {"bytes": lb["bytes"], "flops": lb["flops"], "roofline_ms": t_roof_ms,
+                           "frac": t_roof_ms / ms, "peak_hbm_gbs": hbm, "peak_bf16_tflops": peaks["bf16_tflops"],
+                           "peak_source": peak_src},
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        W = {kk: v for kk, v in cpu.items() if kk not in ("x", "dy", "router_bias")}
+        line["cpu_baseline"] = cpu_oracle_baseline(cfg, cpu["x"], W, cpu["router_bias"])
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

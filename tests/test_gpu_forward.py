@@ -35,10 +35,13 @@ def run_forward(d, k, want_logits=True):
 def check_routes_and_permutation(out, x_cpu, wr_cpu, bias_cpu, k, E):
     gl = out["logits"].double().cpu().numpy()
     ids, w, near, l64 = oracle_routes(x_cpu, wr_cpu, bias_cpu, k, gl)
-    assert np.max(np.abs(gl - l64)) < 2e-5  # FP32 logits vs FP64
+    dl = float(np.max(np.abs(gl - l64)))
+    assert dl < 2e-5  # FP32 logits vs FP64
     gids = out["topk_ids"].cpu().numpy()
     np.testing.assert_array_equal(gids, ids)
-    np.testing.assert_allclose(out["topk_w"].double().cpu().numpy(), w, rtol=0, atol=2e-6)
+    # w = softmax of the selected logits: |dw| <= 2 max|dl| w (+ FP32 rounding of the softmax)
+    gw = out["topk_w"].double().cpu().numpy()
+    assert np.all(np.abs(gw - w) <= 2 * dl * w + 4e-7), float(np.max(np.abs(gw - w)))
     off, srt, pos = oracle.permute(gids, E)
     np.testing.assert_array_equal(out["expert_offsets"].cpu().numpy(), off)
     np.testing.assert_array_equal(out["sorted_route"].cpu().numpy(), srt)
