@@ -156,6 +156,34 @@ int moe_permute(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_of
                 int32_t *sorted_route, int32_t *route_pos, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_permute_noalloc -- moe_permute without a workspace argument.
+ * The paper has no counterpart: this is a convenience of this library.
+ *
+ * For callers that cannot allocate device memory: a custom operator or
+ * plugin hosted by another runtime that owns the device memory pool and
+ * hands out only input and output buffers, or a latency-critical loop that
+ * must not call cudaMalloc because it can synchronise the device.  The
+ * arguments and results are those of moe_permute (bit-identical outputs);
+ * the kernels' scratch lives in a fixed array of
+ * MOE_PERMUTE_NOALLOC_SCRATCH_BYTES in the library's own device memory,
+ * held by every GPU that loads the library until the process exits.  No
+ * cudaMalloc, cudaFree or other allocating routine is called.
+ *
+ * Limit: the scratch needs (ceil(T*k / 512) * E + E) * 4 bytes; larger
+ * sizes return MOE_ERR_UNSUPPORTED before any GPU work (with E = 512: up to
+ * 1,047,552 routes, e.g. T = 104,755 tokens at k = 10).
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call uses the same array: calls that can
+ * overlap on the GPU (different streams, no ordering between them) race and
+ * must be serialised by the caller.  Each call writes every scratch word it
+ * reads, so nothing is carried over from the previous call.
+ */
+#define MOE_PERMUTE_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+int moe_permute_noalloc(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_offsets,
+                        int32_t *sorted_route, int32_t *route_pos, void *stream);
+
+/*
  * moe_grouped_ffn -- per-expert SwiGLU FFN over the expert segments.
  * #503 commit message "Experts": per-route gate_up and down projections
  * through one fixed-configuration grouped GEMM, no routed-weight multiply

@@ -24,7 +24,7 @@ OP = {"route": 0, "permute": 1, "grouped_ffn": 2, "combine": 3, "backward": 4, "
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_WORKSPACE",
           -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE"}
 EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_permute", "moe_grouped_ffn",
-            "moe_combine", "moe_forward", "moe_backward", "moe_device_status")
+            "moe_combine", "moe_forward", "moe_backward", "moe_device_status", "moe_permute_noalloc")
 
 _vp = ctypes.c_void_p
 
@@ -85,6 +85,7 @@ def lib() -> ctypes.CDLL:
                 "moe_forward": ([D, ctypes.POINTER(FwdArgs), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_backward": ([D, ctypes.POINTER(BwdArgs), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_device_status": ([ctypes.c_int, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+                "moe_permute_noalloc": ([D] + [_vp] * 4 + [_vp], ctypes.c_int),
             }
             for name, (args, res) in sigs.items():
                 fn = getattr(L, name)
@@ -143,6 +144,13 @@ def moe_permute(d, topk_ids, expert_offsets, sorted_route, route_pos, ws, stream
     _check("moe_permute", lib().moe_permute(ctypes.byref(d), _p(topk_ids), _p(expert_offsets), _p(sorted_route),
                                             _p(route_pos), _p(ws), 0 if ws is None else ws.numel(),
                                             _stream(stream)))
+
+
+def moe_permute_noalloc(d, topk_ids, expert_offsets, sorted_route, route_pos, stream=None):
+    """moe_permute without a workspace: for callers that cannot allocate device
+    memory (the scratch is a fixed array inside the library; see moe.h)."""
+    _check("moe_permute_noalloc", lib().moe_permute_noalloc(ctypes.byref(d), _p(topk_ids), _p(expert_offsets),
+                                                            _p(sorted_route), _p(route_pos), _stream(stream)))
 
 
 def _saved(saved) -> Saved:

@@ -14,7 +14,7 @@ namespace moe {
 // Device status word: first failed device-side check since the last reset.
 __device__ int g_moe_status;
 
-static int *status_ptr() {
+int *device_status_ptr() {
   static std::mutex mu;
   static int *cache[64] = {};
   int dev = 0;
@@ -186,7 +186,7 @@ MOE_API int moe_permute(const moe_dims_t *d, const int32_t *topk_ids, int32_t *e
       !opt_ok(ws))
     return MOE_ERR_INVALID_ARG;
   if (ws_bytes < ws_size(d, MOE_OP_PERMUTE)) return MOE_ERR_WORKSPACE;
-  return cuda_status(launch_permute(R, d->E, topk_ids, expert_offsets, sorted_route, route_pos, ws, status_ptr(),
+  return cuda_status(launch_permute(R, d->E, topk_ids, expert_offsets, sorted_route, route_pos, ws, device_status_ptr(),
                                     (cudaStream_t)stream));
 }
 

@@ -19,6 +19,10 @@ cudaError_t launch_topk_gate(int dtype, int T, int H, int E, int k, const float 
                              const void *w_shared_gate, int32_t *ids, float *w, float *sig,
                              cudaStream_t stream);
 
+// ---- api.cu ----
+// Device address of the status word on the current device (nullptr on error).
+int *device_status_ptr();
+
 // ---- permute.cu ----
 size_t permute_scratch_bytes(int64_t R, int E);
 cudaError_t launch_permute(int64_t R, int E, const int32_t *ids, int32_t *offsets, int32_t *sorted_route,
