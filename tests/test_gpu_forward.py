@@ -36,7 +36,10 @@ def check_routes_and_permutation(out, x_cpu, wr_cpu, bias_cpu, k, E):
     gl = out["logits"].double().cpu().numpy()
     ids, w, near, l64 = oracle_routes(x_cpu, wr_cpu, bias_cpu, k, gl)
     dl = float(np.max(np.abs(gl - l64)))
-    assert dl < 2e-5  # FP32 logits vs FP64
+    # The near-tie rule (gap < 1e-4 in either precision) is sound only while
+    # 2 max|dl| < 1e-4: then every other token orders the same in both.
+    assert dl < 5e-5, dl
+    print(f"logit max|dl|={dl:.2e} near-tie tokens={int(near.sum())}/{len(near)}")
     gids = out["topk_ids"].cpu().numpy()
     np.testing.assert_array_equal(gids, ids)
     # w = softmax of the selected logits: |dw| <= 2 max|dl| w (+ FP32 rounding of the softmax)

@@ -71,6 +71,7 @@ static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 // ---------------------------------------------------------------- sizes
 static void route_ws(const moe_dims_t *d, Carver &c) {
   c.take((size_t)d->T * d->E * sizeof(float));  // logits when the caller passes none
+  if (d->dtype == MOE_BF16) c.take(router_tc_scratch_bytes(d->E, d->H));  // split router weight
 }
 
 static void permute_ws(const moe_dims_t *d, Carver &c) {
@@ -84,7 +85,7 @@ struct FfnScratch {
 static FfnScratch ffn_ws(const moe_dims_t *d, Carver &c) {
   FfnScratch s;
   const int64_t R = (int64_t)d->T * d->k;
-  s.tiles = c.take(ffn_simt_scratch_bytes(d->E));
+  s.tiles = c.take(d->dtype == MOE_F32 ? ffn_simt_scratch_bytes(d->E) : ffn_tc_scratch_bytes(d->E));
   s.h_routed = c.take((size_t)R * d->I * esize(d));
   s.h_shared = c.take((size_t)d->T * d->Is * esize(d));
   return s;
@@ -171,7 +172,12 @@ MOE_API int moe_route(const moe_dims_t *d, const void *x, const float *w_router,
   Carver c(ws);
   float *lg = (float *)c.take((size_t)T * d->E * sizeof(float));
   if (logits) lg = logits;
-  cudaError_t e = launch_router_logits_simt(d->dtype, d->T, d->H, d->E, x, w_router, router_bias, lg, s);
+  cudaError_t e;
+  if (d->dtype == MOE_F32)
+    e = launch_router_logits_simt(d->T, d->H, d->E, (const float *)x, w_router, router_bias, lg, s);
+  else
+    e = launch_router_logits_tc(d->T, d->H, d->E, x, w_router, router_bias, lg,
+                                c.take(router_tc_scratch_bytes(d->E, d->H)), device_status_ptr(), s);
   if (e == cudaSuccess)
     e = launch_topk_gate(d->dtype, d->T, d->H, d->E, d->k, lg, x, w_shared_gate, topk_ids, topk_w, shared_sig, s);
   return cuda_status(e);
@@ -216,7 +222,8 @@ MOE_API int moe_grouped_ffn(const moe_dims_t *d, const void *x, const int32_t *e
   a.h_shared = (saved && saved->h_shared) ? saved->h_shared : sc.h_shared;
   a.gu_routed = saved ? saved->gu : nullptr;
   a.gu_shared = saved ? saved->gu_shared : nullptr;
-  return cuda_status(launch_ffn_simt(d->dtype, a, sc.tiles, (cudaStream_t)stream));
+  if (d->dtype == MOE_F32) return cuda_status(launch_ffn_simt(a, sc.tiles, (cudaStream_t)stream));
+  return cuda_status(launch_ffn_tc(a, sc.tiles, device_status_ptr(), (cudaStream_t)stream));
 }
 
 MOE_API int moe_combine(const moe_dims_t *d, const void *y_routed, const void *y_shared, const float *topk_w,

@@ -1,4 +1,5 @@
-// Grouped SwiGLU FFN on CUDA cores (the MOE_F32 path).
+// Grouped SwiGLU FFN on CUDA cores (the MOE_F32 path: FP32 has no tensor-core
+// format that keeps the 1e-4 bar, so FP32 products are summed on CUDA cores).
 //
 // RL-Kernel PR #557, embedded #503 commit message, bullet "Experts":
 // per-route gate_up and down projections through one fixed-configuration
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(256) ffn_down_simt_kernel(FfnArgs a, const int
   }
 }
 
-cudaError_t launch_ffn_simt(int dtype, const FfnArgs &a, void *scratch, cudaStream_t stream) {
+cudaError_t launch_ffn_simt(const FfnArgs &a, void *scratch, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
   int32_t *tile_start = (int32_t *)scratch;
   cudaError_t err = launch_build_tiles(a.E, a.T, SIMT_BM, a.offsets, tile_start, stream);
@@ -184,13 +185,8 @@ cudaError_t launch_ffn_simt(int dtype, const FfnArgs &a, void *scratch, cudaStre
   const unsigned gx = (unsigned)(max_tiles < 65535 ? max_tiles : 65535);
   dim3 g1(gx, (unsigned)ceil_div(a.I > a.Is ? a.I : a.Is, 32));
   dim3 g2(gx, (unsigned)ceil_div(a.H, 64));
-  if (dtype == 0) {
-    ffn_gate_up_simt_kernel<float><<<g1, 256, 0, stream>>>(a, tile_start);
-    ffn_down_simt_kernel<float><<<g2, 256, 0, stream>>>(a, tile_start);
-  } else {
-    ffn_gate_up_simt_kernel<__nv_bfloat16><<<g1, 256, 0, stream>>>(a, tile_start);
-    ffn_down_simt_kernel<__nv_bfloat16><<<g2, 256, 0, stream>>>(a, tile_start);
-  }
+  ffn_gate_up_simt_kernel<float><<<g1, 256, 0, stream>>>(a, tile_start);
+  ffn_down_simt_kernel<float><<<g2, 256, 0, stream>>>(a, tile_start);
   return cudaGetLastError();
 }
 

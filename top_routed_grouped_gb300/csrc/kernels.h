@@ -11,9 +11,9 @@ namespace moe {
 
 // ---- route.cu ----
 // logits[t,e] = sum_h x[t,h] * wr[e,h] (+ bias[e]) with FP32 products summed
-// sequentially over h (the MOE_F32 router).
-cudaError_t launch_router_logits_simt(int dtype, int T, int H, int E, const void *x, const float *wr,
-                                      const float *bias, float *logits, cudaStream_t stream);
+// sequentially over h (the MOE_F32 router; x is float).
+cudaError_t launch_router_logits_simt(int T, int H, int E, const float *x, const float *wr, const float *bias,
+                                      float *logits, cudaStream_t stream);
 // Top-k, route weights and shared gate, one warp per token.
 cudaError_t launch_topk_gate(int dtype, int T, int H, int E, int k, const float *logits, const void *x,
                              const void *w_shared_gate, int32_t *ids, float *w, float *sig,
@@ -44,7 +44,17 @@ struct FfnArgs {
   void *gu_routed, *gu_shared;  // saved pre-activations (nullable)
 };
 size_t ffn_simt_scratch_bytes(int E);
-cudaError_t launch_ffn_simt(int dtype, const FfnArgs &a, void *scratch, cudaStream_t stream);
+// The MOE_F32 grouped FFN on CUDA cores (all buffers float).
+cudaError_t launch_ffn_simt(const FfnArgs &a, void *scratch, cudaStream_t stream);
+
+// ---- gemm_tc.cu (bf16 tensor-core path) ----
+size_t router_tc_scratch_bytes(int E, int H);
+// Router logits via the exact three-way bf16 split of w_router (scratch: router_tc_scratch_bytes).
+cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const float *wr, const float *bias,
+                                    float *logits, void *scratch, int *status, cudaStream_t stream);
+size_t ffn_tc_scratch_bytes(int E);
+// gate_up + SwiGLU and down as two persistent tcgen05 grouped GEMMs (scratch: ffn_tc_scratch_bytes).
+cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStream_t stream);
 
 // ---- combine.cu ----
 cudaError_t launch_combine(int dtype, int T, int H, int k, const void *y_routed, const void *y_shared,

@@ -68,15 +68,11 @@ router_logits_simt_kernel(int T, int H, int E, const TX *__restrict__ x, const f
     }
 }
 
-cudaError_t launch_router_logits_simt(int dtype, int T, int H, int E, const void *x, const float *wr,
-                                      const float *bias, float *logits, cudaStream_t stream) {
+cudaError_t launch_router_logits_simt(int T, int H, int E, const float *x, const float *wr, const float *bias,
+                                      float *logits, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   dim3 grid((unsigned)ceil_div(T, 64), (unsigned)ceil_div(E, 64));
-  if (dtype == 0)
-    router_logits_simt_kernel<float><<<grid, 256, 0, stream>>>(T, H, E, (const float *)x, wr, bias, logits);
-  else
-    router_logits_simt_kernel<__nv_bfloat16>
-        <<<grid, 256, 0, stream>>>(T, H, E, (const __nv_bfloat16 *)x, wr, bias, logits);
+  router_logits_simt_kernel<float><<<grid, 256, 0, stream>>>(T, H, E, x, wr, bias, logits);
   return cudaGetLastError();
 }
 
