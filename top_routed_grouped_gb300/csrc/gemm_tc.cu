@@ -10,23 +10,29 @@
 // One persistent kernel skeleton, three uses (MODE):
 //   ROUTER   D[e, t] = sum_k Wr3[e, k] x[t, k mod H], k < 3H, where Wr3 holds
 //            the exact three-way bf16 split of the FP32 router weight
-//            (Wr = W1 + W2 + W3, every product exact); epilogue adds the bias
-//            and writes logits[t, e] in FP32.
-//   GATE_UP  D[f, j] = W_gu[e][f] . x[tok(j)] for the 64 gate and 64 up rows
-//            of a feature tile and up to 256 rows j of expert e's segment
-//            (x rows gathered by TMA gather4); epilogue h = silu(g) * u.
+//            (Wr = W1 + W2 + W3, every product exact).  The K range is cut
+//            into four fixed chunks accumulated in separate TMEM columns and
+//            summed in FP32 in chunk order (four times fewer accumulation
+//            steps per accumulator); epilogue adds the bias, writes logits.
+//   GATE_UP  D[f, j] = W_gu[e][f] . x[tok(j)] for 64 gate and 64 up rows of a
+//            feature tile and up to 256 rows j of expert e's segment; the x
+//            rows are gathered by two warps with 16-byte cp.async into the
+//            swizzled operand layout; epilogue h = silu(g) * u.
 //   DOWN     D[o, j] = W_dn[e][o] . h[j] for 128 output features; epilogue
 //            writes row j to y_routed[sorted_route[j]] (or y_shared).
 // The weights are the M = 128 operand and the tokens the N <= 256 operand,
 // so a short expert segment costs at most 15 padded columns.  Every output
-// element is one FP32 accumulation over K in a fixed order (K blocks of 64,
-// four K = 16 MMAs each); tiling decides only where a column sits, never the
-// order, so a token's values do not depend on T or on its segment.
+// element is accumulated over K in a fixed order (K blocks of 64, four
+// K = 16 MMAs each, fixed chunking); tiling decides only where a column
+// sits, never the order, so a token's values do not depend on T or on its
+// segment.
 //
-// Roles (192 threads): warp 0 issues TMA loads into a 4-stage ring; warp 1
-// allocates 512 TMEM columns (two 256-column accumulators) and one thread
-// issues the MMAs; warps 2-5 drain an accumulator (each warp its 32-lane
-// quarter of TMEM) while the next item accumulates in the other buffer.
+// Roles: warp 0 issues TMA loads (one instruction for a 128 x 64 weight tile,
+// at most a few power-of-two row boxes for a contiguous token tile) into a
+// 4-stage ring; warp 1 allocates 512 TMEM columns and one thread issues the
+// MMAs; warps 2-5 drain an accumulator (each warp its 32-lane quarter of
+// TMEM), staging rows in shared memory so global stores are 16-byte vectors;
+// GATE_UP adds warps 6-7 for the row gather.
 #include <cuda.h>
 
 #include <algorithm>
@@ -41,14 +47,34 @@ namespace moe {
 using namespace umma;
 
 constexpr int TC_STAGES = 4;
-constexpr int TC_NMAX = 256;
-constexpr int TC_A_BYTES = 128 * 128;      // 128 rows x 64 bf16
-constexpr int TC_B_BYTES = TC_NMAX * 128;  // 256 rows x 64 bf16
-constexpr int TC_THREADS = 192;
-constexpr int TC_SMEM_BYTES = 1024 + TC_STAGES * (TC_A_BYTES + TC_B_BYTES) + 256;
+constexpr int TC_A_BYTES = 128 * 128;    // 128 rows x 64 bf16
+constexpr int TC_B_BYTES = 256 * 128;    // up to 256 rows x 64 bf16
+constexpr int TC_EPI_WARPS = 8;          // two warps per TMEM lane quarter, splitting the columns
+constexpr int TC_EPI_FIRST = 2;          // epilogue warps 2..9
+constexpr int TC_GATHER_WARPS = 8;       // GATE_UP row gather, warps 10..17
+constexpr int TC_GATHER_FIRST = TC_EPI_FIRST + TC_EPI_WARPS;
+constexpr int TC_EPI_WARP_BYTES = 4096;  // per epilogue warp staging
+constexpr int TC_TOK_INTS = 256;         // gathered-row token ids (8 warps x 32)
+constexpr int TC_SMEM_BYTES =
+    1024 + TC_STAGES * (TC_A_BYTES + TC_B_BYTES) + TC_EPI_WARPS * TC_EPI_WARP_BYTES + TC_TOK_INTS * 4 + 256;
 constexpr uint32_t TC_TMEM_COLS = 512;
+constexpr int GATHER_THREADS = 32 * TC_GATHER_WARPS;
+constexpr int ROUTER_CHUNKS = 4;
 
 enum { TC_ROUTER = 0, TC_GATE_UP = 1, TC_DOWN = 2 };
+
+template <int MODE>
+struct TcCfg {
+  static constexpr int NMAX = MODE == TC_ROUTER ? 128 : 256;  // router: 4 chunk accumulators of 128 columns
+  static constexpr int THREADS = 32 * (TC_GATHER_FIRST + (MODE == TC_GATE_UP ? TC_GATHER_WARPS : 0));
+};
+
+// Tensor maps.  b[h] / b_sh[h] are the token-tile maps with box height 256 >> h.
+struct TcMaps {
+  CUtensorMap a, a_sh;
+  CUtensorMap b[5];
+  CUtensorMap b_sh[5];
+};
 
 struct TcParams {
   int T, H, E, k, I, Is;
@@ -56,6 +82,7 @@ struct TcParams {
   const int32_t *offsets;
   const int32_t *sorted_route;
   const int32_t *item_start;
+  const __nv_bfloat16 *x;
   const float *bias;
   float *logits;
   __nv_bfloat16 *h_routed, *h_shared;
@@ -73,13 +100,14 @@ struct Item {
   int nk;        // K blocks of 64
 };
 
-// Rows of a segment are cut into ceil(n/256) tiles of equal size rounded up
-// to 16; the cut depends only on the segment's own length.
+// Rows of a segment are cut into ceil(n / NMAX) tiles of equal size rounded
+// up to 16; the cut depends only on the segment's own length.
 template <int MODE>
 __device__ inline Item decode_item(int it, const TcParams &p) {
+  constexpr int NMAX = TcCfg<MODE>::NMAX;
   Item r;
   if (MODE == TC_ROUTER) {
-    const int ntile = (int)ceil_div(p.T, TC_NMAX);
+    const int ntile = (int)ceil_div(p.T, NMAX);
     const int rpt = (int)round_up(ceil_div(p.T, ntile), 16);
     const int nt = it % ntile;
     r.seg = 0;
@@ -98,7 +126,7 @@ __device__ inline Item decode_item(int it, const TcParams &p) {
     const int local = it - __ldg(p.item_start + lo);
     const int64_t base = sh ? 0 : __ldg(p.offsets + lo);
     const int n_s = sh ? p.T : __ldg(p.offsets + lo + 1) - (int)base;
-    const int ntile = (int)ceil_div(n_s, TC_NMAX);
+    const int ntile = (int)ceil_div(n_s, NMAX);
     const int rpt = (int)round_up(ceil_div(n_s, ntile), 16);
     const int nt = local % ntile;
     r.seg = lo;
@@ -119,15 +147,16 @@ __device__ inline bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *a
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(TC_THREADS, 1)
-tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a_sh,
-               const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b_sh,
-               const TcParams p) {
+__global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
+tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+  constexpr int NMAX = TcCfg<MODE>::NMAX;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sa = base;
-  uint8_t *sb = base + TC_STAGES * TC_A_BYTES;
-  uint64_t *bars = (uint64_t *)(sb + TC_STAGES * TC_B_BYTES);
+  uint8_t *sb = sa + TC_STAGES * TC_A_BYTES;
+  uint8_t *epi = sb + TC_STAGES * TC_B_BYTES;
+  int32_t *tok_all = (int32_t *)(epi + TC_EPI_WARPS * TC_EPI_WARP_BYTES);
+  uint64_t *bars = (uint64_t *)(tok_all + TC_TOK_INTS);
   uint64_t *full = bars, *empty = bars + TC_STAGES;
   uint64_t *tfull = bars + 2 * TC_STAGES, *tempty = tfull + 2, *mma_done = tempty + 2;
   uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
@@ -136,24 +165,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < TC_STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 1 + (MODE == TC_GATE_UP ? GATHER_THREADS : 0));
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], 32 * TC_EPI_WARPS);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&map_a);
-    prefetch_tmap(&map_b);
-    if (MODE != TC_ROUTER) {
-      prefetch_tmap(&map_a_sh);
-      if (MODE == TC_DOWN) prefetch_tmap(&map_b_sh);
-    }
+    prefetch_tmap(&maps.a);
+    if (MODE != TC_ROUTER) prefetch_tmap(&maps.a_sh);
   }
   if (warp == 1) tmem_alloc(tmem_slot, TC_TMEM_COLS);
   tc_fence_before();
@@ -163,101 +188,97 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   const int total = MODE == TC_ROUTER ? p.n_items : __ldg(p.item_start + p.E + 1);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    int stage = 0;
-    uint32_t phase = 0;
-    int issued[TC_STAGES];
-    uint32_t issued_phase[TC_STAGES];
-#pragma unroll
-    for (int s = 0; s < TC_STAGES; ++s) issued[s] = 0, issued_phase[s] = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-      const Item im = decode_item<MODE>(it, p);
-      const bool sh = MODE != TC_ROUTER && im.seg == p.E;
-      int gidx[2][4];
-      if (MODE == TC_GATE_UP) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            int r = (lane + 32 * q) * 4 + j;
-            r = r < im.rows ? r : im.rows - 1;  // pad columns repeat the last row
-            const int64_t row = im.row0 + r;
-            gidx[q][j] = sh ? (int)row : __ldg(p.sorted_route + row) / p.k;
-          }
-      }
-      const int b_boxes = (int)ceil_div(im.n, 32);
-      const uint32_t bytes = TC_A_BYTES + (MODE == TC_GATE_UP ? im.n * 128 : b_boxes * 32 * 128);
-      for (int kb = 0; kb < im.nk; ++kb) {
-        if (!warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
-        uint8_t *a_dst = sa + stage * TC_A_BYTES;
-        uint8_t *b_dst = sb + stage * TC_B_BYTES;
-        if (lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      // Weights stream through L2 once; activations are read by several CTAs.
+      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_phase = 0;  // per-stage bits, for draining after an abort
+      bool ok = true;
+      for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        const Item im = decode_item<MODE>(it, p);
+        const bool sh = MODE != TC_ROUTER && im.seg == p.E;
+        const uint32_t bytes = TC_A_BYTES + (MODE == TC_GATE_UP ? 0 : im.n * 128);
+        for (int kb = 0; kb < im.nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], bytes);
+          uint8_t *a_dst = sa + stage * TC_A_BYTES;
+          uint8_t *b_dst = sb + stage * TC_B_BYTES;
           if (MODE == TC_ROUTER) {
-            tma_load_2d(a_dst, &map_a, &full[stage], kb * 64, im.f * 128);
+            tma_load_2d(a_dst, &maps.a, &full[stage], kb * 64, im.f * 128, pol_x);
           } else if (MODE == TC_GATE_UP) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-              tma_load_3d(a_dst + b * 4096, sh ? &map_a_sh : &map_a, &full[stage], kb * 64, im.f * 64 + 16 * b,
-                          sh ? 0 : 2 * im.seg);
+            // One 5-D box: for each of 4 groups of 16 features, 16 gate rows then 16 up rows.
+            tma_load_5d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64, 0, 0, im.f * 4, sh ? 0 : im.seg,
+                        pol_w);
           } else {
-            tma_load_2d(a_dst, sh ? &map_a_sh : &map_a, &full[stage], kb * 64,
-                        sh ? im.f * 128 : im.seg * p.H + im.f * 128);
+            tma_load_2d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64,
+                        sh ? im.f * 128 : im.seg * p.H + im.f * 128, pol_w);
           }
-        }
-        __syncwarp();
-        if (MODE == TC_GATE_UP) {
-          const int n_ops = im.n / 4;
+          if (MODE != TC_GATE_UP) {
+            // Token rows [row0, row0 + n) as power-of-two boxes (n is a multiple of 16).
+            const int kx = MODE == TC_ROUTER ? (kb % (p.H / 64)) * 64 : kb * 64;
+            const CUtensorMap *bm = (MODE == TC_DOWN && sh) ? maps.b_sh : maps.b;
+            int r = 0;
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int g = lane + 32 * q;
-            if (g < n_ops)
-              tma_gather4(b_dst + g * 512, &map_b, &full[stage], kb * 64, gidx[q][0], gidx[q][1], gidx[q][2],
-                          gidx[q][3]);
+            for (int h = 0; h < 5; ++h) {
+              const int box = 256 >> h;
+              if (box > NMAX) continue;
+              while (im.n - r >= box) {
+                tma_load_2d(b_dst + r * 128, &bm[h], &full[stage], kx, (int)(im.row0 + r), pol_x);
+                r += box;
+              }
+            }
           }
-        } else if (lane < b_boxes) {
-          const int kx = MODE == TC_ROUTER ? (kb % (p.H / 64)) * 64 : kb * 64;
-          tma_load_2d(b_dst + lane * 4096, (MODE == TC_DOWN && sh) ? &map_b_sh : &map_b, &full[stage], kx,
-                      (int)(im.row0 + 32 * lane));
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == TC_STAGES) stage = 0, phase ^= 1;
         }
-        issued[stage] = 1;
-        issued_phase[stage] = phase;
-        if (++stage == TC_STAGES) stage = 0, phase ^= 1;
+      }
+      if (!ok) {
+        // Let the copies already in flight land before the CTA exits.
+        volatile int never = 0;
+        for (int s = 0; s < TC_STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1, &never, nullptr, 100000000ull);
       }
     }
-    if (!ok && lane == 0) {
-      // Let the copies already in flight land before the CTA exits.
-      volatile int never = 0;
-      for (int s = 0; s < TC_STAGES; ++s)
-        if (issued[s]) mbar_wait(&full[s], issued_phase[s], &never, nullptr, 100000000ull);
-    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
+      const int nkh = p.H / 64;
       for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
         const Item im = decode_item<MODE>(it, p);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t d = tmem + acc * TC_NMAX;
         const uint32_t idesc = idesc_bf16_f32(128, im.n);
+        uint32_t started = 0;  // ROUTER: chunk accumulators already written
         for (int kb = 0; kb < im.nk; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
+          uint32_t d = tmem + acc * 256;
+          uint32_t accumulate = kb != 0;
+          if (MODE == TC_ROUTER) {
+            const int c = (kb % nkh) * ROUTER_CHUNKS / nkh;  // fixed chunk of this K block
+            d = tmem + c * NMAX;
+            accumulate = (started >> c) & 1u;
+            started |= 1u << c;
+          }
           const uint64_t ad = smem_desc_sw128(smem_u32(sa + stage * TC_A_BYTES));
           const uint64_t bd = smem_desc_sw128(smem_u32(sb + stage * TC_B_BYTES));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA: +32 bytes = +2 in the descriptor address field
-            mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+            mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (accumulate | kk) != 0);
           mma_commit(&empty[stage]);
           if (++stage == TC_STAGES) stage = 0, phase ^= 1;
         }
         if (!ok) break;
         mma_commit(&tfull[acc]);
-        if (++acc == 2) acc = 0, acc_phase ^= 1;
+        if (MODE == TC_ROUTER) acc_phase ^= 1;  // one accumulator set (all 512 columns)
+        else if (++acc == 2) acc = 0, acc_phase ^= 1;
       }
       // Every MMA this thread issued has finished before TMEM is released.
       mma_commit(mma_done);
@@ -265,75 +286,156 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       mbar_wait(mma_done, 0, &never, p.status);
     }
     __syncwarp();
-  } else {
+  } else if (warp < TC_GATHER_FIRST) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;                       // TMEM lane quarter this warp may access
+    const int half = (warp - TC_EPI_FIRST) >> 2;  // the two warps of a quarter take alternate 32-column chunks
+    uint8_t *stg = epi + (warp - TC_EPI_FIRST) * TC_EPI_WARP_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int it = blockIdx.x; it < total; it += gridDim.x) {
       const Item im = decode_item<MODE>(it, p);
       if (!warp_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t tb = tmem + acc * TC_NMAX + ((uint32_t)(q * 32) << 16);
+      const uint32_t tb = tmem + acc * 256 + ((uint32_t)(q * 32) << 16);
       if (MODE == TC_ROUTER) {
         const int e = im.f * 128 + q * 32 + lane;
         const float b = (p.bias && e < p.E) ? __ldg(p.bias + e) : 0.f;
-        for (int c0 = 0; c0 < im.n; c0 += 32) {
-          float v[32];
+        for (int c0 = 32 * half; c0 < im.n; c0 += 64) {
+          float v[32], w[32];
           tmem_ld32(tb + c0, v);
+#pragma unroll
+          for (int c = 1; c < ROUTER_CHUNKS; ++c) {  // ((c0 + c1) + c2) + c3
+            tmem_ld32(tb + c * NMAX + c0, w);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += w[j];
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int c = c0 + j;
-            if (c < im.rows && e < p.E) {
-              float val = v[j];
-              if (p.bias) val += b;
-              p.logits[(im.row0 + c) * p.E + e] = val;
-            }
+            if (c < im.rows && e < p.E) p.logits[(im.row0 + c) * p.E + e] = p.bias ? v[j] + b : v[j];
           }
         }
       } else if (MODE == TC_GATE_UP) {
         const bool sh = im.seg == p.E;
         const int Iseg = sh ? p.Is : p.I;
-        const int f = im.f * 64 + 16 * q + (lane & 15);
+        const int fcol = im.f * 64 + 16 * q;  // first feature of this warp's 16
         __nv_bfloat16 *hout = sh ? p.h_shared : p.h_routed;
         __nv_bfloat16 *guout = sh ? p.gu_shared : p.gu_routed;
-        for (int c0 = 0; c0 < im.n; c0 += 32) {
+        __nv_bfloat16 *stg_h = (__nv_bfloat16 *)stg;               // [32 cols][24] (16 used)
+        __nv_bfloat16 *stg_gu = (__nv_bfloat16 *)(stg + 32 * 48);  // [32 cols][40] (32 used)
+        for (int c0 = 32 * half; c0 < im.n; c0 += 64) {
           float v[32];
           tmem_ld32(tb + c0, v);
+          // Lane i < 16 holds gate g of feature i, lane i + 16 the up value u of
+          // the same feature, for columns c0..c0+31.  One exchange gives lane i
+          // the u of columns 0-15 and lane i + 16 the g of columns 16-31, so
+          // both halves compute h for 16 columns each.
+          const int fl = lane & 15;
+          const int cbase = lane < 16 ? 0 : 16;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            // lanes 0-15 hold gate values, lanes 16-31 the up values of the same features
-            const float other = __shfl_xor_sync(FULL_MASK, v[j], 16);
-            const int c = c0 + j;
-            if (c < im.rows) {
-              const int64_t row = im.row0 + c;
-              if (lane < 16) hout[row * Iseg + f] = __float2bfloat16_rn(silu_f32(v[j]) * other);
-              if (guout) guout[row * 2 * Iseg + (lane < 16 ? 0 : Iseg) + f] = __float2bfloat16_rn(v[j]);
+          for (int j = 0; j < 16; ++j) {
+            const float send = lane < 16 ? v[16 + j] : v[j];
+            const float recv = __shfl_xor_sync(FULL_MASK, send, 16);
+            const float g = lane < 16 ? v[j] : recv;
+            const float u = lane < 16 ? recv : v[16 + j];
+            stg_h[(cbase + j) * 24 + fl] = __float2bfloat16_rn(silu_f32(g) * u);
+          }
+          if (guout) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stg_gu[j * 40 + lane] = __float2bfloat16_rn(v[j]);
+          }
+          __syncwarp();
+          if (c0 + lane < im.rows) {
+            const int64_t row = im.row0 + c0 + lane;
+            const uint4 *s = (const uint4 *)(stg_h + lane * 24);
+            uint4 *d = (uint4 *)(hout + row * Iseg + fcol);
+            d[0] = s[0];
+            d[1] = s[1];
+            if (guout) {
+              const uint4 *sg = (const uint4 *)(stg_gu + lane * 40);
+              uint4 *dg = (uint4 *)(guout + row * 2 * Iseg + fcol);
+              uint4 *du = (uint4 *)(guout + row * 2 * Iseg + Iseg + fcol);
+              dg[0] = sg[0];
+              dg[1] = sg[1];
+              du[0] = sg[2];
+              du[1] = sg[3];
             }
           }
+          __syncwarp();
         }
       } else {
         const bool sh = im.seg == p.E;
-        const int o = im.f * 128 + q * 32 + lane;
-        for (int c0 = 0; c0 < im.n; c0 += 32) {
+        const int ocol = im.f * 128 + q * 32;  // first output feature of this warp's 32
+        __nv_bfloat16 *stg_y = (__nv_bfloat16 *)stg;  // [32 cols][40] (32 used)
+        __nv_bfloat16 *yout = sh ? p.y_shared : p.y_routed;
+        for (int c0 = 32 * half; c0 < im.n; c0 += 64) {
           float v[32];
           tmem_ld32(tb + c0, v);
-          int my_dst = 0;
-          if (c0 + lane < im.rows) my_dst = sh ? (int)(im.row0 + c0 + lane) : __ldg(p.sorted_route + im.row0 + c0 + lane);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int dst = __shfl_sync(FULL_MASK, my_dst, j);
-            if (c0 + j < im.rows) {
-              __nv_bfloat16 *yrow = (sh ? p.y_shared : p.y_routed) + (int64_t)dst * p.H;
-              yrow[o] = __float2bfloat16_rn(v[j]);
-            }
+          for (int j = 0; j < 32; ++j) stg_y[j * 40 + lane] = __float2bfloat16_rn(v[j]);
+          __syncwarp();
+          if (c0 + lane < im.rows) {
+            const int64_t dst = sh ? im.row0 + c0 + lane : (int64_t)__ldg(p.sorted_route + im.row0 + c0 + lane);
+            const uint4 *s = (const uint4 *)(stg_y + lane * 40);
+            uint4 *d = (uint4 *)(yout + dst * p.H + ocol);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[i] = s[i];
           }
+          __syncwarp();
         }
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
-      if (++acc == 2) acc = 0, acc_phase ^= 1;
+      if (MODE == TC_ROUTER) acc_phase ^= 1;
+      else if (++acc == 2) acc = 0, acc_phase ^= 1;
     }
+  } else if (MODE == TC_GATE_UP) {
+    // ------------------------------------------------------------ row gather (warps 10..17)
+    // Warp g copies the rows r = 8 i + g; lane = 8 * (i mod 4) + 16-byte chunk
+    // qc, written at the 128-byte swizzled position (qc ^ g) of row r.  Each
+    // thread arrives on a stage's `full` barrier once its copies into that
+    // stage are complete and fenced for the tensor cores (pad rows past the
+    // segment are left as they are: their accumulator columns are never read).
+    const int g = warp - TC_GATHER_FIRST;
+    const int sub = lane >> 3, qc = lane & 7;
+    int32_t *tok = tok_all + g * 32;
+    int stage = 0, arr_stage = 0, pending = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+      const Item im = decode_item<MODE>(it, p);
+      const bool sh = im.seg == p.E;
+      const int ni = (im.rows - g + 7) / 8;  // rows of this warp: i < ni  (<= 32)
+      __syncwarp();
+      if (lane < ni) {
+        const int64_t row = im.row0 + 8 * lane + g;
+        tok[lane] = sh ? (int)row : __ldg(p.sorted_route + row) / p.k;
+      }
+      __syncwarp();
+      for (int kb = 0; kb < im.nk; ++kb) {
+        if (!warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+        const uint32_t bsm = smem_u32(sb + stage * TC_B_BYTES) + g * 128 + ((qc ^ g) << 4);
+        const __nv_bfloat16 *src = p.x + kb * 64 + qc * 8;
+        for (int i = sub; i < ni; i += 4) cp_async_16(bsm + i * 1024, src + (int64_t)tok[i] * p.H);
+        cp_async_commit();
+        if (++pending > 2) {
+          cp_async_wait<2>();
+          fence_proxy_async_smem();
+          mbar_arrive(&full[arr_stage]);
+          if (++arr_stage == TC_STAGES) arr_stage = 0;
+          --pending;
+        }
+        if (++stage == TC_STAGES) stage = 0, phase ^= 1;
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    if (ok)
+      for (; pending > 0; --pending) {
+        mbar_arrive(&full[arr_stage]);
+        if (++arr_stage == TC_STAGES) arr_stage = 0;
+      }
   }
   tc_fence_before();
   __syncthreads();
@@ -376,8 +478,8 @@ build_items_kernel(int E, int T, int nf_routed, int nf_shared, const int32_t *__
   for (int base = 0; base <= E; base += 1024) {
     const int s = base + threadIdx.x;
     int32_t v = 0;
-    if (s < E) v = (int32_t)ceil_div(offsets[s + 1] - offsets[s], TC_NMAX) * nf_routed;
-    else if (s == E) v = (int32_t)ceil_div(T, TC_NMAX) * nf_shared;
+    if (s < E) v = (int32_t)ceil_div(offsets[s + 1] - offsets[s], 256) * nf_routed;
+    else if (s == E) v = (int32_t)ceil_div(T, 256) * nf_shared;
     buf[threadIdx.x] = v;
     __syncthreads();
     for (int d = 1; d < 1024; d <<= 1) {
@@ -439,13 +541,22 @@ static bool map_2d(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, 
   return encode_map(m, ptr, 2, dims, strides, box);
 }
 
-// Gate/up weights [n_mat, 2*Iw, H] viewed as (H, Iw, 2*n_mat): box (64, 16, 2)
-// = 16 gate rows followed by the 16 up rows of the same features.
+// The five token-tile maps of a row-major [rows, cols] matrix (box heights 256 .. 16).
+static bool map_rows(CUtensorMap *m5, const void *ptr, int64_t rows, int64_t cols) {
+  for (int h = 0; h < 5; ++h)
+    if (!map_2d(&m5[h], ptr, rows, cols, 256u >> h)) return false;
+  return true;
+}
+
+// Gate/up weights [n_mat, 2*Iw, H] viewed as 5-D (H, 16, 2, Iw/16, n_mat):
+// a box (64, 16, 2, 4, 1) holds, for 4 consecutive groups of 16 features,
+// the 16 gate rows followed by the 16 up rows of the same features.
 static bool map_gate_up(CUtensorMap *m, const void *ptr, int n_mat, int Iw, int H) {
-  const uint64_t dims[3] = {(uint64_t)H, (uint64_t)Iw, (uint64_t)2 * n_mat};
-  const uint64_t strides[2] = {(uint64_t)H * 2, (uint64_t)Iw * H * 2};
-  const uint32_t box[3] = {64, 16, 2};
-  return encode_map(m, ptr, 3, dims, strides, box);
+  const uint64_t dims[5] = {(uint64_t)H, 16, 2, (uint64_t)Iw / 16, (uint64_t)n_mat};
+  const uint64_t strides[4] = {(uint64_t)H * 2, (uint64_t)Iw * H * 2, (uint64_t)16 * H * 2,
+                               (uint64_t)2 * Iw * H * 2};
+  const uint32_t box[5] = {64, 16, 2, 4, 1};
+  return encode_map(m, ptr, 5, dims, strides, box);
 }
 
 struct DevInfo {
@@ -465,8 +576,7 @@ static DevInfo &dev_info() {
 }
 
 template <int MODE>
-static cudaError_t launch_tc(const CUtensorMap &a, const CUtensorMap &a_sh, const CUtensorMap &b,
-                             const CUtensorMap &b_sh, const TcParams &p, int grid, cudaStream_t stream) {
+static cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream) {
   DevInfo &di = dev_info();
   if (!di.attr[MODE]) {
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -474,7 +584,7 @@ static cudaError_t launch_tc(const CUtensorMap &a, const CUtensorMap &a_sh, cons
     if (e != cudaSuccess) return e;
     di.attr[MODE] = true;
   }
-  tc_gemm_kernel<MODE><<<grid, TC_THREADS, TC_SMEM_BYTES, stream>>>(a, a_sh, b, b_sh, p);
+  tc_gemm_kernel<MODE><<<grid, TcCfg<MODE>::THREADS, TC_SMEM_BYTES, stream>>>(maps, p);
   return cudaGetLastError();
 }
 
@@ -486,16 +596,18 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
   __nv_bfloat16 *wr3 = (__nv_bfloat16 *)scratch;
   const int64_t n = (int64_t)E * H;
   split_router_weight_kernel<<<(unsigned)ceil_div(n, 256), 256, 0, stream>>>(n, H, wr, wr3);
-  CUtensorMap ma, mb;
-  if (!map_2d(&ma, wr3, E, 3 * (int64_t)H, 128) || !map_2d(&mb, x, T, H, 32)) return cudaErrorInvalidValue;
+  TcMaps m;
+  if (!map_2d(&m.a, wr3, E, 3 * (int64_t)H, 128) || !map_rows(m.b, x, T, H)) return cudaErrorInvalidValue;
+  m.a_sh = m.a;
+  for (int h = 0; h < 5; ++h) m.b_sh[h] = m.b[h];
   TcParams p = {};
   p.T = T; p.H = H; p.E = E;
-  p.n_items = (int)(ceil_div(E, 128) * ceil_div(T, TC_NMAX));
+  p.n_items = (int)(ceil_div(E, 128) * ceil_div(T, TcCfg<TC_ROUTER>::NMAX));
   p.bias = bias;
   p.logits = logits;
   p.status = status;
   const int grid = std::min(p.n_items, dev_info().sms);
-  return launch_tc<TC_ROUTER>(ma, ma, mb, mb, p, grid, stream);
+  return launch_tc<TC_ROUTER>(m, p, grid, stream);
 }
 
 size_t ffn_tc_scratch_bytes(int E) { return (size_t)2 * 256 * (((E + 2) * 4 + 255) / 256); }
@@ -507,16 +619,17 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   build_items_kernel<<<1, 1024, 0, stream>>>(a.E, a.T, a.I / 64, a.Is / 64, a.offsets, items_gu);
   build_items_kernel<<<1, 1024, 0, stream>>>(a.E, a.T, a.H / 128, a.H / 128, a.offsets, items_dn);
   const int64_t R = (int64_t)a.T * a.k;
-  CUtensorMap a_gu, a_gu_sh, b_x, a_dn, a_dn_sh, b_h, b_h_sh;
-  if (!map_gate_up(&a_gu, a.w_gate_up, a.E, a.I, a.H) || !map_gate_up(&a_gu_sh, a.ws_gate_up, 1, a.Is, a.H) ||
-      !map_2d(&b_x, a.x, a.T, a.H, 1) || !map_2d(&a_dn, a.w_down, (int64_t)a.E * a.H, a.I, 128) ||
-      !map_2d(&a_dn_sh, a.ws_down, a.H, a.Is, 128) || !map_2d(&b_h, a.h_routed, R, a.I, 32) ||
-      !map_2d(&b_h_sh, a.h_shared, a.T, a.Is, 32))
+  TcMaps mg, md;
+  if (!map_gate_up(&mg.a, a.w_gate_up, a.E, a.I, a.H) || !map_gate_up(&mg.a_sh, a.ws_gate_up, 1, a.Is, a.H) ||
+      !map_2d(&md.a, a.w_down, (int64_t)a.E * a.H, a.I, 128) || !map_2d(&md.a_sh, a.ws_down, a.H, a.Is, 128) ||
+      !map_rows(md.b, a.h_routed, R, a.I) || !map_rows(md.b_sh, a.h_shared, a.T, a.Is))
     return cudaErrorInvalidValue;
+  for (int h = 0; h < 5; ++h) mg.b[h] = mg.b_sh[h] = mg.a;  // gate_up gathers its token rows with cp.async
   TcParams p = {};
   p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k; p.I = a.I; p.Is = a.Is;
   p.offsets = a.offsets;
   p.sorted_route = a.sorted_route;
+  p.x = (const __nv_bfloat16 *)a.x;
   p.h_routed = (__nv_bfloat16 *)a.h_routed;
   p.h_shared = (__nv_bfloat16 *)a.h_shared;
   p.gu_routed = (__nv_bfloat16 *)a.gu_routed;
@@ -526,10 +639,10 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   p.status = status;
   const int grid = dev_info().sms;
   p.item_start = items_gu;
-  cudaError_t e = launch_tc<TC_GATE_UP>(a_gu, a_gu_sh, b_x, b_x, p, grid, stream);
+  cudaError_t e = launch_tc<TC_GATE_UP>(mg, p, grid, stream);
   if (e != cudaSuccess) return e;
   p.item_start = items_dn;
-  return launch_tc<TC_DOWN>(a_dn, a_dn_sh, b_h, b_h_sh, p, grid, stream);
+  return launch_tc<TC_DOWN>(md, p, grid, stream);
 }
 
 }  // namespace moe
