@@ -80,7 +80,7 @@ enum moe_op {
 /*
  * Layer shape.  Limits: T >= 0, T*k < 2^31; 1 <= k <= 16; k <= E <= 1024.
  * MOE_F32: H, I, Is multiples of 4.
- * MOE_BF16: H a multiple of 128, I and Is multiples of 64.
+ * MOE_BF16: H a multiple of 256, I and Is multiples of 128.
  * Other shapes return MOE_ERR_UNSUPPORTED.
  */
 typedef struct moe_dims {

@@ -71,7 +71,8 @@ def call_route(d, ptr=16, ws_bytes=1 << 40):
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(k=0), -1), (dict(k=17, E=32), -1), (dict(k=5, E=4), -1), (dict(T=-1), -1), (dict(dtype=7), -1),
-    (dict(H=0), -1), (dict(E=2048), -2), (dict(H=2000), -2), (dict(I=100), -2),
+    (dict(H=0), -1), (dict(E=2048), -2), (dict(H=2000), -2), (dict(H=1920), -2), (dict(I=100), -2),
+    (dict(I=192), -2), (dict(Is=64), -2),
     (dict(dtype=moe.MOE_F32, H=130), -2), (dict(T=300_000_000), -2),
 ])
 def test_route_rejects_bad_dims(L, kw, expect):

@@ -42,7 +42,7 @@ def test_noalloc_permute_matches_workspace_permute_twice():
     # First call large, second smaller: the second must not see the first's scratch.
     for T, E, k, seed in [(6000, 512, 10, 1), (333, 64, 8, 2)]:
         ids = random_ids(T, E, k, seed)
-        d = moe.make_dims(T, 128, E, k, 64, 64, moe.MOE_BF16)
+        d = moe.make_dims(T, 256, E, k, 128, 128, moe.MOE_BF16)
         off, srt, pos = outputs(T, E, k)
         rc = L.moe_permute_noalloc(ctypes.byref(d), ctypes.c_void_p(ids.data_ptr()),
                                    ctypes.c_void_p(off.data_ptr()), ctypes.c_void_p(srt.data_ptr()),
@@ -61,7 +61,7 @@ def test_noalloc_permute_refuses_sizes_beyond_its_scratch():
     T, E, k = 40000, 1024, 16  # needs (1250 * 1024 + 1024) * 4 bytes > 4 MiB
     ids = torch.zeros(T, k, dtype=torch.int32, device="cuda")
     off, srt, pos = outputs(T, E, k)
-    d = moe.make_dims(T, 128, E, k, 64, 64, moe.MOE_BF16)
+    d = moe.make_dims(T, 256, E, k, 128, 128, moe.MOE_BF16)
     with pytest.raises(moe.MoEError) as e:
         moe.moe_permute_noalloc(d, ids, off, srt, pos)
     assert e.value.status == -2

@@ -214,7 +214,7 @@ def route(x, w_router, w_shared_gate, k: int, router_bias=None, E: int | None = 
     import torch
     T, H = x.shape
     E = w_router.shape[0]
-    d = make_dims(T, H, E, k, 64, 64, x.dtype)
+    d = make_dims(T, H, E, k, 128, 128, x.dtype)  # I, Is unused by routing
     dev = x.device
     out = {"topk_ids": torch.empty(T, k, dtype=torch.int32, device=dev),
            "topk_w": torch.empty(T, k, dtype=torch.float32, device=dev),
@@ -229,7 +229,7 @@ def permute(topk_ids, E: int, stream=None):
     """Returns dict(expert_offsets [E+1], sorted_route [T*k], route_pos [T*k]), all int32."""
     import torch
     T, k = topk_ids.shape
-    d = make_dims(T, 128, E, k, 64, 64, MOE_BF16)
+    d = make_dims(T, 256, E, k, 128, 128, MOE_BF16)  # H, I, Is unused by the permutation
     dev = topk_ids.device
     out = {"expert_offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
            "sorted_route": torch.empty(T * k, dtype=torch.int32, device=dev),

@@ -53,7 +53,7 @@ static int check_dims(const moe_dims_t *d) {
   if (d->dtype == MOE_F32) {
     if (d->H % 4 || d->I % 4 || d->Is % 4) return MOE_ERR_UNSUPPORTED;
   } else {
-    if (d->H % 128 || d->I % 64 || d->Is % 64) return MOE_ERR_UNSUPPORTED;
+    if (d->H % 256 || d->I % 128 || d->Is % 128) return MOE_ERR_UNSUPPORTED;
   }
   return MOE_OK;
 }
@@ -85,7 +85,7 @@ struct FfnScratch {
 static FfnScratch ffn_ws(const moe_dims_t *d, Carver &c) {
   FfnScratch s;
   const int64_t R = (int64_t)d->T * d->k;
-  s.tiles = c.take(d->dtype == MOE_F32 ? ffn_simt_scratch_bytes(d->E) : ffn_tc_scratch_bytes(d->E));
+  s.tiles = c.take(d->dtype == MOE_F32 ? ffn_simt_scratch_bytes(d->E) : ffn_tc_scratch_bytes(d->T, d->k, d->E, d->H, d->I, d->Is));
   s.h_routed = c.take((size_t)R * d->I * esize(d));
   s.h_shared = c.take((size_t)d->T * d->Is * esize(d));
   return s;

@@ -46,28 +46,49 @@ namespace moe {
 
 using namespace umma;
 
-constexpr int TC_STAGES = 4;
-constexpr int TC_A_BYTES = 128 * 128;    // 128 rows x 64 bf16
-constexpr int TC_B_BYTES = 256 * 128;    // up to 256 rows x 64 bf16
-constexpr int TC_EPI_WARPS = 8;          // two warps per TMEM lane quarter, splitting the columns
-constexpr int TC_EPI_FIRST = 2;          // epilogue warps 2..9
-constexpr int TC_GATHER_WARPS = 8;       // GATE_UP row gather, warps 10..17
+// Per-mode configuration.  GATE_UP and DOWN give each item two M tiles (256
+// weight rows) that share one token tile, so every gathered / loaded token
+// row feeds twice the tensor-core work; the two accumulators take the whole
+// 512 TMEM columns (one accumulator set, drained between items).  ROUTER keeps
+// one M tile and uses the 512 columns as four K-chunk accumulators.
+template <int MODE>
+struct TcCfg;
+constexpr int TC_ROUTER = 0, TC_GATE_UP = 1, TC_DOWN = 2;
+template <>
+struct TcCfg<0> {
+  static constexpr int NMAX = 128, MT = 1, STAGES = 4;
+};
+template <>
+struct TcCfg<1> {
+  static constexpr int NMAX = 256, MT = 2, STAGES = 3;
+};
+template <>
+struct TcCfg<2> {
+  static constexpr int NMAX = 256, MT = 2, STAGES = 3;
+};
+
+static_assert(TcCfg<1>::MT == 2 && TcCfg<2>::MT == 2, "the epilogues drain two M tiles per item together");
+
+constexpr int TC_TILE_A_BYTES = 128 * 128;  // one M tile: 128 rows x 64 bf16
+constexpr int TC_B_BYTES = 256 * 128;       // up to 256 token rows x 64 bf16
+constexpr int TC_EPI_WARPS = 8;             // two warps per TMEM lane quarter, splitting the columns
+constexpr int TC_EPI_FIRST = 2;             // epilogue warps 2..9
+constexpr int TC_GATHER_WARPS = 8;          // GATE_UP row gather, warps 10..17
 constexpr int TC_GATHER_FIRST = TC_EPI_FIRST + TC_EPI_WARPS;
-constexpr int TC_EPI_WARP_BYTES = 4096;  // per epilogue warp staging
-constexpr int TC_TOK_INTS = 256;         // gathered-row token ids (8 warps x 32)
-constexpr int TC_SMEM_BYTES =
-    1024 + TC_STAGES * (TC_A_BYTES + TC_B_BYTES) + TC_EPI_WARPS * TC_EPI_WARP_BYTES + TC_TOK_INTS * 4 + 256;
+constexpr int TC_EPI_WARP_BYTES = 4096;     // per epilogue warp staging
+constexpr int TC_TOK_INTS = 256;            // gathered-row token ids (8 warps x 32)
+constexpr int TC_MAX_STAGES = 4;
+constexpr int TC_SMEM_BYTES = 1024 + 4 * (TC_TILE_A_BYTES + TC_B_BYTES) + TC_EPI_WARPS * TC_EPI_WARP_BYTES +
+                              TC_TOK_INTS * 4 + 256;  // the largest of the three layouts (ROUTER)
+static_assert(3 * (2 * TC_TILE_A_BYTES + TC_B_BYTES) <= 4 * (TC_TILE_A_BYTES + TC_B_BYTES), "stage ring");
 constexpr uint32_t TC_TMEM_COLS = 512;
 constexpr int GATHER_THREADS = 32 * TC_GATHER_WARPS;
 constexpr int ROUTER_CHUNKS = 4;
 
-enum { TC_ROUTER = 0, TC_GATE_UP = 1, TC_DOWN = 2 };
-
 template <int MODE>
-struct TcCfg {
-  static constexpr int NMAX = MODE == TC_ROUTER ? 128 : 256;  // router: 4 chunk accumulators of 128 columns
-  static constexpr int THREADS = 32 * (TC_GATHER_FIRST + (MODE == TC_GATE_UP ? TC_GATHER_WARPS : 0));
-};
+constexpr int tc_threads() {
+  return 32 * (TC_GATHER_FIRST + (MODE == TC_GATE_UP ? TC_GATHER_WARPS : 0));
+}
 
 // Tensor maps.  b[h] / b_sh[h] are the token-tile maps with box height 256 >> h.
 struct TcMaps {
@@ -78,10 +99,11 @@ struct TcMaps {
 
 struct TcParams {
   int T, H, E, k, I, Is;
-  int n_items;  // ROUTER: number of items; others read item_start[E+1]
+  int n_items;              // ROUTER: number of items (others: item_start[E+1])
   const int32_t *offsets;
   const int32_t *sorted_route;
-  const int32_t *item_start;
+  const int32_t *item_start;  // [E+2] prefix of items per segment
+  const int4 *items;          // per item: segment, M-tile pair, first row, rows
   const __nv_bfloat16 *x;
   const float *bias;
   float *logits;
@@ -93,20 +115,18 @@ struct TcParams {
 
 struct Item {
   int seg;       // expert segment (E = shared); ROUTER: unused
-  int f;         // M tile: expert tile (ROUTER), feature tile (GATE_UP, DOWN)
+  int f;         // ROUTER: expert tile; GATE_UP / DOWN: pair of M tiles
   int64_t row0;  // first row of the N tile (token for ROUTER / shared, sorted row otherwise)
   int rows;      // valid rows in the tile
   int n;         // MMA N = rows rounded up to 16
   int nk;        // K blocks of 64
 };
 
-// Rows of a segment are cut into ceil(n / NMAX) tiles of equal size rounded
-// up to 16; the cut depends only on the segment's own length.
 template <int MODE>
 __device__ inline Item decode_item(int it, const TcParams &p) {
-  constexpr int NMAX = TcCfg<MODE>::NMAX;
   Item r;
   if (MODE == TC_ROUTER) {
+    constexpr int NMAX = TcCfg<MODE>::NMAX;
     const int ntile = (int)ceil_div(p.T, NMAX);
     const int rpt = (int)round_up(ceil_div(p.T, ntile), 16);
     const int nt = it % ntile;
@@ -116,24 +136,12 @@ __device__ inline Item decode_item(int it, const TcParams &p) {
     r.rows = min(rpt, p.T - nt * rpt);
     r.nk = 3 * p.H / 64;
   } else {
-    int lo = 0, hi = p.E;
-    while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (__ldg(p.item_start + mid) <= it) lo = mid;
-      else hi = mid - 1;
-    }
-    const bool sh = lo == p.E;
-    const int local = it - __ldg(p.item_start + lo);
-    const int64_t base = sh ? 0 : __ldg(p.offsets + lo);
-    const int n_s = sh ? p.T : __ldg(p.offsets + lo + 1) - (int)base;
-    const int ntile = (int)ceil_div(n_s, NMAX);
-    const int rpt = (int)round_up(ceil_div(n_s, ntile), 16);
-    const int nt = local % ntile;
-    r.seg = lo;
-    r.f = local / ntile;
-    r.row0 = base + (int64_t)nt * rpt;
-    r.rows = min(rpt, n_s - nt * rpt);
-    r.nk = (MODE == TC_GATE_UP ? p.H : (sh ? p.Is : p.I)) / 64;
+    const int4 d = __ldg(p.items + it);
+    r.seg = d.x;
+    r.f = d.y;
+    r.row0 = d.z;
+    r.rows = d.w;
+    r.nk = (MODE == TC_GATE_UP ? p.H : (r.seg == p.E ? p.Is : p.I)) / 64;
   }
   r.n = (int)round_up(r.rows, 16);
   return r;
@@ -147,31 +155,30 @@ __device__ inline bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *a
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(TcCfg<MODE>::THREADS, 1)
+__global__ void __launch_bounds__(tc_threads<MODE>(), 1)
 tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
-  constexpr int NMAX = TcCfg<MODE>::NMAX;
+  constexpr int NMAX = TcCfg<MODE>::NMAX, MT = TcCfg<MODE>::MT, STAGES = TcCfg<MODE>::STAGES;
+  constexpr int A_BYTES = MT * TC_TILE_A_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sa = base;
-  uint8_t *sb = sa + TC_STAGES * TC_A_BYTES;
-  uint8_t *epi = sb + TC_STAGES * TC_B_BYTES;
+  uint8_t *sb = sa + STAGES * A_BYTES;
+  uint8_t *epi = sb + STAGES * TC_B_BYTES;
   int32_t *tok_all = (int32_t *)(epi + TC_EPI_WARPS * TC_EPI_WARP_BYTES);
   uint64_t *bars = (uint64_t *)(tok_all + TC_TOK_INTS);
-  uint64_t *full = bars, *empty = bars + TC_STAGES;
-  uint64_t *tfull = bars + 2 * TC_STAGES, *tempty = tfull + 2, *mma_done = tempty + 2;
+  uint64_t *full = bars, *empty = bars + TC_MAX_STAGES;
+  uint64_t *tfull = bars + 2 * TC_MAX_STAGES, *tempty = tfull + 1, *mma_done = tempty + 1;
   uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < TC_STAGES; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1 + (MODE == TC_GATE_UP ? GATHER_THREADS : 0));
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 32 * TC_EPI_WARPS);
-    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 32 * TC_EPI_WARPS);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -199,21 +206,21 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
         const Item im = decode_item<MODE>(it, p);
         const bool sh = MODE != TC_ROUTER && im.seg == p.E;
-        const uint32_t bytes = TC_A_BYTES + (MODE == TC_GATE_UP ? 0 : im.n * 128);
+        const uint32_t bytes = A_BYTES + (MODE == TC_GATE_UP ? 0 : im.n * 128);
         for (int kb = 0; kb < im.nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], bytes);
-          uint8_t *a_dst = sa + stage * TC_A_BYTES;
+          uint8_t *a_dst = sa + stage * A_BYTES;
           uint8_t *b_dst = sb + stage * TC_B_BYTES;
           if (MODE == TC_ROUTER) {
             tma_load_2d(a_dst, &maps.a, &full[stage], kb * 64, im.f * 128, pol_x);
           } else if (MODE == TC_GATE_UP) {
-            // One 5-D box: for each of 4 groups of 16 features, 16 gate rows then 16 up rows.
-            tma_load_5d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64, 0, 0, im.f * 4, sh ? 0 : im.seg,
+            // One 5-D box: for 8 groups of 16 features (two M tiles), 16 gate rows then 16 up rows.
+            tma_load_5d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64, 0, 0, im.f * 8, sh ? 0 : im.seg,
                         pol_w);
           } else {
             tma_load_2d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64,
-                        sh ? im.f * 128 : im.seg * p.H + im.f * 128, pol_w);
+                        sh ? im.f * 256 : im.seg * p.H + im.f * 256, pol_w);
           }
           if (MODE != TC_GATE_UP) {
             // Token rows [row0, row0 + n) as power-of-two boxes (n is a multiple of 16).
@@ -232,13 +239,13 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           }
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == TC_STAGES) stage = 0, phase ^= 1;
+          if (++stage == STAGES) stage = 0, phase ^= 1;
         }
       }
       if (!ok) {
         // Let the copies already in flight land before the CTA exits.
         volatile int never = 0;
-        for (int s = 0; s < TC_STAGES; ++s)
+        for (int s = 0; s < STAGES; ++s)
           if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1, &never, nullptr, 100000000ull);
       }
     }
@@ -246,39 +253,41 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0, acc = 0;
+      int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       const int nkh = p.H / 64;
       for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
         const Item im = decode_item<MODE>(it, p);
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) break;
+        if (!mbar_wait(tempty, acc_phase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32(128, im.n);
         uint32_t started = 0;  // ROUTER: chunk accumulators already written
         for (int kb = 0; kb < im.nk; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          uint32_t d = tmem + acc * 256;
-          uint32_t accumulate = kb != 0;
-          if (MODE == TC_ROUTER) {
-            const int c = (kb % nkh) * ROUTER_CHUNKS / nkh;  // fixed chunk of this K block
-            d = tmem + c * NMAX;
-            accumulate = (started >> c) & 1u;
-            started |= 1u << c;
-          }
-          const uint64_t ad = smem_desc_sw128(smem_u32(sa + stage * TC_A_BYTES));
           const uint64_t bd = smem_desc_sw128(smem_u32(sb + stage * TC_B_BYTES));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA: +32 bytes = +2 in the descriptor address field
-            mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (accumulate | kk) != 0);
+          for (int mt = 0; mt < MT; ++mt) {
+            uint32_t d = tmem + mt * 256;
+            uint32_t accumulate = kb != 0;
+            if (MODE == TC_ROUTER) {
+              const int c = (kb % nkh) * ROUTER_CHUNKS / nkh;  // fixed chunk of this K block
+              d = tmem + c * NMAX;
+              accumulate = (started >> c) & 1u;
+              started |= 1u << c;
+            }
+            const uint64_t ad = smem_desc_sw128(smem_u32(sa + stage * A_BYTES + mt * TC_TILE_A_BYTES));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA: +32 bytes = +2 in the descriptor address field
+              mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (accumulate | kk) != 0);
+          }
           mma_commit(&empty[stage]);
-          if (++stage == TC_STAGES) stage = 0, phase ^= 1;
+          if (++stage == STAGES) stage = 0, phase ^= 1;
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
-        if (MODE == TC_ROUTER) acc_phase ^= 1;  // one accumulator set (all 512 columns)
-        else if (++acc == 2) acc = 0, acc_phase ^= 1;
+        mma_commit(tfull);
+        acc_phase ^= 1;
       }
       // Every MMA this thread issued has finished before TMEM is released.
       mma_commit(mma_done);
@@ -291,22 +300,21 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     const int q = warp & 3;                       // TMEM lane quarter this warp may access
     const int half = (warp - TC_EPI_FIRST) >> 2;  // the two warps of a quarter take alternate 32-column chunks
     uint8_t *stg = epi + (warp - TC_EPI_FIRST) * TC_EPI_WARP_BYTES;
-    int acc = 0;
     uint32_t acc_phase = 0;
     for (int it = blockIdx.x; it < total; it += gridDim.x) {
       const Item im = decode_item<MODE>(it, p);
-      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
+      if (!warp_wait(tfull, acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t tb = tmem + acc * 256 + ((uint32_t)(q * 32) << 16);
+      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
       if (MODE == TC_ROUTER) {
         const int e = im.f * 128 + q * 32 + lane;
         const float b = (p.bias && e < p.E) ? __ldg(p.bias + e) : 0.f;
         for (int c0 = 32 * half; c0 < im.n; c0 += 64) {
           float v[32], w[32];
-          tmem_ld32(tb + c0, v);
+          tmem_ld32(tq + c0, v);
 #pragma unroll
           for (int c = 1; c < ROUTER_CHUNKS; ++c) {  // ((c0 + c1) + c2) + c3
-            tmem_ld32(tb + c * NMAX + c0, w);
+            tmem_ld32(tq + c * NMAX + c0, w);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] += w[j];
           }
@@ -319,40 +327,58 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       } else if (MODE == TC_GATE_UP) {
         const bool sh = im.seg == p.E;
         const int Iseg = sh ? p.Is : p.I;
-        const int fcol = im.f * 64 + 16 * q;  // first feature of this warp's 16
         __nv_bfloat16 *hout = sh ? p.h_shared : p.h_routed;
         __nv_bfloat16 *guout = sh ? p.gu_shared : p.gu_routed;
-        __nv_bfloat16 *stg_h = (__nv_bfloat16 *)stg;               // [32 cols][24] (16 used)
+        uint32_t *stg_h = (uint32_t *)stg;                         // [32 cols][12 words] (8 used: 16 bf16)
         __nv_bfloat16 *stg_gu = (__nv_bfloat16 *)(stg + 32 * 48);  // [32 cols][40] (32 used)
+        const int fl = lane & 15;
+        const int cbase = lane < 16 ? 0 : 16;
+        const bool odd = lane & 1;
         for (int c0 = 32 * half; c0 < im.n; c0 += 64) {
-          float v[32];
-          tmem_ld32(tb + c0, v);
-          // Lane i < 16 holds gate g of feature i, lane i + 16 the up value u of
-          // the same feature, for columns c0..c0+31.  One exchange gives lane i
-          // the u of columns 0-15 and lane i + 16 the g of columns 16-31, so
-          // both halves compute h for 16 columns each.
-          const int fl = lane & 15;
-          const int cbase = lane < 16 ? 0 : 16;
+          float vt[2][32];
+          tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[1]);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float send = lane < 16 ? v[16 + j] : v[j];
-            const float recv = __shfl_xor_sync(FULL_MASK, send, 16);
-            const float g = lane < 16 ? v[j] : recv;
-            const float u = lane < 16 ? recv : v[16 + j];
-            stg_h[(cbase + j) * 24 + fl] = __float2bfloat16_rn(silu_f32(g) * u);
-          }
-          if (guout) {
+          for (int mt = 0; mt < MT; ++mt) {
+            const float(&v)[32] = vt[mt];
+            const int fcol = (im.f * MT + mt) * 64 + 16 * q;  // first feature of this warp's 16
+            // Lane i < 16 holds gate g of feature i, lane i + 16 the up value u of
+            // the same feature, for columns c0..c0+31.  One exchange gives lane i
+            // the u of columns 0-15 and lane i + 16 the g of columns 16-31, so
+            // both halves compute h for 16 columns each.
+            float hv[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) stg_gu[j * 40 + lane] = __float2bfloat16_rn(v[j]);
-          }
-          __syncwarp();
-          if (c0 + lane < im.rows) {
-            const int64_t row = im.row0 + c0 + lane;
-            const uint4 *s = (const uint4 *)(stg_h + lane * 24);
-            uint4 *d = (uint4 *)(hout + row * Iseg + fcol);
-            d[0] = s[0];
-            d[1] = s[1];
+            for (int j = 0; j < 16; ++j) {
+              const float send = lane < 16 ? v[16 + j] : v[j];
+              const float recv = __shfl_xor_sync(FULL_MASK, send, 16);
+              const float g = lane < 16 ? v[j] : recv;
+              const float u = lane < 16 ? recv : v[16 + j];
+              hv[j] = __fdividef(g, 1.0f + __expf(-g)) * u;
+            }
+            // Pack features (2m, 2m+1) of a column into one bf16x2 word: for the
+            // column pair (j, j+1) the even lane writes column j, the odd lane
+            // column j+1, after swapping one value with its neighbour.
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+              const float x = __shfl_xor_sync(FULL_MASK, odd ? hv[j] : hv[j + 1], 1);
+              const __nv_bfloat162 w2 = odd ? __floats2bfloat162_rn(x, hv[j + 1]) : __floats2bfloat162_rn(hv[j], x);
+              stg_h[(cbase + j + (odd ? 1 : 0)) * 12 + (fl >> 1)] = *reinterpret_cast<const uint32_t *>(&w2);
+            }
             if (guout) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) stg_gu[j * 40 + lane] = __float2bfloat16_rn(v[j]);
+            }
+            __syncwarp();
+            // Two lanes per column row: 16 rows x 32 contiguous bytes per store instruction.
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int r = (lane >> 1) + 16 * i, cc = lane & 1;
+              if (c0 + r < im.rows) {
+                const int64_t row = im.row0 + c0 + r;
+                *(uint4 *)(hout + row * Iseg + fcol + cc * 8) = *(const uint4 *)(stg_h + r * 12 + cc * 4);
+              }
+            }
+            if (guout && c0 + lane < im.rows) {
+              const int64_t row = im.row0 + c0 + lane;
               const uint4 *sg = (const uint4 *)(stg_gu + lane * 40);
               uint4 *dg = (uint4 *)(guout + row * 2 * Iseg + fcol);
               uint4 *du = (uint4 *)(guout + row * 2 * Iseg + Iseg + fcol);
@@ -361,34 +387,47 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
               du[0] = sg[2];
               du[1] = sg[3];
             }
+            __syncwarp();
           }
-          __syncwarp();
         }
       } else {
         const bool sh = im.seg == p.E;
-        const int ocol = im.f * 128 + q * 32;  // first output feature of this warp's 32
-        __nv_bfloat16 *stg_y = (__nv_bfloat16 *)stg;  // [32 cols][40] (32 used)
+        uint32_t *stg_y = (uint32_t *)stg;  // [32 cols][20 words] (16 used: 32 bf16)
         __nv_bfloat16 *yout = sh ? p.y_shared : p.y_routed;
+        const bool odd = lane & 1;
         for (int c0 = 32 * half; c0 < im.n; c0 += 64) {
-          float v[32];
-          tmem_ld32(tb + c0, v);
+          // Destination row of column c0 + lane, fetched before the accumulator loads.
+          int dst = 0;
+          if (c0 + lane < im.rows) dst = sh ? (int)(im.row0 + c0 + lane) : __ldg(p.sorted_route + im.row0 + c0 + lane);
+          float vt[2][32];
+          tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[1]);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) stg_y[j * 40 + lane] = __float2bfloat16_rn(v[j]);
-          __syncwarp();
-          if (c0 + lane < im.rows) {
-            const int64_t dst = sh ? im.row0 + c0 + lane : (int64_t)__ldg(p.sorted_route + im.row0 + c0 + lane);
-            const uint4 *s = (const uint4 *)(stg_y + lane * 40);
-            uint4 *d = (uint4 *)(yout + dst * p.H + ocol);
+          for (int mt = 0; mt < MT; ++mt) {
+            const int ocol = (im.f * MT + mt) * 128 + q * 32;  // first output feature of this warp's 32
+            // Pack features (2m, 2m+1) of a column into one bf16x2 word (see the gate_up epilogue).
 #pragma unroll
-            for (int i = 0; i < 4; ++i) d[i] = s[i];
+            for (int j = 0; j < 32; j += 2) {
+              const float x = __shfl_xor_sync(FULL_MASK, odd ? vt[mt][j] : vt[mt][j + 1], 1);
+              const __nv_bfloat162 w2 =
+                  odd ? __floats2bfloat162_rn(x, vt[mt][j + 1]) : __floats2bfloat162_rn(vt[mt][j], x);
+              stg_y[(j + (odd ? 1 : 0)) * 20 + (lane >> 1)] = *reinterpret_cast<const uint32_t *>(&w2);
+            }
+            __syncwarp();
+            // Four lanes per column row: 8 rows x 64 contiguous bytes per store instruction.
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = (lane >> 2) + 8 * i, cc = lane & 3;
+              const int drow = __shfl_sync(FULL_MASK, dst, r);
+              if (c0 + r < im.rows)
+                *(uint4 *)(yout + (int64_t)drow * p.H + ocol + cc * 8) = *(const uint4 *)(stg_y + r * 20 + cc * 4);
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
-      if (MODE == TC_ROUTER) acc_phase ^= 1;
-      else if (++acc == 2) acc = 0, acc_phase ^= 1;
+      mbar_arrive(tempty);
+      acc_phase ^= 1;
     }
   } else if (MODE == TC_GATE_UP) {
     // ------------------------------------------------------------ row gather (warps 10..17)
@@ -419,14 +458,14 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const __nv_bfloat16 *src = p.x + kb * 64 + qc * 8;
         for (int i = sub; i < ni; i += 4) cp_async_16(bsm + i * 1024, src + (int64_t)tok[i] * p.H);
         cp_async_commit();
-        if (++pending > 2) {
-          cp_async_wait<2>();
+        if (++pending > 1) {
+          cp_async_wait<1>();
           fence_proxy_async_smem();
           mbar_arrive(&full[arr_stage]);
-          if (++arr_stage == TC_STAGES) arr_stage = 0;
+          if (++arr_stage == STAGES) arr_stage = 0;
           --pending;
         }
-        if (++stage == TC_STAGES) stage = 0, phase ^= 1;
+        if (++stage == STAGES) stage = 0, phase ^= 1;
       }
     }
     cp_async_wait<0>();
@@ -434,7 +473,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     if (ok)
       for (; pending > 0; --pending) {
         mbar_arrive(&full[arr_stage]);
-        if (++arr_stage == TC_STAGES) arr_stage = 0;
+        if (++arr_stage == STAGES) arr_stage = 0;
       }
   }
   tc_fence_before();
@@ -467,7 +506,7 @@ __global__ void split_router_weight_kernel(int64_t n, int H, const float *__rest
 }
 
 // item_start[s] = sum_{s' < s} ceil(n_s' / 256) * nf_s', routed segments
-// with nf_routed feature tiles, the shared segment (n = T) with nf_shared.
+// with nf_routed M-tile pairs, the shared segment (n = T) with nf_shared.
 __global__ void __launch_bounds__(1024)
 build_items_kernel(int E, int T, int nf_routed, int nf_shared, const int32_t *__restrict__ offsets,
                    int32_t *__restrict__ item_start) {
@@ -493,6 +532,29 @@ build_items_kernel(int E, int T, int nf_routed, int nf_shared, const int32_t *__
     __syncthreads();
     if (threadIdx.x == 1023) carry += buf[1023];
     __syncthreads();
+  }
+}
+
+// items[it] = (segment, M-tile pair, first row, rows) for it < item_start[E+1]:
+// the rows of a segment are cut into ceil(n / 256) tiles of equal size
+// rounded up to 16, a cut that depends only on the segment's own length.
+__global__ void expand_items_kernel(int E, int T, int max_items, const int32_t *__restrict__ offsets,
+                                    const int32_t *__restrict__ item_start, int4 *__restrict__ items) {
+  const int total = min(item_start[E + 1], max_items);
+  for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < total; it += gridDim.x * blockDim.x) {
+    int lo = 0, hi = E;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (item_start[mid] <= it) lo = mid;
+      else hi = mid - 1;
+    }
+    const int local = it - item_start[lo];
+    const int base = lo == E ? 0 : offsets[lo];
+    const int n_s = lo == E ? T : offsets[lo + 1] - base;
+    const int ntile = (int)ceil_div(n_s, 256);
+    const int rpt = (int)round_up(ceil_div(n_s, ntile), 16);
+    const int nt = local % ntile;
+    items[it] = make_int4(lo, local / ntile, base + nt * rpt, min(rpt, n_s - nt * rpt));
   }
 }
 
@@ -549,13 +611,13 @@ static bool map_rows(CUtensorMap *m5, const void *ptr, int64_t rows, int64_t col
 }
 
 // Gate/up weights [n_mat, 2*Iw, H] viewed as 5-D (H, 16, 2, Iw/16, n_mat):
-// a box (64, 16, 2, 4, 1) holds, for 4 consecutive groups of 16 features,
-// the 16 gate rows followed by the 16 up rows of the same features.
+// a box (64, 16, 2, 8, 1) holds, for 8 consecutive groups of 16 features
+// (two M tiles), the 16 gate rows followed by the 16 up rows of each group.
 static bool map_gate_up(CUtensorMap *m, const void *ptr, int n_mat, int Iw, int H) {
   const uint64_t dims[5] = {(uint64_t)H, 16, 2, (uint64_t)Iw / 16, (uint64_t)n_mat};
   const uint64_t strides[4] = {(uint64_t)H * 2, (uint64_t)Iw * H * 2, (uint64_t)16 * H * 2,
                                (uint64_t)2 * Iw * H * 2};
-  const uint32_t box[5] = {64, 16, 2, 4, 1};
+  const uint32_t box[5] = {64, 16, 2, 8, 1};
   return encode_map(m, ptr, 5, dims, strides, box);
 }
 
@@ -584,7 +646,7 @@ static cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cu
     if (e != cudaSuccess) return e;
     di.attr[MODE] = true;
   }
-  tc_gemm_kernel<MODE><<<grid, TcCfg<MODE>::THREADS, TC_SMEM_BYTES, stream>>>(maps, p);
+  tc_gemm_kernel<MODE><<<grid, tc_threads<MODE>(), TC_SMEM_BYTES, stream>>>(maps, p);
   return cudaGetLastError();
 }
 
@@ -610,18 +672,40 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
   return launch_tc<TC_ROUTER>(m, p, grid, stream);
 }
 
-size_t ffn_tc_scratch_bytes(int E) { return (size_t)2 * 256 * (((E + 2) * 4 + 255) / 256); }
+// Upper bound on the items of a grouped GEMM: sum_s ceil(n_s / 256) <=
+// ceil(R / 256) + E over the routed segments, ceil(T / 256) for the shared one.
+static int64_t max_items(int T, int k, int E, int nf_routed, int nf_shared) {
+  return (ceil_div((int64_t)T * k, 256) + E) * nf_routed + ceil_div(T, 256) * nf_shared;
+}
+
+static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+size_t ffn_tc_scratch_bytes(int T, int k, int E, int H, int I, int Is) {
+  const size_t starts = round256((size_t)(E + 2) * 4);
+  return 2 * starts + round256((size_t)max_items(T, k, E, I / 128, Is / 128) * 16) +
+         round256((size_t)max_items(T, k, E, H / 256, H / 256) * 16);
+}
 
 cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
-  int32_t *items_gu = (int32_t *)scratch;
-  int32_t *items_dn = items_gu + round_up(a.E + 2, 64);
-  build_items_kernel<<<1, 1024, 0, stream>>>(a.E, a.T, a.I / 64, a.Is / 64, a.offsets, items_gu);
-  build_items_kernel<<<1, 1024, 0, stream>>>(a.E, a.T, a.H / 128, a.H / 128, a.offsets, items_dn);
+  const size_t starts = round256((size_t)(a.E + 2) * 4);
+  const int mi_gu = (int)max_items(a.T, a.k, a.E, a.I / 128, a.Is / 128);
+  const int mi_dn = (int)max_items(a.T, a.k, a.E, a.H / 256, a.H / 256);
+  uint8_t *w = (uint8_t *)scratch;
+  int32_t *start_gu = (int32_t *)w;
+  int32_t *start_dn = (int32_t *)(w + starts);
+  int4 *items_gu = (int4 *)(w + 2 * starts);
+  int4 *items_dn = (int4 *)(w + 2 * starts + round256((size_t)mi_gu * 16));
+  build_items_kernel<<<1, 1024, 0, stream>>>(a.E, a.T, a.I / 128, a.Is / 128, a.offsets, start_gu);
+  build_items_kernel<<<1, 1024, 0, stream>>>(a.E, a.T, a.H / 256, a.H / 256, a.offsets, start_dn);
+  expand_items_kernel<<<(unsigned)std::min<int64_t>(ceil_div(mi_gu, 256), 1024), 256, 0, stream>>>(
+      a.E, a.T, mi_gu, a.offsets, start_gu, items_gu);
+  expand_items_kernel<<<(unsigned)std::min<int64_t>(ceil_div(mi_dn, 256), 1024), 256, 0, stream>>>(
+      a.E, a.T, mi_dn, a.offsets, start_dn, items_dn);
   const int64_t R = (int64_t)a.T * a.k;
   TcMaps mg, md;
   if (!map_gate_up(&mg.a, a.w_gate_up, a.E, a.I, a.H) || !map_gate_up(&mg.a_sh, a.ws_gate_up, 1, a.Is, a.H) ||
-      !map_2d(&md.a, a.w_down, (int64_t)a.E * a.H, a.I, 128) || !map_2d(&md.a_sh, a.ws_down, a.H, a.Is, 128) ||
+      !map_2d(&md.a, a.w_down, (int64_t)a.E * a.H, a.I, 256) || !map_2d(&md.a_sh, a.ws_down, a.H, a.Is, 256) ||
       !map_rows(md.b, a.h_routed, R, a.I) || !map_rows(md.b_sh, a.h_shared, a.T, a.Is))
     return cudaErrorInvalidValue;
   for (int h = 0; h < 5; ++h) mg.b[h] = mg.b_sh[h] = mg.a;  // gate_up gathers its token rows with cp.async
@@ -638,10 +722,12 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   p.y_shared = (__nv_bfloat16 *)a.y_shared;
   p.status = status;
   const int grid = dev_info().sms;
-  p.item_start = items_gu;
+  p.item_start = start_gu;
+  p.items = items_gu;
   cudaError_t e = launch_tc<TC_GATE_UP>(mg, p, grid, stream);
   if (e != cudaSuccess) return e;
-  p.item_start = items_dn;
+  p.item_start = start_dn;
+  p.items = items_dn;
   return launch_tc<TC_DOWN>(md, p, grid, stream);
 }
 

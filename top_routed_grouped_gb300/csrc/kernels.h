@@ -52,7 +52,7 @@ size_t router_tc_scratch_bytes(int E, int H);
 // Router logits via the exact three-way bf16 split of w_router (scratch: router_tc_scratch_bytes).
 cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const float *wr, const float *bias,
                                     float *logits, void *scratch, int *status, cudaStream_t stream);
-size_t ffn_tc_scratch_bytes(int E);
+size_t ffn_tc_scratch_bytes(int T, int k, int E, int H, int I, int Is);
 // gate_up + SwiGLU and down as two persistent tcgen05 grouped GEMMs (scratch: ffn_tc_scratch_bytes).
 cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStream_t stream);
 
