@@ -42,21 +42,26 @@ template <> struct Vec16<float> {
     float4 v = *reinterpret_cast<const float4 *>(p);
     o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
   }
+  static __device__ inline void unpack(const uint4 &v, float (&o)[4]) {
+    o[0] = __uint_as_float(v.x); o[1] = __uint_as_float(v.y);
+    o[2] = __uint_as_float(v.z); o[3] = __uint_as_float(v.w);
+  }
   static __device__ inline void store(float *p, const float (&o)[4]) {
     *reinterpret_cast<float4 *>(p) = make_float4(o[0], o[1], o[2], o[3]);
   }
 };
 template <> struct Vec16<__nv_bfloat16> {
   static constexpr int N = 8;
-  static __device__ inline void load(const __nv_bfloat16 *p, float (&o)[8]) {
-    uint4 v = *reinterpret_cast<const uint4 *>(p);
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+  static __device__ inline void unpack(const uint4 &v, float (&o)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float2 f = __bfloat1622float2(h[i]);
-      o[2 * i] = f.x;
-      o[2 * i + 1] = f.y;
+    for (int i = 0; i < 4; ++i) {  // bf16 -> fp32 is a 16-bit shift
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
+  }
+  static __device__ inline void load(const __nv_bfloat16 *p, float (&o)[8]) {
+    unpack(*reinterpret_cast<const uint4 *>(p), o);
   }
   static __device__ inline void store(__nv_bfloat16 *p, const float (&o)[8]) {
     uint4 v;

@@ -14,25 +14,28 @@
 //            into four fixed chunks accumulated in separate TMEM columns and
 //            summed in FP32 in chunk order (four times fewer accumulation
 //            steps per accumulator); epilogue adds the bias, writes logits.
-//   GATE_UP  D[f, j] = W_gu[e][f] . x[tok(j)] for 64 gate and 64 up rows of a
-//            feature tile and up to 256 rows j of expert e's segment; the x
-//            rows are gathered by two warps with 16-byte cp.async into the
-//            swizzled operand layout; epilogue h = silu(g) * u.
-//   DOWN     D[o, j] = W_dn[e][o] . h[j] for 128 output features; epilogue
-//            writes row j to y_routed[sorted_route[j]] (or y_shared).
-// The weights are the M = 128 operand and the tokens the N <= 256 operand,
+//   GATE_UP  D[f, j] = W_gu[e][f] . x[tok(j)] for the gate and up rows of 128
+//            features (two M tiles of 64 gate + 64 up rows) and up to 256 rows
+//            j of expert e's segment; the x rows are gathered by eight warps
+//            with 16-byte cp.async into the swizzled operand layout; epilogue
+//            h = silu(g) * u.
+//   DOWN     D[o, j] = W_dn[e][o] . h[j] for 256 output features (two M
+//            tiles); epilogue writes row j to y_routed[sorted_route[j]] (or
+//            y_shared).
+// The weights are the M operand (128-row tiles) and the tokens the N <= 256 operand,
 // so a short expert segment costs at most 15 padded columns.  Every output
 // element is accumulated over K in a fixed order (K blocks of 64, four
 // K = 16 MMAs each, fixed chunking); tiling decides only where a column
 // sits, never the order, so a token's values do not depend on T or on its
 // segment.
 //
-// Roles: warp 0 issues TMA loads (one instruction for a 128 x 64 weight tile,
-// at most a few power-of-two row boxes for a contiguous token tile) into a
-// 4-stage ring; warp 1 allocates 512 TMEM columns and one thread issues the
-// MMAs; warps 2-5 drain an accumulator (each warp its 32-lane quarter of
-// TMEM), staging rows in shared memory so global stores are 16-byte vectors;
-// GATE_UP adds warps 6-7 for the row gather.
+// Roles: warp 0 issues TMA loads (one instruction per weight tile, at most a
+// few power-of-two row boxes for a contiguous token tile) into a stage ring;
+// warp 1 allocates the 512 TMEM columns and one thread issues the MMAs; the
+// epilogue warps from warp 2 on drain the accumulators (each TMEM lane
+// quarter shared by several warps taking column chunks in turn), staging rows
+// in shared memory so that global stores write contiguous row segments;
+// GATE_UP adds eight warps that gather the token rows.
 #include <cuda.h>
 
 #include <algorithm>
@@ -53,41 +56,40 @@ using namespace umma;
 // one M tile and uses the 512 columns as four K-chunk accumulators.
 template <int MODE>
 struct TcCfg;
-constexpr int TC_ROUTER = 0, TC_GATE_UP = 1, TC_DOWN = 2;
-template <>
-struct TcCfg<0> {
-  static constexpr int NMAX = 128, MT = 1, STAGES = 4;
-};
+constexpr int TC_GATE_UP = 1, TC_DOWN = 2;
+// EPI_WARPS epilogue warps (a multiple of 4: EPI_WARPS / 4 warps per TMEM
+// lane quarter split the columns); EPI_BYTES of row staging per warp.
 template <>
 struct TcCfg<1> {
-  static constexpr int NMAX = 256, MT = 2, STAGES = 3;
+  static constexpr int NMAX = 256, MT = 2, STAGES = 3, EPI_WARPS = 8, EPI_BYTES = 4096;
 };
 template <>
 struct TcCfg<2> {
-  static constexpr int NMAX = 256, MT = 2, STAGES = 3;
+  static constexpr int NMAX = 256, MT = 2, STAGES = 3, EPI_WARPS = 16, EPI_BYTES = 2048;
 };
 
 static_assert(TcCfg<1>::MT == 2 && TcCfg<2>::MT == 2, "the epilogues drain two M tiles per item together");
 
 constexpr int TC_TILE_A_BYTES = 128 * 128;  // one M tile: 128 rows x 64 bf16
 constexpr int TC_B_BYTES = 256 * 128;       // up to 256 token rows x 64 bf16
-constexpr int TC_EPI_WARPS = 8;             // two warps per TMEM lane quarter, splitting the columns
-constexpr int TC_EPI_FIRST = 2;             // epilogue warps 2..9
-constexpr int TC_GATHER_WARPS = 8;          // GATE_UP row gather, warps 10..17
-constexpr int TC_GATHER_FIRST = TC_EPI_FIRST + TC_EPI_WARPS;
-constexpr int TC_EPI_WARP_BYTES = 4096;     // per epilogue warp staging
+constexpr int TC_EPI_FIRST = 2;             // epilogue warps start at warp 2
+constexpr int TC_GATHER_WARPS = 8;          // GATE_UP row gather, after the epilogue warps
 constexpr int TC_TOK_INTS = 256;            // gathered-row token ids (8 warps x 32)
 constexpr int TC_MAX_STAGES = 4;
-constexpr int TC_SMEM_BYTES = 1024 + 4 * (TC_TILE_A_BYTES + TC_B_BYTES) + TC_EPI_WARPS * TC_EPI_WARP_BYTES +
-                              TC_TOK_INTS * 4 + 256;  // the largest of the three layouts (ROUTER)
+constexpr int TC_EPI_MAX_BYTES = 32768;     // largest EPI_WARPS * EPI_BYTES
+constexpr int TC_SMEM_BYTES = 1024 + 4 * (TC_TILE_A_BYTES + TC_B_BYTES) + TC_EPI_MAX_BYTES + TC_TOK_INTS * 4 +
+                              256;  // the largest of the three layouts
 static_assert(3 * (2 * TC_TILE_A_BYTES + TC_B_BYTES) <= 4 * (TC_TILE_A_BYTES + TC_B_BYTES), "stage ring");
 constexpr uint32_t TC_TMEM_COLS = 512;
 constexpr int GATHER_THREADS = 32 * TC_GATHER_WARPS;
-constexpr int ROUTER_CHUNKS = 4;
 
 template <int MODE>
+constexpr int tc_gather_first() {
+  return TC_EPI_FIRST + TcCfg<MODE>::EPI_WARPS;
+}
+template <int MODE>
 constexpr int tc_threads() {
-  return 32 * (TC_GATHER_FIRST + (MODE == TC_GATE_UP ? TC_GATHER_WARPS : 0));
+  return 32 * (tc_gather_first<MODE>() + (MODE == TC_GATE_UP ? TC_GATHER_WARPS : 0));
 }
 
 // Tensor maps.  b[h] / b_sh[h] are the token-tile maps with box height 256 >> h.
@@ -125,24 +127,12 @@ struct Item {
 template <int MODE>
 __device__ inline Item decode_item(int it, const TcParams &p) {
   Item r;
-  if (MODE == TC_ROUTER) {
-    constexpr int NMAX = TcCfg<MODE>::NMAX;
-    const int ntile = (int)ceil_div(p.T, NMAX);
-    const int rpt = (int)round_up(ceil_div(p.T, ntile), 16);
-    const int nt = it % ntile;
-    r.seg = 0;
-    r.f = it / ntile;
-    r.row0 = (int64_t)nt * rpt;
-    r.rows = min(rpt, p.T - nt * rpt);
-    r.nk = 3 * p.H / 64;
-  } else {
-    const int4 d = __ldg(p.items + it);
-    r.seg = d.x;
-    r.f = d.y;
-    r.row0 = d.z;
-    r.rows = d.w;
-    r.nk = (MODE == TC_GATE_UP ? p.H : (r.seg == p.E ? p.Is : p.I)) / 64;
-  }
+  const int4 d = __ldg(p.items + it);
+  r.seg = d.x;
+  r.f = d.y;
+  r.row0 = d.z;
+  r.rows = d.w;
+  r.nk = (MODE == TC_GATE_UP ? p.H : (r.seg == p.E ? p.Is : p.I)) / 64;
   r.n = (int)round_up(r.rows, 16);
   return r;
 }
@@ -159,12 +149,15 @@ __global__ void __launch_bounds__(tc_threads<MODE>(), 1)
 tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   constexpr int NMAX = TcCfg<MODE>::NMAX, MT = TcCfg<MODE>::MT, STAGES = TcCfg<MODE>::STAGES;
   constexpr int A_BYTES = MT * TC_TILE_A_BYTES;
+  constexpr int EPI_WARPS = TcCfg<MODE>::EPI_WARPS, EPI_BYTES = TcCfg<MODE>::EPI_BYTES;
+  constexpr int GATHER_FIRST = tc_gather_first<MODE>();
+  static_assert(EPI_WARPS * EPI_BYTES <= TC_EPI_MAX_BYTES && EPI_WARPS % 4 == 0, "epilogue layout");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sa = base;
   uint8_t *sb = sa + STAGES * A_BYTES;
   uint8_t *epi = sb + STAGES * TC_B_BYTES;
-  int32_t *tok_all = (int32_t *)(epi + TC_EPI_WARPS * TC_EPI_WARP_BYTES);
+  int32_t *tok_all = (int32_t *)(epi + TC_EPI_MAX_BYTES);
   uint64_t *bars = (uint64_t *)(tok_all + TC_TOK_INTS);
   uint64_t *full = bars, *empty = bars + TC_MAX_STAGES;
   uint64_t *tfull = bars + 2 * TC_MAX_STAGES, *tempty = tfull + 1, *mma_done = tempty + 1;
@@ -178,21 +171,21 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 32 * TC_EPI_WARPS);
+    mbar_init(tempty, 32 * EPI_WARPS);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&maps.a);
-    if (MODE != TC_ROUTER) prefetch_tmap(&maps.a_sh);
+    prefetch_tmap(&maps.a_sh);
   }
   if (warp == 1) tmem_alloc(tmem_slot, TC_TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = MODE == TC_ROUTER ? p.n_items : __ldg(p.item_start + p.E + 1);
+  const int total = __ldg(p.item_start + p.E + 1);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -205,16 +198,14 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       bool ok = true;
       for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
         const Item im = decode_item<MODE>(it, p);
-        const bool sh = MODE != TC_ROUTER && im.seg == p.E;
+        const bool sh = im.seg == p.E;
         const uint32_t bytes = A_BYTES + (MODE == TC_GATE_UP ? 0 : im.n * 128);
         for (int kb = 0; kb < im.nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], bytes);
           uint8_t *a_dst = sa + stage * A_BYTES;
           uint8_t *b_dst = sb + stage * TC_B_BYTES;
-          if (MODE == TC_ROUTER) {
-            tma_load_2d(a_dst, &maps.a, &full[stage], kb * 64, im.f * 128, pol_x);
-          } else if (MODE == TC_GATE_UP) {
+          if (MODE == TC_GATE_UP) {
             // One 5-D box: for 8 groups of 16 features (two M tiles), 16 gate rows then 16 up rows.
             tma_load_5d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64, 0, 0, im.f * 8, sh ? 0 : im.seg,
                         pol_w);
@@ -224,8 +215,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           }
           if (MODE != TC_GATE_UP) {
             // Token rows [row0, row0 + n) as power-of-two boxes (n is a multiple of 16).
-            const int kx = MODE == TC_ROUTER ? (kb % (p.H / 64)) * 64 : kb * 64;
-            const CUtensorMap *bm = (MODE == TC_DOWN && sh) ? maps.b_sh : maps.b;
+            const int kx = kb * 64;
+            const CUtensorMap *bm = sh ? maps.b_sh : maps.b;
             int r = 0;
 #pragma unroll
             for (int h = 0; h < 5; ++h) {
@@ -256,27 +247,19 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      const int nkh = p.H / 64;
       for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
         const Item im = decode_item<MODE>(it, p);
         if (!mbar_wait(tempty, acc_phase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32(128, im.n);
-        uint32_t started = 0;  // ROUTER: chunk accumulators already written
         for (int kb = 0; kb < im.nk; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint64_t bd = smem_desc_sw128(smem_u32(sb + stage * TC_B_BYTES));
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
-            uint32_t d = tmem + mt * 256;
-            uint32_t accumulate = kb != 0;
-            if (MODE == TC_ROUTER) {
-              const int c = (kb % nkh) * ROUTER_CHUNKS / nkh;  // fixed chunk of this K block
-              d = tmem + c * NMAX;
-              accumulate = (started >> c) & 1u;
-              started |= 1u << c;
-            }
+            const uint32_t d = tmem + mt * 256;
+            const uint32_t accumulate = kb != 0;
             const uint64_t ad = smem_desc_sw128(smem_u32(sa + stage * A_BYTES + mt * TC_TILE_A_BYTES));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA: +32 bytes = +2 in the descriptor address field
@@ -295,36 +278,20 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       mbar_wait(mma_done, 0, &never, p.status);
     }
     __syncwarp();
-  } else if (warp < TC_GATHER_FIRST) {
+  } else if (warp < GATHER_FIRST) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                       // TMEM lane quarter this warp may access
-    const int half = (warp - TC_EPI_FIRST) >> 2;  // the two warps of a quarter take alternate 32-column chunks
-    uint8_t *stg = epi + (warp - TC_EPI_FIRST) * TC_EPI_WARP_BYTES;
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // The EPI_WARPS / 4 warps of a quarter take 32-column chunks in turn.
+    constexpr int CSTEP = 32 * (EPI_WARPS / 4);
+    const int cfirst = 32 * ((warp - TC_EPI_FIRST) >> 2);
+    uint8_t *stg = epi + (warp - TC_EPI_FIRST) * EPI_BYTES;
     uint32_t acc_phase = 0;
     for (int it = blockIdx.x; it < total; it += gridDim.x) {
       const Item im = decode_item<MODE>(it, p);
       if (!warp_wait(tfull, acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-      if (MODE == TC_ROUTER) {
-        const int e = im.f * 128 + q * 32 + lane;
-        const float b = (p.bias && e < p.E) ? __ldg(p.bias + e) : 0.f;
-        for (int c0 = 32 * half; c0 < im.n; c0 += 64) {
-          float v[32], w[32];
-          tmem_ld32(tq + c0, v);
-#pragma unroll
-          for (int c = 1; c < ROUTER_CHUNKS; ++c) {  // ((c0 + c1) + c2) + c3
-            tmem_ld32(tq + c * NMAX + c0, w);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] += w[j];
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int c = c0 + j;
-            if (c < im.rows && e < p.E) p.logits[(im.row0 + c) * p.E + e] = p.bias ? v[j] + b : v[j];
-          }
-        }
-      } else if (MODE == TC_GATE_UP) {
+      if (MODE == TC_GATE_UP) {
         const bool sh = im.seg == p.E;
         const int Iseg = sh ? p.Is : p.I;
         __nv_bfloat16 *hout = sh ? p.h_shared : p.h_routed;
@@ -334,7 +301,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const int fl = lane & 15;
         const int cbase = lane < 16 ? 0 : 16;
         const bool odd = lane & 1;
-        for (int c0 = 32 * half; c0 < im.n; c0 += 64) {
+        for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
           float vt[2][32];
           tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[1]);
 #pragma unroll
@@ -392,10 +359,12 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
       } else {
         const bool sh = im.seg == p.E;
-        uint32_t *stg_y = (uint32_t *)stg;  // [32 cols][20 words] (16 used: 32 bf16)
+        // [32 cols][16 words]: two consecutive rows span all 32 banks, so the
+        // pair writes and the quarter-warp 16-byte reads are conflict-free.
+        uint32_t *stg_y = (uint32_t *)stg;
         __nv_bfloat16 *yout = sh ? p.y_shared : p.y_routed;
         const bool odd = lane & 1;
-        for (int c0 = 32 * half; c0 < im.n; c0 += 64) {
+        for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
           // Destination row of column c0 + lane, fetched before the accumulator loads.
           int dst = 0;
           if (c0 + lane < im.rows) dst = sh ? (int)(im.row0 + c0 + lane) : __ldg(p.sorted_route + im.row0 + c0 + lane);
@@ -410,7 +379,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
               const float x = __shfl_xor_sync(FULL_MASK, odd ? vt[mt][j] : vt[mt][j + 1], 1);
               const __nv_bfloat162 w2 =
                   odd ? __floats2bfloat162_rn(x, vt[mt][j + 1]) : __floats2bfloat162_rn(vt[mt][j], x);
-              stg_y[(j + (odd ? 1 : 0)) * 20 + (lane >> 1)] = *reinterpret_cast<const uint32_t *>(&w2);
+              stg_y[(j + (odd ? 1 : 0)) * 16 + (lane >> 1)] = *reinterpret_cast<const uint32_t *>(&w2);
             }
             __syncwarp();
             // Four lanes per column row: 8 rows x 64 contiguous bytes per store instruction.
@@ -419,7 +388,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
               const int r = (lane >> 2) + 8 * i, cc = lane & 3;
               const int drow = __shfl_sync(FULL_MASK, dst, r);
               if (c0 + r < im.rows)
-                *(uint4 *)(yout + (int64_t)drow * p.H + ocol + cc * 8) = *(const uint4 *)(stg_y + r * 20 + cc * 4);
+                *(uint4 *)(yout + (int64_t)drow * p.H + ocol + cc * 8) = *(const uint4 *)(stg_y + r * 16 + cc * 4);
             }
             __syncwarp();
           }
@@ -436,7 +405,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     // thread arrives on a stage's `full` barrier once its copies into that
     // stage are complete and fenced for the tensor cores (pad rows past the
     // segment are left as they are: their accumulator columns are never read).
-    const int g = warp - TC_GATHER_FIRST;
+    const int g = warp - GATHER_FIRST;
     const int sub = lane >> 3, qc = lane & 7;
     int32_t *tok = tok_all + g * 32;
     int stage = 0, arr_stage = 0, pending = 0;
@@ -483,6 +452,200 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Router logits on the tensor cores.
+//
+// An item is 128 experts x up to 256 tokens.  A stage holds, for one K block
+// j of 64 hidden units, the x tile once and the three split-weight tiles
+// W1, W2, W3 of the same columns; the three MMA groups read the same x tile.
+// The K range is cut into four fixed chunks of K blocks (chunk c = blocks
+// [c nkh / 4, (c + 1) nkh / 4)); a chunk accumulates in one of two TMEM
+// buffers while the epilogue adds the previous chunk into FP32 registers, so
+// logit = ((chunk0 + chunk1) + chunk2) + chunk3 (+ bias), the same order for
+// every token and every T.
+// ---------------------------------------------------------------------------
+constexpr int RT_NMAX = 256, RT_STAGES = 2, RT_CHUNKS = 4, RT_EPI_WARPS = 8;
+constexpr int RT_A_BYTES = 3 * TC_TILE_A_BYTES;
+constexpr int RT_THREADS = 32 * (TC_EPI_FIRST + RT_EPI_WARPS);
+static_assert(RT_STAGES * (RT_A_BYTES + TC_B_BYTES) + 256 + 1024 <= TC_SMEM_BYTES, "router smem");
+
+struct RtItem {
+  int f;         // expert tile (128 experts)
+  int64_t row0;  // first token
+  int rows, n;
+};
+
+__device__ inline RtItem rt_item(int it, int T) {
+  const int ntile = (int)ceil_div(T, RT_NMAX);
+  const int rpt = (int)round_up(ceil_div(T, ntile), 16);
+  const int nt = it % ntile;
+  RtItem r;
+  r.f = it / ntile;
+  r.row0 = (int64_t)nt * rpt;
+  r.rows = min(rpt, T - nt * rpt);
+  r.n = (int)round_up(r.rows, 16);
+  return r;
+}
+
+__global__ void __launch_bounds__(RT_THREADS, 1)
+tc_router_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *sa = base;
+  uint8_t *sb = sa + RT_STAGES * RT_A_BYTES;
+  uint64_t *bars = (uint64_t *)(sb + RT_STAGES * TC_B_BYTES);
+  uint64_t *full = bars, *empty = bars + RT_STAGES;
+  uint64_t *tfull = bars + 2 * RT_STAGES, *tempty = tfull + 2, *mma_done = tempty + 2;
+  uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
+  volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RT_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 32 * RT_EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&maps.a);
+  if (warp == 1) tmem_alloc(tmem_slot, TC_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int total = p.n_items, nkh = p.H / 64;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();  // split weights and x are read by many CTAs
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_phase = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        const RtItem im = rt_item(it, p.T);
+        const uint32_t bytes = RT_A_BYTES + im.n * 128;
+        for (int j = 0; j < nkh; ++j) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          uint8_t *a_dst = sa + stage * RT_A_BYTES;
+          uint8_t *b_dst = sb + stage * TC_B_BYTES;
+#pragma unroll
+          for (int sp = 0; sp < 3; ++sp)
+            tma_load_2d(a_dst + sp * TC_TILE_A_BYTES, &maps.a, &full[stage], sp * p.H + j * 64, im.f * 128, pol);
+          int r = 0;
+#pragma unroll
+          for (int h = 0; h < 5; ++h) {
+            const int box = 256 >> h;
+            while (im.n - r >= box) {
+              tma_load_2d(b_dst + r * 128, &maps.b[h], &full[stage], j * 64, (int)(im.row0 + r), pol);
+              r += box;
+            }
+          }
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == RT_STAGES) stage = 0, phase ^= 1;
+        }
+      }
+      if (!ok) {
+        volatile int never = 0;
+        for (int s = 0; s < RT_STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1, &never, nullptr, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, uses = 0;  // uses: bit b = parity of the uses of TMEM buffer b
+      bool ok = true;
+      for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        const RtItem im = rt_item(it, p.T);
+        const uint32_t idesc = idesc_bf16_f32(128, im.n);
+        for (int c = 0; c < RT_CHUNKS && ok; ++c) {
+          const int b = c & 1;
+          if (!mbar_wait(&tempty[b], ((uses >> b) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d = tmem + b * 256;
+          const int j0 = c * nkh / RT_CHUNKS, j1 = (c + 1) * nkh / RT_CHUNKS;
+          for (int j = j0; j < j1; ++j) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t bd = smem_desc_sw128(smem_u32(sb + stage * TC_B_BYTES));
+#pragma unroll
+            for (int sp = 0; sp < 3; ++sp) {
+              const uint64_t ad = smem_desc_sw128(smem_u32(sa + stage * RT_A_BYTES + sp * TC_TILE_A_BYTES));
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (j != j0 || sp != 0 || kk != 0) ? 1u : 0u);
+            }
+            mma_commit(&empty[stage]);
+            if (++stage == RT_STAGES) stage = 0, phase ^= 1;
+          }
+          if (!ok) break;
+          mma_commit(&tfull[b]);
+          uses ^= 1u << b;
+        }
+      }
+      mma_commit(mma_done);
+      volatile int never = 0;
+      mbar_wait(mma_done, 0, &never, p.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // Warp (q, hq): TMEM lane quarter q (experts), columns [128 hq, 128 hq + 128).
+    const int q = warp & 3, hq = (warp - TC_EPI_FIRST) >> 2;
+    uint32_t uses = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+      const RtItem im = rt_item(it, p.T);
+      float acc[128];
+#pragma unroll
+      for (int c = 0; c < RT_CHUNKS; ++c) {
+        const int b = c & 1;
+        if (!warp_wait(&tfull[b], (uses >> b) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tb = tmem + b * 256 + ((uint32_t)(q * 32) << 16) + hq * 128;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          if (hq * 128 + cc * 32 < im.n) {
+            float v[32];
+            tmem_ld32(tb + cc * 32, v);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) acc[cc * 32 + jj] = c == 0 ? v[jj] : acc[cc * 32 + jj] + v[jj];
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[b]);
+        uses ^= 1u << b;
+      }
+      if (!ok) break;
+      const int e = im.f * 128 + q * 32 + lane;
+      const float bias = (p.bias && e < p.E) ? __ldg(p.bias + e) : 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int col = hq * 128 + cc * 32 + jj;
+          if (col < im.rows && e < p.E)
+            p.logits[(im.row0 + col) * p.E + e] = p.bias ? acc[cc * 32 + jj] + bias : acc[cc * 32 + jj];
+        }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TC_TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
 // Exact three-way bf16 split of the FP32 router weight: Wr3[e] = [W1 | W2 | W3]
 // with W1 = rn(w), W2 = rn(w - W1), W3 = rn(w - W1 - W2).  Each residual is
 // exact in FP32 and holds at most 16 then 8 significant bits, so W3 captures
@@ -505,11 +668,13 @@ __global__ void split_router_weight_kernel(int64_t n, int H, const float *__rest
   row[2 * H + h] = w3;
 }
 
-// item_start[s] = sum_{s' < s} ceil(n_s' / 256) * nf_s', routed segments
-// with nf_routed M-tile pairs, the shared segment (n = T) with nf_shared.
+// Item prefixes of both grouped GEMMs (one block): start_x[s] = sum_{s' < s}
+// ceil(n_s' / 256) * nf_s', with nf the number of M-tile pairs of routed
+// segments (nf_*_r) and of the shared segment n_E = T (nf_*_s).
 __global__ void __launch_bounds__(1024)
-build_items_kernel(int E, int T, int nf_routed, int nf_shared, const int32_t *__restrict__ offsets,
-                   int32_t *__restrict__ item_start) {
+build_items_kernel(int E, int T, int nf_gu_r, int nf_gu_s, int nf_dn_r, int nf_dn_s,
+                   const int32_t *__restrict__ offsets, int32_t *__restrict__ start_gu,
+                   int32_t *__restrict__ start_dn) {
   __shared__ int32_t buf[1024];
   __shared__ int32_t carry;
   if (threadIdx.x == 0) carry = 0;
@@ -517,8 +682,8 @@ build_items_kernel(int E, int T, int nf_routed, int nf_shared, const int32_t *__
   for (int base = 0; base <= E; base += 1024) {
     const int s = base + threadIdx.x;
     int32_t v = 0;
-    if (s < E) v = (int32_t)ceil_div(offsets[s + 1] - offsets[s], 256) * nf_routed;
-    else if (s == E) v = (int32_t)ceil_div(T, 256) * nf_shared;
+    if (s < E) v = (int32_t)ceil_div(offsets[s + 1] - offsets[s], 256);
+    else if (s == E) v = (int32_t)ceil_div(T, 256);
     buf[threadIdx.x] = v;
     __syncthreads();
     for (int d = 1; d < 1024; d <<= 1) {
@@ -527,34 +692,49 @@ build_items_kernel(int E, int T, int nf_routed, int nf_shared, const int32_t *__
       buf[threadIdx.x] += add;
       __syncthreads();
     }
-    if (s <= E) item_start[s] = carry + buf[threadIdx.x] - v;
-    if (s == E) item_start[E + 1] = carry + buf[threadIdx.x];
+    // tiles before segment s (routed segments only; the shared one is last)
+    const int32_t before = carry + buf[threadIdx.x] - v;
+    if (s <= E) {
+      start_gu[s] = before * nf_gu_r;
+      start_dn[s] = before * nf_dn_r;
+    }
+    if (s == E) {
+      start_gu[E + 1] = before * nf_gu_r + v * nf_gu_s;
+      start_dn[E + 1] = before * nf_dn_r + v * nf_dn_s;
+    }
     __syncthreads();
     if (threadIdx.x == 1023) carry += buf[1023];
     __syncthreads();
   }
 }
 
-// items[it] = (segment, M-tile pair, first row, rows) for it < item_start[E+1]:
-// the rows of a segment are cut into ceil(n / 256) tiles of equal size
-// rounded up to 16, a cut that depends only on the segment's own length.
-__global__ void expand_items_kernel(int E, int T, int max_items, const int32_t *__restrict__ offsets,
-                                    const int32_t *__restrict__ item_start, int4 *__restrict__ items) {
-  const int total = min(item_start[E + 1], max_items);
-  for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < total; it += gridDim.x * blockDim.x) {
-    int lo = 0, hi = E;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (item_start[mid] <= it) lo = mid;
-      else hi = mid - 1;
-    }
-    const int local = it - item_start[lo];
-    const int base = lo == E ? 0 : offsets[lo];
-    const int n_s = lo == E ? T : offsets[lo + 1] - base;
-    const int ntile = (int)ceil_div(n_s, 256);
-    const int rpt = (int)round_up(ceil_div(n_s, ntile), 16);
-    const int nt = local % ntile;
-    items[it] = make_int4(lo, local / ntile, base + nt * rpt, min(rpt, n_s - nt * rpt));
+// items[it] = (segment, M-tile pair, first row, rows) for it < start[E+1], for
+// both tables: the rows of a segment are cut into ceil(n / 256) tiles of equal
+// size rounded up to 16, a cut that depends only on the segment's own length.
+__device__ inline void expand_item(int it, int E, int T, const int32_t *offsets, const int32_t *start,
+                                   int4 *items) {
+  int lo = 0, hi = E;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (start[mid] <= it) lo = mid;
+    else hi = mid - 1;
+  }
+  const int local = it - start[lo];
+  const int base = lo == E ? 0 : offsets[lo];
+  const int n_s = lo == E ? T : offsets[lo + 1] - base;
+  const int ntile = (int)ceil_div(n_s, 256);
+  const int rpt = (int)round_up(ceil_div(n_s, ntile), 16);
+  const int nt = local % ntile;
+  items[it] = make_int4(lo, local / ntile, base + nt * rpt, min(rpt, n_s - nt * rpt));
+}
+
+__global__ void expand_items_kernel(int E, int T, int max_gu, int max_dn, const int32_t *__restrict__ offsets,
+                                    const int32_t *__restrict__ start_gu, const int32_t *__restrict__ start_dn,
+                                    int4 *__restrict__ items_gu, int4 *__restrict__ items_dn) {
+  const int n_gu = min(start_gu[E + 1], max_gu), n_dn = min(start_dn[E + 1], max_dn);
+  for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < max(n_gu, n_dn); it += gridDim.x * blockDim.x) {
+    if (it < n_gu) expand_item(it, E, T, offsets, start_gu, items_gu);
+    if (it < n_dn) expand_item(it, E, T, offsets, start_dn, items_dn);
   }
 }
 
@@ -664,12 +844,19 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
   for (int h = 0; h < 5; ++h) m.b_sh[h] = m.b[h];
   TcParams p = {};
   p.T = T; p.H = H; p.E = E;
-  p.n_items = (int)(ceil_div(E, 128) * ceil_div(T, TcCfg<TC_ROUTER>::NMAX));
+  p.n_items = (int)(ceil_div(E, 128) * ceil_div(T, RT_NMAX));
   p.bias = bias;
   p.logits = logits;
   p.status = status;
-  const int grid = std::min(p.n_items, dev_info().sms);
-  return launch_tc<TC_ROUTER>(m, p, grid, stream);
+  DevInfo &di = dev_info();
+  if (!di.attr[0]) {
+    cudaError_t e = cudaFuncSetAttribute(tc_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    di.attr[0] = true;
+  }
+  const int grid = std::min(p.n_items, di.sms);
+  tc_router_kernel<<<grid, RT_THREADS, TC_SMEM_BYTES, stream>>>(m, p);
+  return cudaGetLastError();
 }
 
 // Upper bound on the items of a grouped GEMM: sum_s ceil(n_s / 256) <=
@@ -696,12 +883,10 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   int32_t *start_dn = (int32_t *)(w + starts);
   int4 *items_gu = (int4 *)(w + 2 * starts);
   int4 *items_dn = (int4 *)(w + 2 * starts + round256((size_t)mi_gu * 16));
-  build_items_kernel<<<1, 1024, 0, stream>>>(a.E, a.T, a.I / 128, a.Is / 128, a.offsets, start_gu);
-  build_items_kernel<<<1, 1024, 0, stream>>>(a.E, a.T, a.H / 256, a.H / 256, a.offsets, start_dn);
-  expand_items_kernel<<<(unsigned)std::min<int64_t>(ceil_div(mi_gu, 256), 1024), 256, 0, stream>>>(
-      a.E, a.T, mi_gu, a.offsets, start_gu, items_gu);
-  expand_items_kernel<<<(unsigned)std::min<int64_t>(ceil_div(mi_dn, 256), 1024), 256, 0, stream>>>(
-      a.E, a.T, mi_dn, a.offsets, start_dn, items_dn);
+  build_items_kernel<<<1, 1024, 0, stream>>>(a.E, a.T, a.I / 128, a.Is / 128, a.H / 256, a.H / 256, a.offsets,
+                                             start_gu, start_dn);
+  expand_items_kernel<<<(unsigned)std::min<int64_t>(ceil_div(std::max(mi_gu, mi_dn), 256), 1024), 256, 0, stream>>>(
+      a.E, a.T, mi_gu, mi_dn, a.offsets, start_gu, start_dn, items_gu, items_dn);
   const int64_t R = (int64_t)a.T * a.k;
   TcMaps mg, md;
   if (!map_gate_up(&mg.a, a.w_gate_up, a.E, a.I, a.H) || !map_gate_up(&mg.a_sh, a.ws_gate_up, 1, a.Is, a.H) ||

@@ -21,6 +21,7 @@ namespace moe {
 constexpr int CHUNK = 512;           // routes per warp
 constexpr int STEPS = CHUNK / 32;    // 32 routes per step
 constexpr int WARPS_PER_BLOCK = 4;
+constexpr int PAST_END = -0x7fffffff - 1;  // lane past the last route (not an id)
 
 size_t permute_scratch_bytes(int64_t R, int E) {
   int64_t n_chunks = ceil_div(R, CHUNK);
@@ -36,16 +37,21 @@ permute_count_kernel(int64_t R, int E, int n_chunks, const int32_t *__restrict__
   if (c >= n_chunks) return;
   int32_t *hist = smem + warp * E;
   for (int i = lane; i < E; i += 32) hist[i] = 0;
-  __syncwarp();
+  int eid[STEPS];  // all loads issued before the dependent match chain
+#pragma unroll
   for (int step = 0; step < STEPS; ++step) {
-    int64_t r = (int64_t)c * CHUNK + step * 32 + lane;
-    int e = -1;
-    if (r < R) {
-      e = ids[r];
-      if (e < 0 || e >= E) {
-        record_status(status, STATUS_BAD_EXPERT_ID);
-        e = -1;
-      }
+    const int64_t r = (int64_t)c * CHUNK + step * 32 + lane;
+    eid[step] = r < R ? __ldg(ids + r) : PAST_END;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int step = 0; step < STEPS; ++step) {
+    int e = eid[step];
+    if (e == PAST_END) {
+      e = -1;
+    } else if (e < 0 || e >= E) {
+      record_status(status, STATUS_BAD_EXPERT_ID);
+      e = -1;
     }
     unsigned peers = __match_any_sync(FULL_MASK, e);
     if (e >= 0 && lane == __ffs(peers) - 1) hist[e] += __popc(peers);
@@ -119,13 +125,17 @@ permute_scatter_kernel(int64_t R, int E, int n_chunks, const int32_t *__restrict
   for (int i = lane; i < E; i += 32) next[i] = offsets[i] + pre[i];
   __syncwarp();
   const unsigned lt = lanemask_lt();
+  int eid[STEPS];
+#pragma unroll
   for (int step = 0; step < STEPS; ++step) {
-    int64_t r = (int64_t)c * CHUNK + step * 32 + lane;
-    int e = -1;
-    if (r < R) {
-      e = ids[r];
-      if (e < 0 || e >= E) e = -1;
-    }
+    const int64_t r = (int64_t)c * CHUNK + step * 32 + lane;
+    eid[step] = r < R ? __ldg(ids + r) : -1;
+  }
+#pragma unroll
+  for (int step = 0; step < STEPS; ++step) {
+    const int64_t r = (int64_t)c * CHUNK + step * 32 + lane;
+    int e = eid[step];
+    if (e < 0 || e >= E) e = -1;
     unsigned peers = __match_any_sync(FULL_MASK, e);
     if (e >= 0) {
       int32_t pos = next[e] + __popc(peers & lt);

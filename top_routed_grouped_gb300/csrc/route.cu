@@ -79,12 +79,13 @@ cudaError_t launch_router_logits_simt(int T, int H, int E, const float *x, const
 // ---------------------------------------------------------------------------
 // Top-k + weights + shared gate, one warp per token.
 //
-// Candidate order: numbers before NaNs before already-taken slots; among
-// numbers the larger logit first; equal keys go to the lower expert id.
-// Each of the k rounds takes the lane-local best, then a butterfly arg-max
-// over the 32 lanes (the comparison is a strict total order, so the winner
-// does not depend on the reduction shape).  Slot s receives the s-th winner,
-// which is the stable descending order of the logits.
+// Each candidate expert e is ranked by (order value of its logit, -e):
+// numbers above NaNs above already-taken slots, larger logit first, equal
+// logits to the lower expert id.  Every lane keeps the best of its own
+// candidates; a round takes the warp maximum (a strict total order, so the
+// result does not depend on the reduction shape) and only the winning lane
+// rescans.  Slot s receives the s-th winner, which is the stable descending
+// order of the logits.
 //
 // Weights: w_s = exp(l_s - l_0) / sum_j exp(l_j - l_0) over the k selected
 // logits (l_0 is the largest), the softmax over all experts followed by
@@ -92,20 +93,31 @@ cudaError_t launch_router_logits_simt(int T, int H, int E, const float *x, const
 // Shared gate: z = x . w_sg, lane-partial sums in ascending h per lane, then
 // a fixed butterfly; sig = 1 / (1 + exp(-z)).
 // ---------------------------------------------------------------------------
-struct Cand {
-  int cls;  // 2 = number, 1 = NaN, 0 = taken / absent
-  float v;
-  int e;
-};
-
-__device__ inline bool better(const Cand &a, const Cand &b) {
-  if (a.cls != b.cls) return a.cls > b.cls;
-  if (a.v != b.v) return a.v > b.v;
-  return a.e < b.e;
+// Unsigned order of a logit: 0 = taken / absent, 1 = NaN, numbers above, a
+// larger logit giving a larger value (-0 and +0 map to the same value).
+__device__ inline uint32_t topk_ord(float l) {
+  if (l != l) return 1u;
+  const uint32_t u = __float_as_uint(l + 0.0f);  // -0 -> +0: equal logits must tie
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+__device__ inline float ord_logit(uint32_t o) {
+  if (o == 1u) return __uint_as_float(0x7FC00000u);  // NaN
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+// (o, e) ranks above (bo, be): larger order value, or equal and lower id.
+__device__ inline bool topk_better(uint32_t o, int e, uint32_t bo, int be) {
+  return o > bo || (o == bo && e < be);
+}
+
+// Order values are formed once per token; the gate operands are loaded in
+// small batches so that the kernel stays within 64 registers (four 256-thread
+// blocks per SM).
+constexpr int GATE_BATCH = 4;  // 16-byte chunks of x / w_sg loaded together per lane
+
 template <typename TX, int EPL>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, const TX *__restrict__ x,
                  const TX *__restrict__ wsg, int32_t *__restrict__ ids, float *__restrict__ w,
                  float *__restrict__ sig) {
@@ -113,71 +125,80 @@ topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, c
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
 
-  float v[EPL];
-  int cls[EPL];
-  const float *lrow = logits + t * E;
+  // Shared-expert gate: lane chunks h = (lane + 32 m) VN, m ascending, summed
+  // in that order per lane, then a fixed butterfly.
+  constexpr int VN = Vec16<TX>::N;
+  const TX *xr = x + t * (int64_t)H;
+  float part = 0.f;
+  for (int h0 = lane * VN; h0 < H; h0 += 32 * VN * GATE_BATCH) {
+    uint4 xa[GATE_BATCH], ga[GATE_BATCH];
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    int e = lane + 32 * i;
-    if (e < E) {
-      float l = lrow[e];
-      bool nan = l != l;
-      v[i] = nan ? -INFINITY : l;
-      cls[i] = nan ? 1 : 2;
-    } else {
-      v[i] = -INFINITY;
-      cls[i] = 0;
+    for (int i = 0; i < GATE_BATCH; ++i) {
+      const int h = h0 + 32 * VN * i;
+      if (h < H) {
+        xa[i] = __ldg(reinterpret_cast<const uint4 *>(xr + h));
+        ga[i] = __ldg(reinterpret_cast<const uint4 *>(wsg + h));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < GATE_BATCH; ++i) {
+      if (h0 + 32 * VN * i < H) {
+        float xv[VN], gv[VN];
+        Vec16<TX>::unpack(xa[i], xv);
+        Vec16<TX>::unpack(ga[i], gv);
+#pragma unroll
+        for (int j = 0; j < VN; ++j) part = fmaf(xv[j], gv[j], part);
+      }
     }
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(FULL_MASK, part, off);
+
+  // Top-k: order values formed once; the winner's owner zeroes its value and rescans.
+  uint32_t ov[EPL];
+  const float *lrow = logits + t * E;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) ov[i] = lane + 32 * i < E ? topk_ord(lrow[lane + 32 * i]) : 0u;
+  uint32_t bo = 0u;
+  int bi = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i)
+    if (ov[i] > bo) bo = ov[i], bi = i;  // ties keep the lower slot = lower id
 
   float sel_v = 0.f;  // lane s keeps the logit of slot s
   int sel_e = 0;
   for (int s = 0; s < k; ++s) {
-    Cand best{-1, -INFINITY, 0x7fffffff};
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      Cand c{cls[i], v[i], lane + 32 * i};
-      if (better(c, best)) best = c;
-    }
+    uint32_t mo = bo;
+    int me = lane + 32 * bi;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      Cand o;
-      o.cls = __shfl_xor_sync(FULL_MASK, best.cls, off);
-      o.v = __shfl_xor_sync(FULL_MASK, best.v, off);
-      o.e = __shfl_xor_sync(FULL_MASK, best.e, off);
-      if (better(o, best)) best = o;
+      const uint32_t oo = __shfl_xor_sync(FULL_MASK, mo, off);
+      const int oe = __shfl_xor_sync(FULL_MASK, me, off);
+      if (topk_better(oo, oe, mo, me)) mo = oo, me = oe;
     }
-#pragma unroll
-    for (int i = 0; i < EPL; ++i)
-      if (lane + 32 * i == best.e) cls[i] = 0;
     if (lane == s) {
-      sel_v = best.v;
-      sel_e = best.e;
+      sel_v = ord_logit(mo);
+      sel_e = me;
+    }
+    if (lane == (me & 31)) {  // the owner drops the winner and rescans
+      bo = 0u;
+      bi = 0;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        if (i == (me >> 5)) ov[i] = 0u;
+        if (ov[i] > bo) bo = ov[i], bi = i;
+      }
     }
   }
 
   // Route weights.  Every lane forms the same denominator in slot order.
-  const float m = __shfl_sync(FULL_MASK, sel_v, 0);
+  const float m0 = __shfl_sync(FULL_MASK, sel_v, 0);
   float z = 0.f;
-  for (int s = 0; s < k; ++s) z += expf(__shfl_sync(FULL_MASK, sel_v, s) - m);
+  for (int s = 0; s < k; ++s) z += expf(__shfl_sync(FULL_MASK, sel_v, s) - m0);
   if (lane < k) {
     ids[t * k + lane] = sel_e;
-    w[t * k + lane] = expf(sel_v - m) / z;
+    w[t * k + lane] = expf(sel_v - m0) / z;
   }
-
-  // Shared-expert gate.
-  constexpr int VN = Vec16<TX>::N;
-  const TX *xr = x + t * (int64_t)H;
-  float part = 0.f;
-  for (int h = lane * VN; h < H; h += 32 * VN) {
-    float xv[VN], gv[VN];
-    Vec16<TX>::load(xr + h, xv);
-    Vec16<TX>::load(wsg + h, gv);
-#pragma unroll
-    for (int j = 0; j < VN; ++j) part = fmaf(xv[j], gv[j], part);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(FULL_MASK, part, off);
   if (lane == 0) sig[t] = sigmoid_f32(part);
 }
 
