@@ -282,6 +282,9 @@ typedef struct moe_bwd_args {
   float *dw_shared_gate; /* [H] */
   float *dws_gate_up;    /* [2Is, H] */
   float *dws_down;       /* [H, Is] */
+  /* optional outputs (NULL: kept in the workspace) */
+  float *dlogit; /* [T, k] gradient of the k selected router logits, slot order */
+  float *dz;     /* [T] gradient of the shared-gate pre-activation x . w_shared_gate */
 } moe_bwd_args_t;
 
 /*
@@ -297,6 +300,11 @@ typedef struct moe_bwd_args {
  *   accumulated in FP32 in that order and cast once.  Weight gradients sum
  *   over their rows in ascending (expert-segment) order in FP32, with no
  *   split-K atomics.  Workspace: BACKWARD.
+ * Inputs are the forward's own results for the same x and weights (the
+ * routes are not recomputed); `saved` must hold all four activations.
+ * Weight gradients are float whatever the dtype; with T = 0 they are
+ * zero-filled.  Errors: MOE_ERR_INVALID_ARG for a NULL or misaligned buffer,
+ * MOE_ERR_WORKSPACE for a short workspace; nothing is launched then.
  */
 int moe_backward(const moe_dims_t *d, const moe_bwd_args_t *a, void *ws, size_t ws_bytes, void *stream);
 

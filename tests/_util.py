@@ -118,3 +118,46 @@ def bits(t: torch.Tensor) -> torch.Tensor:
     view = {torch.bfloat16: torch.int16, torch.float16: torch.int16, torch.float32: torch.int32,
             torch.int32: torch.int32}[t.dtype]
     return t.view(view).cpu()
+
+
+# ---------------------------------------------------------------- backward
+def grad_scale(ref) -> float:
+    """Scale of a gradient tensor for its max-abs bar: max(1, max|ref|).
+
+    Weight gradients are sums over up to T rows, so their entries grow like
+    the square root of the row count; the layer's max-abs bar (stated for
+    outputs of unit scale) is applied relative to that scale."""
+    r = np.asarray(ref, np.float64)
+    return max(1.0, float(np.max(np.abs(r)))) if r.size else 1.0
+
+
+def assert_grad_close(got, ref, what="", f32=False):
+    m, r = err_stats(got, ref)
+    s = grad_scale(ref)
+    if f32:
+        assert m <= F32_MAX_ABS * s, f"{what}: max_abs={m:.3e} scale={s:.3g}"
+    else:
+        assert m <= BF16_MAX_ABS * s and r <= BF16_REL_L2, f"{what}: max_abs={m:.3e} scale={s:.3g} rel_l2={r:.3e}"
+    print(f"{what}: max_abs={m:.3e} scale={s:.3g} rel_l2={r:.3e}")
+    return m, r
+
+
+def oracle_bwd_rows(x_rows, ids_rows, w_rows, sig_rows, dy_rows, W: dict):
+    """Oracle per-token backward (dx, dw, dlogit, dsig) of a few tokens at full
+    size, one token at a time with only its k experts widened to float64.
+    Local ids keep the ascending order of the global ids, so the oracle's
+    ascending-expert sum of the routed input gradients is unchanged."""
+    out = [[], [], [], []]
+    for t in range(x_rows.shape[0]):
+        e = np.asarray(ids_rows[t], dtype=np.int64)
+        srt = np.sort(e)
+        local = np.searchsorted(srt, e).astype(np.int32)[None, :]
+        idx = torch.as_tensor(srt)
+        g = lambda name: W[name].index_select(0, idx.to(W[name].device)).cpu()
+        r = oracle.backward_tokens(x_rows[t:t + 1], local, np.asarray(w_rows[t:t + 1]),
+                                   np.asarray(sig_rows[t:t + 1]), g("w_router"), W["w_shared_gate"].cpu(),
+                                   g("w_gate_up"), g("w_down"), W["ws_gate_up"].cpu(), W["ws_down"].cpu(),
+                                   dy_rows[t:t + 1])
+        for i in range(4):
+            out[i].append(r[i])
+    return tuple(np.concatenate(o) for o in out)

@@ -51,7 +51,7 @@ class BwdArgs(ctypes.Structure):
                                    "sorted_route", "route_pos", "y_routed", "y_shared")] + \
               [("saved", Saved)] + \
               [(n, _vp) for n in ("dy", "dx", "dw_gate_up", "dw_down", "dw_router", "dw_shared_gate",
-                                  "dws_gate_up", "dws_down")]
+                                  "dws_gate_up", "dws_down", "dlogit", "dz")]
 
 
 class MoEError(RuntimeError):
@@ -267,4 +267,32 @@ def forward(x, w_router, w_shared_gate, w_gate_up, w_down, ws_gate_up, ws_down, 
     args = dict(out, x=x, w_router=w_router, router_bias=router_bias, w_shared_gate=w_shared_gate,
                 w_gate_up=w_gate_up, w_down=w_down, ws_gate_up=ws_gate_up, ws_down=ws_down)
     moe_forward(d, args, workspace(d, "forward", dev), stream)
+    return out
+
+
+def backward(fwd: dict, dy, x, w_router, w_shared_gate, w_gate_up, w_down, ws_gate_up, ws_down, ws=None,
+             stream=None):
+    """Layer backward through ``moe_backward`` from the dict ``forward(..., save_for_backward=True)``
+    returned.  Returns dx, the six weight gradients (float) and dlogit [T,k], dz [T].
+    ``ws``: a caller-owned workspace (allocated here when None)."""
+    import torch
+    T, H = x.shape
+    k = fwd["topk_ids"].shape[1]
+    d = dims_of(x, w_router, w_gate_up, ws_gate_up, k)
+    dev, f32 = x.device, torch.float32
+    E, I, Is = d.E, d.I, d.Is
+    out = {"dx": torch.empty(T, H, dtype=x.dtype, device=dev),
+           "dw_gate_up": torch.empty(E, 2 * I, H, dtype=f32, device=dev),
+           "dw_down": torch.empty(E, H, I, dtype=f32, device=dev),
+           "dw_router": torch.empty(E, H, dtype=f32, device=dev),
+           "dw_shared_gate": torch.empty(H, dtype=f32, device=dev),
+           "dws_gate_up": torch.empty(2 * Is, H, dtype=f32, device=dev),
+           "dws_down": torch.empty(H, Is, dtype=f32, device=dev),
+           "dlogit": torch.empty(T, k, dtype=f32, device=dev),
+           "dz": torch.empty(T, dtype=f32, device=dev)}
+    args = dict(out, x=x, w_router=w_router, w_shared_gate=w_shared_gate, w_gate_up=w_gate_up, w_down=w_down,
+                ws_gate_up=ws_gate_up, ws_down=ws_down, dy=dy, saved=fwd["saved"],
+                **{n: fwd[n] for n in ("topk_ids", "topk_w", "shared_sig", "expert_offsets", "sorted_route",
+                                       "route_pos", "y_routed", "y_shared")})
+    moe_backward(d, args, workspace(d, "backward", dev) if ws is None else ws, stream)
     return out

@@ -123,9 +123,31 @@ static FwdScratch fwd_ws(const moe_dims_t *d, Carver &c) {
   return s;
 }
 
+struct BwdScratch {
+  void *dyr, *dys, *dgu_routed, *dgu_shared;
+  float *dxr, *dxs, *dlogit, *dz;
+  void *inner;
+};
+
+static BwdScratch bwd_ws(const moe_dims_t *d, Carver &c) {
+  BwdScratch s;
+  const int64_t T = d->T, R = T * d->k;
+  s.dyr = c.take((size_t)R * d->H * esize(d));
+  s.dys = c.take((size_t)T * d->H * esize(d));
+  s.dgu_routed = c.take((size_t)R * 2 * d->I * esize(d));
+  s.dgu_shared = c.take((size_t)T * 2 * d->Is * esize(d));
+  s.dxr = (float *)c.take((size_t)R * d->H * sizeof(float));
+  s.dxs = (float *)c.take((size_t)T * d->H * sizeof(float));
+  s.dlogit = (float *)c.take((size_t)R * sizeof(float));
+  s.dz = (float *)c.take((size_t)T * sizeof(float));
+  s.inner = c.take(backward_simt_scratch_bytes(d->E));
+  return s;
+}
+
 static size_t ws_size(const moe_dims_t *d, int op) {
   Carver c(nullptr);
   switch (op) {
+    case MOE_OP_BACKWARD: bwd_ws(d, c); break;
     case MOE_OP_ROUTE: route_ws(d, c); break;
     case MOE_OP_PERMUTE: permute_ws(d, c); break;
     case MOE_OP_GROUPED_FFN: ffn_ws(d, c); break;
@@ -267,10 +289,51 @@ MOE_API int moe_forward(const moe_dims_t *d, const moe_fwd_args_t *a, void *ws, 
 }
 
 MOE_API int moe_backward(const moe_dims_t *d, const moe_bwd_args_t *a, void *ws, size_t ws_bytes, void *stream) {
-  (void)a; (void)ws; (void)ws_bytes; (void)stream;
   int st = check_dims(d);
   if (st != MOE_OK) return st;
-  return MOE_ERR_UNSUPPORTED;
+  if (!a || !opt_ok(ws)) return MOE_ERR_INVALID_ARG;
+  const int64_t T = d->T, R = T * d->k, H = d->H, E = d->E, I = d->I, Is = d->Is;
+  if (!buf_ok(a->x, T * H) || !buf_ok(a->w_router, E * H) || !buf_ok(a->w_shared_gate, H) ||
+      !buf_ok(a->w_gate_up, 1) || !buf_ok(a->w_down, 1) || !buf_ok(a->ws_gate_up, 1) || !buf_ok(a->ws_down, 1) ||
+      !buf_ok(a->topk_ids, R) || !buf_ok(a->topk_w, R) || !buf_ok(a->shared_sig, T) ||
+      !buf_ok(a->expert_offsets, 1) || !buf_ok(a->sorted_route, R) || !buf_ok(a->route_pos, R) ||
+      !buf_ok(a->y_routed, R * H) || !buf_ok(a->y_shared, T * H) || !buf_ok(a->saved.gu, R * 2 * I) ||
+      !buf_ok(a->saved.h, R * I) || !buf_ok(a->saved.gu_shared, T * 2 * Is) || !buf_ok(a->saved.h_shared, T * Is) ||
+      !buf_ok(a->dy, T * H) || !buf_ok(a->dx, T * H) || !buf_ok(a->dw_gate_up, 1) || !buf_ok(a->dw_down, 1) ||
+      !buf_ok(a->dw_router, 1) || !buf_ok(a->dw_shared_gate, 1) || !buf_ok(a->dws_gate_up, 1) ||
+      !buf_ok(a->dws_down, 1) || !opt_ok(a->dlogit) || !opt_ok(a->dz))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_size(d, MOE_OP_BACKWARD)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (T == 0) {  // every weight gradient is an empty sum
+    const size_t f = sizeof(float);
+    const void *bufs[6] = {a->dw_gate_up, a->dw_down, a->dw_router, a->dw_shared_gate, a->dws_gate_up, a->dws_down};
+    const size_t bytes[6] = {(size_t)(E * 2 * I * H) * f, (size_t)(E * H * I) * f, (size_t)(E * H) * f,
+                             (size_t)H * f, (size_t)(2 * Is * H) * f, (size_t)(H * Is) * f};
+    for (int i = 0; i < 6; ++i) {
+      cudaError_t e = cudaMemsetAsync((void *)bufs[i], 0, bytes[i], s);
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+  }
+  Carver c(ws);
+  BwdScratch sc = bwd_ws(d, c);
+  BwArgs b;
+  b.T = d->T; b.H = d->H; b.E = d->E; b.k = d->k; b.I = d->I; b.Is = d->Is;
+  b.x = a->x; b.w_router = a->w_router; b.w_shared_gate = a->w_shared_gate;
+  b.w_gate_up = a->w_gate_up; b.w_down = a->w_down; b.ws_gate_up = a->ws_gate_up; b.ws_down = a->ws_down;
+  b.topk_ids = a->topk_ids; b.topk_w = a->topk_w; b.shared_sig = a->shared_sig;
+  b.offsets = a->expert_offsets; b.sorted_route = a->sorted_route; b.route_pos = a->route_pos;
+  b.y_routed = a->y_routed; b.y_shared = a->y_shared;
+  b.gu_routed = a->saved.gu; b.gu_shared = a->saved.gu_shared; b.h_routed = a->saved.h; b.h_shared = a->saved.h_shared;
+  b.dy = a->dy; b.dx = a->dx;
+  b.dw_gate_up = a->dw_gate_up; b.dw_down = a->dw_down; b.dw_router = a->dw_router;
+  b.dw_shared_gate = a->dw_shared_gate; b.dws_gate_up = a->dws_gate_up; b.dws_down = a->dws_down;
+  b.dyr = sc.dyr; b.dys = sc.dys; b.dgu_routed = sc.dgu_routed; b.dgu_shared = sc.dgu_shared;
+  b.dxr = sc.dxr; b.dxs = sc.dxs;
+  b.dlogit = a->dlogit ? a->dlogit : sc.dlogit;
+  b.dz = a->dz ? a->dz : sc.dz;
+  return cuda_status(launch_backward_simt(d->dtype, b, sc.inner, s));
 }
 
 MOE_API int moe_device_status(int reset, int32_t *detail) {

@@ -60,4 +60,34 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
 cudaError_t launch_combine(int dtype, int T, int H, int k, const void *y_routed, const void *y_shared,
                            const float *w, const float *sig, void *y, cudaStream_t stream);
 
+// ---- backward.cu ----
+struct BwArgs {
+  int T, H, E, k, I, Is;
+  // forward inputs and results
+  const void *x;
+  const float *w_router;
+  const void *w_shared_gate, *w_gate_up, *w_down, *ws_gate_up, *ws_down;
+  const int32_t *topk_ids;
+  const float *topk_w, *shared_sig;
+  const int32_t *offsets, *sorted_route, *route_pos;
+  const void *y_routed, *y_shared;
+  const void *gu_routed, *gu_shared, *h_routed, *h_shared;
+  const void *dy;
+  // outputs
+  void *dx;
+  float *dw_gate_up, *dw_down, *dw_router, *dw_shared_gate, *dws_gate_up, *dws_down;
+  // intermediates (workspace)
+  void *dyr;                    // [T*k, H] dtype, sorted order: w * dy of the route
+  void *dys;                    // [T, H] dtype: sig * dy
+  void *dgu_routed;             // [T*k, 2I] dtype, sorted order: [dg | du]
+  void *dgu_shared;             // [T, 2Is] dtype
+  float *dxr;                   // [T*k, H] sorted order: input grad of each route
+  float *dxs;                   // [T, H]: input grad through the shared expert
+  float *dlogit;                // [T, k]
+  float *dz;                    // [T]
+};
+size_t backward_simt_scratch_bytes(int E);
+// The whole backward on CUDA cores (dtype 0 = float, 1 = bf16).
+cudaError_t launch_backward_simt(int dtype, const BwArgs &a, void *scratch, cudaStream_t stream);
+
 }  // namespace moe
