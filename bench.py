@@ -13,6 +13,9 @@ Prints ONE JSON line (rank 0).  Keys beyond the basic contract:
   layer_roofline  the whole step against max(bytes/HBM, FLOPs/tensor peak)
   cpu_baseline the FP64 oracle on the host cores, on a bounded token sample
   clocks       nvidia-smi samples taken during the timed region
+  fwd_bwd      forward (activations saved) + backward at T=4096
+               (bf16_t4096_fwdbwd) through moe_forward / moe_backward, with
+               its own layer roofline (forward and backward bytes and FLOPs)
 
 --impl reference times the oracle itself (the reference arm) on the host.
 Multi-GPU (torchrun): every rank runs its own replica of the workload
@@ -33,6 +36,10 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "MoE layer tokens/sec (fwd, fwd+bwd) on 1 GB300; % of layer roofline"
+# Kernels one forward step launches: router weight split, router, top-k/gate;
+# permute count, chunk scan, expert scan, scatter; item tables (2), gate_up,
+# down; combine.
+LAUNCHES_PER_STEP = 12
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -69,35 +76,56 @@ def barrier(world: int) -> None:
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    """nvidia-smi samples of SM clock and throttle reasons during a region.
+
+    A reader thread timestamps each sample; start() returns once the first
+    sample has arrived, and only samples taken between begin() and end()
+    count."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
-        self.proc = None
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.idx, self.period = gpu_index, period_ms
+        self.proc, self.lines, self.t0, self.t1 = None, [], None, None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line))
 
     def start(self):
+        import threading
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+        deadline = time.perf_counter() + 5.0
+        while not self.lines and time.perf_counter() < deadline and self.proc.poll() is None:
+            time.sleep(0.01)
+
+    def begin(self):
+        self.t0 = time.perf_counter()
+
+    def end(self):
+        self.t1 = time.perf_counter()
 
     def stop(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for ts, line in list(self.lines):
+            if self.t0 is not None and not (self.t0 <= ts <= (self.t1 or ts)):
+                continue
             f = [x.strip() for x in line.split(",")]
             if len(f) < 8:
                 continue
@@ -111,6 +139,21 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# DRAM bytes (read + write) of one moe_grouped_ffn call (gate_up + down) at
+# bf16_t8192, from `ncu --set full` (profiles/grouped_ffn_bf16_t8192.md), valid
+# only for the kernel sources it was taken on (hash below); otherwise null.
+FFN_TRAFFIC = {"sources": "58c4de0163d7166f", "workload": "bf16_t8192",
+               "bytes": 2_347_057_000 + 59_947_264 + 1_315_282_000 + 317_399_296}
+
+
+def kernel_sources_hash() -> str:
+    import hashlib
+    csrc = os.path.join(ROOT, "top_routed_grouped_gb300", "csrc")
+    per = [hashlib.sha256(open(os.path.join(csrc, n), "rb").read()).hexdigest()
+           for n in ("gemm_tc.cu", "umma.cuh", "common.cuh")]
+    return hashlib.sha256("".join(per).encode()).hexdigest()[:16]
 
 
 def layer_bytes_flops(T, H, E, k, I, Is, active_experts, es=2) -> dict:
@@ -132,6 +175,71 @@ def ffn_bytes_flops(T, H, k, I, Is, active_experts, es=2) -> dict:
     w = active_experts * 3 * H * I * es + 3 * H * Is * es
     b = w + T * H * es + (R + T) * H * es + 2 * (R * I + T * Is) * es
     return {"bytes": b, "flops": 6 * H * I * R + 6 * H * Is * T}
+
+
+def bwd_bytes_flops(T, H, E, k, I, Is, es=2) -> dict:
+    """Algorithmic bytes and FLOPs of one layer backward.
+
+    FLOPs: twice the forward's (input and weight gradients): 12 H I per route
+    + 12 H Is per token (the router and gate gradients are not counted).
+    Bytes: every expert weight read once, every weight gradient written once
+    in FP32 (all E experts: empty ones are written as zeros), the router
+    weight read and its gradient written, x and dy read, dx written.
+    """
+    weights = E * 3 * H * I * es + 3 * H * Is * es + E * H * 4 + H * es
+    grads = (E * 3 * H * I + 3 * H * Is + E * H + H) * 4
+    return {"bytes": weights + grads + 3 * T * H * es, "flops": 12 * H * I * T * k + 12 * H * Is * T}
+
+
+def fwd_bwd_bench(cfg, dev_w, steps: int, warmup: int, world: int, peaks: dict) -> dict:
+    """Forward (activations saved) + backward of the layer through moe_forward
+    and moe_backward, inputs and upstream gradient resident in HBM."""
+    import torch
+    import top_routed_grouped_gb300 as moe
+    from top_routed_grouped_gb300 import inputs as I
+    T, H, E, k, Iw, Is = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.Is
+    x = I.normal((T, H), 0, I._STREAM["x"], 1.0, cfg.torch_dtype).cuda()
+    dy = I.normal((T, H), 2, I._STREAM["dy"], 1.0, cfg.torch_dtype).cuda()
+    wargs = [dev_w[n] for n in ("w_router", "w_shared_gate", "w_gate_up", "w_down", "ws_gate_up", "ws_down")]
+    d = moe.make_dims(T, H, E, k, Iw, Is, cfg.torch_dtype)
+    bws = moe.workspace(d, "backward")
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        f = moe.forward(x, *wargs, k, save_for_backward=True, stream=stream)
+        if ev: ev[1].record(stream)
+        moe.backward(f, dy, x, *wargs, ws=bws, stream=stream)
+        if ev: ev[2].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    moe.moe_device_status(reset=True)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    if moe.moe_device_status(reset=True) != 0:
+        raise RuntimeError("a kernel recorded a failed device-side check during the fwd+bwd region")
+    ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[2]) for e in evs), world)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    hbm, tf = float(peaks["hbm_gbs"]), float(peaks["bf16_tflops"])
+    fb = layer_bytes_flops(T, H, E, k, Iw, Is, E)
+    bb = bwd_bytes_flops(T, H, E, k, Iw, Is)
+    roof = lambda b: max(b["bytes"] / (hbm * 1e9), b["flops"] / (tf * 1e12)) * 1e3
+    t_roof = roof(fb) + roof(bb)
+    return {"workload": cfg.name, "T": T, "value": T * world / (ms * 1e-3), "unit": "tokens/s",
+            "ms_per_step": ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "steps": steps, "warmup": warmup,
+            "api": "moe_forward (activations saved) + moe_backward",
+            "gpu_launches_per_step": 20,
+            "layer_roofline": {"fwd_bytes": fb["bytes"], "fwd_flops": fb["flops"], "bwd_bytes": bb["bytes"],
+                               "bwd_flops": bb["flops"], "roofline_ms": t_roof, "frac": t_roof / ms,
+                               "bwd_roofline_ms": roof(bb), "bwd_frac": roof(bb) / bwd_ms}}
 
 
 def cpu_oracle_baseline(cfg, x_cpu, W_cpu, bias, budget_s: float = 12.0, max_tokens: int = 4096) -> dict:
@@ -190,11 +298,12 @@ def run_reference(args, cfg, rank: int) -> None:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="bf16_t8192")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fwd-bwd", action="store_true", help="skip the forward+backward measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -263,11 +372,13 @@ def main():
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
+    clocks.begin()
     start.record(stream)
     for i in range(args.steps):
         step(evs[i])
     end.record(stream)
     torch.cuda.synchronize()
+    clocks.end()
     clk = clocks.stop()
     barrier(world)
     ms_local = start.elapsed_time(end) / args.steps
@@ -320,9 +431,11 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2, "api": "moe_forward"},
-        "gpu_launches": 10 * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "roofline": {"kernel": "moe_grouped_ffn (gate_up+SwiGLU, down)", "bound": "hbm", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": FFN_TRAFFIC["bytes"] if (kernel_sources_hash() == FFN_TRAFFIC["sources"] and
+                                                        cfg.name == FFN_TRAFFIC["workload"]) else None,
                      "peak_source": peak_src, "ms_per_launch": ffn_ms,
                      "algorithmic_bytes": fb["bytes"]},
         "layer_roofline": {"bytes": lb["bytes"], "flops": lb["flops"], "roofline_ms": t_roof_ms,
@@ -330,6 +443,10 @@ def main():
                            "peak_source": peak_src},
         "clocks": clk,
     }
+    if not args.no_fwd_bwd and cfg.dtype == "bf16":
+        del o, ws, fws
+        torch.cuda.empty_cache()
+        line["fwd_bwd"] = fwd_bwd_bench(I.CONFIGS["bf16_t4096_fwdbwd"], dev, args.steps, args.warmup, world, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         W = {kk: v for kk, v in cpu.items() if kk not in ("x", "dy", "router_bias")}
         line["cpu_baseline"] = cpu_oracle_baseline(cfg, cpu["x"], W, cpu["router_bias"])
