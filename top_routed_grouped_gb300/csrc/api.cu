@@ -140,7 +140,7 @@ static BwdScratch bwd_ws(const moe_dims_t *d, Carver &c) {
   s.dxs = (float *)c.take((size_t)T * d->H * sizeof(float));
   s.dlogit = (float *)c.take((size_t)R * sizeof(float));
   s.dz = (float *)c.take((size_t)T * sizeof(float));
-  s.inner = c.take(backward_simt_scratch_bytes(d->E));
+  s.inner = c.take(backward_scratch_bytes(d->dtype, d->T, d->k, d->E, d->H, d->I, d->Is));
   return s;
 }
 
@@ -333,7 +333,7 @@ MOE_API int moe_backward(const moe_dims_t *d, const moe_bwd_args_t *a, void *ws,
   b.dxr = sc.dxr; b.dxs = sc.dxs;
   b.dlogit = a->dlogit ? a->dlogit : sc.dlogit;
   b.dz = a->dz ? a->dz : sc.dz;
-  return cuda_status(launch_backward_simt(d->dtype, b, sc.inner, s));
+  return cuda_status(launch_backward(d->dtype, b, sc.inner, device_status_ptr(), s));
 }
 
 MOE_API int moe_device_status(int reset, int32_t *detail) {

@@ -22,6 +22,8 @@
 //       accumulated in FP32 in that order, cast once.
 // Reductions over hidden use lane-partial sums in ascending h and a fixed
 // butterfly; reductions over a segment's rows run in ascending row order.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -397,35 +399,44 @@ __global__ void __launch_bounds__(256) dx_kernel(BwArgs a) {
 }
 
 // ---------------------------------------------------------------- launcher
-size_t backward_simt_scratch_bytes(int E) { return (size_t)(E + 2) * sizeof(int32_t); }
+size_t backward_scratch_bytes(int dtype, int T, int k, int E, int H, int I, int Is) {
+  const size_t tiles = (size_t)(E + 2) * sizeof(int32_t);
+  if (dtype != 0 && backward_tc_supported(H, I, Is)) return std::max(tiles, dgrad_tc_scratch_bytes(T, k, E, H, I, Is));
+  return tiles;
+}
 
 template <typename TE>
-static cudaError_t run_backward(const BwArgs &a, void *scratch, cudaStream_t stream) {
+static cudaError_t run_backward(const BwArgs &a, void *scratch, int *status, cudaStream_t stream) {
   const int64_t R = (int64_t)a.T * a.k;
   combine_bwd_kernel<TE><<<(unsigned)ceil_div(a.T, 8), 256, 0, stream>>>(
       a.T, a.H, a.k, (const TE *)a.dy, (const TE *)a.y_routed, (const TE *)a.y_shared, a.topk_w, a.shared_sig,
       a.route_pos, (TE *)a.dyr, (TE *)a.dys, a.dlogit, a.dz);
-  int32_t *tile_start = (int32_t *)scratch;
-  cudaError_t err = launch_build_tiles(a.E, a.T, BW_BM, a.offsets, tile_start, stream);
-  if (err != cudaSuccess) return err;
-  const int64_t max_tiles = ceil_div(R + a.T, BW_BM) + a.E + 1;
-  const unsigned gx = (unsigned)(max_tiles < 65535 ? max_tiles : 65535);
+  cudaError_t err;
   const int Imax = a.I > a.Is ? a.I : a.Is;
-  down_dgrad_swiglu_kernel<TE><<<dim3(gx, (unsigned)ceil_div(Imax, 64)), 256, 0, stream>>>(a, tile_start);
-  gate_up_dgrad_kernel<TE><<<dim3(gx, (unsigned)ceil_div(a.H, 64)), 256, 0, stream>>>(a, tile_start);
-  wgrad_kernel<TE, WG_DOWN><<<dim3((unsigned)ceil_div(Imax, 64), (unsigned)ceil_div(a.H, 64), a.E + 1), 256, 0,
-                              stream>>>(a);
-  wgrad_kernel<TE, WG_GATE_UP><<<dim3((unsigned)ceil_div(a.H, 64), (unsigned)ceil_div(2 * Imax, 64), a.E + 1),
-                                 256, 0, stream>>>(a);
+  if (sizeof(TE) == 2 && backward_tc_supported(a.H, a.I, a.Is)) {
+    if ((err = launch_dgrad_tc(a, scratch, status, stream)) != cudaSuccess) return err;
+    if ((err = launch_wgrad_tc(a, status, stream)) != cudaSuccess) return err;
+  } else {
+    int32_t *tile_start = (int32_t *)scratch;
+    if ((err = launch_build_tiles(a.E, a.T, BW_BM, a.offsets, tile_start, stream)) != cudaSuccess) return err;
+    const int64_t max_tiles = ceil_div(R + a.T, BW_BM) + a.E + 1;
+    const unsigned gx = (unsigned)(max_tiles < 65535 ? max_tiles : 65535);
+    down_dgrad_swiglu_kernel<TE><<<dim3(gx, (unsigned)ceil_div(Imax, 64)), 256, 0, stream>>>(a, tile_start);
+    gate_up_dgrad_kernel<TE><<<dim3(gx, (unsigned)ceil_div(a.H, 64)), 256, 0, stream>>>(a, tile_start);
+    wgrad_kernel<TE, WG_DOWN><<<dim3((unsigned)ceil_div(Imax, 64), (unsigned)ceil_div(a.H, 64), a.E + 1), 256, 0,
+                                stream>>>(a);
+    wgrad_kernel<TE, WG_GATE_UP><<<dim3((unsigned)ceil_div(a.H, 64), (unsigned)ceil_div(2 * Imax, 64), a.E + 1),
+                                   256, 0, stream>>>(a);
+  }
   router_gate_wgrad_kernel<TE><<<dim3((unsigned)ceil_div(a.H, 256), a.E + 1), 256, 0, stream>>>(a);
   dx_kernel<TE><<<(unsigned)ceil_div((int64_t)a.T * (a.H / Vec16<TE>::N), 256), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_backward_simt(int dtype, const BwArgs &a, void *scratch, cudaStream_t stream) {
+cudaError_t launch_backward(int dtype, const BwArgs &a, void *scratch, int *status, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
-  if (dtype == 0) return run_backward<float>(a, scratch, stream);
-  return run_backward<__nv_bfloat16>(a, scratch, stream);
+  if (dtype == 0) return run_backward<float>(a, scratch, status, stream);
+  return run_backward<__nv_bfloat16>(a, scratch, status, stream);
 }
 
 }  // namespace moe

@@ -39,10 +39,10 @@
 #include <cuda.h>
 
 #include <algorithm>
-#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_host.h"
 #include "umma.cuh"
 
 namespace moe {
@@ -739,93 +739,10 @@ __global__ void expand_items_kernel(int E, int T, int max_gu, int max_dn, const 
 }
 
 // ---------------------------------------------------------------- host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (EncodeTiledFn)p;
-  });
-  return fn;
-}
-
-// bf16 tensor map, 128-byte swizzle, box inner width 64 elements.
-static bool encode_map(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims, const uint64_t *strides_bytes,
-                       const uint32_t *box) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t gd[5], gs[4];
-  cuuint32_t bx[5], es[5];
-  for (int i = 0; i < rank; ++i) {
-    gd[i] = dims[i];
-    bx[i] = box[i];
-    es[i] = 1;
-    if (i + 1 < rank) gs[i] = strides_bytes[i];
-  }
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(ptr), gd, gs, bx, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Row-major [rows, cols] matrix, box = box_rows x 64.
-static bool map_2d(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, uint32_t box_rows) {
-  const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
-  const uint64_t strides[1] = {(uint64_t)cols * 2};
-  const uint32_t box[2] = {64, box_rows};
-  return encode_map(m, ptr, 2, dims, strides, box);
-}
-
-// The five token-tile maps of a row-major [rows, cols] matrix (box heights 256 .. 16).
-static bool map_rows(CUtensorMap *m5, const void *ptr, int64_t rows, int64_t cols) {
-  for (int h = 0; h < 5; ++h)
-    if (!map_2d(&m5[h], ptr, rows, cols, 256u >> h)) return false;
-  return true;
-}
-
-// Gate/up weights [n_mat, 2*Iw, H] viewed as 5-D (H, 16, 2, Iw/16, n_mat):
-// a box (64, 16, 2, 8, 1) holds, for 8 consecutive groups of 16 features
-// (two M tiles), the 16 gate rows followed by the 16 up rows of each group.
-static bool map_gate_up(CUtensorMap *m, const void *ptr, int n_mat, int Iw, int H) {
-  const uint64_t dims[5] = {(uint64_t)H, 16, 2, (uint64_t)Iw / 16, (uint64_t)n_mat};
-  const uint64_t strides[4] = {(uint64_t)H * 2, (uint64_t)Iw * H * 2, (uint64_t)16 * H * 2,
-                               (uint64_t)2 * Iw * H * 2};
-  const uint32_t box[5] = {64, 16, 2, 8, 1};
-  return encode_map(m, ptr, 5, dims, strides, box);
-}
-
-struct DevInfo {
-  int sms = 0;
-  bool attr[3] = {false, false, false};
-};
-
-static DevInfo &dev_info() {
-  static std::mutex mu;
-  static DevInfo info[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  std::lock_guard<std::mutex> lock(mu);
-  DevInfo &d = info[dev & 63];
-  if (!d.sms) cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-  return d;
-}
-
 template <int MODE>
 static cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream) {
-  DevInfo &di = dev_info();
-  if (!di.attr[MODE]) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TC_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    di.attr[MODE] = true;
-  }
+  cudaError_t e = ensure_smem((const void *)tc_gemm_kernel<MODE>, TC_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   tc_gemm_kernel<MODE><<<grid, tc_threads<MODE>(), TC_SMEM_BYTES, stream>>>(maps, p);
   return cudaGetLastError();
 }
@@ -848,21 +765,29 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
   p.bias = bias;
   p.logits = logits;
   p.status = status;
-  DevInfo &di = dev_info();
-  if (!di.attr[0]) {
-    cudaError_t e = cudaFuncSetAttribute(tc_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    di.attr[0] = true;
-  }
-  const int grid = std::min(p.n_items, di.sms);
+  cudaError_t e = ensure_smem((const void *)tc_router_kernel, TC_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int grid = std::min(p.n_items, device_sms());
   tc_router_kernel<<<grid, RT_THREADS, TC_SMEM_BYTES, stream>>>(m, p);
   return cudaGetLastError();
 }
 
 // Upper bound on the items of a grouped GEMM: sum_s ceil(n_s / 256) <=
 // ceil(R / 256) + E over the routed segments, ceil(T / 256) for the shared one.
-static int64_t max_items(int T, int k, int E, int nf_routed, int nf_shared) {
+int64_t tc_max_items(int T, int k, int E, int nf_routed, int nf_shared) {
   return (ceil_div((int64_t)T * k, 256) + E) * nf_routed + ceil_div(T, 256) * nf_shared;
+}
+static int64_t max_items(int T, int k, int E, int nf_routed, int nf_shared) {
+  return tc_max_items(T, k, E, nf_routed, nf_shared);
+}
+
+cudaError_t launch_item_tables(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s, const int32_t *offsets,
+                               int32_t *start_a, int32_t *start_b, int4 *items_a, int4 *items_b, int max_a,
+                               int max_b, cudaStream_t stream) {
+  build_items_kernel<<<1, 1024, 0, stream>>>(E, T, nf_a_r, nf_a_s, nf_b_r, nf_b_s, offsets, start_a, start_b);
+  expand_items_kernel<<<(unsigned)std::min<int64_t>(ceil_div(std::max(max_a, max_b), 256), 1024), 256, 0, stream>>>(
+      E, T, max_a, max_b, offsets, start_a, start_b, items_a, items_b);
+  return cudaGetLastError();
 }
 
 static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
@@ -883,10 +808,9 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   int32_t *start_dn = (int32_t *)(w + starts);
   int4 *items_gu = (int4 *)(w + 2 * starts);
   int4 *items_dn = (int4 *)(w + 2 * starts + round256((size_t)mi_gu * 16));
-  build_items_kernel<<<1, 1024, 0, stream>>>(a.E, a.T, a.I / 128, a.Is / 128, a.H / 256, a.H / 256, a.offsets,
-                                             start_gu, start_dn);
-  expand_items_kernel<<<(unsigned)std::min<int64_t>(ceil_div(std::max(mi_gu, mi_dn), 256), 1024), 256, 0, stream>>>(
-      a.E, a.T, mi_gu, mi_dn, a.offsets, start_gu, start_dn, items_gu, items_dn);
+  cudaError_t e0 = launch_item_tables(a.E, a.T, a.I / 128, a.Is / 128, a.H / 256, a.H / 256, a.offsets, start_gu,
+                                      start_dn, items_gu, items_dn, mi_gu, mi_dn, stream);
+  if (e0 != cudaSuccess) return e0;
   const int64_t R = (int64_t)a.T * a.k;
   TcMaps mg, md;
   if (!map_gate_up(&mg.a, a.w_gate_up, a.E, a.I, a.H) || !map_gate_up(&mg.a_sh, a.ws_gate_up, 1, a.Is, a.H) ||
@@ -906,7 +830,7 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   p.y_routed = (__nv_bfloat16 *)a.y_routed;
   p.y_shared = (__nv_bfloat16 *)a.y_shared;
   p.status = status;
-  const int grid = dev_info().sms;
+  const int grid = device_sms();
   p.item_start = start_gu;
   p.items = items_gu;
   cudaError_t e = launch_tc<TC_GATE_UP>(mg, p, grid, stream);

@@ -1,0 +1,690 @@
+// Tensor-core (tcgen05 / TMEM / TMA) GEMMs of the bf16 backward.
+//
+// RL-Kernel PR #557 "EP4 distributed logprob parity", embedded #503 commit
+// message "Backward": the per-expert GEMMs write per-route input gradients
+// into one dense buffer (summed per token in ascending expert order
+// elsewhere) and produce per-expert weight gradients; "Results (4 x H100)",
+// footnote 1: every reduction has a fixed order.  ROLL PR #502 "What this
+// changes": one K partition, no atomic split-K accumulation.
+//
+// Input gradients (persistent kernel tc_dgrad_kernel, items = 256 weight
+// features x up to 256 rows of one segment, like the forward):
+//   DGRAD_DOWN     D[i, j] = sum_h Wdn[e][h, i] dYr[j, h]       (K = H)
+//                  epilogue: the SwiGLU backward with the saved [g | u] of
+//                  row j, dg = dh u silu'(g), du = dh silu(g) -> dGU[j] (bf16)
+//   DGRAD_GATE_UP  D[h, j] = sum_f Wgu[e][f, h] dGU[j, f]       (K = 2I)
+//                  epilogue: dXr[j, h] in FP32
+// The weights are the M operand read MN-major straight from their storage
+// layout (one 3-D TMA box per stage: 4 blocks of 64 features x 64 K rows);
+// the gradient rows are the K-major N operand (TMA row boxes).
+//
+// Weight gradients (persistent kernel tc_wgrad_kernel, items = a 128 x 256
+// output tile of one segment, K = the segment's rows in ascending order):
+//   WGRAD_DOWN     dWdn[e][h, i] = sum_j dYr[j, h] h[j, i]
+//   WGRAD_GATE_UP  dWgu[e][f, h] = sum_j dGU[j, f] x[tok(j), h]
+// Both operands are MN-major (a row j of the activations is one K line);
+// rows past the segment's end in its last K block are zeroed in shared
+// memory before the MMAs read them, x rows are gathered by eight warps with
+// cp.async (zero-filled past the end).  Two TMEM accumulators alternate, so
+// the epilogue of one tile overlaps the MMAs of the next; the epilogue
+// stages 32 x 32 FP32 sub-tiles in shared memory and writes them with TMA
+// stores.  Empty segments get zero tiles (every output is written).
+//
+// Every output element is reduced over K in one fixed order (K blocks of
+// 64, four K = 16 MMAs each); the tiling decides where a value is written,
+// never the order of its sum.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_host.h"
+#include "umma.cuh"
+
+namespace moe {
+
+using namespace umma;
+
+constexpr int DGRAD_DOWN = 1, DGRAD_GATE_UP = 2;
+constexpr int WGRAD_DOWN = 1, WGRAD_GATE_UP = 2;
+
+constexpr int GT_EPI_FIRST = 2;  // epilogue warps start at warp 2
+constexpr uint32_t GT_TMEM_COLS = 512;
+
+__device__ inline bool gt_warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status) ? 1 : 0;
+  return __shfl_sync(FULL_MASK, ok, 0) != 0;
+}
+
+// ===========================================================================
+// Input gradients
+// ===========================================================================
+constexpr int DG_STAGES = 3, DG_EPI_WARPS = 8, DG_EPI_BYTES = 4096;
+constexpr int DG_A_BYTES = 4 * 8192;   // 4 blocks of 64 features x 64 K lines (two M tiles)
+constexpr int DG_B_BYTES = 256 * 128;  // up to 256 rows x 64 K
+constexpr int DG_THREADS = 32 * (GT_EPI_FIRST + DG_EPI_WARPS);
+constexpr int DG_SMEM = 1024 + DG_STAGES * (DG_A_BYTES + DG_B_BYTES) + DG_EPI_WARPS * DG_EPI_BYTES + 256;
+static_assert(DG_SMEM <= 232448, "dgrad shared memory");
+
+struct DgMaps {
+  CUtensorMap a, a_sh;        // weights, MN-major boxes (64, 64, 4)
+  CUtensorMap b[5], b_sh[5];  // gradient rows, box heights 256 .. 16
+};
+
+struct DgParams {
+  int T, H, E, k, I, Is;
+  const int32_t *item_start;
+  const int4 *items;
+  const __nv_bfloat16 *gu_routed, *gu_shared;  // DGRAD_DOWN: saved [g | u]
+  __nv_bfloat16 *dgu_routed, *dgu_shared;      // DGRAD_DOWN: out [dg | du]
+  float *dxr, *dxs;                            // DGRAD_GATE_UP: out
+  int *status;
+};
+
+struct DgItem {
+  int seg, f, rows, n, nk;
+  int64_t row0;
+};
+
+template <int MODE>
+__device__ inline DgItem dg_item(int it, const DgParams &p) {
+  const int4 d = __ldg(p.items + it);
+  DgItem r;
+  r.seg = d.x;
+  r.f = d.y;
+  r.row0 = d.z;
+  r.rows = d.w;
+  r.n = (int)round_up(r.rows, 16);
+  r.nk = (MODE == DGRAD_DOWN ? p.H : 2 * (r.seg == p.E ? p.Is : p.I)) / 64;
+  return r;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(DG_THREADS, 1)
+tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *sa = base;
+  uint8_t *sb = sa + DG_STAGES * DG_A_BYTES;
+  uint8_t *epi = sb + DG_STAGES * DG_B_BYTES;
+  uint64_t *bars = (uint64_t *)(epi + DG_EPI_WARPS * DG_EPI_BYTES);
+  uint64_t *full = bars, *empty = bars + DG_STAGES;
+  uint64_t *tfull = bars + 2 * DG_STAGES, *tempty = tfull + 1, *mma_done = tempty + 1;
+  uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
+  volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < DG_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 32 * DG_EPI_WARPS);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&maps.a);
+    prefetch_tmap(&maps.a_sh);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, GT_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int total = __ldg(p.item_start + p.E + 1);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_phase = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        const DgItem im = dg_item<MODE>(it, p);
+        const bool sh = im.seg == p.E;
+        const uint32_t bytes = DG_A_BYTES + im.n * 128;
+        // first weight row of this expert in the [E * rows, cols] view
+        const int wrow = sh ? 0 : im.seg * (MODE == DGRAD_DOWN ? p.H : 2 * p.I);
+        for (int kb = 0; kb < im.nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_3d(sa + stage * DG_A_BYTES, sh ? &maps.a_sh : &maps.a, &full[stage], 0, wrow + kb * 64, im.f * 4,
+                      pol_w);
+          uint8_t *b_dst = sb + stage * DG_B_BYTES;
+          const CUtensorMap *bm = sh ? maps.b_sh : maps.b;
+          int r = 0;
+#pragma unroll
+          for (int h = 0; h < 5; ++h) {
+            const int box = 256 >> h;
+            while (im.n - r >= box) {
+              tma_load_2d(b_dst + r * 128, &bm[h], &full[stage], kb * 64, (int)(im.row0 + r), pol_x);
+              r += box;
+            }
+          }
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == DG_STAGES) stage = 0, phase ^= 1;
+        }
+      }
+      if (!ok) {
+        volatile int never = 0;
+        for (int s = 0; s < DG_STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1, &never, nullptr, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        const DgItem im = dg_item<MODE>(it, p);
+        if (!mbar_wait(tempty, acc_phase ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(128, im.n) | IDESC_A_MN;
+        for (int kb = 0; kb < im.nk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t bd = smem_desc_sw128(smem_u32(sb + stage * DG_B_BYTES));
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            const uint64_t ad = smem_desc_mn_sw128(smem_u32(sa + stage * DG_A_BYTES + mt * 16384), 8192);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // K = 16: A +2048 bytes (MN-major), B +32 bytes (K-major)
+              mma_bf16(tmem + mt * 256, ad + 128 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == DG_STAGES) stage = 0, phase ^= 1;
+        }
+        if (!ok) break;
+        mma_commit(tfull);
+        acc_phase ^= 1;
+      }
+      mma_commit(mma_done);
+      volatile int never = 0;
+      mbar_wait(mma_done, 0, &never, p.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter
+    constexpr int CSTEP = 32 * (DG_EPI_WARPS / 4);
+    const int cfirst = 32 * ((warp - GT_EPI_FIRST) >> 2);
+    uint8_t *stg = epi + (warp - GT_EPI_FIRST) * DG_EPI_BYTES;
+    uint32_t acc_phase = 0;
+    for (int it = blockIdx.x; it < total; it += gridDim.x) {
+      const DgItem im = dg_item<MODE>(it, p);
+      const bool sh = im.seg == p.E;
+      if (!gt_warp_wait(tfull, acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+      for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
+        float vt[2][32];
+        tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[1]);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int f0 = im.f * 256 + mt * 128 + q * 32;  // first feature of this warp's 32
+          if (MODE == DGRAD_DOWN) {
+            // Lane = feature i, column c = row j.  Stage the 32 x 32 tiles of g
+            // and u of these rows (64 bytes per row each), compute dg, du in
+            // place, write the rows back as [dg | du].
+            const int Iseg = sh ? p.Is : p.I;
+            const __nv_bfloat16 *gu = sh ? p.gu_shared : p.gu_routed;
+            __nv_bfloat16 *dgu = sh ? p.dgu_shared : p.dgu_routed;
+            __nv_bfloat16 *G = (__nv_bfloat16 *)stg, *U = G + 32 * 32;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = (lane >> 2) + 8 * i, ch = lane & 3;
+              if (c0 + r < im.rows) {
+                const __nv_bfloat16 *src = gu + (im.row0 + c0 + r) * 2 * Iseg + f0 + ch * 8;
+                *(uint4 *)(G + r * 32 + ch * 8) = *(const uint4 *)src;
+                *(uint4 *)(U + r * 32 + ch * 8) = *(const uint4 *)(src + Iseg);
+              }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float g = __bfloat162float(G[c * 32 + lane]);
+              const float u = __bfloat162float(U[c * 32 + lane]);
+              const float s = sigmoid_f32(g);
+              const float dh = vt[mt][c];
+              G[c * 32 + lane] = __float2bfloat16_rn(dh * u * (s * (1.f + g * (1.f - s))));
+              U[c * 32 + lane] = __float2bfloat16_rn(dh * (g * s));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = (lane >> 2) + 8 * i, ch = lane & 3;
+              if (c0 + r < im.rows) {
+                __nv_bfloat16 *dst = dgu + (im.row0 + c0 + r) * 2 * Iseg + f0 + ch * 8;
+                *(uint4 *)dst = *(const uint4 *)(G + r * 32 + ch * 8);
+                *(uint4 *)(dst + Iseg) = *(const uint4 *)(U + r * 32 + ch * 8);
+              }
+            }
+            __syncwarp();
+          } else {
+            // Lane = hidden unit h, column c = row j: transpose through a
+            // 32 x 32 FP32 tile, then 128-byte row segments of dXr.
+            float *S = (float *)stg;
+            float *out = sh ? p.dxs : p.dxr;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) S[c * 32 + lane] = vt[mt][c];
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = (lane >> 3) + 4 * i, ch = lane & 7;
+              if (c0 + r < im.rows)
+                *(float4 *)(out + (im.row0 + c0 + r) * p.H + f0 + ch * 4) = *(const float4 *)(S + r * 32 + ch * 4);
+            }
+            __syncwarp();
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty);
+      acc_phase ^= 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, GT_TMEM_COLS);
+}
+
+// ===========================================================================
+// Weight gradients
+// ===========================================================================
+constexpr int WG_STAGES = 3, WG_EPI_WARPS = 8, WG_GATHER_WARPS = 8;
+constexpr int WG_A_BYTES = 2 * 8192;  // 128 M x 64 K lines, MN-major
+constexpr int WG_B_BYTES = 4 * 8192;  // 256 N x 64 K lines, MN-major
+constexpr int WG_STG_BYTES = 4096;    // one 32 x 32 FP32 store tile
+constexpr int WG_SMEM = 1024 + WG_STAGES * (WG_A_BYTES + WG_B_BYTES) + (2 * WG_EPI_WARPS + 1) * WG_STG_BYTES + 256;
+static_assert(WG_SMEM <= 232448, "wgrad shared memory");
+
+template <int MODE>
+constexpr int wg_gather_first() {
+  return GT_EPI_FIRST + WG_EPI_WARPS;
+}
+template <int MODE>
+constexpr int wg_threads() {
+  return 32 * (wg_gather_first<MODE>() + (MODE == WGRAD_GATE_UP ? WG_GATHER_WARPS : 0));
+}
+
+struct WgMaps {
+  CUtensorMap a, a_sh;      // A^T operand rows, MN-major boxes (64, 64, 2)
+  CUtensorMap b, b_sh;      // WGRAD_DOWN: h rows, boxes (64, 64, 4)
+  CUtensorMap out, out_sh;  // FP32 gradients, 32 x 32 boxes
+};
+
+struct WgParams {
+  int T, H, E, k, I, Is;
+  const int32_t *offsets, *sorted_route;
+  const __nv_bfloat16 *x;  // WGRAD_GATE_UP: gathered B rows
+  int tm_r, tn_r, tm_s, tn_s;  // output tiles per segment (M x N), routed and shared
+  int total;                   // tm_s * tn_s + E * tm_r * tn_r
+  int *status;
+};
+
+struct WgItem {
+  int seg, mt, nt, rows, nk;
+  int64_t r0;
+};
+
+// The shared segment's tiles come first (their K = T is the longest), then
+// the routed segments in expert order; inside a segment, M tiles major.
+__device__ inline WgItem wg_item(int it, const WgParams &p) {
+  WgItem r;
+  const int n_sh = p.tm_s * p.tn_s;
+  int local;
+  if (it < n_sh) {
+    r.seg = p.E;
+    local = it;
+    r.mt = local / p.tn_s;
+    r.nt = local % p.tn_s;
+    r.r0 = 0;
+    r.rows = p.T;
+  } else {
+    const int per = p.tm_r * p.tn_r;
+    r.seg = (it - n_sh) / per;
+    local = (it - n_sh) % per;
+    r.mt = local / p.tn_r;
+    r.nt = local % p.tn_r;
+    r.r0 = __ldg(p.offsets + r.seg);
+    r.rows = __ldg(p.offsets + r.seg + 1) - (int)r.r0;
+  }
+  r.nk = (int)ceil_div(r.rows, 64);
+  return r;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(wg_threads<MODE>(), 1)
+tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
+  constexpr int GATHER_FIRST = wg_gather_first<MODE>();
+  constexpr int GATHER_THREADS = 32 * WG_GATHER_WARPS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *sa = base;
+  uint8_t *sb = sa + WG_STAGES * WG_A_BYTES;
+  uint8_t *stg_all = sb + WG_STAGES * WG_B_BYTES;
+  uint8_t *zero_tile = stg_all + 2 * WG_EPI_WARPS * WG_STG_BYTES;
+  uint64_t *bars = (uint64_t *)(zero_tile + WG_STG_BYTES);
+  uint64_t *full = bars, *empty = bars + WG_STAGES;
+  uint64_t *tfull = bars + 2 * WG_STAGES, *tempty = tfull + 2, *mma_done = tempty + 2;
+  uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
+  volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < WG_STG_BYTES / 16; i += blockDim.x) ((uint4 *)zero_tile)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < WG_STAGES; ++s) {
+      mbar_init(&full[s], 1 + (MODE == WGRAD_GATE_UP ? GATHER_THREADS : 0));
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 32 * WG_EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&maps.a);
+    prefetch_tmap(&maps.a_sh);
+    prefetch_tmap(&maps.out);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, GT_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();  // rows are read by every tile of their segment
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_phase = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < p.total && ok; it += gridDim.x) {
+        const WgItem im = wg_item(it, p);
+        const bool sh = im.seg == p.E;
+        const uint32_t bytes = WG_A_BYTES + (MODE == WGRAD_DOWN ? WG_B_BYTES : 0);
+        for (int kb = 0; kb < im.nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          const int row = (int)im.r0 + kb * 64;
+          tma_load_3d(sa + stage * WG_A_BYTES, sh ? &maps.a_sh : &maps.a, &full[stage], 0, row, im.mt * 2, pol);
+          if (MODE == WGRAD_DOWN)
+            tma_load_3d(sb + stage * WG_B_BYTES, sh ? &maps.b_sh : &maps.b, &full[stage], 0, row, im.nt * 4, pol);
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == WG_STAGES) stage = 0, phase ^= 1;
+        }
+      }
+      if (!ok) {
+        volatile int never = 0;
+        for (int s = 0; s < WG_STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1, &never, nullptr, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (whole warp: tail zeroing)
+    int stage = 0;
+    uint32_t phase = 0, cnt = 0;
+    bool ok = true;
+    const uint32_t idesc = idesc_bf16_f32(128, 256) | IDESC_A_MN | IDESC_B_MN;
+    for (int it = blockIdx.x; it < p.total && ok; it += gridDim.x) {
+      const WgItem im = wg_item(it, p);
+      if (im.rows == 0) continue;
+      const int b = cnt & 1;
+      if (!gt_warp_wait(&tempty[b], ((cnt >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      for (int kb = 0; kb < im.nk; ++kb) {
+        if (!gt_warp_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+        const int valid = min(64, im.rows - kb * 64);
+        if (valid < 64) {
+          // Lines [valid, 64) of every 64-line block hold rows of the next
+          // segment (or TMA zero fill): clear them for both operands.
+          const int lines = 64 - valid;
+          const int na = WG_A_BYTES / 8192, nbk = MODE == WGRAD_DOWN ? WG_B_BYTES / 8192 : 0;
+          for (int blk = 0; blk < na + nbk; ++blk) {
+            uint8_t *dst = blk < na ? sa + stage * WG_A_BYTES + blk * 8192 : sb + stage * WG_B_BYTES + (blk - na) * 8192;
+            dst += valid * 128;
+            for (int i = lane; i < lines * 8; i += 32) ((uint4 *)dst)[i] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint64_t ad = smem_desc_mn_sw128(smem_u32(sa + stage * WG_A_BYTES), 8192);
+          const uint64_t bd = smem_desc_mn_sw128(smem_u32(sb + stage * WG_B_BYTES), 8192);
+          const int nkk = (valid + 15) >> 4;
+          for (int kk = 0; kk < nkk; ++kk)
+            mma_bf16(tmem + b * 256, ad + 128 * kk, bd + 128 * kk, idesc, (kb | kk) != 0);
+          mma_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == WG_STAGES) stage = 0, phase ^= 1;
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&tfull[b]);
+      __syncwarp();
+      ++cnt;
+    }
+    if (lane == 0) {
+      mma_commit(mma_done);
+      volatile int never = 0;
+      mbar_wait(mma_done, 0, &never, p.status);
+    }
+    __syncwarp();
+  } else if (warp < GATHER_FIRST) {
+    // ------------------------------------------------------------ epilogue
+    // Warp (q, half): TMEM lanes 32q.. (output rows), columns [128 half, +128).
+    const int q = warp & 3, half = (warp - GT_EPI_FIRST) >> 2;
+    uint8_t *stg0 = stg_all + (warp - GT_EPI_FIRST) * 2 * WG_STG_BYTES;
+    uint32_t cnt = 0, sbuf = 0;
+    const int Mr = MODE == WGRAD_DOWN ? p.H : 2 * p.I;  // output rows per routed expert
+    for (int it = blockIdx.x; it < p.total; it += gridDim.x) {
+      const WgItem im = wg_item(it, p);
+      const bool sh = im.seg == p.E;
+      const CUtensorMap *om = sh ? &maps.out_sh : &maps.out;
+      const int mrow = (sh ? 0 : im.seg * Mr) + im.mt * 128 + q * 32;
+      const int ncol = im.nt * 256 + half * 128;
+      if (im.rows == 0) {
+        if (lane == 0) {
+          for (int cc = 0; cc < 4; ++cc) tma_store_2d(om, zero_tile, ncol + cc * 32, mrow);
+          bulk_commit();
+        }
+        __syncwarp();
+        continue;
+      }
+      const int b = cnt & 1;
+      if (!gt_warp_wait(&tfull[b], (cnt >> 1) & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem + b * 256 + ((uint32_t)(q * 32) << 16) + half * 128;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        float v[32];
+        tmem_ld32(tb + cc * 32, v);
+        uint8_t *stg = stg0 + sbuf * WG_STG_BYTES;
+        if (lane == 0) bulk_wait_read<1>();  // the store issued from this buffer two tiles ago has read it
+        __syncwarp();
+        // Row `lane` of the 32 x 32 tile: 16-byte chunk j at (j ^ (lane % 8)), the 128-byte swizzle.
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *(float4 *)(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(om, stg, ncol + cc * 32, mrow);
+          bulk_commit();
+        }
+        sbuf ^= 1;
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[b]);
+      ++cnt;
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  } else if (MODE == WGRAD_GATE_UP) {
+    // ------------------------------------------------------------ x row gather (MN-major B)
+    // Warp g fills K lines kr = g + 8 i (i < 8) of a stage: lane = (block mb
+    // of 64 hidden units, 16-byte chunk ch), written at chunk position
+    // (ch ^ kr % 8) of line kr in block mb; lines past the segment are zeros.
+    const int g = warp - GATHER_FIRST;
+    const int mb = lane >> 3, ch = lane & 7;
+    int stage = 0, arr_stage = 0, pending = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.total && ok; it += gridDim.x) {
+      const WgItem im = wg_item(it, p);
+      if (im.rows == 0) continue;
+      const bool sh = im.seg == p.E;
+      const int h0 = im.nt * 256 + mb * 64 + ch * 8;
+      for (int kb = 0; kb < im.nk; ++kb) {
+        int tokv = -1;
+        if (lane < 8) {
+          const int j = kb * 64 + g + 8 * lane;
+          if (j < im.rows) tokv = sh ? (int)im.r0 + j : __ldg(p.sorted_route + im.r0 + j) / p.k;
+        }
+        if (!gt_warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+        const uint32_t bsm = smem_u32(sb + stage * WG_B_BYTES) + mb * 8192;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int tok = __shfl_sync(FULL_MASK, tokv, i);
+          const int kr = g + 8 * i;
+          const uint32_t dst = bsm + kr * 128 + ((ch ^ (kr & 7)) << 4);
+          if (tok >= 0) cp_async_16(dst, p.x + (int64_t)tok * p.H + h0);
+          else cp_async_16_zfill(dst, p.x, 0);
+        }
+        cp_async_commit();
+        if (++pending > 1) {
+          cp_async_wait<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(&full[arr_stage]);
+          if (++arr_stage == WG_STAGES) arr_stage = 0;
+          --pending;
+        }
+        if (++stage == WG_STAGES) stage = 0, phase ^= 1;
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    if (ok)
+      for (; pending > 0; --pending) {
+        mbar_arrive(&full[arr_stage]);
+        if (++arr_stage == WG_STAGES) arr_stage = 0;
+      }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, GT_TMEM_COLS);
+}
+
+// ===========================================================================
+// Host side
+// ===========================================================================
+bool backward_tc_supported(int H, int I, int Is) { return H % 256 == 0 && I % 256 == 0 && Is % 256 == 0; }
+
+size_t dgrad_tc_scratch_bytes(int T, int k, int E, int H, int I, int Is) {
+  const size_t starts = (size_t)round_up((E + 2) * 4, 256);
+  return 2 * starts + (size_t)round_up(tc_max_items(T, k, E, I / 256, Is / 256) * 16, 256) +
+         (size_t)round_up(tc_max_items(T, k, E, H / 256, H / 256) * 16, 256);
+}
+
+cudaError_t launch_dgrad_tc(const BwArgs &a, void *scratch, int *status, cudaStream_t stream) {
+  const size_t starts = (size_t)round_up((a.E + 2) * 4, 256);
+  const int mi_dn = (int)tc_max_items(a.T, a.k, a.E, a.I / 256, a.Is / 256);
+  const int mi_gu = (int)tc_max_items(a.T, a.k, a.E, a.H / 256, a.H / 256);
+  uint8_t *w = (uint8_t *)scratch;
+  int32_t *start_dn = (int32_t *)w;
+  int32_t *start_gu = (int32_t *)(w + starts);
+  int4 *items_dn = (int4 *)(w + 2 * starts);
+  int4 *items_gu = (int4 *)(w + 2 * starts + round_up((int64_t)mi_dn * 16, 256));
+  cudaError_t e = launch_item_tables(a.E, a.T, a.I / 256, a.Is / 256, a.H / 256, a.H / 256, a.offsets, start_dn,
+                                     start_gu, items_dn, items_gu, mi_dn, mi_gu, stream);
+  if (e != cudaSuccess) return e;
+  const int64_t R = (int64_t)a.T * a.k;
+  DgMaps md, mg;
+  if (!map_col_blocks(&md.a, a.w_down, (int64_t)a.E * a.H, a.I, 64, 4) ||
+      !map_col_blocks(&md.a_sh, a.ws_down, a.H, a.Is, 64, 4) || !map_rows(md.b, a.dyr, R, a.H) ||
+      !map_rows(md.b_sh, a.dys, a.T, a.H) ||
+      !map_col_blocks(&mg.a, a.w_gate_up, (int64_t)a.E * 2 * a.I, a.H, 64, 4) ||
+      !map_col_blocks(&mg.a_sh, a.ws_gate_up, 2 * (int64_t)a.Is, a.H, 64, 4) ||
+      !map_rows(mg.b, a.dgu_routed, R, 2 * (int64_t)a.I) || !map_rows(mg.b_sh, a.dgu_shared, a.T, 2 * (int64_t)a.Is))
+    return cudaErrorInvalidValue;
+  DgParams p = {};
+  p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k; p.I = a.I; p.Is = a.Is;
+  p.gu_routed = (const __nv_bfloat16 *)a.gu_routed;
+  p.gu_shared = (const __nv_bfloat16 *)a.gu_shared;
+  p.dgu_routed = (__nv_bfloat16 *)a.dgu_routed;
+  p.dgu_shared = (__nv_bfloat16 *)a.dgu_shared;
+  p.dxr = a.dxr;
+  p.dxs = a.dxs;
+  p.status = status;
+  const int grid = device_sms();
+  if ((e = ensure_smem((const void *)tc_dgrad_kernel<DGRAD_DOWN>, DG_SMEM)) != cudaSuccess) return e;
+  if ((e = ensure_smem((const void *)tc_dgrad_kernel<DGRAD_GATE_UP>, DG_SMEM)) != cudaSuccess) return e;
+  p.item_start = start_dn;
+  p.items = items_dn;
+  tc_dgrad_kernel<DGRAD_DOWN><<<grid, DG_THREADS, DG_SMEM, stream>>>(md, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  p.item_start = start_gu;
+  p.items = items_gu;
+  tc_dgrad_kernel<DGRAD_GATE_UP><<<grid, DG_THREADS, DG_SMEM, stream>>>(mg, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wgrad_tc(const BwArgs &a, int *status, cudaStream_t stream) {
+  const int64_t R = (int64_t)a.T * a.k;
+  WgMaps md, mg;
+  // Row counts of the A / B maps are at least 1 so that an empty batch still encodes.
+  const int64_t Rm = std::max<int64_t>(R, 1), Tm = std::max(a.T, 1);
+  if (!map_col_blocks(&md.a, a.dyr, Rm, a.H, 64, 2) || !map_col_blocks(&md.a_sh, a.dys, Tm, a.H, 64, 2) ||
+      !map_col_blocks(&md.b, a.h_routed, Rm, a.I, 64, 4) || !map_col_blocks(&md.b_sh, a.h_shared, Tm, a.Is, 64, 4) ||
+      !map_f32_tile(&md.out, a.dw_down, (int64_t)a.E * a.H, a.I) || !map_f32_tile(&md.out_sh, a.dws_down, a.H, a.Is) ||
+      !map_col_blocks(&mg.a, a.dgu_routed, Rm, 2 * (int64_t)a.I, 64, 2) ||
+      !map_col_blocks(&mg.a_sh, a.dgu_shared, Tm, 2 * (int64_t)a.Is, 64, 2) ||
+      !map_f32_tile(&mg.out, a.dw_gate_up, (int64_t)a.E * 2 * a.I, a.H) ||
+      !map_f32_tile(&mg.out_sh, a.dws_gate_up, 2 * (int64_t)a.Is, a.H))
+    return cudaErrorInvalidValue;
+  mg.b = mg.a;  // the gate_up B operand is gathered with cp.async
+  mg.b_sh = mg.a_sh;
+  WgParams p = {};
+  p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k; p.I = a.I; p.Is = a.Is;
+  p.offsets = a.offsets;
+  p.sorted_route = a.sorted_route;
+  p.x = (const __nv_bfloat16 *)a.x;
+  p.status = status;
+  const int sms = device_sms();
+  cudaError_t e;
+  if ((e = ensure_smem((const void *)tc_wgrad_kernel<WGRAD_DOWN>, WG_SMEM)) != cudaSuccess) return e;
+  if ((e = ensure_smem((const void *)tc_wgrad_kernel<WGRAD_GATE_UP>, WG_SMEM)) != cudaSuccess) return e;
+  // down: M = H, N = I
+  p.tm_r = a.H / 128; p.tn_r = a.I / 256; p.tm_s = a.H / 128; p.tn_s = a.Is / 256;
+  p.total = p.tm_s * p.tn_s + a.E * p.tm_r * p.tn_r;
+  tc_wgrad_kernel<WGRAD_DOWN><<<std::min(p.total, sms), wg_threads<WGRAD_DOWN>(), WG_SMEM, stream>>>(md, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // gate_up: M = 2I, N = H
+  p.tm_r = 2 * a.I / 128; p.tn_r = a.H / 256; p.tm_s = 2 * a.Is / 128; p.tn_s = a.H / 256;
+  p.total = p.tm_s * p.tn_s + a.E * p.tm_r * p.tn_r;
+  tc_wgrad_kernel<WGRAD_GATE_UP><<<std::min(p.total, sms), wg_threads<WGRAD_GATE_UP>(), WG_SMEM, stream>>>(mg, p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -55,6 +55,13 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
 size_t ffn_tc_scratch_bytes(int T, int k, int E, int H, int I, int Is);
 // gate_up + SwiGLU and down as two persistent tcgen05 grouped GEMMs (scratch: ffn_tc_scratch_bytes).
 cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStream_t stream);
+// Item tables of two grouped GEMMs over the same segments: per segment,
+// ceil(n_s / 256) token tiles times nf_*_r (routed) or nf_*_s (shared) M-tile
+// pairs; items = int4 (segment, pair, first row, rows).
+int64_t tc_max_items(int T, int k, int E, int nf_routed, int nf_shared);
+cudaError_t launch_item_tables(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s, const int32_t *offsets,
+                               int32_t *start_a, int32_t *start_b, int4 *items_a, int4 *items_b, int max_a,
+                               int max_b, cudaStream_t stream);
 
 // ---- combine.cu ----
 cudaError_t launch_combine(int dtype, int T, int H, int k, const void *y_routed, const void *y_shared,
@@ -86,8 +93,17 @@ struct BwArgs {
   float *dlogit;                // [T, k]
   float *dz;                    // [T]
 };
-size_t backward_simt_scratch_bytes(int E);
-// The whole backward on CUDA cores (dtype 0 = float, 1 = bf16).
-cudaError_t launch_backward_simt(int dtype, const BwArgs &a, void *scratch, cudaStream_t stream);
+size_t backward_scratch_bytes(int dtype, int T, int k, int E, int H, int I, int Is);
+// The backward (dtype 0 = float, 1 = bf16): the four expert GEMMs on the
+// tensor cores for bf16 when backward_tc_supported, else on CUDA cores.
+cudaError_t launch_backward(int dtype, const BwArgs &a, void *scratch, int *status, cudaStream_t stream);
+
+// ---- grad_tc.cu (bf16 tensor-core backward GEMMs) ----
+bool backward_tc_supported(int H, int I, int Is);
+size_t dgrad_tc_scratch_bytes(int T, int k, int E, int H, int I, int Is);
+// dGU = SwiGLU-backward(dYr Wdn) and dXr = dGU Wgu (and the shared expert's) (scratch: dgrad_tc_scratch_bytes).
+cudaError_t launch_dgrad_tc(const BwArgs &a, void *scratch, int *status, cudaStream_t stream);
+// dWdn, dWgu and the shared expert's weight gradients.
+cudaError_t launch_wgrad_tc(const BwArgs &a, int *status, cudaStream_t stream);
 
 }  // namespace moe

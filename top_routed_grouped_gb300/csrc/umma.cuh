@@ -1,8 +1,9 @@
 // Inline-PTX wrappers for the sm_103a tensor-core path: mbarriers (with
 // bounded waits), TMA tile / gather4 loads, tensor memory (TMEM) allocation
 // and loads, and tcgen05.mma with its shared-memory and instruction
-// descriptors.  Only the operand formats the MoE kernels use are covered:
-// bf16 A and B, K-major, 128-byte swizzle, FP32 accumulator, M = 128.
+// descriptors, TMA tile stores.  Only the operand formats the MoE kernels
+// use are covered: bf16 A and B, K-major or MN-major, 128-byte swizzle,
+// FP32 accumulator, M = 128.
 #pragma once
 
 #include <cuda.h>
@@ -121,10 +122,28 @@ __device__ inline void tma_gather4(void *dst, const CUtensorMap *m, uint64_t *ba
       : "memory");
 }
 
+// Tile store shared -> global through a tensor map (bulk-group completion).
+__device__ inline void tma_store_2d(const CUtensorMap *m, const void *src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(m), "r"(c0),
+               "r"(c1), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ inline void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N committed bulk groups still read their shared-memory source.
+template <int N>
+__device__ inline void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+// Wait until at most N committed bulk groups are incomplete (writes done).
+template <int N>
+__device__ inline void bulk_wait() { asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory"); }
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy through L2 (LSU path, generic proxy).
 __device__ inline void cp_async_16(uint32_t dst_smem, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+// The same copy reading only `src_bytes` (0 or 16) bytes; the rest is zero-filled.
+__device__ inline void cp_async_16_zfill(uint32_t dst_smem, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ inline void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -198,6 +217,16 @@ __device__ inline uint64_t smem_desc_sw128(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
+
+// Descriptor of an MN-major bf16 tile with the 128-byte swizzle: blocks of
+// 64 MN elements (128-byte lines, one per K index) `lbo` bytes apart along
+// MN, 8-line K groups 1024 bytes apart.  A K = 16 step is +2048 bytes.
+__device__ inline uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t lbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction-descriptor bits that mark A / B as MN-major.
+constexpr uint32_t IDESC_A_MN = 1u << 15, IDESC_B_MN = 1u << 16;
 
 // Instruction descriptor, kind::f16: FP32 accumulator (bits 4-5 = 1), A and
 // B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
