@@ -304,6 +304,8 @@ def main():
     ap.add_argument("--workload", default="bf16_t8192")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fwd-bwd", action="store_true", help="skip the forward+backward measurement")
+    ap.add_argument("--fwd-bwd-workload", default="bf16_t4096_fwdbwd",
+                    help="workload of the forward+backward measurement (same layer shape as --workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -446,7 +448,9 @@ def main():
     if not args.no_fwd_bwd and cfg.dtype == "bf16":
         del o, ws, fws
         torch.cuda.empty_cache()
-        line["fwd_bwd"] = fwd_bwd_bench(I.CONFIGS["bf16_t4096_fwdbwd"], dev, args.steps, args.warmup, world, peaks)
+        fb_cfg = I.CONFIGS[args.fwd_bwd_workload]
+        assert (fb_cfg.H, fb_cfg.E, fb_cfg.I, fb_cfg.Is) == (H, E, Iw, Is), "fwd+bwd workload must share the layer"
+        line["fwd_bwd"] = fwd_bwd_bench(fb_cfg, dev, args.steps, args.warmup, world, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         W = {kk: v for kk, v in cpu.items() if kk not in ("x", "dy", "router_bias")}
         line["cpu_baseline"] = cpu_oracle_baseline(cfg, cpu["x"], W, cpu["router_bias"])

@@ -183,3 +183,68 @@ def test_backward_rejects_missing_saved_and_small_workspace():
     assert e.value.status == -3
     g = moe.backward(f, dy, x, *args, ws=torch.empty(need, dtype=torch.uint8, device="cuda"))
     assert torch.isfinite(g["dx"].float()).all()
+
+
+def test_bf16_skewed_routing_t4096():
+    """Zipf-biased routing (64 experts with no routes, the largest segment far
+    above the mean): zero gradients for empty experts, long K loops for the
+    large ones, sampled tokens against the oracle."""
+    W = full_weights()
+    T = 4096
+    x, dy = full_x(T), full_dy(T)
+    bias = I.zipf_bias(512)
+    d = to_dev(dict(W, x=x))
+    f, g = fwd_bwd(d, dy.cuda(), 10, bias=bias.cuda())
+    ids, w, sig = checked_routes(f, x, W, bias, 10)
+    loads = np.bincount(ids.reshape(-1), minlength=512)
+    empty = np.flatnonzero(loads == 0)
+    assert len(empty) >= 64
+    et = torch.as_tensor(empty, device="cuda")
+    for key in ("dw_gate_up", "dw_down", "dw_router"):
+        assert torch.count_nonzero(g[key][et]) == 0, key
+    rng = np.random.default_rng(6)
+    sample = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 10, replace=False)]))
+    dx, dw, dl, ds = oracle_bwd_rows(x[sample], ids[sample], w[sample], sig[sample], dy[sample], W)
+    st = torch.as_tensor(sample, device="cuda")
+    assert_grad_close(g["dx"][st], dx, "dx sampled")
+    assert_grad_close(g["dlogit"][st], dl, "dlogit sampled")
+    big = int(np.argmax(loads))
+    assert loads[big] > 5 * loads.mean()
+    for e in (big, int(np.argsort(loads)[len(loads) // 2])):
+        dwgu, dwdn = oracle.backward_expert_weights(x, ids, w, dy, W["w_gate_up"], W["w_down"], e, e + 1)
+        assert_grad_close(g["dw_gate_up"][e:e + 1], dwgu, f"dw_gate_up[{e}] ({loads[e]} routes)")
+        assert_grad_close(g["dw_down"][e:e + 1], dwdn, f"dw_down[{e}]")
+    assert moe.moe_device_status(reset=True) == 0
+
+
+def small_layer(T, H, E, k, I_, Is, seed=11):
+    """A small bf16 layer of the given shape (same recipe as the workloads)."""
+    s = seed
+    return {"x": I.normal((T, H), s, 0, 1.0, torch.bfloat16),
+            "w_router": I.normal((E, H), s, 1, 0.02, torch.float32),
+            "w_shared_gate": I.normal((H,), s, 2, 0.02, torch.bfloat16),
+            "w_gate_up": I.normal((E, 2 * I_, H), s, 4, 0.02, torch.bfloat16),
+            "w_down": I.normal((E, H, I_), s, 5, 0.02, torch.bfloat16),
+            "ws_gate_up": I.normal((2 * Is, H), s, 6, 0.02, torch.bfloat16),
+            "ws_down": I.normal((H, Is), s, 7, 0.02, torch.bfloat16),
+            "dy": I.normal((T, H), s + 1, 8, 1.0, torch.bfloat16)}
+
+
+@pytest.mark.parametrize("shape", [(600, 256, 4, 2, 256, 512), (77, 256, 16, 4, 128, 384)],
+                         ids=["tensor-core", "cuda-core"])
+def test_bf16_small_shapes_every_gradient(shape):
+    """Every gradient of a small bf16 layer against the oracle's full backward:
+    one shape on the tensor-core GEMMs (H, I, Is multiples of 256, several
+    row tiles per expert and ragged tails), one on the CUDA-core kernels
+    (I, Is multiples of 128 only)."""
+    T, H, E, k, I_, Is = shape
+    c = small_layer(T, H, E, k, I_, Is)
+    d = to_dev(c)
+    f, g = fwd_bwd(d, d["dy"], k)
+    ids, w, sig = checked_routes(f, c["x"], c, None, k)
+    ref = oracle.layer_backward(c["x"], ids, w, sig, *[c[n] for n in WKEYS], c["dy"])
+    for key in ("dx", "dw_gate_up", "dw_down", "dws_gate_up", "dws_down", "dw_router", "dw_shared_gate",
+                "dlogit"):
+        assert_grad_close(g[key], ref[key], key)
+    assert_grad_close(g["dz"], dz_of(ref["dsig"], sig), "dz")
+    assert moe.moe_device_status(reset=True) == 0

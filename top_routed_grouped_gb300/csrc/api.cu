@@ -126,6 +126,7 @@ static FwdScratch fwd_ws(const moe_dims_t *d, Carver &c) {
 struct BwdScratch {
   void *dyr, *dys, *dgu_routed, *dgu_shared;
   float *dxr, *dxs, *dlogit, *dz;
+  void *x_sorted;
   void *inner;
 };
 
@@ -140,6 +141,8 @@ static BwdScratch bwd_ws(const moe_dims_t *d, Carver &c) {
   s.dxs = (float *)c.take((size_t)T * d->H * sizeof(float));
   s.dlogit = (float *)c.take((size_t)R * sizeof(float));
   s.dz = (float *)c.take((size_t)T * sizeof(float));
+  s.x_sorted = (d->dtype == MOE_BF16 && backward_tc_supported(d->H, d->I, d->Is))
+                   ? c.take((size_t)R * d->H * esize(d)) : nullptr;
   s.inner = c.take(backward_scratch_bytes(d->dtype, d->T, d->k, d->E, d->H, d->I, d->Is));
   return s;
 }
@@ -330,7 +333,7 @@ MOE_API int moe_backward(const moe_dims_t *d, const moe_bwd_args_t *a, void *ws,
   b.dw_gate_up = a->dw_gate_up; b.dw_down = a->dw_down; b.dw_router = a->dw_router;
   b.dw_shared_gate = a->dw_shared_gate; b.dws_gate_up = a->dws_gate_up; b.dws_down = a->dws_down;
   b.dyr = sc.dyr; b.dys = sc.dys; b.dgu_routed = sc.dgu_routed; b.dgu_shared = sc.dgu_shared;
-  b.dxr = sc.dxr; b.dxs = sc.dxs;
+  b.dxr = sc.dxr; b.dxs = sc.dxs; b.x_sorted = sc.x_sorted;
   b.dlogit = a->dlogit ? a->dlogit : sc.dlogit;
   b.dz = a->dz ? a->dz : sc.dz;
   return cuda_status(launch_backward(d->dtype, b, sc.inner, device_status_ptr(), s));

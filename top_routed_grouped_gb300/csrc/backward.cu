@@ -102,7 +102,8 @@ struct BwTile {
   int64_t r0, r1;
 };
 
-__device__ inline BwTile bw_decode(int ti, int E, int T, const int32_t *tile_start, const int32_t *offsets) {
+__device__ inline BwTile bw_decode(int ti, int E, int T, const int32_t *tile_start, const int32_t *offsets,
+                                   int bm = BW_BM) {
   int lo = 0, hi = E;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
@@ -113,11 +114,11 @@ __device__ inline BwTile bw_decode(int ti, int E, int T, const int32_t *tile_sta
   tr.seg = lo;
   const int i = ti - tile_start[lo];
   if (lo < E) {
-    tr.r0 = offsets[lo] + (int64_t)i * BW_BM;
-    tr.r1 = min((int64_t)offsets[lo + 1], tr.r0 + BW_BM);
+    tr.r0 = offsets[lo] + (int64_t)i * bm;
+    tr.r1 = min((int64_t)offsets[lo + 1], tr.r0 + bm);
   } else {
-    tr.r0 = (int64_t)i * BW_BM;
-    tr.r1 = min((int64_t)T, tr.r0 + BW_BM);
+    tr.r0 = (int64_t)i * bm;
+    tr.r1 = min((int64_t)T, tr.r0 + bm);
   }
   return tr;
 }
@@ -309,64 +310,92 @@ __global__ void __launch_bounds__(256) wgrad_kernel(BwArgs a) {
     }
 }
 
-// b7: dWr[e, h] = sum over e's sorted rows j (ascending) of dlogit[route] x[tok, h];
-// b6: dw_sg[h] = sum_t dz[t] x[t, h] (segment E).  One thread per (segment, h).
+// b7: dWr[e, h] = sum over e's sorted rows j of dlogit[route] x[tok, h];
+// b6: dw_sg[h] = sum_t dz[t] x[t, h] (segment E).  Two passes with a fixed
+// order: a segment's rows are cut into chunks of RG_CHUNK consecutive rows,
+// pass 1 sums each chunk in ascending row order into a partial row, pass 2
+// sums a segment's partial rows in ascending chunk order.
+constexpr int RG_CHUNK = 64;
+
 template <typename TE>
-__global__ void __launch_bounds__(256) router_gate_wgrad_kernel(BwArgs a) {
-  const int seg = blockIdx.y;
-  const int h = blockIdx.x * blockDim.x + threadIdx.x;
-  if (h >= a.H) return;
+__global__ void __launch_bounds__(256)
+router_gate_partial_kernel(BwArgs a, const int32_t *__restrict__ chunk_start, float *__restrict__ partial) {
+  __shared__ int64_t srow[RG_CHUNK];  // element offset of each row's x
+  __shared__ float scoef[RG_CHUNK];
+  const int total = chunk_start[a.E + 1];
+  const int h = blockIdx.y * 256 + threadIdx.x;
   const TE *x = (const TE *)a.x;
-  float acc = 0.f;
-  if (seg < a.E) {
-    for (int64_t j = a.offsets[seg]; j < a.offsets[seg + 1]; ++j) {
-      const int r = a.sorted_route[j];
-      acc = fmaf(a.dlogit[r], Elem<TE>::load(x + (int64_t)(r / a.k) * a.H + h), acc);
+  for (int c = blockIdx.x; c < total; c += gridDim.x) {
+    const BwTile tr = bw_decode(c, a.E, a.T, chunk_start, a.offsets, RG_CHUNK);
+    const int n = (int)(tr.r1 - tr.r0);
+    __syncthreads();
+    if (threadIdx.x < n) {
+      const int64_t j = tr.r0 + threadIdx.x;
+      if (tr.seg < a.E) {
+        const int r = a.sorted_route[j];
+        srow[threadIdx.x] = (int64_t)(r / a.k) * a.H;
+        scoef[threadIdx.x] = a.dlogit[r];
+      } else {
+        srow[threadIdx.x] = j * a.H;
+        scoef[threadIdx.x] = a.dz[j];
+      }
     }
-    a.dw_router[(int64_t)seg * a.H + h] = acc;
-  } else {
-    for (int64_t t = 0; t < a.T; ++t) acc = fmaf(a.dz[t], Elem<TE>::load(x + t * a.H + h), acc);
-    a.dw_shared_gate[h] = acc;
+    __syncthreads();
+    if (h >= a.H) continue;
+    float acc = 0.f;
+#pragma unroll 16
+    for (int i = 0; i < n; ++i) acc = fmaf(scoef[i], Elem<TE>::load(x + srow[i] + h), acc);
+    partial[(int64_t)c * a.H + h] = acc;
   }
 }
 
+__global__ void __launch_bounds__(256)
+router_gate_reduce_kernel(BwArgs a, const int32_t *__restrict__ chunk_start, const float *__restrict__ partial) {
+  const int seg = blockIdx.y;
+  const int h = blockIdx.x * 256 + threadIdx.x;
+  if (h >= a.H) return;
+  float acc = 0.f;
+  for (int c = chunk_start[seg]; c < chunk_start[seg + 1]; ++c) acc += partial[(int64_t)c * a.H + h];
+  if (seg < a.E) a.dw_router[(int64_t)seg * a.H + h] = acc;
+  else a.dw_shared_gate[h] = acc;
+}
+
 // ---------------------------------------------------------------- b8
-// One thread per (token, 16-byte chunk of the row).
+// One warp per (token, 32 x 16-byte chunk of the row): the slots are ranked
+// by expert id (ids of a token are distinct), then each lane assembles one
+// 16-byte chunk.
 template <typename TE>
 __global__ void __launch_bounds__(256) dx_kernel(BwArgs a) {
   constexpr int VN = Vec16<TE>::N;
-  const int per_row = a.H / VN;
-  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (gid >= (int64_t)a.T * per_row) return;
-  const int64_t t = gid / per_row;
-  const int h = (int)(gid % per_row) * VN;
+  const int lane = threadIdx.x & 31;
+  const int per_row = a.H / (32 * VN);  // warps per token (H is a multiple of 32 VN here)
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (gw >= (int64_t)a.T * per_row) return;
+  const int64_t t = gw / per_row;
+  const int h = (int)(gw % per_row) * 32 * VN + lane * VN;
   const int k = a.k;
-  // slots in ascending expert id (ids of a token are distinct)
-  int order[16];
-  for (int s = 0; s < k; ++s) order[s] = s;
-  for (int i = 1; i < k; ++i) {
-    const int cur = order[i];
-    const int ecur = a.topk_ids[t * k + cur];
-    int j = i - 1;
-    while (j >= 0 && a.topk_ids[t * k + order[j]] > ecur) {
-      order[j + 1] = order[j];
-      --j;
-    }
-    order[j + 1] = cur;
-  }
+  const int id = lane < k ? a.topk_ids[t * k + lane] : 0x7fffffff;
+  int rank = 0;
+  for (int s = 0; s < k; ++s) rank += __shfl_sync(FULL_MASK, id, s) < id;
+  const int pos = lane < k ? a.route_pos[t * k + lane] : 0;
+  const float dl = lane < k ? a.dlogit[t * k + lane] : 0.f;
   float acc[VN];
 #pragma unroll
   for (int v = 0; v < VN; ++v) acc[v] = 0.f;
-  for (int i = 0; i < k; ++i) {
-    const int64_t row = a.route_pos[t * k + order[i]];
-    const float4 *src = reinterpret_cast<const float4 *>(a.dxr + row * a.H + h);
 #pragma unroll
-    for (int v = 0; v < VN / 4; ++v) {
-      const float4 q = src[v];
-      acc[4 * v] += q.x;
-      acc[4 * v + 1] += q.y;
-      acc[4 * v + 2] += q.z;
-      acc[4 * v + 3] += q.w;
+  for (int i = 0; i < 16; ++i) {
+    const unsigned m = __ballot_sync(FULL_MASK, lane < k && rank == i);
+    const int64_t row = __shfl_sync(FULL_MASK, pos, m ? __ffs(m) - 1 : 0);
+    if (i < k) {
+      const float4 *src = reinterpret_cast<const float4 *>(a.dxr + row * a.H + h);
+#pragma unroll
+      for (int v = 0; v < VN / 4; ++v) {
+        const float4 q = src[v];
+        acc[4 * v] += q.x;
+        acc[4 * v + 1] += q.y;
+        acc[4 * v + 2] += q.z;
+        acc[4 * v + 3] += q.w;
+      }
     }
   }
   {
@@ -383,15 +412,87 @@ __global__ void __launch_bounds__(256) dx_kernel(BwArgs a) {
   float rt[VN];
 #pragma unroll
   for (int v = 0; v < VN; ++v) rt[v] = 0.f;
-  for (int s = 0; s < k; ++s) {
-    const float dl = a.dlogit[t * k + s];
-    const float *wr = a.w_router + (int64_t)a.topk_ids[t * k + s] * a.H + h;
 #pragma unroll
-    for (int v = 0; v < VN; ++v) rt[v] = fmaf(dl, wr[v], rt[v]);
+  for (int s = 0; s < 16; ++s) {
+    const int e = __shfl_sync(FULL_MASK, id, s);
+    const float d = __shfl_sync(FULL_MASK, dl, s);
+    if (s < k) {
+      const float4 *wr = reinterpret_cast<const float4 *>(a.w_router + (int64_t)e * a.H + h);
+#pragma unroll
+      for (int v = 0; v < VN / 4; ++v) {
+        const float4 q = wr[v];
+        rt[4 * v] = fmaf(d, q.x, rt[4 * v]);
+        rt[4 * v + 1] = fmaf(d, q.y, rt[4 * v + 1]);
+        rt[4 * v + 2] = fmaf(d, q.z, rt[4 * v + 2]);
+        rt[4 * v + 3] = fmaf(d, q.w, rt[4 * v + 3]);
+      }
+    }
   }
-  const float dzt = a.dz[t];
   float gv[VN];
   Vec16<TE>::load((const TE *)a.w_shared_gate + h, gv);
+  const float dzt = a.dz[t];
+  float o[VN];
+#pragma unroll
+  for (int v = 0; v < VN; ++v) o[v] = fmaf(dzt, gv[v], acc[v] + rt[v]);
+  Vec16<TE>::store((TE *)a.dx + t * a.H + h, o);
+}
+
+// Simple variant for rows whose length is not a multiple of 32 x 16 bytes:
+// one thread per (token, 16-byte chunk), same order of the sums.
+template <typename TE>
+__global__ void __launch_bounds__(256) dx_thread_kernel(BwArgs a) {
+  constexpr int VN = Vec16<TE>::N;
+  const int per_row = a.H / VN;
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= (int64_t)a.T * per_row) return;
+  const int64_t t = gid / per_row;
+  const int h = (int)(gid % per_row) * VN;
+  const int k = a.k;
+  float acc[VN];
+#pragma unroll
+  for (int v = 0; v < VN; ++v) acc[v] = 0.f;
+  int order[16];  // slots in ascending expert id (insertion sort; ids are distinct)
+  for (int s = 0; s < k; ++s) {
+    const int e = a.topk_ids[t * k + s];
+    int j = s - 1;
+    while (j >= 0 && a.topk_ids[t * k + order[j]] > e) {
+      order[j + 1] = order[j];
+      --j;
+    }
+    order[j + 1] = s;
+  }
+  for (int i = 0; i < k; ++i) {
+    const float4 *src = reinterpret_cast<const float4 *>(a.dxr + (int64_t)a.route_pos[t * k + order[i]] * a.H + h);
+#pragma unroll
+    for (int v = 0; v < VN / 4; ++v) {
+      const float4 q = src[v];
+      acc[4 * v] += q.x;
+      acc[4 * v + 1] += q.y;
+      acc[4 * v + 2] += q.z;
+      acc[4 * v + 3] += q.w;
+    }
+  }
+  const float4 *src = reinterpret_cast<const float4 *>(a.dxs + t * a.H + h);
+#pragma unroll
+  for (int v = 0; v < VN / 4; ++v) {
+    const float4 q = src[v];
+    acc[4 * v] += q.x;
+    acc[4 * v + 1] += q.y;
+    acc[4 * v + 2] += q.z;
+    acc[4 * v + 3] += q.w;
+  }
+  float rt[VN];
+#pragma unroll
+  for (int v = 0; v < VN; ++v) rt[v] = 0.f;
+  for (int s = 0; s < k; ++s) {
+    const float d = a.dlogit[t * k + s];
+    const float *wr = a.w_router + (int64_t)a.topk_ids[t * k + s] * a.H + h;
+#pragma unroll
+    for (int v = 0; v < VN; ++v) rt[v] = fmaf(d, wr[v], rt[v]);
+  }
+  float gv[VN];
+  Vec16<TE>::load((const TE *)a.w_shared_gate + h, gv);
+  const float dzt = a.dz[t];
   float o[VN];
 #pragma unroll
   for (int v = 0; v < VN; ++v) o[v] = fmaf(dzt, gv[v], acc[v] + rt[v]);
@@ -399,10 +500,17 @@ __global__ void __launch_bounds__(256) dx_kernel(BwArgs a) {
 }
 
 // ---------------------------------------------------------------- launcher
-size_t backward_scratch_bytes(int dtype, int T, int k, int E, int H, int I, int Is) {
+// Scratch: [GEMM tiles or item tables][chunk starts (E+2)][partial rows].
+static size_t gemm_scratch_bytes(int dtype, int T, int k, int E, int H, int I, int Is) {
   const size_t tiles = (size_t)(E + 2) * sizeof(int32_t);
   if (dtype != 0 && backward_tc_supported(H, I, Is)) return std::max(tiles, dgrad_tc_scratch_bytes(T, k, E, H, I, Is));
   return tiles;
+}
+static int64_t max_chunks(int T, int k, int E) { return ceil_div((int64_t)T * k + T, RG_CHUNK) + E + 1; }
+
+size_t backward_scratch_bytes(int dtype, int T, int k, int E, int H, int I, int Is) {
+  return (size_t)round_up((int64_t)gemm_scratch_bytes(dtype, T, k, E, H, I, Is), 256) +
+         (size_t)round_up((int64_t)(E + 2) * 4, 256) + (size_t)max_chunks(T, k, E) * H * sizeof(float);
 }
 
 template <typename TE>
@@ -428,8 +536,19 @@ static cudaError_t run_backward(const BwArgs &a, void *scratch, int *status, cud
     wgrad_kernel<TE, WG_GATE_UP><<<dim3((unsigned)ceil_div(a.H, 64), (unsigned)ceil_div(2 * Imax, 64), a.E + 1),
                                    256, 0, stream>>>(a);
   }
-  router_gate_wgrad_kernel<TE><<<dim3((unsigned)ceil_div(a.H, 256), a.E + 1), 256, 0, stream>>>(a);
-  dx_kernel<TE><<<(unsigned)ceil_div((int64_t)a.T * (a.H / Vec16<TE>::N), 256), 256, 0, stream>>>(a);
+  const int dtype = sizeof(TE) == 4 ? 0 : 1;
+  uint8_t *rest = (uint8_t *)scratch + round_up((int64_t)gemm_scratch_bytes(dtype, a.T, a.k, a.E, a.H, a.I, a.Is), 256);
+  int32_t *chunk_start = (int32_t *)rest;
+  float *partial = (float *)(rest + round_up((int64_t)(a.E + 2) * 4, 256));
+  if ((err = launch_build_tiles(a.E, a.T, RG_CHUNK, a.offsets, chunk_start, stream)) != cudaSuccess) return err;
+  const int64_t mc = max_chunks(a.T, a.k, a.E);
+  router_gate_partial_kernel<TE><<<dim3((unsigned)std::min<int64_t>(mc, 65535), (unsigned)ceil_div(a.H, 256)), 256, 0,
+                                   stream>>>(a, chunk_start, partial);
+  router_gate_reduce_kernel<<<dim3((unsigned)ceil_div(a.H, 256), a.E + 1), 256, 0, stream>>>(a, chunk_start, partial);
+  if (a.H % (32 * Vec16<TE>::N) == 0)
+    dx_kernel<TE><<<(unsigned)ceil_div((int64_t)a.T * (a.H / (32 * Vec16<TE>::N)), 8), 256, 0, stream>>>(a);
+  else
+    dx_thread_kernel<TE><<<(unsigned)ceil_div((int64_t)a.T * (a.H / Vec16<TE>::N), 256), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -61,12 +61,22 @@ __device__ inline bool gt_warp_wait(uint64_t *bar, uint32_t parity, volatile int
 // ===========================================================================
 // Input gradients
 // ===========================================================================
-constexpr int DG_STAGES = 3, DG_EPI_WARPS = 8, DG_EPI_BYTES = 4096;
-constexpr int DG_A_BYTES = 4 * 8192;   // 4 blocks of 64 features x 64 K lines (two M tiles)
+// MT = M tiles (128 weight features each) per item.  MT = 2: two
+// accumulators of up to 256 columns fill TMEM (drained between items); MT = 1:
+// two accumulator buffers alternate, so the epilogue of one item overlaps the
+// mainloop of the next.
+constexpr int DG_EPI_WARPS = 8, DG_EPI_BYTES = 4096;
 constexpr int DG_B_BYTES = 256 * 128;  // up to 256 rows x 64 K
 constexpr int DG_THREADS = 32 * (GT_EPI_FIRST + DG_EPI_WARPS);
-constexpr int DG_SMEM = 1024 + DG_STAGES * (DG_A_BYTES + DG_B_BYTES) + DG_EPI_WARPS * DG_EPI_BYTES + 256;
-static_assert(DG_SMEM <= 232448, "dgrad shared memory");
+template <int MT>
+struct DgCfg {
+  static constexpr int A_BYTES = MT * 2 * 8192;  // 2 MT blocks of 64 features x 64 K lines
+  static constexpr int STAGES = MT == 1 ? 4 : 3;
+  static constexpr int NBUF = MT == 1 ? 2 : 1;
+  static constexpr int SMEM = 1024 + STAGES * (A_BYTES + DG_B_BYTES) + DG_EPI_WARPS * DG_EPI_BYTES + 256;
+  static_assert(SMEM <= 232448, "dgrad shared memory");
+  static_assert(NBUF * MT * 256 <= 512, "TMEM columns");
+};
 
 struct DgMaps {
   CUtensorMap a, a_sh;        // weights, MN-major boxes (64, 64, 4)
@@ -101,9 +111,10 @@ __device__ inline DgItem dg_item(int it, const DgParams &p) {
   return r;
 }
 
-template <int MODE>
+template <int MODE, int MT>
 __global__ void __launch_bounds__(DG_THREADS, 1)
 tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
+  constexpr int DG_STAGES = DgCfg<MT>::STAGES, DG_A_BYTES = DgCfg<MT>::A_BYTES, NBUF = DgCfg<MT>::NBUF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sa = base;
@@ -111,7 +122,7 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
   uint8_t *epi = sb + DG_STAGES * DG_B_BYTES;
   uint64_t *bars = (uint64_t *)(epi + DG_EPI_WARPS * DG_EPI_BYTES);
   uint64_t *full = bars, *empty = bars + DG_STAGES;
-  uint64_t *tfull = bars + 2 * DG_STAGES, *tempty = tfull + 1, *mma_done = tempty + 1;
+  uint64_t *tfull = bars + 2 * DG_STAGES, *tempty = tfull + NBUF, *mma_done = tempty + NBUF;
   uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
 
@@ -121,8 +132,10 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, 32 * DG_EPI_WARPS);
+    for (int b = 0; b < NBUF; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 32 * DG_EPI_WARPS);
+    }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -154,8 +167,8 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
         for (int kb = 0; kb < im.nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_3d(sa + stage * DG_A_BYTES, sh ? &maps.a_sh : &maps.a, &full[stage], 0, wrow + kb * 64, im.f * 4,
-                      pol_w);
+          tma_load_3d(sa + stage * DG_A_BYTES, sh ? &maps.a_sh : &maps.a, &full[stage], 0, wrow + kb * 64,
+                      im.f * 2 * MT, pol_w);
           uint8_t *b_dst = sb + stage * DG_B_BYTES;
           const CUtensorMap *bm = sh ? maps.b_sh : maps.b;
           int r = 0;
@@ -183,11 +196,12 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      uint32_t phase = 0, cnt = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
         const DgItem im = dg_item<MODE>(it, p);
-        if (!mbar_wait(tempty, acc_phase ^ 1, abort_flag, p.status)) break;
+        const int b = cnt % NBUF;
+        if (!mbar_wait(&tempty[b], ((cnt / NBUF) & 1) ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32(128, im.n) | IDESC_A_MN;
         for (int kb = 0; kb < im.nk; ++kb) {
@@ -195,18 +209,18 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
           tc_fence_after();
           const uint64_t bd = smem_desc_sw128(smem_u32(sb + stage * DG_B_BYTES));
 #pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
+          for (int mt = 0; mt < MT; ++mt) {
             const uint64_t ad = smem_desc_mn_sw128(smem_u32(sa + stage * DG_A_BYTES + mt * 16384), 8192);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)  // K = 16: A +2048 bytes (MN-major), B +32 bytes (K-major)
-              mma_bf16(tmem + mt * 256, ad + 128 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+              mma_bf16(tmem + (b * MT + mt) * 256, ad + 128 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
           }
           mma_commit(&empty[stage]);
           if (++stage == DG_STAGES) stage = 0, phase ^= 1;
         }
         if (!ok) break;
-        mma_commit(tfull);
-        acc_phase ^= 1;
+        mma_commit(&tfull[b]);
+        ++cnt;
       }
       mma_commit(mma_done);
       volatile int never = 0;
@@ -219,19 +233,21 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
     constexpr int CSTEP = 32 * (DG_EPI_WARPS / 4);
     const int cfirst = 32 * ((warp - GT_EPI_FIRST) >> 2);
     uint8_t *stg = epi + (warp - GT_EPI_FIRST) * DG_EPI_BYTES;
-    uint32_t acc_phase = 0;
+    uint32_t cnt = 0;
     for (int it = blockIdx.x; it < total; it += gridDim.x) {
       const DgItem im = dg_item<MODE>(it, p);
       const bool sh = im.seg == p.E;
-      if (!gt_warp_wait(tfull, acc_phase, abort_flag, p.status)) break;
+      const int b = cnt % NBUF;
+      if (!gt_warp_wait(&tfull[b], (cnt / NBUF) & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+      const uint32_t tq = tmem + b * MT * 256 + ((uint32_t)(q * 32) << 16);
       for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
-        float vt[2][32];
-        tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[1]);
+        float vt[MT][32];
+        if (MT == 2) tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[MT - 1]);
+        else tmem_ld32(tq + c0, vt[0]);
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          const int f0 = im.f * 256 + mt * 128 + q * 32;  // first feature of this warp's 32
+        for (int mt = 0; mt < MT; ++mt) {
+          const int f0 = im.f * 128 * MT + mt * 128 + q * 32;  // first feature of this warp's 32
           if (MODE == DGRAD_DOWN) {
             // Lane = feature i, column c = row j.  Stage the 32 x 32 tiles of g
             // and u of these rows (64 bytes per row each), compute dg, du in
@@ -289,8 +305,8 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
         }
       }
       tc_fence_before();
-      mbar_arrive(tempty);
-      acc_phase ^= 1;
+      mbar_arrive(&tempty[b]);
+      ++cnt;
     }
   }
   tc_fence_before();
@@ -302,32 +318,28 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
 // ===========================================================================
 // Weight gradients
 // ===========================================================================
-constexpr int WG_STAGES = 3, WG_EPI_WARPS = 8, WG_GATHER_WARPS = 8;
+// A stage holds one K block of both operands: A = 2 blocks (128 M) and B = 4
+// blocks (256 N) of 64 MN elements, each block hb K lines of 128 bytes, where
+// hb (64, 32 or 16) is the smallest box height that covers the rows left in
+// the segment; lines past the segment's end (at most 15 per block) are
+// zeroed before the MMAs read them.
+constexpr int WG_STAGES = 3, WG_EPI_WARPS = 8;
 constexpr int WG_A_BYTES = 2 * 8192;  // 128 M x 64 K lines, MN-major
 constexpr int WG_B_BYTES = 4 * 8192;  // 256 N x 64 K lines, MN-major
-constexpr int WG_STG_BYTES = 4096;    // one 32 x 32 FP32 store tile
+constexpr int WG_STG_BYTES = 4096;    // one 32 x 32 FP32 store tile; two per epilogue warp
+constexpr int WG_THREADS = 32 * (GT_EPI_FIRST + WG_EPI_WARPS);
 constexpr int WG_SMEM = 1024 + WG_STAGES * (WG_A_BYTES + WG_B_BYTES) + (2 * WG_EPI_WARPS + 1) * WG_STG_BYTES + 256;
 static_assert(WG_SMEM <= 232448, "wgrad shared memory");
 
-template <int MODE>
-constexpr int wg_gather_first() {
-  return GT_EPI_FIRST + WG_EPI_WARPS;
-}
-template <int MODE>
-constexpr int wg_threads() {
-  return 32 * (wg_gather_first<MODE>() + (MODE == WGRAD_GATE_UP ? WG_GATHER_WARPS : 0));
-}
-
 struct WgMaps {
-  CUtensorMap a, a_sh;      // A^T operand rows, MN-major boxes (64, 64, 2)
-  CUtensorMap b, b_sh;      // WGRAD_DOWN: h rows, boxes (64, 64, 4)
-  CUtensorMap out, out_sh;  // FP32 gradients, 32 x 32 boxes
+  CUtensorMap a[3], a_sh[3];  // A^T operand rows, boxes (64, hb, 2) for hb = 64, 32, 16
+  CUtensorMap b[3], b_sh[3];  // B^T operand rows, boxes (64, hb, 4)
+  CUtensorMap out, out_sh;    // FP32 gradients, 32 x 32 boxes
 };
 
 struct WgParams {
   int T, H, E, k, I, Is;
-  const int32_t *offsets, *sorted_route;
-  const __nv_bfloat16 *x;  // WGRAD_GATE_UP: gathered B rows
+  const int32_t *offsets;
   int tm_r, tn_r, tm_s, tn_s;  // output tiles per segment (M x N), routed and shared
   int total;                   // tm_s * tn_s + E * tm_r * tn_r
   int *status;
@@ -364,11 +376,12 @@ __device__ inline WgItem wg_item(int it, const WgParams &p) {
   return r;
 }
 
+// Box height index (0: 64, 1: 32, 2: 16 lines) for `valid` rows of a K block.
+__device__ inline int wg_box(int valid) { return valid > 32 ? 0 : (valid > 16 ? 1 : 2); }
+
 template <int MODE>
-__global__ void __launch_bounds__(wg_threads<MODE>(), 1)
+__global__ void __launch_bounds__(WG_THREADS, 1)
 tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
-  constexpr int GATHER_FIRST = wg_gather_first<MODE>();
-  constexpr int GATHER_THREADS = 32 * WG_GATHER_WARPS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sa = base;
@@ -386,7 +399,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
     for (int s = 0; s < WG_STAGES; ++s) {
-      mbar_init(&full[s], 1 + (MODE == WGRAD_GATE_UP ? GATHER_THREADS : 0));
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -398,8 +411,8 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&maps.a);
-    prefetch_tmap(&maps.a_sh);
+    prefetch_tmap(&maps.a[0]);
+    prefetch_tmap(&maps.b[0]);
     prefetch_tmap(&maps.out);
   }
   if (warp == 1) tmem_alloc(tmem_slot, GT_TMEM_COLS);
@@ -418,14 +431,14 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
       for (int it = blockIdx.x; it < p.total && ok; it += gridDim.x) {
         const WgItem im = wg_item(it, p);
         const bool sh = im.seg == p.E;
-        const uint32_t bytes = WG_A_BYTES + (MODE == WGRAD_DOWN ? WG_B_BYTES : 0);
         for (int kb = 0; kb < im.nk; ++kb) {
+          const int hi = wg_box(min(64, im.rows - kb * 64));
+          const uint32_t bytes = (uint32_t)(WG_A_BYTES + WG_B_BYTES) >> hi;
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], bytes);
           const int row = (int)im.r0 + kb * 64;
-          tma_load_3d(sa + stage * WG_A_BYTES, sh ? &maps.a_sh : &maps.a, &full[stage], 0, row, im.mt * 2, pol);
-          if (MODE == WGRAD_DOWN)
-            tma_load_3d(sb + stage * WG_B_BYTES, sh ? &maps.b_sh : &maps.b, &full[stage], 0, row, im.nt * 4, pol);
+          tma_load_3d(sa + stage * WG_A_BYTES, sh ? &maps.a_sh[hi] : &maps.a[hi], &full[stage], 0, row, im.mt * 2, pol);
+          tma_load_3d(sb + stage * WG_B_BYTES, sh ? &maps.b_sh[hi] : &maps.b[hi], &full[stage], 0, row, im.nt * 4, pol);
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == WG_STAGES) stage = 0, phase ^= 1;
@@ -453,23 +466,25 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
       for (int kb = 0; kb < im.nk; ++kb) {
         if (!gt_warp_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
         const int valid = min(64, im.rows - kb * 64);
-        if (valid < 64) {
-          // Lines [valid, 64) of every 64-line block hold rows of the next
-          // segment (or TMA zero fill): clear them for both operands.
-          const int lines = 64 - valid;
-          const int na = WG_A_BYTES / 8192, nbk = MODE == WGRAD_DOWN ? WG_B_BYTES / 8192 : 0;
-          for (int blk = 0; blk < na + nbk; ++blk) {
-            uint8_t *dst = blk < na ? sa + stage * WG_A_BYTES + blk * 8192 : sb + stage * WG_B_BYTES + (blk - na) * 8192;
-            dst += valid * 128;
-            for (int i = lane; i < lines * 8; i += 32) ((uint4 *)dst)[i] = make_uint4(0, 0, 0, 0);
+        const int hb = 64 >> wg_box(valid);  // lines per block in this stage
+        if (valid < hb) {
+          // Lines [valid, hb) of each block hold rows of the next segment (or
+          // TMA zero fill): clear them in both operands (6 blocks).
+          const int lines = hb - valid;
+          for (int i = lane; i < 6 * lines * 8; i += 32) {
+            const int blk = i / (lines * 8), rem = i % (lines * 8);
+            uint8_t *blk_base = blk < 2 ? sa + stage * WG_A_BYTES + blk * hb * 128
+                                        : sb + stage * WG_B_BYTES + (blk - 2) * hb * 128;
+            ((uint4 *)(blk_base + valid * 128))[rem] = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
         }
         if (lane == 0) {
           tc_fence_after();
-          const uint64_t ad = smem_desc_mn_sw128(smem_u32(sa + stage * WG_A_BYTES), 8192);
-          const uint64_t bd = smem_desc_mn_sw128(smem_u32(sb + stage * WG_B_BYTES), 8192);
+          const uint32_t lbo = (uint32_t)hb * 128;  // stride between 64-element MN blocks
+          const uint64_t ad = smem_desc_mn_sw128(smem_u32(sa + stage * WG_A_BYTES), lbo);
+          const uint64_t bd = smem_desc_mn_sw128(smem_u32(sb + stage * WG_B_BYTES), lbo);
           const int nkk = (valid + 15) >> 4;
           for (int kk = 0; kk < nkk; ++kk)
             mma_bf16(tmem + b * 256, ad + 128 * kk, bd + 128 * kk, idesc, (kb | kk) != 0);
@@ -489,7 +504,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
       mbar_wait(mma_done, 0, &never, p.status);
     }
     __syncwarp();
-  } else if (warp < GATHER_FIRST) {
+  } else {
     // ------------------------------------------------------------ epilogue
     // Warp (q, half): TMEM lanes 32q.. (output rows), columns [128 half, +128).
     const int q = warp & 3, half = (warp - GT_EPI_FIRST) >> 2;
@@ -540,55 +555,6 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
     }
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
-  } else if (MODE == WGRAD_GATE_UP) {
-    // ------------------------------------------------------------ x row gather (MN-major B)
-    // Warp g fills K lines kr = g + 8 i (i < 8) of a stage: lane = (block mb
-    // of 64 hidden units, 16-byte chunk ch), written at chunk position
-    // (ch ^ kr % 8) of line kr in block mb; lines past the segment are zeros.
-    const int g = warp - GATHER_FIRST;
-    const int mb = lane >> 3, ch = lane & 7;
-    int stage = 0, arr_stage = 0, pending = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; it < p.total && ok; it += gridDim.x) {
-      const WgItem im = wg_item(it, p);
-      if (im.rows == 0) continue;
-      const bool sh = im.seg == p.E;
-      const int h0 = im.nt * 256 + mb * 64 + ch * 8;
-      for (int kb = 0; kb < im.nk; ++kb) {
-        int tokv = -1;
-        if (lane < 8) {
-          const int j = kb * 64 + g + 8 * lane;
-          if (j < im.rows) tokv = sh ? (int)im.r0 + j : __ldg(p.sorted_route + im.r0 + j) / p.k;
-        }
-        if (!gt_warp_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
-        const uint32_t bsm = smem_u32(sb + stage * WG_B_BYTES) + mb * 8192;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int tok = __shfl_sync(FULL_MASK, tokv, i);
-          const int kr = g + 8 * i;
-          const uint32_t dst = bsm + kr * 128 + ((ch ^ (kr & 7)) << 4);
-          if (tok >= 0) cp_async_16(dst, p.x + (int64_t)tok * p.H + h0);
-          else cp_async_16_zfill(dst, p.x, 0);
-        }
-        cp_async_commit();
-        if (++pending > 1) {
-          cp_async_wait<1>();
-          fence_proxy_async_smem();
-          mbar_arrive(&full[arr_stage]);
-          if (++arr_stage == WG_STAGES) arr_stage = 0;
-          --pending;
-        }
-        if (++stage == WG_STAGES) stage = 0, phase ^= 1;
-      }
-    }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (ok)
-      for (; pending > 0; --pending) {
-        mbar_arrive(&full[arr_stage]);
-        if (++arr_stage == WG_STAGES) arr_stage = 0;
-      }
   }
   tc_fence_before();
   __syncthreads();
@@ -596,33 +562,55 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
   if (warp == 1) tmem_dealloc(tmem, GT_TMEM_COLS);
 }
 
+// x rows in sorted (expert-segment) order: xs[j] = x[sorted_route[j] / k], one
+// warp per row, 16 bytes per lane.
+__global__ void __launch_bounds__(256) gather_sorted_rows_kernel(int64_t R, int H, int k, const int32_t *sorted_route,
+                                                                 const __nv_bfloat16 *x, __nv_bfloat16 *xs) {
+  const int64_t j = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (j >= R) return;
+  const uint4 *src = (const uint4 *)(x + (int64_t)(__ldg(sorted_route + j) / k) * H);
+  uint4 *dst = (uint4 *)(xs + j * H);
+  for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
+}
+
 // ===========================================================================
 // Host side
 // ===========================================================================
 bool backward_tc_supported(int H, int I, int Is) { return H % 256 == 0 && I % 256 == 0 && Is % 256 == 0; }
 
+// Down dgrad: items of one M tile (128 features of I); gate_up dgrad: items
+// of two M tiles (256 hidden units).
 size_t dgrad_tc_scratch_bytes(int T, int k, int E, int H, int I, int Is) {
   const size_t starts = (size_t)round_up((E + 2) * 4, 256);
-  return 2 * starts + (size_t)round_up(tc_max_items(T, k, E, I / 256, Is / 256) * 16, 256) +
+  return 2 * starts + (size_t)round_up(tc_max_items(T, k, E, I / 128, Is / 128) * 16, 256) +
          (size_t)round_up(tc_max_items(T, k, E, H / 256, H / 256) * 16, 256);
+}
+
+template <int MODE, int MT>
+static cudaError_t launch_dgrad(const DgMaps &m, const DgParams &p, int grid, cudaStream_t stream) {
+  cudaError_t e = ensure_smem((const void *)tc_dgrad_kernel<MODE, MT>, DgCfg<MT>::SMEM);
+  if (e != cudaSuccess) return e;
+  tc_dgrad_kernel<MODE, MT><<<grid, DG_THREADS, DgCfg<MT>::SMEM, stream>>>(m, p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_dgrad_tc(const BwArgs &a, void *scratch, int *status, cudaStream_t stream) {
   const size_t starts = (size_t)round_up((a.E + 2) * 4, 256);
-  const int mi_dn = (int)tc_max_items(a.T, a.k, a.E, a.I / 256, a.Is / 256);
+  const int mi_dn = (int)tc_max_items(a.T, a.k, a.E, a.I / 128, a.Is / 128);
   const int mi_gu = (int)tc_max_items(a.T, a.k, a.E, a.H / 256, a.H / 256);
   uint8_t *w = (uint8_t *)scratch;
   int32_t *start_dn = (int32_t *)w;
   int32_t *start_gu = (int32_t *)(w + starts);
   int4 *items_dn = (int4 *)(w + 2 * starts);
   int4 *items_gu = (int4 *)(w + 2 * starts + round_up((int64_t)mi_dn * 16, 256));
-  cudaError_t e = launch_item_tables(a.E, a.T, a.I / 256, a.Is / 256, a.H / 256, a.H / 256, a.offsets, start_dn,
+  cudaError_t e = launch_item_tables(a.E, a.T, a.I / 128, a.Is / 128, a.H / 256, a.H / 256, a.offsets, start_dn,
                                      start_gu, items_dn, items_gu, mi_dn, mi_gu, stream);
   if (e != cudaSuccess) return e;
   const int64_t R = (int64_t)a.T * a.k;
   DgMaps md, mg;
-  if (!map_col_blocks(&md.a, a.w_down, (int64_t)a.E * a.H, a.I, 64, 4) ||
-      !map_col_blocks(&md.a_sh, a.ws_down, a.H, a.Is, 64, 4) || !map_rows(md.b, a.dyr, R, a.H) ||
+  if (!map_col_blocks(&md.a, a.w_down, (int64_t)a.E * a.H, a.I, 64, 2) ||
+      !map_col_blocks(&md.a_sh, a.ws_down, a.H, a.Is, 64, 2) || !map_rows(md.b, a.dyr, R, a.H) ||
       !map_rows(md.b_sh, a.dys, a.T, a.H) ||
       !map_col_blocks(&mg.a, a.w_gate_up, (int64_t)a.E * 2 * a.I, a.H, 64, 4) ||
       !map_col_blocks(&mg.a_sh, a.ws_gate_up, 2 * (int64_t)a.Is, a.H, 64, 4) ||
@@ -638,53 +626,54 @@ cudaError_t launch_dgrad_tc(const BwArgs &a, void *scratch, int *status, cudaStr
   p.dxs = a.dxs;
   p.status = status;
   const int grid = device_sms();
-  if ((e = ensure_smem((const void *)tc_dgrad_kernel<DGRAD_DOWN>, DG_SMEM)) != cudaSuccess) return e;
-  if ((e = ensure_smem((const void *)tc_dgrad_kernel<DGRAD_GATE_UP>, DG_SMEM)) != cudaSuccess) return e;
   p.item_start = start_dn;
   p.items = items_dn;
-  tc_dgrad_kernel<DGRAD_DOWN><<<grid, DG_THREADS, DG_SMEM, stream>>>(md, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_dgrad<DGRAD_DOWN, 1>(md, p, grid, stream)) != cudaSuccess) return e;
   p.item_start = start_gu;
   p.items = items_gu;
-  tc_dgrad_kernel<DGRAD_GATE_UP><<<grid, DG_THREADS, DG_SMEM, stream>>>(mg, p);
+  return launch_dgrad<DGRAD_GATE_UP, 2>(mg, p, grid, stream);
+}
+
+static bool wg_maps(CUtensorMap *m3, const void *ptr, int64_t rows, int64_t cols, uint32_t nblk) {
+  for (int i = 0; i < 3; ++i)
+    if (!map_col_blocks(&m3[i], ptr, rows, cols, 64u >> i, nblk)) return false;
+  return true;
+}
+
+template <int MODE>
+static cudaError_t launch_wgrad(const WgMaps &m, const WgParams &p, cudaStream_t stream) {
+  cudaError_t e = ensure_smem((const void *)tc_wgrad_kernel<MODE>, WG_SMEM);
+  if (e != cudaSuccess) return e;
+  tc_wgrad_kernel<MODE><<<std::min(p.total, device_sms()), WG_THREADS, WG_SMEM, stream>>>(m, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_wgrad_tc(const BwArgs &a, int *status, cudaStream_t stream) {
   const int64_t R = (int64_t)a.T * a.k;
+  gather_sorted_rows_kernel<<<(unsigned)ceil_div(R, 8), 256, 0, stream>>>(
+      R, a.H, a.k, a.sorted_route, (const __nv_bfloat16 *)a.x, (__nv_bfloat16 *)a.x_sorted);
   WgMaps md, mg;
-  // Row counts of the A / B maps are at least 1 so that an empty batch still encodes.
-  const int64_t Rm = std::max<int64_t>(R, 1), Tm = std::max(a.T, 1);
-  if (!map_col_blocks(&md.a, a.dyr, Rm, a.H, 64, 2) || !map_col_blocks(&md.a_sh, a.dys, Tm, a.H, 64, 2) ||
-      !map_col_blocks(&md.b, a.h_routed, Rm, a.I, 64, 4) || !map_col_blocks(&md.b_sh, a.h_shared, Tm, a.Is, 64, 4) ||
+  if (!wg_maps(md.a, a.dyr, R, a.H, 2) || !wg_maps(md.a_sh, a.dys, a.T, a.H, 2) ||
+      !wg_maps(md.b, a.h_routed, R, a.I, 4) || !wg_maps(md.b_sh, a.h_shared, a.T, a.Is, 4) ||
       !map_f32_tile(&md.out, a.dw_down, (int64_t)a.E * a.H, a.I) || !map_f32_tile(&md.out_sh, a.dws_down, a.H, a.Is) ||
-      !map_col_blocks(&mg.a, a.dgu_routed, Rm, 2 * (int64_t)a.I, 64, 2) ||
-      !map_col_blocks(&mg.a_sh, a.dgu_shared, Tm, 2 * (int64_t)a.Is, 64, 2) ||
+      !wg_maps(mg.a, a.dgu_routed, R, 2 * (int64_t)a.I, 2) || !wg_maps(mg.a_sh, a.dgu_shared, a.T, 2 * (int64_t)a.Is, 2) ||
+      !wg_maps(mg.b, a.x_sorted, R, a.H, 4) || !wg_maps(mg.b_sh, a.x, a.T, a.H, 4) ||
       !map_f32_tile(&mg.out, a.dw_gate_up, (int64_t)a.E * 2 * a.I, a.H) ||
       !map_f32_tile(&mg.out_sh, a.dws_gate_up, 2 * (int64_t)a.Is, a.H))
     return cudaErrorInvalidValue;
-  mg.b = mg.a;  // the gate_up B operand is gathered with cp.async
-  mg.b_sh = mg.a_sh;
   WgParams p = {};
   p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k; p.I = a.I; p.Is = a.Is;
   p.offsets = a.offsets;
-  p.sorted_route = a.sorted_route;
-  p.x = (const __nv_bfloat16 *)a.x;
   p.status = status;
-  const int sms = device_sms();
-  cudaError_t e;
-  if ((e = ensure_smem((const void *)tc_wgrad_kernel<WGRAD_DOWN>, WG_SMEM)) != cudaSuccess) return e;
-  if ((e = ensure_smem((const void *)tc_wgrad_kernel<WGRAD_GATE_UP>, WG_SMEM)) != cudaSuccess) return e;
   // down: M = H, N = I
   p.tm_r = a.H / 128; p.tn_r = a.I / 256; p.tm_s = a.H / 128; p.tn_s = a.Is / 256;
   p.total = p.tm_s * p.tn_s + a.E * p.tm_r * p.tn_r;
-  tc_wgrad_kernel<WGRAD_DOWN><<<std::min(p.total, sms), wg_threads<WGRAD_DOWN>(), WG_SMEM, stream>>>(md, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaError_t e = launch_wgrad<WGRAD_DOWN>(md, p, stream);
+  if (e != cudaSuccess) return e;
   // gate_up: M = 2I, N = H
   p.tm_r = 2 * a.I / 128; p.tn_r = a.H / 256; p.tm_s = 2 * a.Is / 128; p.tn_s = a.H / 256;
   p.total = p.tm_s * p.tn_s + a.E * p.tm_r * p.tn_r;
-  tc_wgrad_kernel<WGRAD_GATE_UP><<<std::min(p.total, sms), wg_threads<WGRAD_GATE_UP>(), WG_SMEM, stream>>>(mg, p);
-  return cudaGetLastError();
+  return launch_wgrad<WGRAD_GATE_UP>(mg, p, stream);
 }
 
 }  // namespace moe

@@ -90,6 +90,7 @@ struct BwArgs {
   void *dgu_shared;             // [T, 2Is] dtype
   float *dxr;                   // [T*k, H] sorted order: input grad of each route
   float *dxs;                   // [T, H]: input grad through the shared expert
+  void *x_sorted;               // [T*k, H] dtype, sorted order: x of the route's token (tensor-core path)
   float *dlogit;                // [T, k]
   float *dz;                    // [T]
 };

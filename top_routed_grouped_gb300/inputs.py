@@ -19,6 +19,9 @@ bf16_t1024             1024    2048  512  10  512  512  bf16   near-uniform rout
 bf16_t8192             8192    2048  512  10  512  512  bf16   one 8K packed sequence
 bf16_t16384_zipf       16384   2048  512  10  512  512  bf16   Zipf(1.1) logit bias
 bf16_t4096_fwdbwd      4096    2048  512  10  512  512  bf16   forward + backward
+bf16_e64_t512          512     2048  64   10  512  512  bf16   small profiling case:
+                                                               80 routes per expert
+                                                               as at T=4096, ~1 GB
 =====================  ======  ====  ===  ==  ===  ===  =====  ====================
 
 Distributions: x ~ N(0,1); every weight ~ N(0, 0.02) (the router weight is
@@ -80,6 +83,7 @@ CONFIGS = {
     "bf16_t8192": MoEConfig("bf16_t8192", 8192, 2048, 512, 10, 512, 512, "bf16"),
     "bf16_t16384_zipf": MoEConfig("bf16_t16384_zipf", 16384, 2048, 512, 10, 512, 512, "bf16", zipf=True),
     "bf16_t4096_fwdbwd": MoEConfig("bf16_t4096_fwdbwd", 4096, 2048, 512, 10, 512, 512, "bf16", backward=True),
+    "bf16_e64_t512": MoEConfig("bf16_e64_t512", 512, 2048, 64, 10, 512, 512, "bf16", backward=True),
 }
 
 
