@@ -236,7 +236,7 @@ def fwd_bwd_bench(cfg, dev_w, steps: int, warmup: int, world: int, peaks: dict) 
     return {"workload": cfg.name, "T": T, "value": T * world / (ms * 1e-3), "unit": "tokens/s",
             "ms_per_step": ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "steps": steps, "warmup": warmup,
             "api": "moe_forward (activations saved) + moe_backward",
-            "gpu_launches_per_step": 20,
+            "gpu_launches_per_step": 24,
             "layer_roofline": {"fwd_bytes": fb["bytes"], "fwd_flops": fb["flops"], "bwd_bytes": bb["bytes"],
                                "bwd_flops": bb["flops"], "roofline_ms": t_roof, "frac": t_roof / ms,
                                "bwd_roofline_ms": roof(bb), "bwd_frac": roof(bb) / bwd_ms}}

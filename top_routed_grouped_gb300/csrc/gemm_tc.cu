@@ -65,10 +65,16 @@ struct TcCfg<1> {
 };
 template <>
 struct TcCfg<2> {
-  static constexpr int NMAX = 256, MT = 2, STAGES = 3, EPI_WARPS = 16, EPI_BYTES = 2048;
+  static constexpr int NMAX = 256, MT = 1, STAGES = 4, EPI_WARPS = 16, EPI_BYTES = 2048;
 };
-
-static_assert(TcCfg<1>::MT == 2 && TcCfg<2>::MT == 2, "the epilogues drain two M tiles per item together");
+// MT = 1: two accumulator buffers of 256 columns alternate between items, so
+// an item's epilogue overlaps the next item's mainloop.  MT = 2: the two M
+// tiles' accumulators fill TMEM and are drained between items.
+template <int MODE>
+constexpr int tc_nbuf() {
+  return TcCfg<MODE>::MT == 1 ? 2 : 1;
+}
+static_assert(TcCfg<1>::MT == 2, "the gate_up epilogue drains two M tiles per item");
 
 constexpr int TC_TILE_A_BYTES = 128 * 128;  // one M tile: 128 rows x 64 bf16
 constexpr int TC_B_BYTES = 256 * 128;       // up to 256 token rows x 64 bf16
@@ -102,6 +108,7 @@ struct TcMaps {
 struct TcParams {
   int T, H, E, k, I, Is;
   int n_items;              // ROUTER: number of items (others: item_start[E+1])
+  int rt_ntile, rt_rpt;     // ROUTER: token tiles and rows per tile
   const int32_t *offsets;
   const int32_t *sorted_route;
   const int32_t *item_start;  // [E+2] prefix of items per segment
@@ -124,10 +131,19 @@ struct Item {
   int nk;        // K blocks of 64
 };
 
+// Item `it` of the persistent loop.  The shared segment's items (the last
+// ones of the table; its row tiles are the largest) are taken first, so the
+// heaviest items do not form the tail of the launch.
+__device__ inline int item_slot(int it, const int32_t *item_start, int E) {
+  const int routed = __ldg(item_start + E), total = __ldg(item_start + E + 1);
+  const int n_sh = total - routed;
+  return it < n_sh ? routed + it : it - n_sh;
+}
+
 template <int MODE>
 __device__ inline Item decode_item(int it, const TcParams &p) {
   Item r;
-  const int4 d = __ldg(p.items + it);
+  const int4 d = __ldg(p.items + item_slot(it, p.item_start, p.E));
   r.seg = d.x;
   r.f = d.y;
   r.row0 = d.z;
@@ -160,7 +176,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   int32_t *tok_all = (int32_t *)(epi + TC_EPI_MAX_BYTES);
   uint64_t *bars = (uint64_t *)(tok_all + TC_TOK_INTS);
   uint64_t *full = bars, *empty = bars + TC_MAX_STAGES;
-  uint64_t *tfull = bars + 2 * TC_MAX_STAGES, *tempty = tfull + 1, *mma_done = tempty + 1;
+  constexpr int NBUF = tc_nbuf<MODE>();
+  uint64_t *tfull = bars + 2 * TC_MAX_STAGES, *tempty = tfull + NBUF, *mma_done = tempty + NBUF;
   uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
 
@@ -170,8 +187,10 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       mbar_init(&full[s], 1 + (MODE == TC_GATE_UP ? GATHER_THREADS : 0));
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, 32 * EPI_WARPS);
+    for (int b = 0; b < NBUF; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 32 * EPI_WARPS);
+    }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -211,7 +230,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                         pol_w);
           } else {
             tma_load_2d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64,
-                        sh ? im.f * 256 : im.seg * p.H + im.f * 256, pol_w);
+                        (sh ? 0 : im.seg * p.H) + im.f * 128 * MT, pol_w);
           }
           if (MODE != TC_GATE_UP) {
             // Token rows [row0, row0 + n) as power-of-two boxes (n is a multiple of 16).
@@ -245,11 +264,12 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      uint32_t phase = 0, cnt = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
         const Item im = decode_item<MODE>(it, p);
-        if (!mbar_wait(tempty, acc_phase ^ 1, abort_flag, p.status)) break;
+        const int b = cnt % NBUF;
+        if (!mbar_wait(&tempty[b], ((cnt / NBUF) & 1) ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32(128, im.n);
         for (int kb = 0; kb < im.nk; ++kb) {
@@ -258,7 +278,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           const uint64_t bd = smem_desc_sw128(smem_u32(sb + stage * TC_B_BYTES));
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
-            const uint32_t d = tmem + mt * 256;
+            const uint32_t d = tmem + (b * MT + mt) * 256;
             const uint32_t accumulate = kb != 0;
             const uint64_t ad = smem_desc_sw128(smem_u32(sa + stage * A_BYTES + mt * TC_TILE_A_BYTES));
 #pragma unroll
@@ -269,8 +289,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
         if (!ok) break;
-        mma_commit(tfull);
-        acc_phase ^= 1;
+        mma_commit(&tfull[b]);
+        ++cnt;
       }
       // Every MMA this thread issued has finished before TMEM is released.
       mma_commit(mma_done);
@@ -285,12 +305,13 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     constexpr int CSTEP = 32 * (EPI_WARPS / 4);
     const int cfirst = 32 * ((warp - TC_EPI_FIRST) >> 2);
     uint8_t *stg = epi + (warp - TC_EPI_FIRST) * EPI_BYTES;
-    uint32_t acc_phase = 0;
+    uint32_t cnt = 0;
     for (int it = blockIdx.x; it < total; it += gridDim.x) {
       const Item im = decode_item<MODE>(it, p);
-      if (!warp_wait(tfull, acc_phase, abort_flag, p.status)) break;
+      const int b = cnt % NBUF;
+      if (!warp_wait(&tfull[b], (cnt / NBUF) & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+      const uint32_t tq = tmem + b * MT * 256 + ((uint32_t)(q * 32) << 16);
       if (MODE == TC_GATE_UP) {
         const bool sh = im.seg == p.E;
         const int Iseg = sh ? p.Is : p.I;
@@ -368,8 +389,9 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           // Destination row of column c0 + lane, fetched before the accumulator loads.
           int dst = 0;
           if (c0 + lane < im.rows) dst = sh ? (int)(im.row0 + c0 + lane) : __ldg(p.sorted_route + im.row0 + c0 + lane);
-          float vt[2][32];
-          tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[1]);
+          float vt[MT][32];
+          if (MT == 2) tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[MT - 1]);
+          else tmem_ld32(tq + c0, vt[0]);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             const int ocol = (im.f * MT + mt) * 128 + q * 32;  // first output feature of this warp's 32
@@ -395,8 +417,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
       }
       tc_fence_before();
-      mbar_arrive(tempty);
-      acc_phase ^= 1;
+      mbar_arrive(&tempty[b]);
+      ++cnt;
     }
   } else if (MODE == TC_GATE_UP) {
     // ------------------------------------------------------------ row gather (warps 10..17)
@@ -474,14 +496,15 @@ struct RtItem {
   int rows, n;
 };
 
-__device__ inline RtItem rt_item(int it, int T) {
-  const int ntile = (int)ceil_div(T, RT_NMAX);
-  const int rpt = (int)round_up(ceil_div(T, ntile), 16);
-  const int nt = it % ntile;
+// Token tiles of rt_rpt rows (a multiple of 16, at most 256); the host picks
+// the tile count so that the items fill the SMs.  A logit's K order does not
+// depend on the tile its token falls in.
+__device__ inline RtItem rt_item(int it, const TcParams &p) {
+  const int nt = it % p.rt_ntile;
   RtItem r;
-  r.f = it / ntile;
-  r.row0 = (int64_t)nt * rpt;
-  r.rows = min(rpt, T - nt * rpt);
+  r.f = it / p.rt_ntile;
+  r.row0 = (int64_t)nt * p.rt_rpt;
+  r.rows = min(p.rt_rpt, p.T - nt * p.rt_rpt);
   r.n = (int)round_up(r.rows, 16);
   return r;
 }
@@ -528,7 +551,7 @@ tc_router_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       uint32_t phase = 0, issued = 0, issued_phase = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-        const RtItem im = rt_item(it, p.T);
+        const RtItem im = rt_item(it, p);
         const uint32_t bytes = RT_A_BYTES + im.n * 128;
         for (int j = 0; j < nkh; ++j) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
@@ -566,7 +589,7 @@ tc_router_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       uint32_t phase = 0, uses = 0;  // uses: bit b = parity of the uses of TMEM buffer b
       bool ok = true;
       for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-        const RtItem im = rt_item(it, p.T);
+        const RtItem im = rt_item(it, p);
         const uint32_t idesc = idesc_bf16_f32(128, im.n);
         for (int c = 0; c < RT_CHUNKS && ok; ++c) {
           const int b = c & 1;
@@ -605,7 +628,7 @@ tc_router_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     uint32_t uses = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
-      const RtItem im = rt_item(it, p.T);
+      const RtItem im = rt_item(it, p);
       float acc[128];
 #pragma unroll
       for (int c = 0; c < RT_CHUNKS; ++c) {
@@ -651,90 +674,106 @@ tc_router_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
 // exact in FP32 and holds at most 16 then 8 significant bits, so W3 captures
 // the rest and W1 + W2 + W3 = w exactly.
 // ---------------------------------------------------------------------------
-__global__ void split_router_weight_kernel(int64_t n, int H, const float *__restrict__ wr,
+__global__ void split_router_weight_kernel(int64_t n4, int H, const float4 *__restrict__ wr,
                                            __nv_bfloat16 *__restrict__ wr3) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  const int64_t e = i / H, h = i % H;
-  const float w = wr[i];
-  const __nv_bfloat16 w1 = __float2bfloat16_rn(w);
-  const float r1 = w - __bfloat162float(w1);
-  const __nv_bfloat16 w2 = __float2bfloat16_rn(r1);
-  const float r2 = r1 - __bfloat162float(w2);
-  const __nv_bfloat16 w3 = __float2bfloat16_rn(r2);
-  __nv_bfloat16 *row = wr3 + e * 3 * H;
-  row[h] = w1;
-  row[H + h] = w2;
-  row[2 * H + h] = w3;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // four consecutive weights
+  if (i >= n4) return;
+  const int64_t e = (i * 4) / H, h = (i * 4) % H;  // H % 4 == 0: the four share a row
+  const float4 w4 = __ldg(wr + i);
+  const float w[4] = {w4.x, w4.y, w4.z, w4.w};
+  __nv_bfloat162 p1[2], p2[2], p3[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    __nv_bfloat16 a[2], b[2], c[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float v = w[2 * j + q];
+      a[q] = __float2bfloat16_rn(v);
+      const float r1 = v - __bfloat162float(a[q]);
+      b[q] = __float2bfloat16_rn(r1);
+      const float r2 = r1 - __bfloat162float(b[q]);
+      c[q] = __float2bfloat16_rn(r2);
+    }
+    p1[j] = __halves2bfloat162(a[0], a[1]);
+    p2[j] = __halves2bfloat162(b[0], b[1]);
+    p3[j] = __halves2bfloat162(c[0], c[1]);
+  }
+  __nv_bfloat16 *row = wr3 + e * 3 * H + h;
+  *(uint2 *)row = *(const uint2 *)p1;
+  *(uint2 *)(row + H) = *(const uint2 *)p2;
+  *(uint2 *)(row + 2 * H) = *(const uint2 *)p3;
 }
 
-// Item prefixes of both grouped GEMMs (one block): start_x[s] = sum_{s' < s}
-// ceil(n_s' / 256) * nf_s', with nf the number of M-tile pairs of routed
-// segments (nf_*_r) and of the shared segment n_E = T (nf_*_s).
+// Item tables of two grouped GEMMs over the same segments, one block of 1024
+// threads.  start_x[s] = sum_{s' < s} ceil(n_s' / 256) * nf_s' (nf_*_r for the
+// routed segments, nf_*_s for the shared segment n_E = T); items[it] =
+// (segment, M-tile pair, first row, rows): the rows of a segment are cut into
+// ceil(n / 256) tiles of equal size rounded up to 16, a cut that depends only
+// on the segment's own length.  One block forms the prefixes; the expansion
+// runs one warp per segment.
+constexpr int IT_MAX_E = 1024;
+
 __global__ void __launch_bounds__(1024)
-build_items_kernel(int E, int T, int nf_gu_r, int nf_gu_s, int nf_dn_r, int nf_dn_s,
-                   const int32_t *__restrict__ offsets, int32_t *__restrict__ start_gu,
-                   int32_t *__restrict__ start_dn) {
+item_tables_kernel(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s, const int32_t *__restrict__ offsets,
+                   int32_t *__restrict__ start_a, int32_t *__restrict__ start_b, int4 *__restrict__ items_a,
+                   int4 *__restrict__ items_b, int max_a, int max_b) {
+  __shared__ int32_t s_off[IT_MAX_E + 1], s_a[IT_MAX_E + 2], s_b[IT_MAX_E + 2];
   __shared__ int32_t buf[1024];
   __shared__ int32_t carry;
+  for (int i = threadIdx.x; i <= E; i += 1024) s_off[i] = offsets[i];
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   for (int base = 0; base <= E; base += 1024) {
     const int s = base + threadIdx.x;
     int32_t v = 0;
-    if (s < E) v = (int32_t)ceil_div(offsets[s + 1] - offsets[s], 256);
+    if (s < E) v = (int32_t)ceil_div(s_off[s + 1] - s_off[s], 256);
     else if (s == E) v = (int32_t)ceil_div(T, 256);
     buf[threadIdx.x] = v;
     __syncthreads();
     for (int d = 1; d < 1024; d <<= 1) {
-      int32_t add = (int)threadIdx.x >= d ? buf[threadIdx.x - d] : 0;
+      const int32_t add = (int)threadIdx.x >= d ? buf[threadIdx.x - d] : 0;
       __syncthreads();
       buf[threadIdx.x] += add;
       __syncthreads();
     }
-    // tiles before segment s (routed segments only; the shared one is last)
-    const int32_t before = carry + buf[threadIdx.x] - v;
+    const int32_t before = carry + buf[threadIdx.x] - v;  // row tiles before segment s
     if (s <= E) {
-      start_gu[s] = before * nf_gu_r;
-      start_dn[s] = before * nf_dn_r;
+      s_a[s] = before * nf_a_r;
+      s_b[s] = before * nf_b_r;
     }
     if (s == E) {
-      start_gu[E + 1] = before * nf_gu_r + v * nf_gu_s;
-      start_dn[E + 1] = before * nf_dn_r + v * nf_dn_s;
+      s_a[E + 1] = before * nf_a_r + v * nf_a_s;
+      s_b[E + 1] = before * nf_b_r + v * nf_b_s;
     }
     __syncthreads();
     if (threadIdx.x == 1023) carry += buf[1023];
     __syncthreads();
   }
-}
-
-// items[it] = (segment, M-tile pair, first row, rows) for it < start[E+1], for
-// both tables: the rows of a segment are cut into ceil(n / 256) tiles of equal
-// size rounded up to 16, a cut that depends only on the segment's own length.
-__device__ inline void expand_item(int it, int E, int T, const int32_t *offsets, const int32_t *start,
-                                   int4 *items) {
-  int lo = 0, hi = E;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (start[mid] <= it) lo = mid;
-    else hi = mid - 1;
+  for (int i = threadIdx.x; i <= E + 1; i += 1024) {
+    start_a[i] = s_a[i];
+    start_b[i] = s_b[i];
   }
-  const int local = it - start[lo];
-  const int base = lo == E ? 0 : offsets[lo];
-  const int n_s = lo == E ? T : offsets[lo + 1] - base;
-  const int ntile = (int)ceil_div(n_s, 256);
-  const int rpt = (int)round_up(ceil_div(n_s, ntile), 16);
-  const int nt = local % ntile;
-  items[it] = make_int4(lo, local / ntile, base + nt * rpt, min(rpt, n_s - nt * rpt));
 }
 
-__global__ void expand_items_kernel(int E, int T, int max_gu, int max_dn, const int32_t *__restrict__ offsets,
-                                    const int32_t *__restrict__ start_gu, const int32_t *__restrict__ start_dn,
-                                    int4 *__restrict__ items_gu, int4 *__restrict__ items_dn) {
-  const int n_gu = min(start_gu[E + 1], max_gu), n_dn = min(start_dn[E + 1], max_dn);
-  for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < max(n_gu, n_dn); it += gridDim.x * blockDim.x) {
-    if (it < n_gu) expand_item(it, E, T, offsets, start_gu, items_gu);
-    if (it < n_dn) expand_item(it, E, T, offsets, start_dn, items_dn);
+// Expansion: one warp per segment writes that segment's items of both tables.
+__global__ void __launch_bounds__(256)
+item_expand_kernel(int E, int T, const int32_t *__restrict__ offsets, const int32_t *__restrict__ start_a,
+                   const int32_t *__restrict__ start_b, int4 *__restrict__ items_a, int4 *__restrict__ items_b,
+                   int max_a, int max_b) {
+  const int sg = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+  if (sg > E) return;
+  const int base = sg == E ? 0 : __ldg(offsets + sg);
+  const int n_s = sg == E ? T : __ldg(offsets + sg + 1) - base;
+  if (n_s == 0) return;
+  const int ntile = (n_s + 255) >> 8;
+  const int rpt = ((n_s + ntile - 1) / ntile + 15) & ~15;
+  const int a0 = __ldg(start_a + sg), na = __ldg(start_a + sg + 1) - a0;
+  const int b0 = __ldg(start_b + sg), nb = __ldg(start_b + sg + 1) - b0;
+  for (int local = lane; local < max(na, nb); local += 32) {
+    const int nt = local % ntile;
+    const int4 v = make_int4(sg, local / ntile, base + nt * rpt, min(rpt, n_s - nt * rpt));
+    if (local < na && a0 + local < max_a) items_a[a0 + local] = v;
+    if (local < nb && b0 + local < max_b) items_b[b0 + local] = v;
   }
 }
 
@@ -753,21 +792,25 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
                                     float *logits, void *scratch, int *status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   __nv_bfloat16 *wr3 = (__nv_bfloat16 *)scratch;
-  const int64_t n = (int64_t)E * H;
-  split_router_weight_kernel<<<(unsigned)ceil_div(n, 256), 256, 0, stream>>>(n, H, wr, wr3);
+  const int64_t n4 = (int64_t)E * H / 4;
+  split_router_weight_kernel<<<(unsigned)ceil_div(n4, 256), 256, 0, stream>>>(n4, H, (const float4 *)wr, wr3);
   TcMaps m;
   if (!map_2d(&m.a, wr3, E, 3 * (int64_t)H, 128) || !map_rows(m.b, x, T, H)) return cudaErrorInvalidValue;
   m.a_sh = m.a;
   for (int h = 0; h < 5; ++h) m.b_sh[h] = m.b[h];
   TcParams p = {};
   p.T = T; p.H = H; p.E = E;
-  p.n_items = (int)(ceil_div(E, 128) * ceil_div(T, RT_NMAX));
+  const int etiles = (int)ceil_div(E, 128), sms = device_sms();
+  const int want = std::max<int>((int)ceil_div(T, RT_NMAX), std::min<int>(sms / etiles, (int)ceil_div(T, 16)));
+  p.rt_rpt = (int)round_up(ceil_div(T, want), 16);
+  p.rt_ntile = (int)ceil_div(T, p.rt_rpt);
+  p.n_items = etiles * p.rt_ntile;
   p.bias = bias;
   p.logits = logits;
   p.status = status;
   cudaError_t e = ensure_smem((const void *)tc_router_kernel, TC_SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int grid = std::min(p.n_items, device_sms());
+  const int grid = std::min(p.n_items, sms);
   tc_router_kernel<<<grid, RT_THREADS, TC_SMEM_BYTES, stream>>>(m, p);
   return cudaGetLastError();
 }
@@ -784,9 +827,11 @@ static int64_t max_items(int T, int k, int E, int nf_routed, int nf_shared) {
 cudaError_t launch_item_tables(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s, const int32_t *offsets,
                                int32_t *start_a, int32_t *start_b, int4 *items_a, int4 *items_b, int max_a,
                                int max_b, cudaStream_t stream) {
-  build_items_kernel<<<1, 1024, 0, stream>>>(E, T, nf_a_r, nf_a_s, nf_b_r, nf_b_s, offsets, start_a, start_b);
-  expand_items_kernel<<<(unsigned)std::min<int64_t>(ceil_div(std::max(max_a, max_b), 256), 1024), 256, 0, stream>>>(
-      E, T, max_a, max_b, offsets, start_a, start_b, items_a, items_b);
+  if (E > IT_MAX_E) return cudaErrorInvalidValue;
+  item_tables_kernel<<<1, 1024, 0, stream>>>(E, T, nf_a_r, nf_a_s, nf_b_r, nf_b_s, offsets, start_a, start_b, items_a,
+                                             items_b, max_a, max_b);
+  item_expand_kernel<<<(unsigned)ceil_div((int64_t)(E + 1) * 32, 256), 256, 0, stream>>>(E, T, offsets, start_a, start_b,
+                                                                                      items_a, items_b, max_a, max_b);
   return cudaGetLastError();
 }
 
@@ -794,27 +839,29 @@ static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 size_t ffn_tc_scratch_bytes(int T, int k, int E, int H, int I, int Is) {
   const size_t starts = round256((size_t)(E + 2) * 4);
+  constexpr int DN_ROWS = 128 * TcCfg<TC_DOWN>::MT;  // output features per down item
   return 2 * starts + round256((size_t)max_items(T, k, E, I / 128, Is / 128) * 16) +
-         round256((size_t)max_items(T, k, E, H / 256, H / 256) * 16);
+         round256((size_t)max_items(T, k, E, H / DN_ROWS, H / DN_ROWS) * 16);
 }
 
 cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
   const size_t starts = round256((size_t)(a.E + 2) * 4);
   const int mi_gu = (int)max_items(a.T, a.k, a.E, a.I / 128, a.Is / 128);
-  const int mi_dn = (int)max_items(a.T, a.k, a.E, a.H / 256, a.H / 256);
+  constexpr int DN_ROWS = 128 * TcCfg<TC_DOWN>::MT;
+  const int mi_dn = (int)max_items(a.T, a.k, a.E, a.H / DN_ROWS, a.H / DN_ROWS);
   uint8_t *w = (uint8_t *)scratch;
   int32_t *start_gu = (int32_t *)w;
   int32_t *start_dn = (int32_t *)(w + starts);
   int4 *items_gu = (int4 *)(w + 2 * starts);
   int4 *items_dn = (int4 *)(w + 2 * starts + round256((size_t)mi_gu * 16));
-  cudaError_t e0 = launch_item_tables(a.E, a.T, a.I / 128, a.Is / 128, a.H / 256, a.H / 256, a.offsets, start_gu,
-                                      start_dn, items_gu, items_dn, mi_gu, mi_dn, stream);
+  cudaError_t e0 = launch_item_tables(a.E, a.T, a.I / 128, a.Is / 128, a.H / DN_ROWS, a.H / DN_ROWS, a.offsets,
+                                      start_gu, start_dn, items_gu, items_dn, mi_gu, mi_dn, stream);
   if (e0 != cudaSuccess) return e0;
   const int64_t R = (int64_t)a.T * a.k;
   TcMaps mg, md;
   if (!map_gate_up(&mg.a, a.w_gate_up, a.E, a.I, a.H) || !map_gate_up(&mg.a_sh, a.ws_gate_up, 1, a.Is, a.H) ||
-      !map_2d(&md.a, a.w_down, (int64_t)a.E * a.H, a.I, 256) || !map_2d(&md.a_sh, a.ws_down, a.H, a.Is, 256) ||
+      !map_2d(&md.a, a.w_down, (int64_t)a.E * a.H, a.I, DN_ROWS) || !map_2d(&md.a_sh, a.ws_down, a.H, a.Is, DN_ROWS) ||
       !map_rows(md.b, a.h_routed, R, a.I) || !map_rows(md.b_sh, a.h_shared, a.T, a.Is))
     return cudaErrorInvalidValue;
   for (int h = 0; h < 5; ++h) mg.b[h] = mg.b_sh[h] = mg.a;  // gate_up gathers its token rows with cp.async

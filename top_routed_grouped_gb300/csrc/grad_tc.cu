@@ -98,9 +98,12 @@ struct DgItem {
   int64_t row0;
 };
 
+// The shared segment's items (last in the table, the largest row tiles) first.
 template <int MODE>
 __device__ inline DgItem dg_item(int it, const DgParams &p) {
-  const int4 d = __ldg(p.items + it);
+  const int routed = __ldg(p.item_start + p.E), total = __ldg(p.item_start + p.E + 1);
+  const int n_sh = total - routed;
+  const int4 d = __ldg(p.items + (it < n_sh ? routed + it : it - n_sh));
   DgItem r;
   r.seg = d.x;
   r.f = d.y;

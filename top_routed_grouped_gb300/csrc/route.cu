@@ -125,6 +125,13 @@ topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, c
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
 
+  // The token's logits are requested first, so that they arrive while the
+  // gate operands stream in.
+  float lv[EPL];
+  const float *lrow = logits + t * E;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) lv[i] = lane + 32 * i < E ? __ldg(lrow + lane + 32 * i) : 0.f;
+
   // Shared-expert gate: lane chunks h = (lane + 32 m) VN, m ascending, summed
   // in that order per lane, then a fixed butterfly.
   constexpr int VN = Vec16<TX>::N;
@@ -156,9 +163,8 @@ topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, c
 
   // Top-k: order values formed once; the winner's owner zeroes its value and rescans.
   uint32_t ov[EPL];
-  const float *lrow = logits + t * E;
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) ov[i] = lane + 32 * i < E ? topk_ord(lrow[lane + 32 * i]) : 0u;
+  for (int i = 0; i < EPL; ++i) ov[i] = lane + 32 * i < E ? topk_ord(lv[i]) : 0u;
   uint32_t bo = 0u;
   int bi = 0;
 #pragma unroll
@@ -168,14 +174,10 @@ topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, c
   float sel_v = 0.f;  // lane s keeps the logit of slot s
   int sel_e = 0;
   for (int s = 0; s < k; ++s) {
-    uint32_t mo = bo;
-    int me = lane + 32 * bi;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const uint32_t oo = __shfl_xor_sync(FULL_MASK, mo, off);
-      const int oe = __shfl_xor_sync(FULL_MASK, me, off);
-      if (topk_better(oo, oe, mo, me)) mo = oo, me = oe;
-    }
+    // Warp maximum of the lanes' best order values, then the lowest expert
+    // id among the lanes that hold it (the strict total order of above).
+    const uint32_t mo = __reduce_max_sync(FULL_MASK, bo);
+    const int me = (int)__reduce_min_sync(FULL_MASK, bo == mo ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
     if (lane == s) {
       sel_v = ord_logit(mo);
       sel_e = me;
@@ -191,13 +193,14 @@ topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, c
     }
   }
 
-  // Route weights.  Every lane forms the same denominator in slot order.
+  // Route weights: lane s forms exp(l_s - l_0) once; every lane sums them in slot order.
   const float m0 = __shfl_sync(FULL_MASK, sel_v, 0);
+  const float ex = lane < k ? expf(sel_v - m0) : 0.f;
   float z = 0.f;
-  for (int s = 0; s < k; ++s) z += expf(__shfl_sync(FULL_MASK, sel_v, s) - m0);
+  for (int s = 0; s < k; ++s) z += __shfl_sync(FULL_MASK, ex, s);
   if (lane < k) {
     ids[t * k + lane] = sel_e;
-    w[t * k + lane] = expf(sel_v - m0) / z;
+    w[t * k + lane] = ex / z;
   }
   if (lane == 0) sig[t] = sigmoid_f32(part);
 }
