@@ -36,6 +36,8 @@ combine_bwd_kernel(int T, int H, int k, const TE *__restrict__ dy, const TE *__r
                    const TE *__restrict__ ys, const float *__restrict__ w, const float *__restrict__ sig,
                    const int32_t *__restrict__ route_pos, TE *__restrict__ dyr_sorted, TE *__restrict__ dys,
                    float *__restrict__ dlogit, float *__restrict__ dz) {
+  griddep_launch();
+  griddep_wait();
   constexpr int VN = Vec16<TE>::N;
   const int lane = threadIdx.x & 31;
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -129,6 +131,8 @@ __device__ inline BwTile bw_decode(int ti, int E, int T, const int32_t *tile_sta
 template <typename TE>
 __global__ void __launch_bounds__(256)
 down_dgrad_swiglu_kernel(BwArgs a, const int32_t *__restrict__ tile_start) {
+  griddep_launch();
+  griddep_wait();
   __shared__ float ds[32][BW_BM + 1];   // [h][row]
   __shared__ float wd[32][65];          // [h][i]
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -191,6 +195,8 @@ down_dgrad_swiglu_kernel(BwArgs a, const int32_t *__restrict__ tile_start) {
 template <typename TE>
 __global__ void __launch_bounds__(256)
 gate_up_dgrad_kernel(BwArgs a, const int32_t *__restrict__ tile_start) {
+  griddep_launch();
+  griddep_wait();
   __shared__ float gs[32][BW_BM + 1];  // [f][row]
   __shared__ float wg[32][65];         // [f][h]
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -250,6 +256,8 @@ enum { WG_DOWN = 0, WG_GATE_UP = 1 };
 
 template <typename TE, int KIND>
 __global__ void __launch_bounds__(256) wgrad_kernel(BwArgs a) {
+  griddep_launch();
+  griddep_wait();
   __shared__ float as[16][65];  // [row][m]
   __shared__ float bs[16][65];  // [row][n]
   const int seg = blockIdx.z;
@@ -320,6 +328,8 @@ constexpr int RG_CHUNK = 64;
 template <typename TE>
 __global__ void __launch_bounds__(256)
 router_gate_partial_kernel(BwArgs a, const int32_t *__restrict__ chunk_start, float *__restrict__ partial) {
+  griddep_launch();
+  griddep_wait();
   __shared__ int64_t srow[RG_CHUNK];  // element offset of each row's x
   __shared__ float scoef[RG_CHUNK];
   const int total = chunk_start[a.E + 1];
@@ -351,6 +361,8 @@ router_gate_partial_kernel(BwArgs a, const int32_t *__restrict__ chunk_start, fl
 
 __global__ void __launch_bounds__(256)
 router_gate_reduce_kernel(BwArgs a, const int32_t *__restrict__ chunk_start, const float *__restrict__ partial) {
+  griddep_launch();
+  griddep_wait();
   const int seg = blockIdx.y;
   const int h = blockIdx.x * 256 + threadIdx.x;
   if (h >= a.H) return;
@@ -366,6 +378,8 @@ router_gate_reduce_kernel(BwArgs a, const int32_t *__restrict__ chunk_start, con
 // 16-byte chunk.
 template <typename TE>
 __global__ void __launch_bounds__(256) dx_kernel(BwArgs a) {
+  griddep_launch();
+  griddep_wait();
   constexpr int VN = Vec16<TE>::N;
   const int lane = threadIdx.x & 31;
   const int per_row = a.H / (32 * VN);  // warps per token (H is a multiple of 32 VN here)
@@ -441,6 +455,8 @@ __global__ void __launch_bounds__(256) dx_kernel(BwArgs a) {
 // one thread per (token, 16-byte chunk), same order of the sums.
 template <typename TE>
 __global__ void __launch_bounds__(256) dx_thread_kernel(BwArgs a) {
+  griddep_launch();
+  griddep_wait();
   constexpr int VN = Vec16<TE>::N;
   const int per_row = a.H / VN;
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -516,40 +532,51 @@ size_t backward_scratch_bytes(int dtype, int T, int k, int E, int H, int I, int 
 template <typename TE>
 static cudaError_t run_backward(const BwArgs &a, void *scratch, int *status, cudaStream_t stream) {
   const int64_t R = (int64_t)a.T * a.k;
-  combine_bwd_kernel<TE><<<(unsigned)ceil_div(a.T, 8), 256, 0, stream>>>(
-      a.T, a.H, a.k, (const TE *)a.dy, (const TE *)a.y_routed, (const TE *)a.y_shared, a.topk_w, a.shared_sig,
-      a.route_pos, (TE *)a.dyr, (TE *)a.dys, a.dlogit, a.dz);
   cudaError_t err;
+#define MOE_TRY(x) \
+  if ((err = (x)) != cudaSuccess) return err
+  MOE_TRY(launch_pdl(combine_bwd_kernel<TE>, dim3((unsigned)ceil_div(a.T, 8)), dim3(256), 0, stream, a.T, a.H, a.k,
+                     (const TE *)a.dy, (const TE *)a.y_routed, (const TE *)a.y_shared, a.topk_w, a.shared_sig,
+                     a.route_pos, (TE *)a.dyr, (TE *)a.dys, a.dlogit, a.dz));
   const int Imax = a.I > a.Is ? a.I : a.Is;
   if (sizeof(TE) == 2 && backward_tc_supported(a.H, a.I, a.Is)) {
-    if ((err = launch_dgrad_tc(a, scratch, status, stream)) != cudaSuccess) return err;
-    if ((err = launch_wgrad_tc(a, status, stream)) != cudaSuccess) return err;
+    MOE_TRY(launch_dgrad_tc(a, scratch, status, stream));
+    MOE_TRY(launch_wgrad_tc(a, status, stream));
   } else {
     int32_t *tile_start = (int32_t *)scratch;
-    if ((err = launch_build_tiles(a.E, a.T, BW_BM, a.offsets, tile_start, stream)) != cudaSuccess) return err;
+    const int32_t *ts = tile_start;
+    MOE_TRY(launch_build_tiles(a.E, a.T, BW_BM, a.offsets, tile_start, stream));
     const int64_t max_tiles = ceil_div(R + a.T, BW_BM) + a.E + 1;
     const unsigned gx = (unsigned)(max_tiles < 65535 ? max_tiles : 65535);
-    down_dgrad_swiglu_kernel<TE><<<dim3(gx, (unsigned)ceil_div(Imax, 64)), 256, 0, stream>>>(a, tile_start);
-    gate_up_dgrad_kernel<TE><<<dim3(gx, (unsigned)ceil_div(a.H, 64)), 256, 0, stream>>>(a, tile_start);
-    wgrad_kernel<TE, WG_DOWN><<<dim3((unsigned)ceil_div(Imax, 64), (unsigned)ceil_div(a.H, 64), a.E + 1), 256, 0,
-                                stream>>>(a);
-    wgrad_kernel<TE, WG_GATE_UP><<<dim3((unsigned)ceil_div(a.H, 64), (unsigned)ceil_div(2 * Imax, 64), a.E + 1),
-                                   256, 0, stream>>>(a);
+    MOE_TRY(launch_pdl(down_dgrad_swiglu_kernel<TE>, dim3(gx, (unsigned)ceil_div(Imax, 64)), dim3(256), 0, stream, a,
+                       ts));
+    MOE_TRY(launch_pdl(gate_up_dgrad_kernel<TE>, dim3(gx, (unsigned)ceil_div(a.H, 64)), dim3(256), 0, stream, a, ts));
+    MOE_TRY(launch_pdl(wgrad_kernel<TE, WG_DOWN>,
+                       dim3((unsigned)ceil_div(Imax, 64), (unsigned)ceil_div(a.H, 64), a.E + 1), dim3(256), 0, stream,
+                       a));
+    MOE_TRY(launch_pdl(wgrad_kernel<TE, WG_GATE_UP>,
+                       dim3((unsigned)ceil_div(a.H, 64), (unsigned)ceil_div(2 * Imax, 64), a.E + 1), dim3(256), 0,
+                       stream, a));
   }
   const int dtype = sizeof(TE) == 4 ? 0 : 1;
   uint8_t *rest = (uint8_t *)scratch + round_up((int64_t)gemm_scratch_bytes(dtype, a.T, a.k, a.E, a.H, a.I, a.Is), 256);
   int32_t *chunk_start = (int32_t *)rest;
+  const int32_t *cs = chunk_start;
   float *partial = (float *)(rest + round_up((int64_t)(a.E + 2) * 4, 256));
-  if ((err = launch_build_tiles(a.E, a.T, RG_CHUNK, a.offsets, chunk_start, stream)) != cudaSuccess) return err;
+  const float *pc = partial;
+  MOE_TRY(launch_build_tiles(a.E, a.T, RG_CHUNK, a.offsets, chunk_start, stream));
   const int64_t mc = max_chunks(a.T, a.k, a.E);
-  router_gate_partial_kernel<TE><<<dim3((unsigned)std::min<int64_t>(mc, 65535), (unsigned)ceil_div(a.H, 256)), 256, 0,
-                                   stream>>>(a, chunk_start, partial);
-  router_gate_reduce_kernel<<<dim3((unsigned)ceil_div(a.H, 256), a.E + 1), 256, 0, stream>>>(a, chunk_start, partial);
+  MOE_TRY(launch_pdl(router_gate_partial_kernel<TE>,
+                     dim3((unsigned)std::min<int64_t>(mc, 65535), (unsigned)ceil_div(a.H, 256)), dim3(256), 0, stream,
+                     a, cs, partial));
+  MOE_TRY(launch_pdl(router_gate_reduce_kernel, dim3((unsigned)ceil_div(a.H, 256), a.E + 1), dim3(256), 0, stream, a,
+                     cs, pc));
   if (a.H % (32 * Vec16<TE>::N) == 0)
-    dx_kernel<TE><<<(unsigned)ceil_div((int64_t)a.T * (a.H / (32 * Vec16<TE>::N)), 8), 256, 0, stream>>>(a);
-  else
-    dx_thread_kernel<TE><<<(unsigned)ceil_div((int64_t)a.T * (a.H / Vec16<TE>::N), 256), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+    return launch_pdl(dx_kernel<TE>, dim3((unsigned)ceil_div((int64_t)a.T * (a.H / (32 * Vec16<TE>::N)), 8)),
+                      dim3(256), 0, stream, a);
+  return launch_pdl(dx_thread_kernel<TE>, dim3((unsigned)ceil_div((int64_t)a.T * (a.H / Vec16<TE>::N), 256)),
+                    dim3(256), 0, stream, a);
+#undef MOE_TRY
 }
 
 cudaError_t launch_backward(int dtype, const BwArgs &a, void *scratch, int *status, cudaStream_t stream) {

@@ -19,6 +19,8 @@ template <typename TE>
 __global__ void __launch_bounds__(256)
 combine_kernel(int T, int H, int k, const TE *__restrict__ yr, const TE *__restrict__ ys,
                const float *__restrict__ w, const float *__restrict__ sig, TE *__restrict__ y) {
+  griddep_launch();
+  griddep_wait();
   constexpr int VN = Vec16<TE>::N;
   const int vec_per_row = H / VN;
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -50,13 +52,10 @@ cudaError_t launch_combine(int dtype, int T, int H, int k, const void *y_routed,
   const int64_t n = (int64_t)T * (H / VN);
   const unsigned blocks = (unsigned)ceil_div(n, 256);
   if (dtype == 0)
-    combine_kernel<float><<<blocks, 256, 0, stream>>>(T, H, k, (const float *)y_routed, (const float *)y_shared,
-                                                      w, sig, (float *)y);
-  else
-    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(T, H, k, (const __nv_bfloat16 *)y_routed,
-                                                              (const __nv_bfloat16 *)y_shared, w, sig,
-                                                              (__nv_bfloat16 *)y);
-  return cudaGetLastError();
+    return launch_pdl(combine_kernel<float>, dim3(blocks), dim3(256), 0, stream, T, H, k, (const float *)y_routed,
+                      (const float *)y_shared, w, sig, (float *)y);
+  return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, stream, T, H, k,
+                    (const __nv_bfloat16 *)y_routed, (const __nv_bfloat16 *)y_shared, w, sig, (__nv_bfloat16 *)y);
 }
 
 }  // namespace moe

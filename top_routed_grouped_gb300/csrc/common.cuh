@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace moe {
 
 constexpr unsigned FULL_MASK = 0xffffffffu;
@@ -71,6 +73,34 @@ template <> struct Vec16<__nv_bfloat16> {
     *reinterpret_cast<uint4 *>(p) = v;
   }
 };
+
+// ---- programmatic dependent launch ----
+// Kernels of the layer are launched with programmatic stream serialization:
+// a kernel may be scheduled while its predecessor on the stream is still
+// running, so each one first lets its own dependents launch, does only
+// set-up work that touches no global memory, and waits for the predecessor
+// grid to complete (and its memory to be visible) before its first global
+// access.
+__device__ inline void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ inline void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kernel` on `stream` with programmatic stream serialization.  The
+// kernel must call griddep_wait() before reading or writing global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 __device__ inline float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 __device__ inline float sigmoid_f32(float z) { return 1.0f / (1.0f + expf(-z)); }

@@ -50,6 +50,8 @@ __device__ inline TileRows decode_tile(int ti, int E, int T, const int32_t *tile
 // 2ty, 2ty+1 and features 2tx, 2tx+1 (gate and up for each).
 template <typename TE>
 __global__ void __launch_bounds__(256) ffn_gate_up_simt_kernel(FfnArgs a, const int32_t *__restrict__ tile_start) {
+  griddep_launch();
+  griddep_wait();
   __shared__ float xs[SIMT_BK][SIMT_BM + 1];
   __shared__ float wg[SIMT_BK][33];
   __shared__ float wu[SIMT_BK][33];
@@ -122,6 +124,8 @@ __global__ void __launch_bounds__(256) ffn_gate_up_simt_kernel(FfnArgs a, const 
 // and outputs 4tx..4tx+3.  Routed row j is written to y_routed[sorted_route[j]].
 template <typename TE>
 __global__ void __launch_bounds__(256) ffn_down_simt_kernel(FfnArgs a, const int32_t *__restrict__ tile_start) {
+  griddep_launch();
+  griddep_wait();
   __shared__ float hs[SIMT_BK][SIMT_BM + 1];
   __shared__ float wd[SIMT_BK][65];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -185,9 +189,10 @@ cudaError_t launch_ffn_simt(const FfnArgs &a, void *scratch, cudaStream_t stream
   const unsigned gx = (unsigned)(max_tiles < 65535 ? max_tiles : 65535);
   dim3 g1(gx, (unsigned)ceil_div(a.I > a.Is ? a.I : a.Is, 32));
   dim3 g2(gx, (unsigned)ceil_div(a.H, 64));
-  ffn_gate_up_simt_kernel<float><<<g1, 256, 0, stream>>>(a, tile_start);
-  ffn_down_simt_kernel<float><<<g2, 256, 0, stream>>>(a, tile_start);
-  return cudaGetLastError();
+  const int32_t *ts = tile_start;
+  err = launch_pdl(ffn_gate_up_simt_kernel<float>, g1, dim3(256), 0, stream, a, ts);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(ffn_down_simt_kernel<float>, g2, dim3(256), 0, stream, a, ts);
 }
 
 }  // namespace moe

@@ -204,6 +204,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_launch();
+  griddep_wait();
   const int total = __ldg(p.item_start + p.E + 1);
 
   if (warp == 0) {
@@ -541,6 +543,8 @@ tc_router_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_launch();
+  griddep_wait();
   const int total = p.n_items, nkh = p.H / 64;
 
   if (warp == 0) {
@@ -676,6 +680,8 @@ tc_router_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
 // ---------------------------------------------------------------------------
 __global__ void split_router_weight_kernel(int64_t n4, int H, const float4 *__restrict__ wr,
                                            __nv_bfloat16 *__restrict__ wr3) {
+  griddep_launch();
+  griddep_wait();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // four consecutive weights
   if (i >= n4) return;
   const int64_t e = (i * 4) / H, h = (i * 4) % H;  // H % 4 == 0: the four share a row
@@ -717,6 +723,8 @@ __global__ void __launch_bounds__(1024)
 item_tables_kernel(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s, const int32_t *__restrict__ offsets,
                    int32_t *__restrict__ start_a, int32_t *__restrict__ start_b, int4 *__restrict__ items_a,
                    int4 *__restrict__ items_b, int max_a, int max_b) {
+  griddep_launch();
+  griddep_wait();
   __shared__ int32_t s_off[IT_MAX_E + 1], s_a[IT_MAX_E + 2], s_b[IT_MAX_E + 2];
   __shared__ int32_t buf[1024];
   __shared__ int32_t carry;
@@ -760,6 +768,8 @@ __global__ void __launch_bounds__(256)
 item_expand_kernel(int E, int T, const int32_t *__restrict__ offsets, const int32_t *__restrict__ start_a,
                    const int32_t *__restrict__ start_b, int4 *__restrict__ items_a, int4 *__restrict__ items_b,
                    int max_a, int max_b) {
+  griddep_launch();
+  griddep_wait();
   const int sg = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
   if (sg > E) return;
   const int base = sg == E ? 0 : __ldg(offsets + sg);
@@ -782,8 +792,7 @@ template <int MODE>
 static cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream) {
   cudaError_t e = ensure_smem((const void *)tc_gemm_kernel<MODE>, TC_SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  tc_gemm_kernel<MODE><<<grid, tc_threads<MODE>(), TC_SMEM_BYTES, stream>>>(maps, p);
-  return cudaGetLastError();
+  return launch_pdl(tc_gemm_kernel<MODE>, dim3(grid), dim3(tc_threads<MODE>()), TC_SMEM_BYTES, stream, maps, p);
 }
 
 size_t router_tc_scratch_bytes(int E, int H) { return (size_t)E * 3 * H * 2; }
@@ -793,7 +802,9 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
   if (T == 0) return cudaSuccess;
   __nv_bfloat16 *wr3 = (__nv_bfloat16 *)scratch;
   const int64_t n4 = (int64_t)E * H / 4;
-  split_router_weight_kernel<<<(unsigned)ceil_div(n4, 256), 256, 0, stream>>>(n4, H, (const float4 *)wr, wr3);
+  cudaError_t e = launch_pdl(split_router_weight_kernel, dim3((unsigned)ceil_div(n4, 256)), dim3(256), 0, stream, n4, H,
+                             (const float4 *)wr, wr3);
+  if (e != cudaSuccess) return e;
   TcMaps m;
   if (!map_2d(&m.a, wr3, E, 3 * (int64_t)H, 128) || !map_rows(m.b, x, T, H)) return cudaErrorInvalidValue;
   m.a_sh = m.a;
@@ -808,11 +819,10 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
   p.bias = bias;
   p.logits = logits;
   p.status = status;
-  cudaError_t e = ensure_smem((const void *)tc_router_kernel, TC_SMEM_BYTES);
+  e = ensure_smem((const void *)tc_router_kernel, TC_SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int grid = std::min(p.n_items, sms);
-  tc_router_kernel<<<grid, RT_THREADS, TC_SMEM_BYTES, stream>>>(m, p);
-  return cudaGetLastError();
+  return launch_pdl(tc_router_kernel, dim3(grid), dim3(RT_THREADS), TC_SMEM_BYTES, stream, m, p);
 }
 
 // Upper bound on the items of a grouped GEMM: sum_s ceil(n_s / 256) <=
@@ -828,11 +838,11 @@ cudaError_t launch_item_tables(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r,
                                int32_t *start_a, int32_t *start_b, int4 *items_a, int4 *items_b, int max_a,
                                int max_b, cudaStream_t stream) {
   if (E > IT_MAX_E) return cudaErrorInvalidValue;
-  item_tables_kernel<<<1, 1024, 0, stream>>>(E, T, nf_a_r, nf_a_s, nf_b_r, nf_b_s, offsets, start_a, start_b, items_a,
-                                             items_b, max_a, max_b);
-  item_expand_kernel<<<(unsigned)ceil_div((int64_t)(E + 1) * 32, 256), 256, 0, stream>>>(E, T, offsets, start_a, start_b,
-                                                                                      items_a, items_b, max_a, max_b);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(item_tables_kernel, dim3(1), dim3(1024), 0, stream, E, T, nf_a_r, nf_a_s, nf_b_r, nf_b_s,
+                             offsets, start_a, start_b, items_a, items_b, max_a, max_b);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(item_expand_kernel, dim3((unsigned)ceil_div((int64_t)(E + 1) * 32, 256)), dim3(256), 0, stream, E,
+                    T, offsets, (const int32_t *)start_a, (const int32_t *)start_b, items_a, items_b, max_a, max_b);
 }
 
 static size_t round256(size_t b) { return (b + 255) / 256 * 256; }

@@ -152,6 +152,8 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_launch();
+  griddep_wait();
   const int total = __ldg(p.item_start + p.E + 1);
 
   if (warp == 0) {
@@ -423,6 +425,8 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_launch();
+  griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -569,6 +573,8 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
 // warp per row, 16 bytes per lane.
 __global__ void __launch_bounds__(256) gather_sorted_rows_kernel(int64_t R, int H, int k, const int32_t *sorted_route,
                                                                  const __nv_bfloat16 *x, __nv_bfloat16 *xs) {
+  griddep_launch();
+  griddep_wait();
   const int64_t j = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (j >= R) return;
@@ -594,8 +600,7 @@ template <int MODE, int MT>
 static cudaError_t launch_dgrad(const DgMaps &m, const DgParams &p, int grid, cudaStream_t stream) {
   cudaError_t e = ensure_smem((const void *)tc_dgrad_kernel<MODE, MT>, DgCfg<MT>::SMEM);
   if (e != cudaSuccess) return e;
-  tc_dgrad_kernel<MODE, MT><<<grid, DG_THREADS, DgCfg<MT>::SMEM, stream>>>(m, p);
-  return cudaGetLastError();
+  return launch_pdl(tc_dgrad_kernel<MODE, MT>, dim3(grid), dim3(DG_THREADS), DgCfg<MT>::SMEM, stream, m, p);
 }
 
 cudaError_t launch_dgrad_tc(const BwArgs &a, void *scratch, int *status, cudaStream_t stream) {
@@ -647,14 +652,15 @@ template <int MODE>
 static cudaError_t launch_wgrad(const WgMaps &m, const WgParams &p, cudaStream_t stream) {
   cudaError_t e = ensure_smem((const void *)tc_wgrad_kernel<MODE>, WG_SMEM);
   if (e != cudaSuccess) return e;
-  tc_wgrad_kernel<MODE><<<std::min(p.total, device_sms()), WG_THREADS, WG_SMEM, stream>>>(m, p);
-  return cudaGetLastError();
+  return launch_pdl(tc_wgrad_kernel<MODE>, dim3(std::min(p.total, device_sms())), dim3(WG_THREADS), WG_SMEM, stream, m,
+                    p);
 }
 
 cudaError_t launch_wgrad_tc(const BwArgs &a, int *status, cudaStream_t stream) {
   const int64_t R = (int64_t)a.T * a.k;
-  gather_sorted_rows_kernel<<<(unsigned)ceil_div(R, 8), 256, 0, stream>>>(
-      R, a.H, a.k, a.sorted_route, (const __nv_bfloat16 *)a.x, (__nv_bfloat16 *)a.x_sorted);
+  cudaError_t e0 = launch_pdl(gather_sorted_rows_kernel, dim3((unsigned)ceil_div(R, 8)), dim3(256), 0, stream, R, a.H,
+                              a.k, a.sorted_route, (const __nv_bfloat16 *)a.x, (__nv_bfloat16 *)a.x_sorted);
+  if (e0 != cudaSuccess) return e0;
   WgMaps md, mg;
   if (!wg_maps(md.a, a.dyr, R, a.H, 2) || !wg_maps(md.a_sh, a.dys, a.T, a.H, 2) ||
       !wg_maps(md.b, a.h_routed, R, a.I, 4) || !wg_maps(md.b_sh, a.h_shared, a.T, a.Is, 4) ||

@@ -31,6 +31,8 @@ size_t permute_scratch_bytes(int64_t R, int E) {
 __global__ void __launch_bounds__(32 * WARPS_PER_BLOCK)
 permute_count_kernel(int64_t R, int E, int n_chunks, const int32_t *__restrict__ ids, int32_t *__restrict__ counts,
                      int *status) {
+  griddep_launch();
+  griddep_wait();
   extern __shared__ int32_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * WARPS_PER_BLOCK + warp;
@@ -64,6 +66,8 @@ permute_count_kernel(int64_t R, int E, int n_chunks, const int32_t *__restrict__
 // grid: ceil(E/32) blocks of 32 warps; lane = expert, warp = range of chunks.
 __global__ void __launch_bounds__(1024)
 permute_scan_chunks_kernel(int E, int n_chunks, int32_t *__restrict__ counts, int32_t *__restrict__ totals) {
+  griddep_launch();
+  griddep_wait();
   __shared__ int32_t part[32][33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 32 + lane;
@@ -97,6 +101,8 @@ permute_scan_chunks_kernel(int E, int n_chunks, int32_t *__restrict__ counts, in
 // One block of 1024 threads: offsets[e] = sum_{e' < e} totals[e'], offsets[E] = total.
 __global__ void __launch_bounds__(1024)
 permute_scan_experts_kernel(int E, const int32_t *__restrict__ totals, int32_t *__restrict__ offsets) {
+  griddep_launch();
+  griddep_wait();
   __shared__ int32_t buf[1024];
   const int i = threadIdx.x;
   int32_t v = i < E ? totals[i] : 0;
@@ -116,6 +122,8 @@ __global__ void __launch_bounds__(32 * WARPS_PER_BLOCK)
 permute_scatter_kernel(int64_t R, int E, int n_chunks, const int32_t *__restrict__ ids,
                        const int32_t *__restrict__ chunk_prefix, const int32_t *__restrict__ offsets,
                        int32_t *__restrict__ sorted_route, int32_t *__restrict__ route_pos) {
+  griddep_launch();
+  griddep_wait();
   extern __shared__ int32_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * WARPS_PER_BLOCK + warp;
@@ -155,18 +163,21 @@ cudaError_t launch_permute(int64_t R, int E, const int32_t *ids, int32_t *offset
   int32_t *totals = counts + (int64_t)n_chunks * E;
   const size_t smem = (size_t)WARPS_PER_BLOCK * E * sizeof(int32_t);
   const unsigned blocks = (unsigned)ceil_div(n_chunks, WARPS_PER_BLOCK);
+  cudaError_t err;
   if (n_chunks > 0) {
-    permute_count_kernel<<<blocks, 32 * WARPS_PER_BLOCK, smem, stream>>>(R, E, n_chunks, ids, counts, status);
-    permute_scan_chunks_kernel<<<(unsigned)ceil_div(E, 32), 1024, 0, stream>>>(E, n_chunks, counts, totals);
-  } else {
-    cudaError_t err = cudaMemsetAsync(totals, 0, sizeof(int32_t) * E, stream);
+    err = launch_pdl(permute_count_kernel, dim3(blocks), dim3(32 * WARPS_PER_BLOCK), smem, stream, R, E, n_chunks, ids,
+                     counts, status);
     if (err != cudaSuccess) return err;
+    err = launch_pdl(permute_scan_chunks_kernel, dim3((unsigned)ceil_div(E, 32)), dim3(1024), 0, stream, E, n_chunks,
+                     counts, totals);
+  } else {
+    err = cudaMemsetAsync(totals, 0, sizeof(int32_t) * E, stream);
   }
-  permute_scan_experts_kernel<<<1, 1024, 0, stream>>>(E, totals, offsets);
-  if (n_chunks > 0)
-    permute_scatter_kernel<<<blocks, 32 * WARPS_PER_BLOCK, smem, stream>>>(R, E, n_chunks, ids, counts, offsets,
-                                                                         sorted_route, route_pos);
-  return cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(permute_scan_experts_kernel, dim3(1), dim3(1024), 0, stream, E, (const int32_t *)totals, offsets);
+  if (err != cudaSuccess || n_chunks == 0) return err;
+  return launch_pdl(permute_scatter_kernel, dim3(blocks), dim3(32 * WARPS_PER_BLOCK), smem, stream, R, E, n_chunks, ids,
+                    (const int32_t *)counts, (const int32_t *)offsets, sorted_route, route_pos);
 }
 
 // ---------------------------------------------------------------------------
@@ -177,6 +188,8 @@ cudaError_t launch_permute(int64_t R, int E, const int32_t *ids, int32_t *offset
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
 build_tiles_kernel(int E, int T, int bn, const int32_t *__restrict__ offsets, int32_t *__restrict__ tile_start) {
+  griddep_launch();
+  griddep_wait();
   __shared__ int32_t buf[1024];
   __shared__ int32_t carry;
   if (threadIdx.x == 0) carry = 0;
@@ -205,8 +218,7 @@ build_tiles_kernel(int E, int T, int bn, const int32_t *__restrict__ offsets, in
 
 cudaError_t launch_build_tiles(int E, int T, int bn, const int32_t *offsets, int32_t *tile_start,
                                cudaStream_t stream) {
-  build_tiles_kernel<<<1, 1024, 0, stream>>>(E, T, bn, offsets, tile_start);
-  return cudaGetLastError();
+  return launch_pdl(build_tiles_kernel, dim3(1), dim3(1024), 0, stream, E, T, bn, offsets, tile_start);
 }
 
 }  // namespace moe

@@ -23,6 +23,8 @@ template <typename TX>
 __global__ void __launch_bounds__(256)
 router_logits_simt_kernel(int T, int H, int E, const TX *__restrict__ x, const float *__restrict__ wr,
                           const float *__restrict__ bias, float *__restrict__ logits) {
+  griddep_launch();
+  griddep_wait();
   __shared__ float xs[32][68];
   __shared__ float wsm[32][68];
   const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
@@ -72,8 +74,7 @@ cudaError_t launch_router_logits_simt(int T, int H, int E, const float *x, const
                                       float *logits, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   dim3 grid((unsigned)ceil_div(T, 64), (unsigned)ceil_div(E, 64));
-  router_logits_simt_kernel<float><<<grid, 256, 0, stream>>>(T, H, E, x, wr, bias, logits);
-  return cudaGetLastError();
+  return launch_pdl(router_logits_simt_kernel<float>, grid, dim3(256), 0, stream, T, H, E, x, wr, bias, logits);
 }
 
 // ---------------------------------------------------------------------------
@@ -121,6 +122,8 @@ __global__ void __launch_bounds__(256, 4)
 topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, const TX *__restrict__ x,
                  const TX *__restrict__ wsg, int32_t *__restrict__ ids, float *__restrict__ w,
                  float *__restrict__ sig) {
+  griddep_launch();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
@@ -211,15 +214,15 @@ static cudaError_t topk_dispatch(int T, int H, int E, int k, const float *logits
   dim3 grid((unsigned)ceil_div(T, 8));
   const TX *xx = (const TX *)x;
   const TX *gg = (const TX *)wsg;
-#define MOE_TOPK(EPL) topk_gate_kernel<TX, EPL><<<grid, 256, 0, stream>>>(T, H, E, k, logits, xx, gg, ids, w, sig)
-  if (E <= 32) MOE_TOPK(1);
-  else if (E <= 64) MOE_TOPK(2);
-  else if (E <= 128) MOE_TOPK(4);
-  else if (E <= 256) MOE_TOPK(8);
-  else if (E <= 512) MOE_TOPK(16);
-  else MOE_TOPK(32);
+#define MOE_TOPK(EPL) \
+  launch_pdl(topk_gate_kernel<TX, EPL>, grid, dim3(256), 0, stream, T, H, E, k, logits, xx, gg, ids, w, sig)
+  if (E <= 32) return MOE_TOPK(1);
+  if (E <= 64) return MOE_TOPK(2);
+  if (E <= 128) return MOE_TOPK(4);
+  if (E <= 256) return MOE_TOPK(8);
+  if (E <= 512) return MOE_TOPK(16);
+  return MOE_TOPK(32);
 #undef MOE_TOPK
-  return cudaGetLastError();
 }
 
 cudaError_t launch_topk_gate(int dtype, int T, int H, int E, int k, const float *logits, const void *x,
