@@ -74,7 +74,6 @@ template <int MODE>
 constexpr int tc_nbuf() {
   return TcCfg<MODE>::MT == 1 ? 2 : 1;
 }
-static_assert(TcCfg<1>::MT == 2, "the gate_up epilogue drains two M tiles per item");
 
 constexpr int TC_TILE_A_BYTES = 128 * 128;  // one M tile: 128 rows x 64 bf16
 constexpr int TC_B_BYTES = 256 * 128;       // up to 256 token rows x 64 bf16
@@ -228,7 +227,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           uint8_t *b_dst = sb + stage * TC_B_BYTES;
           if (MODE == TC_GATE_UP) {
             // One 5-D box: for 8 groups of 16 features (two M tiles), 16 gate rows then 16 up rows.
-            tma_load_5d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64, 0, 0, im.f * 8, sh ? 0 : im.seg,
+            tma_load_5d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64, 0, 0, im.f * 4 * MT, sh ? 0 : im.seg,
                         pol_w);
           } else {
             tma_load_2d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64,
@@ -276,6 +275,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const uint32_t idesc = idesc_bf16_f32(128, im.n);
         for (int kb = 0; kb < im.nk; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          if (MODE == TC_GATE_UP) fence_proxy_async_smem();  // the gathered rows: generic -> async proxy
           tc_fence_after();
           const uint64_t bd = smem_desc_sw128(smem_u32(sb + stage * TC_B_BYTES));
 #pragma unroll
@@ -325,8 +325,9 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const int cbase = lane < 16 ? 0 : 16;
         const bool odd = lane & 1;
         for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
-          float vt[2][32];
-          tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[1]);
+          float vt[MT][32];
+          if (MT == 2) tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[MT - 1]);
+          else tmem_ld32(tq + c0, vt[0]);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             const float(&v)[32] = vt[mt];
@@ -423,16 +424,17 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       ++cnt;
     }
   } else if (MODE == TC_GATE_UP) {
-    // ------------------------------------------------------------ row gather (warps 10..17)
+    // ------------------------------------------------------------ row gather
     // Warp g copies the rows r = 8 i + g; lane = 8 * (i mod 4) + 16-byte chunk
     // qc, written at the 128-byte swizzled position (qc ^ g) of row r.  Each
-    // thread arrives on a stage's `full` barrier once its copies into that
-    // stage are complete and fenced for the tensor cores (pad rows past the
+    // thread's copies into a stage arrive on the stage's `full` barrier when
+    // they land, so the warps run ahead as far as free stages allow; the MMA
+    // thread fences them into the async proxy after its wait (pad rows past the
     // segment are left as they are: their accumulator columns are never read).
     const int g = warp - GATHER_FIRST;
     const int sub = lane >> 3, qc = lane & 7;
     int32_t *tok = tok_all + g * 32;
-    int stage = 0, arr_stage = 0, pending = 0;
+    int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
@@ -450,24 +452,11 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const uint32_t bsm = smem_u32(sb + stage * TC_B_BYTES) + g * 128 + ((qc ^ g) << 4);
         const __nv_bfloat16 *src = p.x + kb * 64 + qc * 8;
         for (int i = sub; i < ni; i += 4) cp_async_16(bsm + i * 1024, src + (int64_t)tok[i] * p.H);
-        cp_async_commit();
-        if (++pending > 1) {
-          cp_async_wait<1>();
-          fence_proxy_async_smem();
-          mbar_arrive(&full[arr_stage]);
-          if (++arr_stage == STAGES) arr_stage = 0;
-          --pending;
-        }
+        cp_async_mbar_arrive(&full[stage]);
         if (++stage == STAGES) stage = 0, phase ^= 1;
       }
     }
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (ok)
-      for (; pending > 0; --pending) {
-        mbar_arrive(&full[arr_stage]);
-        if (++arr_stage == STAGES) arr_stage = 0;
-      }
   }
   tc_fence_before();
   __syncthreads();
@@ -850,14 +839,16 @@ static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 size_t ffn_tc_scratch_bytes(int T, int k, int E, int H, int I, int Is) {
   const size_t starts = round256((size_t)(E + 2) * 4);
   constexpr int DN_ROWS = 128 * TcCfg<TC_DOWN>::MT;  // output features per down item
-  return 2 * starts + round256((size_t)max_items(T, k, E, I / 128, Is / 128) * 16) +
+  constexpr int GU_FEAT = 64 * TcCfg<TC_GATE_UP>::MT;  // features (gate + up row pairs) per gate_up item
+  return 2 * starts + round256((size_t)max_items(T, k, E, I / GU_FEAT, Is / GU_FEAT) * 16) +
          round256((size_t)max_items(T, k, E, H / DN_ROWS, H / DN_ROWS) * 16);
 }
 
 cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
   const size_t starts = round256((size_t)(a.E + 2) * 4);
-  const int mi_gu = (int)max_items(a.T, a.k, a.E, a.I / 128, a.Is / 128);
+  constexpr int GU_FEAT = 64 * TcCfg<TC_GATE_UP>::MT;
+  const int mi_gu = (int)max_items(a.T, a.k, a.E, a.I / GU_FEAT, a.Is / GU_FEAT);
   constexpr int DN_ROWS = 128 * TcCfg<TC_DOWN>::MT;
   const int mi_dn = (int)max_items(a.T, a.k, a.E, a.H / DN_ROWS, a.H / DN_ROWS);
   uint8_t *w = (uint8_t *)scratch;
@@ -865,12 +856,13 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   int32_t *start_dn = (int32_t *)(w + starts);
   int4 *items_gu = (int4 *)(w + 2 * starts);
   int4 *items_dn = (int4 *)(w + 2 * starts + round256((size_t)mi_gu * 16));
-  cudaError_t e0 = launch_item_tables(a.E, a.T, a.I / 128, a.Is / 128, a.H / DN_ROWS, a.H / DN_ROWS, a.offsets,
+  cudaError_t e0 = launch_item_tables(a.E, a.T, a.I / GU_FEAT, a.Is / GU_FEAT, a.H / DN_ROWS, a.H / DN_ROWS, a.offsets,
                                       start_gu, start_dn, items_gu, items_dn, mi_gu, mi_dn, stream);
   if (e0 != cudaSuccess) return e0;
   const int64_t R = (int64_t)a.T * a.k;
   TcMaps mg, md;
-  if (!map_gate_up(&mg.a, a.w_gate_up, a.E, a.I, a.H) || !map_gate_up(&mg.a_sh, a.ws_gate_up, 1, a.Is, a.H) ||
+  if (!map_gate_up(&mg.a, a.w_gate_up, a.E, a.I, a.H, 4 * TcCfg<TC_GATE_UP>::MT) ||
+      !map_gate_up(&mg.a_sh, a.ws_gate_up, 1, a.Is, a.H, 4 * TcCfg<TC_GATE_UP>::MT) ||
       !map_2d(&md.a, a.w_down, (int64_t)a.E * a.H, a.I, DN_ROWS) || !map_2d(&md.a_sh, a.ws_down, a.H, a.Is, DN_ROWS) ||
       !map_rows(md.b, a.h_routed, R, a.I) || !map_rows(md.b_sh, a.h_shared, a.T, a.Is))
     return cudaErrorInvalidValue;

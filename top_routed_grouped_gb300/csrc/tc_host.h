@@ -86,13 +86,14 @@ inline bool map_f32_tile(CUtensorMap *m, const void *ptr, int64_t rows, int64_t 
 }
 
 // Gate/up weights [n_mat, 2*Iw, H] viewed as 5-D (H, 16, 2, Iw/16, n_mat):
-// a box (64, 16, 2, 8, 1) holds, for 8 consecutive groups of 16 features
-// (two M tiles), the 16 gate rows followed by the 16 up rows of each group.
-inline bool map_gate_up(CUtensorMap *m, const void *ptr, int n_mat, int Iw, int H) {
+// a box (64, 16, 2, groups, 1) holds, for `groups` consecutive groups of 16
+// features (four groups = one 128-row M tile), the 16 gate rows followed by
+// the 16 up rows of each group.
+inline bool map_gate_up(CUtensorMap *m, const void *ptr, int n_mat, int Iw, int H, uint32_t groups) {
   const uint64_t dims[5] = {(uint64_t)H, 16, 2, (uint64_t)Iw / 16, (uint64_t)n_mat};
   const uint64_t strides[4] = {(uint64_t)H * 2, (uint64_t)Iw * H * 2, (uint64_t)16 * H * 2,
                                (uint64_t)2 * Iw * H * 2};
-  const uint32_t box[5] = {64, 16, 2, 8, 1};
+  const uint32_t box[5] = {64, 16, 2, groups, 1};
   return encode_map(m, ptr, 5, dims, strides, box);
 }
 

@@ -145,6 +145,11 @@ __device__ inline void cp_async_16(uint32_t dst_smem, const void *src) {
 __device__ inline void cp_async_16_zfill(uint32_t dst_smem, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes) : "memory");
 }
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count includes this arrival).
+__device__ inline void cp_async_mbar_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ inline void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ inline void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
