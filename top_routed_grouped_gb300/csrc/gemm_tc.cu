@@ -61,7 +61,7 @@ constexpr int TC_GATE_UP = 1, TC_DOWN = 2;
 // lane quarter split the columns); EPI_BYTES of row staging per warp.
 template <>
 struct TcCfg<1> {
-  static constexpr int NMAX = 256, MT = 2, STAGES = 3, EPI_WARPS = 8, EPI_BYTES = 4096;
+  static constexpr int NMAX = 256, MT = 2, STAGES = 3, EPI_WARPS = 8, EPI_BYTES = 2560;
 };
 template <>
 struct TcCfg<2> {
@@ -319,8 +319,9 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const int Iseg = sh ? p.Is : p.I;
         __nv_bfloat16 *hout = sh ? p.h_shared : p.h_routed;
         __nv_bfloat16 *guout = sh ? p.gu_shared : p.gu_routed;
-        uint32_t *stg_h = (uint32_t *)stg;                         // [32 cols][12 words] (8 used: 16 bf16)
-        __nv_bfloat16 *stg_gu = (__nv_bfloat16 *)(stg + 32 * 48);  // [32 cols][40] (32 used)
+        // The h and the g/u staging share the warp's buffer, one after the other.
+        uint32_t *stg_h = (uint32_t *)stg;              // [32 cols][12 words] (8 used: 16 bf16)
+        __nv_bfloat16 *stg_gu = (__nv_bfloat16 *)stg;  // [32 cols][40] (32 used)
         const int fl = lane & 15;
         const int cbase = lane < 16 ? 0 : 16;
         const bool odd = lane & 1;
@@ -354,10 +355,6 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
               const __nv_bfloat162 w2 = odd ? __floats2bfloat162_rn(x, hv[j + 1]) : __floats2bfloat162_rn(hv[j], x);
               stg_h[(cbase + j + (odd ? 1 : 0)) * 12 + (fl >> 1)] = *reinterpret_cast<const uint32_t *>(&w2);
             }
-            if (guout) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) stg_gu[j * 40 + lane] = __float2bfloat16_rn(v[j]);
-            }
             __syncwarp();
             // Two lanes per column row: 16 rows x 32 contiguous bytes per store instruction.
 #pragma unroll
@@ -368,17 +365,23 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                 *(uint4 *)(hout + row * Iseg + fcol + cc * 8) = *(const uint4 *)(stg_h + r * 12 + cc * 4);
               }
             }
-            if (guout && c0 + lane < im.rows) {
-              const int64_t row = im.row0 + c0 + lane;
-              const uint4 *sg = (const uint4 *)(stg_gu + lane * 40);
-              uint4 *dg = (uint4 *)(guout + row * 2 * Iseg + fcol);
-              uint4 *du = (uint4 *)(guout + row * 2 * Iseg + Iseg + fcol);
-              dg[0] = sg[0];
-              dg[1] = sg[1];
-              du[0] = sg[2];
-              du[1] = sg[3];
-            }
             __syncwarp();
+            if (guout) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) stg_gu[j * 40 + lane] = __float2bfloat16_rn(v[j]);
+              __syncwarp();
+              if (c0 + lane < im.rows) {
+                const int64_t row = im.row0 + c0 + lane;
+                const uint4 *sg = (const uint4 *)(stg_gu + lane * 40);
+                uint4 *dg = (uint4 *)(guout + row * 2 * Iseg + fcol);
+                uint4 *du = (uint4 *)(guout + row * 2 * Iseg + Iseg + fcol);
+                dg[0] = sg[0];
+                dg[1] = sg[1];
+                du[0] = sg[2];
+                du[1] = sg[3];
+              }
+              __syncwarp();
+            }
           }
         }
       } else {

@@ -24,9 +24,14 @@ cudaError_t launch_topk_gate(int dtype, int T, int H, int E, int k, const float 
 int *device_status_ptr();
 
 // ---- permute.cu ----
-size_t permute_scratch_bytes(int64_t R, int E);
+// Routes per warp of the count and scatter kernels: 128 by default (more
+// warps in flight), 512 where the scratch (ceil(R / chunk) * E + E ints) must
+// stay small.  The result does not depend on the chunk.
+constexpr int PERMUTE_CHUNK_SMALL = 128, PERMUTE_CHUNK_LARGE = 512;
+size_t permute_scratch_bytes(int64_t R, int E, int chunk = PERMUTE_CHUNK_SMALL);
 cudaError_t launch_permute(int64_t R, int E, const int32_t *ids, int32_t *offsets, int32_t *sorted_route,
-                           int32_t *route_pos, void *scratch, int *status, cudaStream_t stream);
+                           int32_t *route_pos, void *scratch, int *status, cudaStream_t stream,
+                           int chunk = PERMUTE_CHUNK_SMALL);
 // tile_start[s] for s in [0, E+1]: prefix of ceil(n_s / bn) over the E routed
 // segments (n_s from offsets) and the shared segment (n_E = T).
 cudaError_t launch_build_tiles(int E, int T, int bn, const int32_t *offsets, int32_t *tile_start,

@@ -4,8 +4,8 @@
 // dispatch is a local selection of the routes each expert owns; embedded
 // #503 commit message, "Experts": every (token, route) row has one writer.
 //
-// Routes r = t*k + s are cut into chunks of CHUNK consecutive routes, one
-// warp per chunk.  (1) count: per-chunk expert histogram.  (2) scan_chunks:
+// Routes r = t*k + s are cut into chunks of CH consecutive routes (128, or
+// 512 where the scratch must stay small), one warp per chunk.  (1) count: per-chunk expert histogram.  (2) scan_chunks:
 // per expert, the exclusive prefix of the histogram over chunks, and the
 // expert total.  (3) scan_experts: exclusive prefix of the totals = the
 // segment offsets.  (4) scatter: each warp walks its chunk in ascending r;
@@ -18,16 +18,15 @@
 
 namespace moe {
 
-constexpr int CHUNK = 512;           // routes per warp
-constexpr int STEPS = CHUNK / 32;    // 32 routes per step
 constexpr int WARPS_PER_BLOCK = 4;
 constexpr int PAST_END = -0x7fffffff - 1;  // lane past the last route (not an id)
 
-size_t permute_scratch_bytes(int64_t R, int E) {
-  int64_t n_chunks = ceil_div(R, CHUNK);
+size_t permute_scratch_bytes(int64_t R, int E, int chunk) {
+  int64_t n_chunks = ceil_div(R, chunk);
   return (size_t)(n_chunks * E + E) * sizeof(int32_t);
 }
 
+template <int CH>
 __global__ void __launch_bounds__(32 * WARPS_PER_BLOCK)
 permute_count_kernel(int64_t R, int E, int n_chunks, const int32_t *__restrict__ ids, int32_t *__restrict__ counts,
                      int *status) {
@@ -37,12 +36,13 @@ permute_count_kernel(int64_t R, int E, int n_chunks, const int32_t *__restrict__
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * WARPS_PER_BLOCK + warp;
   if (c >= n_chunks) return;
+  constexpr int STEPS = CH / 32;  // 32 routes per step
   int32_t *hist = smem + warp * E;
   for (int i = lane; i < E; i += 32) hist[i] = 0;
   int eid[STEPS];  // all loads issued before the dependent match chain
 #pragma unroll
   for (int step = 0; step < STEPS; ++step) {
-    const int64_t r = (int64_t)c * CHUNK + step * 32 + lane;
+    const int64_t r = (int64_t)c * CH + step * 32 + lane;
     eid[step] = r < R ? __ldg(ids + r) : PAST_END;
   }
   __syncwarp();
@@ -118,6 +118,7 @@ permute_scan_experts_kernel(int E, const int32_t *__restrict__ totals, int32_t *
   if (i == E - 1) offsets[E] = buf[i];
 }
 
+template <int CH>
 __global__ void __launch_bounds__(32 * WARPS_PER_BLOCK)
 permute_scatter_kernel(int64_t R, int E, int n_chunks, const int32_t *__restrict__ ids,
                        const int32_t *__restrict__ chunk_prefix, const int32_t *__restrict__ offsets,
@@ -133,15 +134,16 @@ permute_scatter_kernel(int64_t R, int E, int n_chunks, const int32_t *__restrict
   for (int i = lane; i < E; i += 32) next[i] = offsets[i] + pre[i];
   __syncwarp();
   const unsigned lt = lanemask_lt();
+  constexpr int STEPS = CH / 32;
   int eid[STEPS];
 #pragma unroll
   for (int step = 0; step < STEPS; ++step) {
-    const int64_t r = (int64_t)c * CHUNK + step * 32 + lane;
+    const int64_t r = (int64_t)c * CH + step * 32 + lane;
     eid[step] = r < R ? __ldg(ids + r) : -1;
   }
 #pragma unroll
   for (int step = 0; step < STEPS; ++step) {
-    const int64_t r = (int64_t)c * CHUNK + step * 32 + lane;
+    const int64_t r = (int64_t)c * CH + step * 32 + lane;
     int e = eid[step];
     if (e < 0 || e >= E) e = -1;
     unsigned peers = __match_any_sync(FULL_MASK, e);
@@ -156,17 +158,18 @@ permute_scatter_kernel(int64_t R, int E, int n_chunks, const int32_t *__restrict
   }
 }
 
-cudaError_t launch_permute(int64_t R, int E, const int32_t *ids, int32_t *offsets, int32_t *sorted_route,
-                           int32_t *route_pos, void *scratch, int *status, cudaStream_t stream) {
-  const int n_chunks = (int)ceil_div(R, CHUNK);
+template <int CH>
+static cudaError_t run_permute(int64_t R, int E, const int32_t *ids, int32_t *offsets, int32_t *sorted_route,
+                               int32_t *route_pos, void *scratch, int *status, cudaStream_t stream) {
+  const int n_chunks = (int)ceil_div(R, CH);
   int32_t *counts = (int32_t *)scratch;
   int32_t *totals = counts + (int64_t)n_chunks * E;
   const size_t smem = (size_t)WARPS_PER_BLOCK * E * sizeof(int32_t);
   const unsigned blocks = (unsigned)ceil_div(n_chunks, WARPS_PER_BLOCK);
   cudaError_t err;
   if (n_chunks > 0) {
-    err = launch_pdl(permute_count_kernel, dim3(blocks), dim3(32 * WARPS_PER_BLOCK), smem, stream, R, E, n_chunks, ids,
-                     counts, status);
+    err = launch_pdl(permute_count_kernel<CH>, dim3(blocks), dim3(32 * WARPS_PER_BLOCK), smem, stream, R, E, n_chunks,
+                     ids, counts, status);
     if (err != cudaSuccess) return err;
     err = launch_pdl(permute_scan_chunks_kernel, dim3((unsigned)ceil_div(E, 32)), dim3(1024), 0, stream, E, n_chunks,
                      counts, totals);
@@ -176,8 +179,17 @@ cudaError_t launch_permute(int64_t R, int E, const int32_t *ids, int32_t *offset
   if (err != cudaSuccess) return err;
   err = launch_pdl(permute_scan_experts_kernel, dim3(1), dim3(1024), 0, stream, E, (const int32_t *)totals, offsets);
   if (err != cudaSuccess || n_chunks == 0) return err;
-  return launch_pdl(permute_scatter_kernel, dim3(blocks), dim3(32 * WARPS_PER_BLOCK), smem, stream, R, E, n_chunks, ids,
-                    (const int32_t *)counts, (const int32_t *)offsets, sorted_route, route_pos);
+  return launch_pdl(permute_scatter_kernel<CH>, dim3(blocks), dim3(32 * WARPS_PER_BLOCK), smem, stream, R, E, n_chunks,
+                    ids, (const int32_t *)counts, (const int32_t *)offsets, sorted_route, route_pos);
+}
+
+cudaError_t launch_permute(int64_t R, int E, const int32_t *ids, int32_t *offsets, int32_t *sorted_route,
+                           int32_t *route_pos, void *scratch, int *status, cudaStream_t stream, int chunk) {
+  if (chunk == PERMUTE_CHUNK_SMALL)
+    return run_permute<PERMUTE_CHUNK_SMALL>(R, E, ids, offsets, sorted_route, route_pos, scratch, status, stream);
+  if (chunk == PERMUTE_CHUNK_LARGE)
+    return run_permute<PERMUTE_CHUNK_LARGE>(R, E, ids, offsets, sorted_route, route_pos, scratch, status, stream);
+  return cudaErrorInvalidValue;
 }
 
 // ---------------------------------------------------------------------------

@@ -55,13 +55,16 @@ MOE_API int moe_permute_noalloc(const moe_dims_t *d, const int32_t *topk_ids, in
   auto ok = [](const void *p, int64_t n) { return n == 0 || (p != nullptr && ((uintptr_t)p & 15) == 0); };
   if (!ok(topk_ids, R) || !ok(expert_offsets, 1) || !ok(sorted_route, R) || !ok(route_pos, R))
     return MOE_ERR_INVALID_ARG;
-  // Sizes whose scratch does not fit the fixed array are refused before any GPU work.
-  if (permute_scratch_bytes(R, d->E) > MOE_PERMUTE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
+  // The default chunk where its scratch fits the fixed array, else the large
+  // chunk (same result); sizes that fit neither are refused before any GPU work.
+  int chunk = PERMUTE_CHUNK_SMALL;
+  if (permute_scratch_bytes(R, d->E, chunk) > MOE_PERMUTE_NOALLOC_SCRATCH_BYTES) chunk = PERMUTE_CHUNK_LARGE;
+  if (permute_scratch_bytes(R, d->E, chunk) > MOE_PERMUTE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
   int32_t *scratch = permute_scratch_device_ptr();
   if (!scratch) return MOE_ERR_CUDA;
   // Every scratch word the kernels read is written earlier by the same call,
   // so the previous call's contents never leak into this one.
   cudaError_t e = launch_permute(R, d->E, topk_ids, expert_offsets, sorted_route, route_pos, scratch,
-                                 device_status_ptr(), (cudaStream_t)stream);
+                                 device_status_ptr(), (cudaStream_t)stream, chunk);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
