@@ -75,6 +75,7 @@ permute_scan_chunks_kernel(int E, int n_chunks, int32_t *__restrict__ counts, in
   const int c0 = warp * cpw, c1 = min(n_chunks, c0 + cpw);
   int32_t local = 0;
   if (e < E)
+#pragma unroll 8
     for (int c = c0; c < c1; ++c) local += counts[(int64_t)c * E + e];
   part[warp][lane] = local;
   __syncthreads();
@@ -90,6 +91,7 @@ permute_scan_chunks_kernel(int E, int n_chunks, int32_t *__restrict__ counts, in
   __syncthreads();
   if (e < E) {
     int32_t run = part[warp][lane];
+#pragma unroll 8
     for (int c = c0; c < c1; ++c) {
       int32_t v = counts[(int64_t)c * E + e];
       counts[(int64_t)c * E + e] = run;
