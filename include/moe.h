@@ -139,6 +139,29 @@ int moe_route(const moe_dims_t *d, const void *x, const float *w_router, const f
               float *logits, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_route_replay -- route weights and shared gate for GIVEN expert ids.
+ * SkyRL PR #2513, section "chunked_mlp fixes (#2532, merged)": per-chunk
+ * router replay; SkyRL docs page "Qwen3.8-Flash-Next", section "Example
+ * scripts": rollout routing replay.  A training pass reuses the expert
+ * choices of an earlier (rollout) pass instead of selecting its own; the
+ * router logits are recomputed so that the weights carry their gradient.
+ *
+ *   topk_ids       [T, k]  int32   in: the replayed expert ids, slot order as given
+ *   topk_w         [T, k]  float   out: w_s = exp(l_s - m) / sum_j exp(l_j - m) over
+ *                                  the given slots, m = the largest of the k logits
+ *   (x, w_router, router_bias, w_shared_gate, shared_sig, logits as moe_route)
+ *
+ * With the ids moe_route chose, topk_w and shared_sig equal moe_route's bit
+ * for bit.  Ids outside [0, E) or repeated within a token fail closed: that
+ * token's weights are written as zeros and the device status word records
+ * code 1 (out of range) or 4 (repeated); check moe_device_status.
+ * moe_backward accepts replayed routes unchanged.  Workspace: ROUTE.
+ */
+int moe_route_replay(const moe_dims_t *d, const void *x, const float *w_router, const float *router_bias,
+                     const void *w_shared_gate, const int32_t *topk_ids, float *topk_w, float *shared_sig,
+                     float *logits, void *ws, size_t ws_bytes, void *stream);
+
+/*
  * moe_permute -- dispatch as a stable counting sort of the routes.
  * RL-Kernel PR #557 "What": dispatch is a local selection of the routes;
  * #503 "Experts": one writer per (token, route) row.  Route r = t*k + s.
@@ -246,6 +269,10 @@ typedef struct moe_fwd_args {
   void *y_routed;          /* [T*k, H] dtype */
   void *y_shared;          /* [T, H] dtype */
   moe_saved_t saved;
+  /* Router replay: if not NULL, these [T, k] ids are the routes (see
+   * moe_route_replay) instead of the top-k selection; topk_ids, if given,
+   * receives a copy. */
+  const int32_t *replay_ids;
 } moe_fwd_args_t;
 
 /* moe_forward -- moe_route, moe_permute, moe_grouped_ffn, moe_combine on one
@@ -313,7 +340,8 @@ int moe_backward(const moe_dims_t *d, const moe_bwd_args_t *a, void *ws, size_t 
  * of the current device.  Synchronises the device.  Returns MOE_OK when no
  * kernel recorded a failed check since the last reset, MOE_ERR_DEVICE when
  * one did (`*detail`, if not NULL, receives the first recorded code), or
- * MOE_ERR_CUDA.  Codes: 1 = expert id out of range in moe_permute,
+ * MOE_ERR_CUDA.  Codes: 1 = expert id out of range in moe_permute or
+ * moe_route_replay, 4 = expert id repeated within a token in moe_route_replay,
  * 2 = a pipeline wait in a tensor-core kernel timed out,
  * 3 = tensor-memory allocation failed.
  */

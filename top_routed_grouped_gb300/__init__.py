@@ -24,7 +24,8 @@ OP = {"route": 0, "permute": 1, "grouped_ffn": 2, "combine": 3, "backward": 4, "
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_WORKSPACE",
           -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE"}
 EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_permute", "moe_grouped_ffn",
-            "moe_combine", "moe_forward", "moe_backward", "moe_device_status", "moe_permute_noalloc")
+            "moe_combine", "moe_forward", "moe_backward", "moe_device_status", "moe_permute_noalloc",
+            "moe_route_replay")
 
 _vp = ctypes.c_void_p
 
@@ -42,7 +43,7 @@ class FwdArgs(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("x", "w_router", "router_bias", "w_shared_gate", "w_gate_up", "w_down",
                                    "ws_gate_up", "ws_down", "y", "topk_ids", "topk_w", "shared_sig", "logits",
                                    "expert_offsets", "sorted_route", "route_pos", "y_routed", "y_shared")] + \
-              [("saved", Saved)]
+              [("saved", Saved), ("replay_ids", _vp)]
 
 
 class BwdArgs(ctypes.Structure):
@@ -78,6 +79,7 @@ def lib() -> ctypes.CDLL:
                 "moe_workspace_size": ([D, ctypes.c_int], ctypes.c_size_t),
                 "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
                 "moe_route": ([D] + [_vp] * 8 + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
+                "moe_route_replay": ([D] + [_vp] * 8 + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_permute": ([D] + [_vp] * 4 + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_grouped_ffn": ([D] + [_vp] * 9 + [ctypes.POINTER(Saved), _vp, ctypes.c_size_t, _vp],
                                     ctypes.c_int),
@@ -140,6 +142,13 @@ def moe_route(d, x, w_router, router_bias, w_shared_gate, topk_ids, topk_w, shar
                                         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def moe_route_replay(d, x, w_router, router_bias, w_shared_gate, topk_ids, topk_w, shared_sig, logits, ws,
+                     stream=None):
+    _check("moe_route_replay", lib().moe_route_replay(
+        ctypes.byref(d), _p(x), _p(w_router), _p(router_bias), _p(w_shared_gate), _p(topk_ids), _p(topk_w),
+        _p(shared_sig), _p(logits), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def moe_permute(d, topk_ids, expert_offsets, sorted_route, route_pos, ws, stream=None):
     _check("moe_permute", lib().moe_permute(ctypes.byref(d), _p(topk_ids), _p(expert_offsets), _p(sorted_route),
                                             _p(route_pos), _p(ws), 0 if ws is None else ws.numel(),
@@ -176,7 +185,7 @@ def moe_forward(d, args: dict, ws, stream=None):
     fa = FwdArgs()
     for name, _ in FwdArgs._fields_:
         if name != "saved":
-            setattr(fa, name, _p(args.get(name)))
+            setattr(fa, name, _p(args.get(name)))  # replay_ids: NULL unless given
     fa.saved = _saved(args.get("saved"))
     _check("moe_forward", lib().moe_forward(ctypes.byref(d), ctypes.byref(fa), _p(ws),
                                             0 if ws is None else ws.numel(), _stream(stream)))
@@ -225,6 +234,24 @@ def route(x, w_router, w_shared_gate, k: int, router_bias=None, E: int | None = 
     return out
 
 
+def route_replay(x, w_router, w_shared_gate, topk_ids, router_bias=None, want_logits=False, stream=None):
+    """Route weights and shared gate for given expert ids [T,k] (router replay).
+    Returns dict(topk_ids (the input), topk_w, shared_sig, logits or None)."""
+    import torch
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    E = w_router.shape[0]
+    d = make_dims(T, H, E, k, 128, 128, x.dtype)  # I, Is unused by routing
+    dev = x.device
+    out = {"topk_ids": topk_ids,
+           "topk_w": torch.empty(T, k, dtype=torch.float32, device=dev),
+           "shared_sig": torch.empty(T, dtype=torch.float32, device=dev),
+           "logits": torch.empty(T, E, dtype=torch.float32, device=dev) if want_logits else None}
+    moe_route_replay(d, x, w_router, router_bias, w_shared_gate, topk_ids, out["topk_w"], out["shared_sig"],
+                     out["logits"], workspace(d, "route", dev), stream)
+    return out
+
+
 def permute(topk_ids, E: int, stream=None):
     """Returns dict(expert_offsets [E+1], sorted_route [T*k], route_pos [T*k]), all int32."""
     import torch
@@ -240,8 +267,9 @@ def permute(topk_ids, E: int, stream=None):
 
 
 def forward(x, w_router, w_shared_gate, w_gate_up, w_down, ws_gate_up, ws_down, k: int, router_bias=None,
-            save_for_backward: bool = False, want_logits: bool = False, stream=None):
-    """Full layer forward through ``moe_forward``.  Returns a dict with ``y`` and every intermediate."""
+            save_for_backward: bool = False, want_logits: bool = False, replay_ids=None, stream=None):
+    """Full layer forward through ``moe_forward``.  Returns a dict with ``y`` and every intermediate.
+    ``replay_ids`` [T,k] int32: route with these experts instead of the top-k (router replay)."""
     import torch
     T, H = x.shape
     d = dims_of(x, w_router, w_gate_up, ws_gate_up, k)
@@ -265,7 +293,7 @@ def forward(x, w_router, w_shared_gate, w_gate_up, w_down, ws_gate_up, ws_down, 
                         "gu_shared": torch.empty(T, 2 * Is, dtype=dt, device=dev),
                         "h_shared": torch.empty(T, Is, dtype=dt, device=dev)}
     args = dict(out, x=x, w_router=w_router, router_bias=router_bias, w_shared_gate=w_shared_gate,
-                w_gate_up=w_gate_up, w_down=w_down, ws_gate_up=ws_gate_up, ws_down=ws_down)
+                w_gate_up=w_gate_up, w_down=w_down, ws_gate_up=ws_gate_up, ws_down=ws_down, replay_ids=replay_ids)
     moe_forward(d, args, workspace(d, "forward", dev), stream)
     return out
 

@@ -208,6 +208,33 @@ MOE_API int moe_route(const moe_dims_t *d, const void *x, const float *w_router,
   return cuda_status(e);
 }
 
+MOE_API int moe_route_replay(const moe_dims_t *d, const void *x, const float *w_router, const float *router_bias,
+                             const void *w_shared_gate, const int32_t *topk_ids, float *topk_w, float *shared_sig,
+                             float *logits, void *ws, size_t ws_bytes, void *stream) {
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  const int64_t T = d->T, R = T * d->k;
+  if (!buf_ok(x, T * d->H) || !buf_ok(w_router, 1) || !opt_ok(router_bias) || !buf_ok(w_shared_gate, 1) ||
+      !buf_ok(topk_ids, R) || !buf_ok(topk_w, R) || !buf_ok(shared_sig, T) || !opt_ok(logits) || !opt_ok(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_size(d, MOE_OP_ROUTE)) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  Carver c(ws);
+  float *lg = (float *)c.take((size_t)T * d->E * sizeof(float));
+  if (logits) lg = logits;
+  cudaError_t e;
+  if (d->dtype == MOE_F32)
+    e = launch_router_logits_simt(d->T, d->H, d->E, (const float *)x, w_router, router_bias, lg, s);
+  else
+    e = launch_router_logits_tc(d->T, d->H, d->E, x, w_router, router_bias, lg,
+                                c.take(router_tc_scratch_bytes(d->E, d->H)), device_status_ptr(), s);
+  if (e == cudaSuccess)
+    e = launch_replay_gate(d->dtype, d->T, d->H, d->E, d->k, lg, x, w_shared_gate, topk_ids, topk_w, shared_sig,
+                           device_status_ptr(), s);
+  return cuda_status(e);
+}
+
 MOE_API int moe_permute(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_offsets,
                         int32_t *sorted_route, int32_t *route_pos, void *ws, size_t ws_bytes, void *stream) {
   int st = check_dims(d);
@@ -280,9 +307,21 @@ MOE_API int moe_forward(const moe_dims_t *d, const moe_fwd_args_t *a, void *ws, 
   int32_t *pos = a->route_pos ? a->route_pos : s.route_pos;
   void *yr = a->y_routed ? a->y_routed : s.y_routed;
   void *ys = a->y_shared ? a->y_shared : s.y_shared;
-  st = moe_route(d, a->x, a->w_router, a->router_bias, a->w_shared_gate, ids, w, sig, a->logits, s.inner,
-                 s.inner_bytes, stream);
-  if (st != MOE_OK) return st;
+  if (a->replay_ids) {
+    if (!buf_ok(a->replay_ids, T * d->k)) return MOE_ERR_INVALID_ARG;
+    st = moe_route_replay(d, a->x, a->w_router, a->router_bias, a->w_shared_gate, a->replay_ids, w, sig, a->logits,
+                          s.inner, s.inner_bytes, stream);
+    if (st != MOE_OK) return st;
+    if (a->topk_ids && a->topk_ids != a->replay_ids && T > 0 &&
+        cudaMemcpyAsync(a->topk_ids, a->replay_ids, (size_t)T * d->k * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                        (cudaStream_t)stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    ids = (int32_t *)a->replay_ids;  // read only from here on
+  } else {
+    st = moe_route(d, a->x, a->w_router, a->router_bias, a->w_shared_gate, ids, w, sig, a->logits, s.inner,
+                   s.inner_bytes, stream);
+    if (st != MOE_OK) return st;
+  }
   st = moe_permute(d, ids, off, srt, pos, s.inner, s.inner_bytes, stream);
   if (st != MOE_OK) return st;
   st = moe_grouped_ffn(d, a->x, off, srt, a->w_gate_up, a->w_down, a->ws_gate_up, a->ws_down, yr, ys, &a->saved,

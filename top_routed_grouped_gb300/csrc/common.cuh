@@ -13,7 +13,7 @@ namespace moe {
 constexpr unsigned FULL_MASK = 0xffffffffu;
 
 // Device status codes (documented with moe_device_status in moe.h).
-enum : int { STATUS_BAD_EXPERT_ID = 1, STATUS_WAIT_TIMEOUT = 2, STATUS_TMEM_ALLOC = 3 };
+enum : int { STATUS_BAD_EXPERT_ID = 1, STATUS_WAIT_TIMEOUT = 2, STATUS_TMEM_ALLOC = 3, STATUS_REPEATED_EXPERT_ID = 4 };
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }

@@ -19,6 +19,11 @@ cudaError_t launch_topk_gate(int dtype, int T, int H, int E, int k, const float 
                              const void *w_shared_gate, int32_t *ids, float *w, float *sig,
                              cudaStream_t stream);
 
+// Route weights and shared gate for given expert ids (router replay).
+cudaError_t launch_replay_gate(int dtype, int T, int H, int E, int k, const float *logits, const void *x,
+                               const void *w_shared_gate, const int32_t *ids, float *w, float *sig, int *status,
+                               cudaStream_t stream);
+
 // ---- api.cu ----
 // Device address of the status word on the current device (nullptr on error).
 int *device_status_ptr();

@@ -117,28 +117,12 @@ __device__ inline bool topk_better(uint32_t o, int e, uint32_t bo, int be) {
 // blocks per SM).
 constexpr int GATE_BATCH = 4;  // 16-byte chunks of x / w_sg loaded together per lane
 
-template <typename TX, int EPL>
-__global__ void __launch_bounds__(256, 4)
-topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, const TX *__restrict__ x,
-                 const TX *__restrict__ wsg, int32_t *__restrict__ ids, float *__restrict__ w,
-                 float *__restrict__ sig) {
-  griddep_launch();
-  griddep_wait();
-  const int lane = threadIdx.x & 31;
-  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (t >= T) return;
-
-  // The token's logits are requested first, so that they arrive while the
-  // gate operands stream in.
-  float lv[EPL];
-  const float *lrow = logits + t * E;
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) lv[i] = lane + 32 * i < E ? __ldg(lrow + lane + 32 * i) : 0.f;
-
-  // Shared-expert gate: lane chunks h = (lane + 32 m) VN, m ascending, summed
-  // in that order per lane, then a fixed butterfly.
+// Shared-expert gate logit x_t . w_sg of one token, by one warp: lane chunks
+// h = (lane + 32 m) VN, m ascending, summed in that order per lane, then a
+// fixed butterfly (every lane returns the same value).
+template <typename TX>
+__device__ inline float gate_dot(const TX *__restrict__ xr, const TX *__restrict__ wsg, int H, int lane) {
   constexpr int VN = Vec16<TX>::N;
-  const TX *xr = x + t * (int64_t)H;
   float part = 0.f;
   for (int h0 = lane * VN; h0 < H; h0 += 32 * VN * GATE_BATCH) {
     uint4 xa[GATE_BATCH], ga[GATE_BATCH];
@@ -163,6 +147,28 @@ topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, c
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(FULL_MASK, part, off);
+  return part;
+}
+
+template <typename TX, int EPL>
+__global__ void __launch_bounds__(256, 4)
+topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, const TX *__restrict__ x,
+                 const TX *__restrict__ wsg, int32_t *__restrict__ ids, float *__restrict__ w,
+                 float *__restrict__ sig) {
+  griddep_launch();
+  griddep_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+
+  // The token's logits are requested first, so that they arrive while the
+  // gate operands stream in.
+  float lv[EPL];
+  const float *lrow = logits + t * E;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) lv[i] = lane + 32 * i < E ? __ldg(lrow + lane + 32 * i) : 0.f;
+
+  const float part = gate_dot<TX>(x + t * (int64_t)H, wsg, H, lane);
 
   // Top-k: order values formed once; the winner's owner zeroes its value and rescans.
   uint32_t ov[EPL];
@@ -206,6 +212,58 @@ topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, c
     w[t * k + lane] = ex / z;
   }
   if (lane == 0) sig[t] = sigmoid_f32(part);
+}
+
+// ---------------------------------------------------------------------------
+// Router replay: the k experts of each token are given (the routes of an
+// earlier pass); only the route weights and the shared gate are computed,
+// with the same formulas as above: w_s = exp(l_s - m) / sum_j exp(l_j - m)
+// over the given slots in their order, m = the largest of the k logits.  Ids
+// out of range or repeated within a token fail closed: the token's weights
+// are written as zeros and the device status records code 1 (out of range)
+// or 4 (repeated).
+// ---------------------------------------------------------------------------
+template <typename TX>
+__global__ void __launch_bounds__(256)
+replay_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, const TX *__restrict__ x,
+                   const TX *__restrict__ wsg, const int32_t *__restrict__ ids, float *__restrict__ w,
+                   float *__restrict__ sig, int *status) {
+  griddep_launch();
+  griddep_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  const int e = lane < k ? __ldg(ids + t * k + lane) : -1;
+  const bool in_range = e >= 0 && e < E;
+  const unsigned dup = __match_any_sync(FULL_MASK, e);
+  const bool bad_range = __any_sync(FULL_MASK, lane < k && !in_range);
+  const bool bad_dup = __any_sync(FULL_MASK, lane < k && __popc(dup) > 1);
+  const float l = lane < k && in_range ? __ldg(logits + t * E + e) : -INFINITY;
+  const float part = gate_dot<TX>(x + t * (int64_t)H, wsg, H, lane);
+  float m = l;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL_MASK, m, off));
+  const float ex = lane < k ? expf(l - m) : 0.f;
+  float z = 0.f;
+  for (int s = 0; s < k; ++s) z += __shfl_sync(FULL_MASK, ex, s);
+  if (lane < k) w[t * k + lane] = (bad_range || bad_dup) ? 0.f : ex / z;
+  if (lane == 0) {
+    sig[t] = sigmoid_f32(part);
+    if (bad_range) record_status(status, STATUS_BAD_EXPERT_ID);
+    else if (bad_dup) record_status(status, STATUS_REPEATED_EXPERT_ID);
+  }
+}
+
+cudaError_t launch_replay_gate(int dtype, int T, int H, int E, int k, const float *logits, const void *x,
+                               const void *w_shared_gate, const int32_t *ids, float *w, float *sig, int *status,
+                               cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const dim3 grid((unsigned)ceil_div(T, 8));
+  if (dtype == 0)
+    return launch_pdl(replay_gate_kernel<float>, grid, dim3(256), 0, stream, T, H, E, k, logits, (const float *)x,
+                      (const float *)w_shared_gate, ids, w, sig, status);
+  return launch_pdl(replay_gate_kernel<__nv_bfloat16>, grid, dim3(256), 0, stream, T, H, E, k, logits,
+                    (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)w_shared_gate, ids, w, sig, status);
 }
 
 template <typename TX>
