@@ -246,6 +246,41 @@ int moe_grouped_ffn(const moe_dims_t *d, const void *x, const int32_t *expert_of
 int moe_combine(const moe_dims_t *d, const void *y_routed, const void *y_shared, const float *topk_w,
                 const float *shared_sig, void *y, void *stream);
 
+/*
+ * moe_grouped_ffn_ep -- moe_grouped_ffn for one rank of an expert partition.
+ * RL-Kernel PR #557 "What": experts are split into contiguous ranges across
+ * ranks, every rank computes the same routes and runs only the segments of
+ * its own experts, one all_gather of the routed rows (a byte copy) follows,
+ * and the combine is local (moe_combine_sorted).  This call is one rank's
+ * expert part; the exchange belongs to the caller (on one GPU, several calls
+ * with disjoint ranges write disjoint row blocks of one buffer).
+ *
+ *   e_begin, e_end  the rank's experts [e_begin, e_end), 0 <= e_begin <= e_end <= E
+ *   with_shared     1: also compute the shared expert into y_shared; 0: leave it
+ *   w_gate_up [e_end-e_begin, 2I, H], w_down [e_end-e_begin, H, I]: the rank's
+ *                   experts only (expert e at index e - e_begin); NULL if the
+ *                   range is empty.  ws_gate_up / ws_down: NULL if !with_shared.
+ *   y_sorted [T*k, H] dtype  out: routed rows in SORTED order (row j = route
+ *                   sorted_route[j]); only rows expert_offsets[e_begin] ..
+ *                   expert_offsets[e_end] - 1 are written, so each rank's
+ *                   result is one contiguous block.
+ * Every value equals the single-call moe_grouped_ffn's for the same row bit for
+ * bit.  Errors as moe_grouped_ffn; a bad range is MOE_ERR_INVALID_ARG.
+ * Workspace: GROUPED_FFN.
+ */
+int moe_grouped_ffn_ep(const moe_dims_t *d, int32_t e_begin, int32_t e_end, int32_t with_shared, const void *x,
+                       const int32_t *expert_offsets, const int32_t *sorted_route, const void *w_gate_up,
+                       const void *w_down, const void *ws_gate_up, const void *ws_down, void *y_sorted,
+                       void *y_shared, const moe_saved_t *saved, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_combine_sorted -- moe_combine reading the routed rows in sorted order
+ * (route r at row route_pos[r]), the layout moe_grouped_ffn_ep writes.  Same
+ * arithmetic and order as moe_combine, so the same output bits.  No workspace.
+ */
+int moe_combine_sorted(const moe_dims_t *d, const void *y_sorted, const int32_t *route_pos, const void *y_shared,
+                       const float *topk_w, const float *shared_sig, void *y, void *stream);
+
 /* Everything moe_forward reads and writes. */
 typedef struct moe_fwd_args {
   const void *x;             /* [T, H] dtype */

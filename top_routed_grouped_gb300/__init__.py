@@ -25,7 +25,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
           -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE"}
 EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_permute", "moe_grouped_ffn",
             "moe_combine", "moe_forward", "moe_backward", "moe_device_status", "moe_permute_noalloc",
-            "moe_route_replay")
+            "moe_route_replay", "moe_grouped_ffn_ep", "moe_combine_sorted")
 
 _vp = ctypes.c_void_p
 
@@ -84,6 +84,9 @@ def lib() -> ctypes.CDLL:
                 "moe_grouped_ffn": ([D] + [_vp] * 9 + [ctypes.POINTER(Saved), _vp, ctypes.c_size_t, _vp],
                                     ctypes.c_int),
                 "moe_combine": ([D] + [_vp] * 5 + [_vp], ctypes.c_int),
+                "moe_grouped_ffn_ep": ([D, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32] + [_vp] * 9 +
+                                       [ctypes.POINTER(Saved), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
+                "moe_combine_sorted": ([D] + [_vp] * 6 + [_vp], ctypes.c_int),
                 "moe_forward": ([D, ctypes.POINTER(FwdArgs), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_backward": ([D, ctypes.POINTER(BwdArgs), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_device_status": ([ctypes.c_int, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
@@ -174,6 +177,21 @@ def moe_grouped_ffn(d, x, expert_offsets, sorted_route, w_gate_up, w_down, ws_ga
         ctypes.byref(d), _p(x), _p(expert_offsets), _p(sorted_route), _p(w_gate_up), _p(w_down), _p(ws_gate_up),
         _p(ws_down), _p(y_routed), _p(y_shared), ctypes.byref(s), _p(ws), 0 if ws is None else ws.numel(),
         _stream(stream)))
+
+
+def moe_grouped_ffn_ep(d, e_begin, e_end, with_shared, x, expert_offsets, sorted_route, w_gate_up, w_down,
+                       ws_gate_up, ws_down, y_sorted, y_shared, saved, ws, stream=None):
+    """One rank's part of the expert-partitioned grouped FFN (see moe.h)."""
+    sv = _saved(saved)
+    _check("moe_grouped_ffn_ep", lib().moe_grouped_ffn_ep(
+        ctypes.byref(d), int(e_begin), int(e_end), int(with_shared), _p(x), _p(expert_offsets), _p(sorted_route),
+        _p(w_gate_up), _p(w_down), _p(ws_gate_up), _p(ws_down), _p(y_sorted), _p(y_shared), ctypes.byref(sv), _p(ws),
+        0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def moe_combine_sorted(d, y_sorted, route_pos, y_shared, topk_w, shared_sig, y, stream=None):
+    _check("moe_combine_sorted", lib().moe_combine_sorted(ctypes.byref(d), _p(y_sorted), _p(route_pos), _p(y_shared),
+                                                          _p(topk_w), _p(shared_sig), _p(y), _stream(stream)))
 
 
 def moe_combine(d, y_routed, y_shared, topk_w, shared_sig, y, stream=None):

@@ -278,6 +278,57 @@ MOE_API int moe_grouped_ffn(const moe_dims_t *d, const void *x, const int32_t *e
   return cuda_status(launch_ffn_tc(a, sc.tiles, device_status_ptr(), (cudaStream_t)stream));
 }
 
+MOE_API int moe_grouped_ffn_ep(const moe_dims_t *d, int32_t e_begin, int32_t e_end, int32_t with_shared,
+                               const void *x, const int32_t *expert_offsets, const int32_t *sorted_route,
+                               const void *w_gate_up, const void *w_down, const void *ws_gate_up, const void *ws_down,
+                               void *y_sorted, void *y_shared, const moe_saved_t *saved, void *ws, size_t ws_bytes,
+                               void *stream) {
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (e_begin < 0 || e_end < e_begin || e_end > d->E || (with_shared != 0 && with_shared != 1))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t T = d->T, R = T * d->k, n_local = e_end - e_begin;
+  if (!buf_ok(x, T * d->H) || !buf_ok(expert_offsets, 1) || !buf_ok(sorted_route, R) || !buf_ok(w_gate_up, n_local) ||
+      !buf_ok(w_down, n_local) || !buf_ok(ws_gate_up, with_shared) || !buf_ok(ws_down, with_shared) ||
+      !buf_ok(y_sorted, n_local ? R * d->H : 0) || !buf_ok(y_shared, with_shared ? T * d->H : 0) || !opt_ok(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (saved && (!opt_ok(saved->gu) || !opt_ok(saved->h) || !opt_ok(saved->gu_shared) || !opt_ok(saved->h_shared)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_size(d, MOE_OP_GROUPED_FFN)) return MOE_ERR_WORKSPACE;
+  if (T == 0 || (n_local == 0 && !with_shared)) return MOE_OK;
+  Carver c(ws);
+  FfnScratch sc = ffn_ws(d, c);
+  FfnArgs a;
+  a.T = d->T; a.H = d->H; a.E = d->E; a.k = d->k; a.I = d->I; a.Is = d->Is;
+  a.x = x; a.offsets = expert_offsets; a.sorted_route = sorted_route;
+  // The maps of an unused half still need a valid address; nothing is read through them.
+  a.w_gate_up = n_local ? w_gate_up : ws_gate_up;
+  a.w_down = n_local ? w_down : ws_down;
+  a.ws_gate_up = with_shared ? ws_gate_up : a.w_gate_up;
+  a.ws_down = with_shared ? ws_down : a.w_down;
+  a.y_routed = y_sorted; a.y_shared = y_shared;
+  a.h_routed = (saved && saved->h) ? saved->h : sc.h_routed;
+  a.h_shared = (saved && saved->h_shared) ? saved->h_shared : sc.h_shared;
+  a.gu_routed = saved ? saved->gu : nullptr;
+  a.gu_shared = saved ? saved->gu_shared : nullptr;
+  a.e_begin = e_begin; a.e_end = e_end; a.with_shared = with_shared; a.y_sorted = 1;
+  if (d->dtype == MOE_F32) return cuda_status(launch_ffn_simt(a, sc.tiles, (cudaStream_t)stream));
+  return cuda_status(launch_ffn_tc(a, sc.tiles, device_status_ptr(), (cudaStream_t)stream));
+}
+
+MOE_API int moe_combine_sorted(const moe_dims_t *d, const void *y_sorted, const int32_t *route_pos,
+                               const void *y_shared, const float *topk_w, const float *shared_sig, void *y,
+                               void *stream) {
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  const int64_t T = d->T, R = T * d->k;
+  if (!buf_ok(y_sorted, R * d->H) || !buf_ok(route_pos, R) || !buf_ok(y_shared, T * d->H) || !buf_ok(topk_w, R) ||
+      !buf_ok(shared_sig, T) || !buf_ok(y, T * d->H))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(d->dtype, d->T, d->H, d->k, y_sorted, y_shared, topk_w, shared_sig, y,
+                                    (cudaStream_t)stream, route_pos));
+}
+
 MOE_API int moe_combine(const moe_dims_t *d, const void *y_routed, const void *y_shared, const float *topk_w,
                         const float *shared_sig, void *y, void *stream) {
   int st = check_dims(d);

@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(256) ffn_gate_up_simt_kernel(FfnArgs a, const 
     const int Iseg = shared ? a.Is : a.I;
     const int f0 = blockIdx.y * 32;
     if (f0 >= Iseg) continue;  // uniform over the block
-    const TE *wgu = shared ? (const TE *)a.ws_gate_up : (const TE *)a.w_gate_up + (int64_t)tr.seg * 2 * a.I * a.H;
+    const TE *wgu =
+        shared ? (const TE *)a.ws_gate_up : (const TE *)a.w_gate_up + (int64_t)(tr.seg - a.e_begin) * 2 * a.I * a.H;
     if (threadIdx.x < SIMT_BM) {
       int64_t j = tr.r0 + threadIdx.x;
       tok[threadIdx.x] = j < tr.r1 ? (shared ? j : (int64_t)(a.sorted_route[j] / a.k)) : -1;
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(256) ffn_down_simt_kernel(FfnArgs a, const int
     const bool shared = tr.seg == a.E;
     const int Iseg = shared ? a.Is : a.I;
     const TE *hin = shared ? (const TE *)a.h_shared : (const TE *)a.h_routed;
-    const TE *wdn = shared ? (const TE *)a.ws_down : (const TE *)a.w_down + (int64_t)tr.seg * a.H * a.I;
+    const TE *wdn = shared ? (const TE *)a.ws_down : (const TE *)a.w_down + (int64_t)(tr.seg - a.e_begin) * a.H * a.I;
     float acc[2][4];
 #pragma unroll
     for (int i = 0; i < 2; ++i)
@@ -169,7 +170,8 @@ __global__ void __launch_bounds__(256) ffn_down_simt_kernel(FfnArgs a, const int
     for (int i = 0; i < 2; ++i) {
       int64_t row = tr.r0 + 2 * ty + i;
       if (row >= tr.r1) continue;
-      TE *dst = shared ? (TE *)a.y_shared + row * a.H : (TE *)a.y_routed + (int64_t)a.sorted_route[row] * a.H;
+      TE *dst = shared ? (TE *)a.y_shared + row * a.H
+                       : (TE *)a.y_routed + (a.y_sorted ? row : (int64_t)a.sorted_route[row]) * a.H;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         int o = o0 + 4 * tx + j;
@@ -182,7 +184,8 @@ __global__ void __launch_bounds__(256) ffn_down_simt_kernel(FfnArgs a, const int
 cudaError_t launch_ffn_simt(const FfnArgs &a, void *scratch, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
   int32_t *tile_start = (int32_t *)scratch;
-  cudaError_t err = launch_build_tiles(a.E, a.T, SIMT_BM, a.offsets, tile_start, stream);
+  cudaError_t err = launch_build_tiles(a.E, a.T, SIMT_BM, a.offsets, tile_start, stream, a.e_begin, a.e_end,
+                                       a.with_shared);
   if (err != cudaSuccess) return err;
   const int64_t R = (int64_t)a.T * a.k;
   const int64_t max_tiles = ceil_div(R + a.T, SIMT_BM) + a.E + 1;

@@ -108,6 +108,8 @@ struct TcParams {
   int T, H, E, k, I, Is;
   int n_items;              // ROUTER: number of items (others: item_start[E+1])
   int rt_ntile, rt_rpt;     // ROUTER: token tiles and rows per tile
+  int e0;                   // first expert of the weight arrays (expert partition)
+  int y_sorted;             // DOWN: routed rows in sorted order
   const int32_t *offsets;
   const int32_t *sorted_route;
   const int32_t *item_start;  // [E+2] prefix of items per segment
@@ -227,11 +229,11 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           uint8_t *b_dst = sb + stage * TC_B_BYTES;
           if (MODE == TC_GATE_UP) {
             // One 5-D box: for 8 groups of 16 features (two M tiles), 16 gate rows then 16 up rows.
-            tma_load_5d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64, 0, 0, im.f * 4 * MT, sh ? 0 : im.seg,
+            tma_load_5d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64, 0, 0, im.f * 4 * MT, sh ? 0 : im.seg - p.e0,
                         pol_w);
           } else {
             tma_load_2d(a_dst, sh ? &maps.a_sh : &maps.a, &full[stage], kb * 64,
-                        (sh ? 0 : im.seg * p.H) + im.f * 128 * MT, pol_w);
+                        (sh ? 0 : (im.seg - p.e0) * p.H) + im.f * 128 * MT, pol_w);
           }
           if (MODE != TC_GATE_UP) {
             // Token rows [row0, row0 + n) as power-of-two boxes (n is a multiple of 16).
@@ -394,7 +396,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
           // Destination row of column c0 + lane, fetched before the accumulator loads.
           int dst = 0;
-          if (c0 + lane < im.rows) dst = sh ? (int)(im.row0 + c0 + lane) : __ldg(p.sorted_route + im.row0 + c0 + lane);
+          if (c0 + lane < im.rows)
+            dst = (sh || p.y_sorted) ? (int)(im.row0 + c0 + lane) : __ldg(p.sorted_route + im.row0 + c0 + lane);
           float vt[MT][32];
           if (MT == 2) tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[MT - 1]);
           else tmem_ld32(tq + c0, vt[0]);
@@ -713,8 +716,8 @@ constexpr int IT_MAX_E = 1024;
 
 __global__ void __launch_bounds__(1024)
 item_tables_kernel(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s, const int32_t *__restrict__ offsets,
-                   int32_t *__restrict__ start_a, int32_t *__restrict__ start_b, int4 *__restrict__ items_a,
-                   int4 *__restrict__ items_b, int max_a, int max_b) {
+                   int32_t *__restrict__ start_a, int32_t *__restrict__ start_b, int e_begin, int e_end,
+                   int with_shared) {
   griddep_launch();
   griddep_wait();
   __shared__ int32_t s_off[IT_MAX_E + 1], s_a[IT_MAX_E + 2], s_b[IT_MAX_E + 2];
@@ -726,8 +729,8 @@ item_tables_kernel(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s,
   for (int base = 0; base <= E; base += 1024) {
     const int s = base + threadIdx.x;
     int32_t v = 0;
-    if (s < E) v = (int32_t)ceil_div(s_off[s + 1] - s_off[s], 256);
-    else if (s == E) v = (int32_t)ceil_div(T, 256);
+    if (s < E) v = (s >= e_begin && s < e_end) ? (int32_t)ceil_div(s_off[s + 1] - s_off[s], 256) : 0;
+    else if (s == E) v = with_shared ? (int32_t)ceil_div(T, 256) : 0;
     buf[threadIdx.x] = v;
     __syncthreads();
     for (int d = 1; d < 1024; d <<= 1) {
@@ -766,7 +769,8 @@ item_expand_kernel(int E, int T, const int32_t *__restrict__ offsets, const int3
   if (sg > E) return;
   const int base = sg == E ? 0 : __ldg(offsets + sg);
   const int n_s = sg == E ? T : __ldg(offsets + sg + 1) - base;
-  if (n_s == 0) return;
+  if (n_s == 0 || __ldg(start_a + sg + 1) == __ldg(start_a + sg) && __ldg(start_b + sg + 1) == __ldg(start_b + sg))
+    return;  // empty, or outside the expert range
   const int ntile = (n_s + 255) >> 8;
   const int rpt = ((n_s + ntile - 1) / ntile + 15) & ~15;
   const int a0 = __ldg(start_a + sg), na = __ldg(start_a + sg + 1) - a0;
@@ -828,10 +832,11 @@ static int64_t max_items(int T, int k, int E, int nf_routed, int nf_shared) {
 
 cudaError_t launch_item_tables(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s, const int32_t *offsets,
                                int32_t *start_a, int32_t *start_b, int4 *items_a, int4 *items_b, int max_a,
-                               int max_b, cudaStream_t stream) {
+                               int max_b, cudaStream_t stream, int e_begin, int e_end, int with_shared) {
   if (E > IT_MAX_E) return cudaErrorInvalidValue;
+  if (e_end < 0) e_end = E;
   cudaError_t e = launch_pdl(item_tables_kernel, dim3(1), dim3(1024), 0, stream, E, T, nf_a_r, nf_a_s, nf_b_r, nf_b_s,
-                             offsets, start_a, start_b, items_a, items_b, max_a, max_b);
+                             offsets, start_a, start_b, e_begin, e_end, with_shared);
   if (e != cudaSuccess) return e;
   return launch_pdl(item_expand_kernel, dim3((unsigned)ceil_div((int64_t)(E + 1) * 32, 256)), dim3(256), 0, stream, E,
                     T, offsets, (const int32_t *)start_a, (const int32_t *)start_b, items_a, items_b, max_a, max_b);
@@ -859,14 +864,16 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   int32_t *start_dn = (int32_t *)(w + starts);
   int4 *items_gu = (int4 *)(w + 2 * starts);
   int4 *items_dn = (int4 *)(w + 2 * starts + round256((size_t)mi_gu * 16));
+  const int eb = a.e_begin, ee = a.e_end < 0 ? a.E : a.e_end, n_local = ee - eb;
   cudaError_t e0 = launch_item_tables(a.E, a.T, a.I / GU_FEAT, a.Is / GU_FEAT, a.H / DN_ROWS, a.H / DN_ROWS, a.offsets,
-                                      start_gu, start_dn, items_gu, items_dn, mi_gu, mi_dn, stream);
+                                      start_gu, start_dn, items_gu, items_dn, mi_gu, mi_dn, stream, eb, ee,
+                                      a.with_shared);
   if (e0 != cudaSuccess) return e0;
   const int64_t R = (int64_t)a.T * a.k;
   TcMaps mg, md;
-  if (!map_gate_up(&mg.a, a.w_gate_up, a.E, a.I, a.H, 4 * TcCfg<TC_GATE_UP>::MT) ||
+  if (!map_gate_up(&mg.a, a.w_gate_up, std::max(n_local, 1), a.I, a.H, 4 * TcCfg<TC_GATE_UP>::MT) ||
       !map_gate_up(&mg.a_sh, a.ws_gate_up, 1, a.Is, a.H, 4 * TcCfg<TC_GATE_UP>::MT) ||
-      !map_2d(&md.a, a.w_down, (int64_t)a.E * a.H, a.I, DN_ROWS) || !map_2d(&md.a_sh, a.ws_down, a.H, a.Is, DN_ROWS) ||
+      !map_2d(&md.a, a.w_down, (int64_t)std::max(n_local, 1) * a.H, a.I, DN_ROWS) || !map_2d(&md.a_sh, a.ws_down, a.H, a.Is, DN_ROWS) ||
       !map_rows(md.b, a.h_routed, R, a.I) || !map_rows(md.b_sh, a.h_shared, a.T, a.Is))
     return cudaErrorInvalidValue;
   for (int h = 0; h < 5; ++h) mg.b[h] = mg.b_sh[h] = mg.a;  // gate_up gathers its token rows with cp.async
@@ -881,6 +888,8 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   p.gu_shared = (__nv_bfloat16 *)a.gu_shared;
   p.y_routed = (__nv_bfloat16 *)a.y_routed;
   p.y_shared = (__nv_bfloat16 *)a.y_shared;
+  p.e0 = eb;
+  p.y_sorted = a.y_sorted;
   p.status = status;
   const int grid = device_sms();
   p.item_start = start_gu;

@@ -38,9 +38,11 @@ cudaError_t launch_permute(int64_t R, int E, const int32_t *ids, int32_t *offset
                            int32_t *route_pos, void *scratch, int *status, cudaStream_t stream,
                            int chunk = PERMUTE_CHUNK_SMALL);
 // tile_start[s] for s in [0, E+1]: prefix of ceil(n_s / bn) over the E routed
-// segments (n_s from offsets) and the shared segment (n_E = T).
+// segments (n_s from offsets) and the shared segment (n_E = T); only routed
+// segments in [e_begin, e_end) (e_end < 0: E) and, if with_shared, the shared
+// segment get tiles.
 cudaError_t launch_build_tiles(int E, int T, int bn, const int32_t *offsets, int32_t *tile_start,
-                               cudaStream_t stream);
+                               cudaStream_t stream, int e_begin = 0, int e_end = -1, int with_shared = 1);
 
 // ---- ffn_simt.cu ----
 struct FfnArgs {
@@ -52,6 +54,11 @@ struct FfnArgs {
   void *y_routed, *y_shared;
   void *h_routed, *h_shared;    // intermediate h (required)
   void *gu_routed, *gu_shared;  // saved pre-activations (nullable)
+  // Expert partition: only the routed segments in [e_begin, e_end) (weights
+  // w_gate_up / w_down hold those experts only, expert e at index e - e_begin)
+  // and, if with_shared, the shared expert; y_sorted: routed rows written in
+  // sorted order (row j) instead of route order (row sorted_route[j]).
+  int e_begin = 0, e_end = -1, with_shared = 1, y_sorted = 0;
 };
 size_t ffn_simt_scratch_bytes(int E);
 // The MOE_F32 grouped FFN on CUDA cores (all buffers float).
@@ -71,11 +78,13 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
 int64_t tc_max_items(int T, int k, int E, int nf_routed, int nf_shared);
 cudaError_t launch_item_tables(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s, const int32_t *offsets,
                                int32_t *start_a, int32_t *start_b, int4 *items_a, int4 *items_b, int max_a,
-                               int max_b, cudaStream_t stream);
+                               int max_b, cudaStream_t stream, int e_begin = 0, int e_end = -1, int with_shared = 1);
 
 // ---- combine.cu ----
+// route_pos != nullptr: y_routed rows are in sorted order (route r at row route_pos[r]).
 cudaError_t launch_combine(int dtype, int T, int H, int k, const void *y_routed, const void *y_shared,
-                           const float *w, const float *sig, void *y, cudaStream_t stream);
+                           const float *w, const float *sig, void *y, cudaStream_t stream,
+                           const int32_t *route_pos = nullptr);
 
 // ---- backward.cu ----
 struct BwArgs {

@@ -198,10 +198,13 @@ cudaError_t launch_permute(int64_t R, int E, const int32_t *ids, int32_t *offset
 // Tile list of the grouped GEMMs: segment s in [0, E) holds the routes of
 // expert s (offsets[s]..offsets[s+1]), segment E the T tokens of the shared
 // expert.  tile_start[s] = sum_{s' < s} ceil(n_s' / bn), tile_start[E+1] =
-// total.  One block; integer prefix, exact.
+// total, counting only the routed segments in [e_begin, e_end) and the
+// shared one if `with_shared` (the others get no tiles).  One block; integer
+// prefix, exact.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
-build_tiles_kernel(int E, int T, int bn, const int32_t *__restrict__ offsets, int32_t *__restrict__ tile_start) {
+build_tiles_kernel(int E, int T, int bn, const int32_t *__restrict__ offsets, int32_t *__restrict__ tile_start,
+                   int e_begin, int e_end, int with_shared) {
   griddep_launch();
   griddep_wait();
   __shared__ int32_t buf[1024];
@@ -211,8 +214,8 @@ build_tiles_kernel(int E, int T, int bn, const int32_t *__restrict__ offsets, in
   for (int base = 0; base <= E; base += 1024) {
     const int s = base + threadIdx.x;
     int32_t n = 0;
-    if (s < E) n = offsets[s + 1] - offsets[s];
-    else if (s == E) n = T;
+    if (s < E) n = (s >= e_begin && s < e_end) ? offsets[s + 1] - offsets[s] : 0;
+    else if (s == E) n = with_shared ? T : 0;
     int32_t v = (n + bn - 1) / bn;
     buf[threadIdx.x] = v;
     __syncthreads();
@@ -231,8 +234,10 @@ build_tiles_kernel(int E, int T, int bn, const int32_t *__restrict__ offsets, in
 }
 
 cudaError_t launch_build_tiles(int E, int T, int bn, const int32_t *offsets, int32_t *tile_start,
-                               cudaStream_t stream) {
-  return launch_pdl(build_tiles_kernel, dim3(1), dim3(1024), 0, stream, E, T, bn, offsets, tile_start);
+                               cudaStream_t stream, int e_begin, int e_end, int with_shared) {
+  if (e_end < 0) e_end = E;
+  return launch_pdl(build_tiles_kernel, dim3(1), dim3(1024), 0, stream, E, T, bn, offsets, tile_start, e_begin, e_end,
+                    with_shared);
 }
 
 }  // namespace moe
