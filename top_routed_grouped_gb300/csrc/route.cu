@@ -174,11 +174,17 @@ topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, c
   uint32_t ov[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) ov[i] = lane + 32 * i < E ? topk_ord(lv[i]) : 0u;
-  uint32_t bo = 0u;
-  int bi = 0;
+  // Each lane keeps its best and second-best candidates (ties: lower slot =
+  // lower id first).  When the lane's best wins, the second is promoted; only
+  // when no valid second is left does the lane rescan its candidates.
+  uint32_t bo = 0u, bo2 = 0u;
+  int bi = 0, bi2 = 0;
 #pragma unroll
-  for (int i = 0; i < EPL; ++i)
-    if (ov[i] > bo) bo = ov[i], bi = i;  // ties keep the lower slot = lower id
+  for (int i = 0; i < EPL; ++i) {
+    if (ov[i] > bo) bo2 = bo, bi2 = bi, bo = ov[i], bi = i;
+    else if (ov[i] > bo2) bo2 = ov[i], bi2 = i;
+  }
+  bool has2 = true;
 
   float sel_v = 0.f;  // lane s keeps the logit of slot s
   int sel_e = 0;
@@ -191,13 +197,21 @@ topk_gate_kernel(int T, int H, int E, int k, const float *__restrict__ logits, c
       sel_v = ord_logit(mo);
       sel_e = me;
     }
-    if (lane == (me & 31)) {  // the owner drops the winner and rescans
-      bo = 0u;
-      bi = 0;
+    if (lane == (me & 31)) {  // the owner drops the winner
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        if (i == (me >> 5)) ov[i] = 0u;
-        if (ov[i] > bo) bo = ov[i], bi = i;
+      for (int i = 0; i < EPL; ++i)
+        if (i == bi) ov[i] = 0u;
+      if (has2) {
+        bo = bo2, bi = bi2, has2 = false;
+      } else {
+        bo = bo2 = 0u;
+        bi = bi2 = 0;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          if (ov[i] > bo) bo2 = bo, bi2 = bi, bo = ov[i], bi = i;
+          else if (ov[i] > bo2) bo2 = ov[i], bi2 = i;
+        }
+        has2 = true;
       }
     }
   }
