@@ -328,12 +328,15 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
 // hb (64, 32 or 16) is the smallest box height that covers the rows left in
 // the segment; lines past the segment's end (at most 15 per block) are
 // zeroed before the MMAs read them.
-constexpr int WG_STAGES = 3, WG_EPI_WARPS = 8;
+// WG_EPI_WARPS epilogue warps, WG_EPI_WARPS / 4 per TMEM lane quarter, each
+// draining WG_COLS of the 256 accumulator columns through WG_NSTG staging tiles.
+constexpr int WG_STAGES = 3, WG_EPI_WARPS = 8, WG_NSTG = 2;
+constexpr int WG_COLS = 1024 / WG_EPI_WARPS;
 constexpr int WG_A_BYTES = 2 * 8192;  // 128 M x 64 K lines, MN-major
 constexpr int WG_B_BYTES = 4 * 8192;  // 256 N x 64 K lines, MN-major
-constexpr int WG_STG_BYTES = 4096;    // one 32 x 32 FP32 store tile; two per epilogue warp
+constexpr int WG_STG_BYTES = 4096;    // one 32 x 32 FP32 store tile
 constexpr int WG_THREADS = 32 * (GT_EPI_FIRST + WG_EPI_WARPS);
-constexpr int WG_SMEM = 1024 + WG_STAGES * (WG_A_BYTES + WG_B_BYTES) + (2 * WG_EPI_WARPS + 1) * WG_STG_BYTES + 256;
+constexpr int WG_SMEM = 1024 + WG_STAGES * (WG_A_BYTES + WG_B_BYTES) + (WG_NSTG * WG_EPI_WARPS + 1) * WG_STG_BYTES + 256;
 static_assert(WG_SMEM <= 232448, "wgrad shared memory");
 
 struct WgMaps {
@@ -392,7 +395,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
   uint8_t *sa = base;
   uint8_t *sb = sa + WG_STAGES * WG_A_BYTES;
   uint8_t *stg_all = sb + WG_STAGES * WG_B_BYTES;
-  uint8_t *zero_tile = stg_all + 2 * WG_EPI_WARPS * WG_STG_BYTES;
+  uint8_t *zero_tile = stg_all + WG_NSTG * WG_EPI_WARPS * WG_STG_BYTES;
   uint64_t *bars = (uint64_t *)(zero_tile + WG_STG_BYTES);
   uint64_t *full = bars, *empty = bars + WG_STAGES;
   uint64_t *tfull = bars + 2 * WG_STAGES, *tempty = tfull + 2, *mma_done = tempty + 2;
@@ -513,9 +516,9 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // Warp (q, half): TMEM lanes 32q.. (output rows), columns [128 half, +128).
+    // Warp (q, part): TMEM lanes 32q.. (output rows), columns [WG_COLS part, +WG_COLS).
     const int q = warp & 3, half = (warp - GT_EPI_FIRST) >> 2;
-    uint8_t *stg0 = stg_all + (warp - GT_EPI_FIRST) * 2 * WG_STG_BYTES;
+    uint8_t *stg0 = stg_all + (warp - GT_EPI_FIRST) * WG_NSTG * WG_STG_BYTES;
     uint32_t cnt = 0, sbuf = 0;
     const int Mr = MODE == WGRAD_DOWN ? p.H : 2 * p.I;  // output rows per routed expert
     for (int it = blockIdx.x; it < p.total; it += gridDim.x) {
@@ -523,10 +526,10 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
       const bool sh = im.seg == p.E;
       const CUtensorMap *om = sh ? &maps.out_sh : &maps.out;
       const int mrow = (sh ? 0 : im.seg * Mr) + im.mt * 128 + q * 32;
-      const int ncol = im.nt * 256 + half * 128;
+      const int ncol = im.nt * 256 + half * WG_COLS;
       if (im.rows == 0) {
         if (lane == 0) {
-          for (int cc = 0; cc < 4; ++cc) tma_store_2d(om, zero_tile, ncol + cc * 32, mrow);
+          for (int cc = 0; cc < WG_COLS / 32; ++cc) tma_store_2d(om, zero_tile, ncol + cc * 32, mrow);
           bulk_commit();
         }
         __syncwarp();
@@ -535,13 +538,13 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
       const int b = cnt & 1;
       if (!gt_warp_wait(&tfull[b], (cnt >> 1) & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t tb = tmem + b * 256 + ((uint32_t)(q * 32) << 16) + half * 128;
+      const uint32_t tb = tmem + b * 256 + ((uint32_t)(q * 32) << 16) + half * WG_COLS;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < WG_COLS / 32; ++cc) {
         float v[32];
         tmem_ld32(tb + cc * 32, v);
         uint8_t *stg = stg0 + sbuf * WG_STG_BYTES;
-        if (lane == 0) bulk_wait_read<1>();  // the store issued from this buffer two tiles ago has read it
+        if (lane == 0) bulk_wait_read<WG_NSTG - 1>();  // the last store from this buffer has read it
         __syncwarp();
         // Row `lane` of the 32 x 32 tile: 16-byte chunk j at (j ^ (lane % 8)), the 128-byte swizzle.
 #pragma unroll
@@ -554,7 +557,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
           tma_store_2d(om, stg, ncol + cc * 32, mrow);
           bulk_commit();
         }
-        sbuf ^= 1;
+        if (++sbuf == WG_NSTG) sbuf = 0;
       }
       tc_fence_before();
       mbar_arrive(&tempty[b]);
