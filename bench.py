@@ -144,8 +144,8 @@ class ClockSampler:
 # DRAM bytes (read + write) of one moe_grouped_ffn call (gate_up + down) at
 # bf16_t8192, from `ncu --set full` (profiles/grouped_ffn_bf16_t8192.md), valid
 # only for the kernel sources it was taken on (hash below); otherwise null.
-FFN_TRAFFIC = {"sources": "58c4de0163d7166f", "workload": "bf16_t8192",
-               "bytes": 2_347_057_000 + 59_947_264 + 1_315_282_000 + 317_399_296}
+FFN_TRAFFIC = {"sources": "75e8ad112b9b06bf", "workload": "bf16_t8192",
+               "bytes": 2_339_181_000 + 60_803_328 + 1_233_498_000 + 319_333_376}
 
 
 def kernel_sources_hash() -> str:
