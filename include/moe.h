@@ -139,6 +139,19 @@ int moe_route(const moe_dims_t *d, const void *x, const float *w_router, const f
               float *logits, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_router_logits -- the router GEMM alone, for measuring it.
+ * RL-Kernel PR #557, #503 commit message "Routing": the router runs in FP32;
+ * "Results (4 x H100)": BF16 routing is the variant that drifts.
+ *   exact = 1: the logits moe_route uses (bit for bit).
+ *   exact = 0: the BF16-router ablation: the weight rounded once to bf16, the
+ *              same FP32 accumulation order otherwise (MOE_BF16 only;
+ *              MOE_F32 returns MOE_ERR_UNSUPPORTED).
+ *   logits [T, E] float out (with router_bias if not NULL).  Workspace: ROUTE.
+ */
+int moe_router_logits(const moe_dims_t *d, const void *x, const float *w_router, const float *router_bias,
+                      int32_t exact, float *logits, void *ws, size_t ws_bytes, void *stream);
+
+/*
  * moe_route_replay -- route weights and shared gate for GIVEN expert ids.
  * SkyRL PR #2513, section "chunked_mlp fixes (#2532, merged)": per-chunk
  * router replay; SkyRL docs page "Qwen3.8-Flash-Next", section "Example

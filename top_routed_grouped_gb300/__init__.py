@@ -25,7 +25,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
           -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE"}
 EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_permute", "moe_grouped_ffn",
             "moe_combine", "moe_forward", "moe_backward", "moe_device_status", "moe_permute_noalloc",
-            "moe_route_replay", "moe_grouped_ffn_ep", "moe_combine_sorted")
+            "moe_route_replay", "moe_grouped_ffn_ep", "moe_combine_sorted", "moe_router_logits")
 
 _vp = ctypes.c_void_p
 
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
                 "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
                 "moe_route": ([D] + [_vp] * 8 + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_route_replay": ([D] + [_vp] * 8 + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
+                "moe_router_logits": ([D, _vp, _vp, _vp, ctypes.c_int32, _vp, _vp, ctypes.c_size_t, _vp],
+                                      ctypes.c_int),
                 "moe_permute": ([D] + [_vp] * 4 + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_grouped_ffn": ([D] + [_vp] * 9 + [ctypes.POINTER(Saved), _vp, ctypes.c_size_t, _vp],
                                     ctypes.c_int),
@@ -143,6 +145,24 @@ def moe_route(d, x, w_router, router_bias, w_shared_gate, topk_ids, topk_w, shar
     _check("moe_route", lib().moe_route(ctypes.byref(d), _p(x), _p(w_router), _p(router_bias), _p(w_shared_gate),
                                         _p(topk_ids), _p(topk_w), _p(shared_sig), _p(logits), _p(ws),
                                         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_router_logits(d, x, w_router, router_bias, exact, logits, ws, stream=None):
+    _check("moe_router_logits", lib().moe_router_logits(
+        ctypes.byref(d), _p(x), _p(w_router), _p(router_bias), int(exact), _p(logits), _p(ws),
+        0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def router_logits(x, w_router, router_bias=None, exact: bool = True, stream=None):
+    """Router logits [T, E] float: exact FP32-equivalent (default) or the
+    BF16-router ablation (weight rounded once to bf16)."""
+    import torch
+    T, H = x.shape
+    E = w_router.shape[0]
+    d = make_dims(T, H, E, 1, 128, 128, x.dtype)  # k, I, Is unused
+    out = torch.empty(T, E, dtype=torch.float32, device=x.device)
+    moe_router_logits(d, x, w_router, router_bias, 1 if exact else 0, out, workspace(d, "route", x.device), stream)
+    return out
 
 
 def moe_route_replay(d, x, w_router, router_bias, w_shared_gate, topk_ids, topk_w, shared_sig, logits, ws,

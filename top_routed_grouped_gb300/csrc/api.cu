@@ -208,6 +208,28 @@ MOE_API int moe_route(const moe_dims_t *d, const void *x, const float *w_router,
   return cuda_status(e);
 }
 
+MOE_API int moe_router_logits(const moe_dims_t *d, const void *x, const float *w_router, const float *router_bias,
+                              int32_t exact, float *logits, void *ws, size_t ws_bytes, void *stream) {
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (exact != 0 && exact != 1) return MOE_ERR_INVALID_ARG;
+  const int64_t T = d->T;
+  if (!buf_ok(x, T * d->H) || !buf_ok(w_router, 1) || !opt_ok(router_bias) || !buf_ok(logits, T * d->E) ||
+      !opt_ok(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (d->dtype == MOE_F32 && !exact) return MOE_ERR_UNSUPPORTED;
+  if (ws_bytes < ws_size(d, MOE_OP_ROUTE)) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  Carver c(ws);
+  c.take((size_t)T * d->E * sizeof(float));  // the logits slot of the ROUTE layout (unused here)
+  if (d->dtype == MOE_F32)
+    return cuda_status(launch_router_logits_simt(d->T, d->H, d->E, (const float *)x, w_router, router_bias, logits, s));
+  return cuda_status(launch_router_logits_tc(d->T, d->H, d->E, x, w_router, router_bias, logits,
+                                             c.take(router_tc_scratch_bytes(d->E, d->H)), device_status_ptr(), s,
+                                             exact ? 3 : 1));
+}
+
 MOE_API int moe_route_replay(const moe_dims_t *d, const void *x, const float *w_router, const float *router_bias,
                              const void *w_shared_gate, const int32_t *topk_ids, float *topk_w, float *shared_sig,
                              float *logits, void *ws, size_t ws_bytes, void *stream) {

@@ -108,6 +108,7 @@ struct TcParams {
   int T, H, E, k, I, Is;
   int n_items;              // ROUTER: number of items (others: item_start[E+1])
   int rt_ntile, rt_rpt;     // ROUTER: token tiles and rows per tile
+  int rt_splits;            // ROUTER: bf16 terms of the weight used (3: exact; 1: weight rounded to bf16)
   int e0;                   // first expert of the weight arrays (expert partition)
   int y_sorted;             // DOWN: routed rows in sorted order
   const int32_t *offsets;
@@ -551,14 +552,14 @@ tc_router_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       bool ok = true;
       for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
         const RtItem im = rt_item(it, p);
-        const uint32_t bytes = RT_A_BYTES + im.n * 128;
+        const uint32_t bytes = p.rt_splits * TC_TILE_A_BYTES + im.n * 128;
         for (int j = 0; j < nkh; ++j) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], bytes);
           uint8_t *a_dst = sa + stage * RT_A_BYTES;
           uint8_t *b_dst = sb + stage * TC_B_BYTES;
 #pragma unroll
-          for (int sp = 0; sp < 3; ++sp)
+          for (int sp = 0; sp < p.rt_splits; ++sp)
             tma_load_2d(a_dst + sp * TC_TILE_A_BYTES, &maps.a, &full[stage], sp * p.H + j * 64, im.f * 128, pol);
           int r = 0;
 #pragma unroll
@@ -601,7 +602,7 @@ tc_router_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             tc_fence_after();
             const uint64_t bd = smem_desc_sw128(smem_u32(sb + stage * TC_B_BYTES));
 #pragma unroll
-            for (int sp = 0; sp < 3; ++sp) {
+            for (int sp = 0; sp < p.rt_splits; ++sp) {
               const uint64_t ad = smem_desc_sw128(smem_u32(sa + stage * RT_A_BYTES + sp * TC_TILE_A_BYTES));
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
@@ -794,7 +795,8 @@ static cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cu
 size_t router_tc_scratch_bytes(int E, int H) { return (size_t)E * 3 * H * 2; }
 
 cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const float *wr, const float *bias,
-                                    float *logits, void *scratch, int *status, cudaStream_t stream) {
+                                    float *logits, void *scratch, int *status, cudaStream_t stream, int splits) {
+  if (splits != 1 && splits != 3) return cudaErrorInvalidValue;
   if (T == 0) return cudaSuccess;
   __nv_bfloat16 *wr3 = (__nv_bfloat16 *)scratch;
   const int64_t n4 = (int64_t)E * H / 4;
@@ -807,6 +809,7 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
   for (int h = 0; h < 5; ++h) m.b_sh[h] = m.b[h];
   TcParams p = {};
   p.T = T; p.H = H; p.E = E;
+  p.rt_splits = splits;
   const int etiles = (int)ceil_div(E, 128), sms = device_sms();
   const int want = std::max<int>((int)ceil_div(T, RT_NMAX), std::min<int>(sms / etiles, (int)ceil_div(T, 16)));
   p.rt_rpt = (int)round_up(ceil_div(T, want), 16);

@@ -66,9 +66,11 @@ cudaError_t launch_ffn_simt(const FfnArgs &a, void *scratch, cudaStream_t stream
 
 // ---- gemm_tc.cu (bf16 tensor-core path) ----
 size_t router_tc_scratch_bytes(int E, int H);
-// Router logits via the exact three-way bf16 split of w_router (scratch: router_tc_scratch_bytes).
+// Router logits via the exact three-way bf16 split of w_router (splits = 3), or
+// with the weight rounded once to bf16 (splits = 1, the BF16-router ablation)
+// (scratch: router_tc_scratch_bytes).
 cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const float *wr, const float *bias,
-                                    float *logits, void *scratch, int *status, cudaStream_t stream);
+                                    float *logits, void *scratch, int *status, cudaStream_t stream, int splits = 3);
 size_t ffn_tc_scratch_bytes(int T, int k, int E, int H, int I, int Is);
 // gate_up + SwiGLU and down as two persistent tcgen05 grouped GEMMs (scratch: ffn_tc_scratch_bytes).
 cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStream_t stream);
