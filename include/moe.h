@@ -22,6 +22,7 @@
  *   moe_combine      ordered FP32 sum of the k weighted rows, plus the gated
  *                    shared row, one rounding to the output type
  *   moe_backward     all gradients, reduced in fixed orders
+ *   moe_backward_ep  one rank's part of moe_backward under an expert partition
  *   moe_forward      the four forward calls in sequence, intermediates in the
  *                    caller's workspace
  *
@@ -382,6 +383,45 @@ typedef struct moe_bwd_args {
  * MOE_ERR_WORKSPACE for a short workspace; nothing is launched then.
  */
 int moe_backward(const moe_dims_t *d, const moe_bwd_args_t *a, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_backward_ep -- moe_backward for one rank of an expert partition, in two
+ * phases around the exchange of the routed input gradients.  RL-Kernel PR
+ * #557 "What" (experts split into contiguous ranges, one all_gather of the
+ * rows, the reductions local and in ascending expert order) and #503 commit
+ * message "Backward" (per-expert GEMMs write per-route input gradients into
+ * one dense buffer, which dx sums).
+ *
+ *   phase 1  the combine backward (route-weight and gate gradients), the
+ *            shared expert's gradients, the router and gate weight gradients
+ *            (all replicated: every rank computes them in full), and for the
+ *            rank's experts [e_begin, e_end) their weight gradients and the
+ *            routed input gradients of their rows;
+ *   phase 2  dx, from all rows of dxr_sorted;
+ *   phase 3  both (with a single rank, [0, E), this is moe_backward).
+ * Between phase 1 and phase 2 the caller exchanges the row blocks of
+ * dxr_sorted (a byte copy); phase 2 must get the same d, a, workspace and
+ * range as phase 1 (the workspace carries the shared expert's input gradient
+ * and, when a->dlogit / a->dz are NULL, those gradients, from one to the
+ * other).
+ *
+ *   a->y_routed     [T*k, H] dtype in SORTED order (route r at row route_pos[r]),
+ *                   the layout of moe_grouped_ffn_ep after the row exchange
+ *   a->saved.gu, a->saved.h  sorted order as moe_grouped_ffn writes them; only
+ *                   the rows of the rank's experts are read
+ *   a->w_gate_up, a->w_down, a->dw_gate_up, a->dw_down  the rank's experts
+ *                   only (expert e at index e - e_begin); NULL if the range is
+ *                   empty
+ *   dxr_sorted      [T*k, H] float, sorted order: phase 1 writes rows
+ *                   expert_offsets[e_begin] .. expert_offsets[e_end] - 1 (one
+ *                   contiguous block per rank); phase 2 reads every row
+ * Every value equals the single-call moe_backward's bit for bit: the same
+ * kernels with the same reduction orders run on the same rows.  Errors as
+ * moe_backward; a bad range or phase is MOE_ERR_INVALID_ARG.  Workspace:
+ * BACKWARD.
+ */
+int moe_backward_ep(const moe_dims_t *d, int32_t e_begin, int32_t e_end, int32_t phase, const moe_bwd_args_t *a,
+                    float *dxr_sorted, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * moe_device_status -- read (and, if `reset`, clear) the device status word

@@ -161,3 +161,16 @@ def oracle_bwd_rows(x_rows, ids_rows, w_rows, sig_rows, dy_rows, W: dict):
         for i in range(4):
             out[i].append(r[i])
     return tuple(np.concatenate(o) for o in out)
+
+
+def small_layer(T, H, E, k, I_, Is, seed=11):
+    """A small bf16 layer of the given shape (same recipe as the workloads)."""
+    s = seed
+    return {"x": I.normal((T, H), s, 0, 1.0, torch.bfloat16),
+            "w_router": I.normal((E, H), s, 1, 0.02, torch.float32),
+            "w_shared_gate": I.normal((H,), s, 2, 0.02, torch.bfloat16),
+            "w_gate_up": I.normal((E, 2 * I_, H), s, 4, 0.02, torch.bfloat16),
+            "w_down": I.normal((E, H, I_), s, 5, 0.02, torch.bfloat16),
+            "ws_gate_up": I.normal((2 * Is, H), s, 6, 0.02, torch.bfloat16),
+            "ws_down": I.normal((H, Is), s, 7, 0.02, torch.bfloat16),
+            "dy": I.normal((T, H), s + 1, 8, 1.0, torch.bfloat16)}

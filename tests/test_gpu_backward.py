@@ -17,7 +17,8 @@ import top_routed_grouped_gb300 as moe
 from top_routed_grouped_gb300 import build
 from top_routed_grouped_gb300 import inputs as I
 
-from _util import (assert_grad_close, bits, full_dy, full_weights, full_x, oracle_bwd_rows, oracle_routes, to_dev)
+from _util import (assert_grad_close, bits, full_dy, full_weights, full_x, oracle_bwd_rows, oracle_routes, small_layer,
+                   to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -215,19 +216,6 @@ def test_bf16_skewed_routing_t4096():
         assert_grad_close(g["dw_gate_up"][e:e + 1], dwgu, f"dw_gate_up[{e}] ({loads[e]} routes)")
         assert_grad_close(g["dw_down"][e:e + 1], dwdn, f"dw_down[{e}]")
     assert moe.moe_device_status(reset=True) == 0
-
-
-def small_layer(T, H, E, k, I_, Is, seed=11):
-    """A small bf16 layer of the given shape (same recipe as the workloads)."""
-    s = seed
-    return {"x": I.normal((T, H), s, 0, 1.0, torch.bfloat16),
-            "w_router": I.normal((E, H), s, 1, 0.02, torch.float32),
-            "w_shared_gate": I.normal((H,), s, 2, 0.02, torch.bfloat16),
-            "w_gate_up": I.normal((E, 2 * I_, H), s, 4, 0.02, torch.bfloat16),
-            "w_down": I.normal((E, H, I_), s, 5, 0.02, torch.bfloat16),
-            "ws_gate_up": I.normal((2 * Is, H), s, 6, 0.02, torch.bfloat16),
-            "ws_down": I.normal((H, Is), s, 7, 0.02, torch.bfloat16),
-            "dy": I.normal((T, H), s + 1, 8, 1.0, torch.bfloat16)}
 
 
 @pytest.mark.parametrize("shape", [(600, 256, 4, 2, 256, 512), (77, 256, 16, 4, 128, 384)],

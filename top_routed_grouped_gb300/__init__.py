@@ -25,7 +25,8 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
           -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE"}
 EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_permute", "moe_grouped_ffn",
             "moe_combine", "moe_forward", "moe_backward", "moe_device_status", "moe_permute_noalloc",
-            "moe_route_replay", "moe_grouped_ffn_ep", "moe_combine_sorted", "moe_router_logits")
+            "moe_route_replay", "moe_grouped_ffn_ep", "moe_combine_sorted", "moe_router_logits",
+            "moe_backward_ep")
 
 _vp = ctypes.c_void_p
 
@@ -91,6 +92,8 @@ def lib() -> ctypes.CDLL:
                 "moe_combine_sorted": ([D] + [_vp] * 6 + [_vp], ctypes.c_int),
                 "moe_forward": ([D, ctypes.POINTER(FwdArgs), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_backward": ([D, ctypes.POINTER(BwdArgs), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
+                "moe_backward_ep": ([D, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(BwdArgs), _vp,
+                                     _vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_device_status": ([ctypes.c_int, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
                 "moe_permute_noalloc": ([D] + [_vp] * 4 + [_vp], ctypes.c_int),
             }
@@ -229,14 +232,28 @@ def moe_forward(d, args: dict, ws, stream=None):
                                             0 if ws is None else ws.numel(), _stream(stream)))
 
 
-def moe_backward(d, args: dict, ws, stream=None):
+def _bwd_args(args: dict):
     ba = BwdArgs()
     for name, _ in BwdArgs._fields_:
         if name != "saved":
             setattr(ba, name, _p(args.get(name)))
     ba.saved = _saved(args.get("saved"))
+    return ba
+
+
+def moe_backward(d, args: dict, ws, stream=None):
+    ba = _bwd_args(args)
     _check("moe_backward", lib().moe_backward(ctypes.byref(d), ctypes.byref(ba), _p(ws),
                                               0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def moe_backward_ep(d, e_begin, e_end, phase, args: dict, dxr_sorted, ws, stream=None):
+    """One rank's part of the expert-partitioned backward (see moe.h): phase 1
+    up to the rank's routed input-gradient rows, phase 2 dx, 3 both."""
+    ba = _bwd_args(args)
+    _check("moe_backward_ep", lib().moe_backward_ep(
+        ctypes.byref(d), int(e_begin), int(e_end), int(phase), ctypes.byref(ba), _p(dxr_sorted), _p(ws),
+        0 if ws is None else ws.numel(), _stream(stream)))
 
 
 def moe_device_status(reset: bool = True) -> int:

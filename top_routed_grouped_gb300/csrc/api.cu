@@ -403,29 +403,35 @@ MOE_API int moe_forward(const moe_dims_t *d, const moe_fwd_args_t *a, void *ws, 
   return moe_combine(d, yr, ys, w, sig, a->y, stream);
 }
 
-MOE_API int moe_backward(const moe_dims_t *d, const moe_bwd_args_t *a, void *ws, size_t ws_bytes, void *stream) {
+// moe_backward and moe_backward_ep: experts [eb, ee) run their GEMMs, weight
+// arrays hold those experts only; dxr (if not NULL) receives the routed input
+// gradients in sorted order instead of the workspace.
+static int backward_impl(const moe_dims_t *d, const moe_bwd_args_t *a, int eb, int ee, int phase, int yr_sorted,
+                         float *dxr, void *ws, size_t ws_bytes, void *stream) {
   int st = check_dims(d);
   if (st != MOE_OK) return st;
-  if (!a || !opt_ok(ws)) return MOE_ERR_INVALID_ARG;
-  const int64_t T = d->T, R = T * d->k, H = d->H, E = d->E, I = d->I, Is = d->Is;
+  if (!a || !opt_ok(ws) || !opt_ok(dxr)) return MOE_ERR_INVALID_ARG;
+  const int64_t T = d->T, R = T * d->k, H = d->H, E = d->E, I = d->I, Is = d->Is, nl = ee - eb;
   if (!buf_ok(a->x, T * H) || !buf_ok(a->w_router, E * H) || !buf_ok(a->w_shared_gate, H) ||
-      !buf_ok(a->w_gate_up, 1) || !buf_ok(a->w_down, 1) || !buf_ok(a->ws_gate_up, 1) || !buf_ok(a->ws_down, 1) ||
+      !buf_ok(a->w_gate_up, nl) || !buf_ok(a->w_down, nl) || !buf_ok(a->ws_gate_up, 1) || !buf_ok(a->ws_down, 1) ||
       !buf_ok(a->topk_ids, R) || !buf_ok(a->topk_w, R) || !buf_ok(a->shared_sig, T) ||
       !buf_ok(a->expert_offsets, 1) || !buf_ok(a->sorted_route, R) || !buf_ok(a->route_pos, R) ||
       !buf_ok(a->y_routed, R * H) || !buf_ok(a->y_shared, T * H) || !buf_ok(a->saved.gu, R * 2 * I) ||
       !buf_ok(a->saved.h, R * I) || !buf_ok(a->saved.gu_shared, T * 2 * Is) || !buf_ok(a->saved.h_shared, T * Is) ||
-      !buf_ok(a->dy, T * H) || !buf_ok(a->dx, T * H) || !buf_ok(a->dw_gate_up, 1) || !buf_ok(a->dw_down, 1) ||
+      !buf_ok(a->dy, T * H) || !buf_ok(a->dx, T * H) || !buf_ok(a->dw_gate_up, nl) || !buf_ok(a->dw_down, nl) ||
       !buf_ok(a->dw_router, 1) || !buf_ok(a->dw_shared_gate, 1) || !buf_ok(a->dws_gate_up, 1) ||
       !buf_ok(a->dws_down, 1) || !opt_ok(a->dlogit) || !opt_ok(a->dz))
     return MOE_ERR_INVALID_ARG;
   if (ws_bytes < ws_size(d, MOE_OP_BACKWARD)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
   if (T == 0) {  // every weight gradient is an empty sum
+    if (!(phase & BWD_PHASE_EXPERTS)) return MOE_OK;
     const size_t f = sizeof(float);
     const void *bufs[6] = {a->dw_gate_up, a->dw_down, a->dw_router, a->dw_shared_gate, a->dws_gate_up, a->dws_down};
-    const size_t bytes[6] = {(size_t)(E * 2 * I * H) * f, (size_t)(E * H * I) * f, (size_t)(E * H) * f,
+    const size_t bytes[6] = {(size_t)(nl * 2 * I * H) * f, (size_t)(nl * H * I) * f, (size_t)(E * H) * f,
                              (size_t)H * f, (size_t)(2 * Is * H) * f, (size_t)(H * Is) * f};
     for (int i = 0; i < 6; ++i) {
+      if (bytes[i] == 0) continue;
       cudaError_t e = cudaMemsetAsync((void *)bufs[i], 0, bytes[i], s);
       if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
@@ -436,19 +442,40 @@ MOE_API int moe_backward(const moe_dims_t *d, const moe_bwd_args_t *a, void *ws,
   BwArgs b;
   b.T = d->T; b.H = d->H; b.E = d->E; b.k = d->k; b.I = d->I; b.Is = d->Is;
   b.x = a->x; b.w_router = a->w_router; b.w_shared_gate = a->w_shared_gate;
-  b.w_gate_up = a->w_gate_up; b.w_down = a->w_down; b.ws_gate_up = a->ws_gate_up; b.ws_down = a->ws_down;
+  // The maps of an empty partition still need a valid address; nothing is read or written through them.
+  b.w_gate_up = nl ? a->w_gate_up : a->ws_gate_up;
+  b.w_down = nl ? a->w_down : a->ws_down;
+  b.ws_gate_up = a->ws_gate_up; b.ws_down = a->ws_down;
   b.topk_ids = a->topk_ids; b.topk_w = a->topk_w; b.shared_sig = a->shared_sig;
   b.offsets = a->expert_offsets; b.sorted_route = a->sorted_route; b.route_pos = a->route_pos;
   b.y_routed = a->y_routed; b.y_shared = a->y_shared;
   b.gu_routed = a->saved.gu; b.gu_shared = a->saved.gu_shared; b.h_routed = a->saved.h; b.h_shared = a->saved.h_shared;
   b.dy = a->dy; b.dx = a->dx;
-  b.dw_gate_up = a->dw_gate_up; b.dw_down = a->dw_down; b.dw_router = a->dw_router;
+  b.dw_gate_up = nl ? a->dw_gate_up : a->dws_gate_up;
+  b.dw_down = nl ? a->dw_down : a->dws_down;
+  b.dw_router = a->dw_router;
   b.dw_shared_gate = a->dw_shared_gate; b.dws_gate_up = a->dws_gate_up; b.dws_down = a->dws_down;
   b.dyr = sc.dyr; b.dys = sc.dys; b.dgu_routed = sc.dgu_routed; b.dgu_shared = sc.dgu_shared;
-  b.dxr = sc.dxr; b.dxs = sc.dxs; b.x_sorted = sc.x_sorted;
+  b.dxr = dxr ? dxr : sc.dxr;
+  b.dxs = sc.dxs; b.x_sorted = sc.x_sorted;
   b.dlogit = a->dlogit ? a->dlogit : sc.dlogit;
   b.dz = a->dz ? a->dz : sc.dz;
-  return cuda_status(launch_backward(d->dtype, b, sc.inner, device_status_ptr(), s));
+  b.e_begin = eb;
+  b.e_end = ee;
+  b.yr_sorted = yr_sorted;
+  return cuda_status(launch_backward(d->dtype, b, sc.inner, device_status_ptr(), s, phase));
+}
+
+MOE_API int moe_backward(const moe_dims_t *d, const moe_bwd_args_t *a, void *ws, size_t ws_bytes, void *stream) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  return backward_impl(d, a, 0, d->E, BWD_PHASE_ALL, 0, nullptr, ws, ws_bytes, stream);
+}
+
+MOE_API int moe_backward_ep(const moe_dims_t *d, int32_t e_begin, int32_t e_end, int32_t phase,
+                            const moe_bwd_args_t *a, float *dxr_sorted, void *ws, size_t ws_bytes, void *stream) {
+  if (!d || e_begin < 0 || e_end < e_begin || e_end > d->E || phase < 1 || phase > 3) return MOE_ERR_INVALID_ARG;
+  if (!buf_ok(dxr_sorted, (int64_t)d->T * d->k * d->H)) return MOE_ERR_INVALID_ARG;
+  return backward_impl(d, a, e_begin, e_end, phase, 1, dxr_sorted, ws, ws_bytes, stream);
 }
 
 MOE_API int moe_device_status(int reset, int32_t *detail) {

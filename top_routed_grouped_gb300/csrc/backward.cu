@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(256)
 combine_bwd_kernel(int T, int H, int k, const TE *__restrict__ dy, const TE *__restrict__ yr,
                    const TE *__restrict__ ys, const float *__restrict__ w, const float *__restrict__ sig,
                    const int32_t *__restrict__ route_pos, TE *__restrict__ dyr_sorted, TE *__restrict__ dys,
-                   float *__restrict__ dlogit, float *__restrict__ dz) {
+                   float *__restrict__ dlogit, float *__restrict__ dz, int yr_sorted) {
   griddep_launch();
   griddep_wait();
   constexpr int VN = Vec16<TE>::N;
@@ -45,7 +45,7 @@ combine_bwd_kernel(int T, int H, int k, const TE *__restrict__ dy, const TE *__r
   const TE *dyr = dy + t * H;
   float dws[16];
   for (int s = 0; s < k; ++s) {
-    const TE *row = yr + (t * k + s) * H;
+    const TE *row = yr + (yr_sorted ? (int64_t)route_pos[t * k + s] : t * k + s) * H;
     float part = 0.f;
     for (int h = lane * VN; h < H; h += 32 * VN) {
       float a[VN], b[VN];
@@ -144,7 +144,7 @@ down_dgrad_swiglu_kernel(BwArgs a, const int32_t *__restrict__ tile_start) {
     const int Iseg = sh ? a.Is : a.I;
     if (i0 >= Iseg) continue;
     const TE *dyrow = sh ? (const TE *)a.dys : (const TE *)a.dyr;
-    const TE *wdn = sh ? (const TE *)a.ws_down : (const TE *)a.w_down + (int64_t)tr.seg * a.H * a.I;
+    const TE *wdn = sh ? (const TE *)a.ws_down : (const TE *)a.w_down + (int64_t)(tr.seg - a.e_begin) * a.H * a.I;
     float acc[2][4] = {};
     for (int h0 = 0; h0 < a.H; h0 += 32) {
       for (int idx = threadIdx.x; idx < BW_BM * 32; idx += 256) {
@@ -207,7 +207,8 @@ gate_up_dgrad_kernel(BwArgs a, const int32_t *__restrict__ tile_start) {
     const bool sh = tr.seg == a.E;
     const int Iseg = sh ? a.Is : a.I;
     const TE *dgu = sh ? (const TE *)a.dgu_shared : (const TE *)a.dgu_routed;
-    const TE *wgu = sh ? (const TE *)a.ws_gate_up : (const TE *)a.w_gate_up + (int64_t)tr.seg * 2 * a.I * a.H;
+    const TE *wgu =
+        sh ? (const TE *)a.ws_gate_up : (const TE *)a.w_gate_up + (int64_t)(tr.seg - a.e_begin) * 2 * a.I * a.H;
     float acc[2][4] = {};
     for (int f0 = 0; f0 < 2 * Iseg; f0 += 32) {
       for (int idx = threadIdx.x; idx < BW_BM * 32; idx += 256) {
@@ -260,7 +261,9 @@ __global__ void __launch_bounds__(256) wgrad_kernel(BwArgs a) {
   griddep_wait();
   __shared__ float as[16][65];  // [row][m]
   __shared__ float bs[16][65];  // [row][n]
-  const int seg = blockIdx.z;
+  // blockIdx.z: the partition's experts in order, then the shared expert
+  const int n_local = (a.e_end < 0 ? a.E : a.e_end) - a.e_begin;
+  const int seg = (int)blockIdx.z < n_local ? a.e_begin + (int)blockIdx.z : a.E;
   const bool sh = seg == a.E;
   const int Iseg = sh ? a.Is : a.I;
   const int M = KIND == WG_DOWN ? a.H : 2 * Iseg;
@@ -307,8 +310,9 @@ __global__ void __launch_bounds__(256) wgrad_kernel(BwArgs a) {
     }
     __syncthreads();
   }
-  float *out = KIND == WG_DOWN ? (sh ? a.dws_down : a.dw_down + (int64_t)seg * a.H * a.I)
-                               : (sh ? a.dws_gate_up : a.dw_gate_up + (int64_t)seg * 2 * a.I * a.H);
+  const int64_t le = seg - a.e_begin;  // index in the partition's weight arrays
+  float *out = KIND == WG_DOWN ? (sh ? a.dws_down : a.dw_down + le * a.H * a.I)
+                               : (sh ? a.dws_gate_up : a.dw_gate_up + le * 2 * a.I * a.H);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -530,47 +534,53 @@ size_t backward_scratch_bytes(int dtype, int T, int k, int E, int H, int I, int 
 }
 
 template <typename TE>
-static cudaError_t run_backward(const BwArgs &a, void *scratch, int *status, cudaStream_t stream) {
+static cudaError_t run_backward(const BwArgs &a, void *scratch, int *status, cudaStream_t stream, int phase) {
   const int64_t R = (int64_t)a.T * a.k;
+  const int eb = a.e_begin, ee = a.e_end < 0 ? a.E : a.e_end;
   cudaError_t err;
 #define MOE_TRY(x) \
   if ((err = (x)) != cudaSuccess) return err
-  MOE_TRY(launch_pdl(combine_bwd_kernel<TE>, dim3((unsigned)ceil_div(a.T, 8)), dim3(256), 0, stream, a.T, a.H, a.k,
-                     (const TE *)a.dy, (const TE *)a.y_routed, (const TE *)a.y_shared, a.topk_w, a.shared_sig,
-                     a.route_pos, (TE *)a.dyr, (TE *)a.dys, a.dlogit, a.dz));
-  const int Imax = a.I > a.Is ? a.I : a.Is;
-  if (sizeof(TE) == 2 && backward_tc_supported(a.H, a.I, a.Is)) {
-    MOE_TRY(launch_dgrad_tc(a, scratch, status, stream));
-    MOE_TRY(launch_wgrad_tc(a, status, stream));
-  } else {
-    int32_t *tile_start = (int32_t *)scratch;
-    const int32_t *ts = tile_start;
-    MOE_TRY(launch_build_tiles(a.E, a.T, BW_BM, a.offsets, tile_start, stream));
-    const int64_t max_tiles = ceil_div(R + a.T, BW_BM) + a.E + 1;
-    const unsigned gx = (unsigned)(max_tiles < 65535 ? max_tiles : 65535);
-    MOE_TRY(launch_pdl(down_dgrad_swiglu_kernel<TE>, dim3(gx, (unsigned)ceil_div(Imax, 64)), dim3(256), 0, stream, a,
-                       ts));
-    MOE_TRY(launch_pdl(gate_up_dgrad_kernel<TE>, dim3(gx, (unsigned)ceil_div(a.H, 64)), dim3(256), 0, stream, a, ts));
-    MOE_TRY(launch_pdl(wgrad_kernel<TE, WG_DOWN>,
-                       dim3((unsigned)ceil_div(Imax, 64), (unsigned)ceil_div(a.H, 64), a.E + 1), dim3(256), 0, stream,
-                       a));
-    MOE_TRY(launch_pdl(wgrad_kernel<TE, WG_GATE_UP>,
-                       dim3((unsigned)ceil_div(a.H, 64), (unsigned)ceil_div(2 * Imax, 64), a.E + 1), dim3(256), 0,
-                       stream, a));
+  if (phase & BWD_PHASE_EXPERTS) {
+    MOE_TRY(launch_pdl(combine_bwd_kernel<TE>, dim3((unsigned)ceil_div(a.T, 8)), dim3(256), 0, stream, a.T, a.H, a.k,
+                       (const TE *)a.dy, (const TE *)a.y_routed, (const TE *)a.y_shared, a.topk_w, a.shared_sig,
+                       a.route_pos, (TE *)a.dyr, (TE *)a.dys, a.dlogit, a.dz, a.yr_sorted));
+    const int Imax = a.I > a.Is ? a.I : a.Is;
+    if (sizeof(TE) == 2 && backward_tc_supported(a.H, a.I, a.Is)) {
+      MOE_TRY(launch_dgrad_tc(a, scratch, status, stream));
+      MOE_TRY(launch_wgrad_tc(a, status, stream));
+    } else {
+      int32_t *tile_start = (int32_t *)scratch;
+      const int32_t *ts = tile_start;
+      MOE_TRY(launch_build_tiles(a.E, a.T, BW_BM, a.offsets, tile_start, stream, eb, ee, 1));
+      const int64_t max_tiles = ceil_div(R + a.T, BW_BM) + a.E + 1;
+      const unsigned gx = (unsigned)(max_tiles < 65535 ? max_tiles : 65535);
+      const unsigned nseg = (unsigned)(ee - eb + 1);
+      MOE_TRY(launch_pdl(down_dgrad_swiglu_kernel<TE>, dim3(gx, (unsigned)ceil_div(Imax, 64)), dim3(256), 0, stream,
+                         a, ts));
+      MOE_TRY(launch_pdl(gate_up_dgrad_kernel<TE>, dim3(gx, (unsigned)ceil_div(a.H, 64)), dim3(256), 0, stream, a,
+                         ts));
+      MOE_TRY(launch_pdl(wgrad_kernel<TE, WG_DOWN>, dim3((unsigned)ceil_div(Imax, 64), (unsigned)ceil_div(a.H, 64), nseg),
+                         dim3(256), 0, stream, a));
+      MOE_TRY(launch_pdl(wgrad_kernel<TE, WG_GATE_UP>,
+                         dim3((unsigned)ceil_div(a.H, 64), (unsigned)ceil_div(2 * Imax, 64), nseg), dim3(256), 0,
+                         stream, a));
+    }
+    const int dtype = sizeof(TE) == 4 ? 0 : 1;
+    uint8_t *rest =
+        (uint8_t *)scratch + round_up((int64_t)gemm_scratch_bytes(dtype, a.T, a.k, a.E, a.H, a.I, a.Is), 256);
+    int32_t *chunk_start = (int32_t *)rest;
+    const int32_t *cs = chunk_start;
+    float *partial = (float *)(rest + round_up((int64_t)(a.E + 2) * 4, 256));
+    const float *pc = partial;
+    MOE_TRY(launch_build_tiles(a.E, a.T, RG_CHUNK, a.offsets, chunk_start, stream));
+    const int64_t mc = max_chunks(a.T, a.k, a.E);
+    MOE_TRY(launch_pdl(router_gate_partial_kernel<TE>,
+                       dim3((unsigned)std::min<int64_t>(mc, 65535), (unsigned)ceil_div(a.H, 256)), dim3(256), 0,
+                       stream, a, cs, partial));
+    MOE_TRY(launch_pdl(router_gate_reduce_kernel, dim3((unsigned)ceil_div(a.H, 256), a.E + 1), dim3(256), 0, stream,
+                       a, cs, pc));
   }
-  const int dtype = sizeof(TE) == 4 ? 0 : 1;
-  uint8_t *rest = (uint8_t *)scratch + round_up((int64_t)gemm_scratch_bytes(dtype, a.T, a.k, a.E, a.H, a.I, a.Is), 256);
-  int32_t *chunk_start = (int32_t *)rest;
-  const int32_t *cs = chunk_start;
-  float *partial = (float *)(rest + round_up((int64_t)(a.E + 2) * 4, 256));
-  const float *pc = partial;
-  MOE_TRY(launch_build_tiles(a.E, a.T, RG_CHUNK, a.offsets, chunk_start, stream));
-  const int64_t mc = max_chunks(a.T, a.k, a.E);
-  MOE_TRY(launch_pdl(router_gate_partial_kernel<TE>,
-                     dim3((unsigned)std::min<int64_t>(mc, 65535), (unsigned)ceil_div(a.H, 256)), dim3(256), 0, stream,
-                     a, cs, partial));
-  MOE_TRY(launch_pdl(router_gate_reduce_kernel, dim3((unsigned)ceil_div(a.H, 256), a.E + 1), dim3(256), 0, stream, a,
-                     cs, pc));
+  if (!(phase & BWD_PHASE_DX)) return cudaSuccess;
   if (a.H % (32 * Vec16<TE>::N) == 0)
     return launch_pdl(dx_kernel<TE>, dim3((unsigned)ceil_div((int64_t)a.T * (a.H / (32 * Vec16<TE>::N)), 8)),
                       dim3(256), 0, stream, a);
@@ -579,10 +589,10 @@ static cudaError_t run_backward(const BwArgs &a, void *scratch, int *status, cud
 #undef MOE_TRY
 }
 
-cudaError_t launch_backward(int dtype, const BwArgs &a, void *scratch, int *status, cudaStream_t stream) {
+cudaError_t launch_backward(int dtype, const BwArgs &a, void *scratch, int *status, cudaStream_t stream, int phase) {
   if (a.T == 0) return cudaSuccess;
-  if (dtype == 0) return run_backward<float>(a, scratch, status, stream);
-  return run_backward<__nv_bfloat16>(a, scratch, status, stream);
+  if (dtype == 0) return run_backward<float>(a, scratch, status, stream, phase);
+  return run_backward<__nv_bfloat16>(a, scratch, status, stream, phase);
 }
 
 }  // namespace moe

@@ -85,6 +85,7 @@ struct DgMaps {
 
 struct DgParams {
   int T, H, E, k, I, Is;
+  int e0;  // first expert of the weight arrays (expert partition)
   const int32_t *item_start;
   const int4 *items;
   const __nv_bfloat16 *gu_routed, *gu_shared;  // DGRAD_DOWN: saved [g | u]
@@ -168,7 +169,7 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
         const bool sh = im.seg == p.E;
         const uint32_t bytes = DG_A_BYTES + im.n * 128;
         // first weight row of this expert in the [E * rows, cols] view
-        const int wrow = sh ? 0 : im.seg * (MODE == DGRAD_DOWN ? p.H : 2 * p.I);
+        const int wrow = sh ? 0 : (im.seg - p.e0) * (MODE == DGRAD_DOWN ? p.H : 2 * p.I);
         for (int kb = 0; kb < im.nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], bytes);
@@ -349,7 +350,8 @@ struct WgParams {
   int T, H, E, k, I, Is;
   const int32_t *offsets;
   int tm_r, tn_r, tm_s, tn_s;  // output tiles per segment (M x N), routed and shared
-  int total;                   // tm_s * tn_s + E * tm_r * tn_r
+  int e0;                      // first expert of the partition (its weight gradients start at index 0)
+  int total;                   // tm_s * tn_s + (experts of the partition) * tm_r * tn_r
   int *status;
 };
 
@@ -373,7 +375,7 @@ __device__ inline WgItem wg_item(int it, const WgParams &p) {
     r.rows = p.T;
   } else {
     const int per = p.tm_r * p.tn_r;
-    r.seg = (it - n_sh) / per;
+    r.seg = p.e0 + (it - n_sh) / per;
     local = (it - n_sh) % per;
     r.mt = local / p.tn_r;
     r.nt = local % p.tn_r;
@@ -525,7 +527,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
       const WgItem im = wg_item(it, p);
       const bool sh = im.seg == p.E;
       const CUtensorMap *om = sh ? &maps.out_sh : &maps.out;
-      const int mrow = (sh ? 0 : im.seg * Mr) + im.mt * 128 + q * 32;
+      const int mrow = (sh ? 0 : (im.seg - p.e0) * Mr) + im.mt * 128 + q * 32;
       const int ncol = im.nt * 256 + half * WG_COLS;
       if (im.rows == 0) {
         if (lane == 0) {
@@ -573,14 +575,15 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
 }
 
 // x rows in sorted (expert-segment) order: xs[j] = x[sorted_route[j] / k], one
-// warp per row, 16 bytes per lane.
-__global__ void __launch_bounds__(256) gather_sorted_rows_kernel(int64_t R, int H, int k, const int32_t *sorted_route,
-                                                                 const __nv_bfloat16 *x, __nv_bfloat16 *xs) {
+// warp per row, 16 bytes per lane; only the rows of experts [e_begin, e_end).
+__global__ void __launch_bounds__(256)
+gather_sorted_rows_kernel(int64_t R, int H, int k, const int32_t *sorted_route, const int32_t *offsets, int e_begin,
+                          int e_end, const __nv_bfloat16 *x, __nv_bfloat16 *xs) {
   griddep_launch();
   griddep_wait();
   const int64_t j = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (j >= R) return;
+  if (j >= R || j < __ldg(offsets + e_begin) || j >= __ldg(offsets + e_end)) return;
   const uint4 *src = (const uint4 *)(x + (int64_t)(__ldg(sorted_route + j) / k) * H);
   uint4 *dst = (uint4 *)(xs + j * H);
   for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
@@ -615,20 +618,23 @@ cudaError_t launch_dgrad_tc(const BwArgs &a, void *scratch, int *status, cudaStr
   int32_t *start_gu = (int32_t *)(w + starts);
   int4 *items_dn = (int4 *)(w + 2 * starts);
   int4 *items_gu = (int4 *)(w + 2 * starts + round_up((int64_t)mi_dn * 16, 256));
+  const int eb = a.e_begin, ee = a.e_end < 0 ? a.E : a.e_end;
+  const int64_t nl = std::max(ee - eb, 1);  // expert rows of the weight maps (one when the partition is empty)
   cudaError_t e = launch_item_tables(a.E, a.T, a.I / 128, a.Is / 128, a.H / 256, a.H / 256, a.offsets, start_dn,
-                                     start_gu, items_dn, items_gu, mi_dn, mi_gu, stream);
+                                     start_gu, items_dn, items_gu, mi_dn, mi_gu, stream, eb, ee, 1);
   if (e != cudaSuccess) return e;
   const int64_t R = (int64_t)a.T * a.k;
   DgMaps md, mg;
-  if (!map_col_blocks(&md.a, a.w_down, (int64_t)a.E * a.H, a.I, 64, 2) ||
+  if (!map_col_blocks(&md.a, a.w_down, nl * a.H, a.I, 64, 2) ||
       !map_col_blocks(&md.a_sh, a.ws_down, a.H, a.Is, 64, 2) || !map_rows(md.b, a.dyr, R, a.H) ||
       !map_rows(md.b_sh, a.dys, a.T, a.H) ||
-      !map_col_blocks(&mg.a, a.w_gate_up, (int64_t)a.E * 2 * a.I, a.H, 64, 4) ||
+      !map_col_blocks(&mg.a, a.w_gate_up, nl * 2 * a.I, a.H, 64, 4) ||
       !map_col_blocks(&mg.a_sh, a.ws_gate_up, 2 * (int64_t)a.Is, a.H, 64, 4) ||
       !map_rows(mg.b, a.dgu_routed, R, 2 * (int64_t)a.I) || !map_rows(mg.b_sh, a.dgu_shared, a.T, 2 * (int64_t)a.Is))
     return cudaErrorInvalidValue;
   DgParams p = {};
   p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k; p.I = a.I; p.Is = a.Is;
+  p.e0 = eb;
   p.gu_routed = (const __nv_bfloat16 *)a.gu_routed;
   p.gu_shared = (const __nv_bfloat16 *)a.gu_shared;
   p.dgu_routed = (__nv_bfloat16 *)a.dgu_routed;
@@ -661,30 +667,34 @@ static cudaError_t launch_wgrad(const WgMaps &m, const WgParams &p, cudaStream_t
 
 cudaError_t launch_wgrad_tc(const BwArgs &a, int *status, cudaStream_t stream) {
   const int64_t R = (int64_t)a.T * a.k;
+  const int eb = a.e_begin, ee = a.e_end < 0 ? a.E : a.e_end;
+  const int64_t nl = std::max(ee - eb, 1);  // expert rows of the output maps (one when the partition is empty)
   cudaError_t e0 = launch_pdl(gather_sorted_rows_kernel, dim3((unsigned)ceil_div(R, 8)), dim3(256), 0, stream, R, a.H,
-                              a.k, a.sorted_route, (const __nv_bfloat16 *)a.x, (__nv_bfloat16 *)a.x_sorted);
+                              a.k, a.sorted_route, a.offsets, eb, ee, (const __nv_bfloat16 *)a.x,
+                              (__nv_bfloat16 *)a.x_sorted);
   if (e0 != cudaSuccess) return e0;
   WgMaps md, mg;
   if (!wg_maps(md.a, a.dyr, R, a.H, 2) || !wg_maps(md.a_sh, a.dys, a.T, a.H, 2) ||
       !wg_maps(md.b, a.h_routed, R, a.I, 4) || !wg_maps(md.b_sh, a.h_shared, a.T, a.Is, 4) ||
-      !map_f32_tile(&md.out, a.dw_down, (int64_t)a.E * a.H, a.I) || !map_f32_tile(&md.out_sh, a.dws_down, a.H, a.Is) ||
+      !map_f32_tile(&md.out, a.dw_down, nl * a.H, a.I) || !map_f32_tile(&md.out_sh, a.dws_down, a.H, a.Is) ||
       !wg_maps(mg.a, a.dgu_routed, R, 2 * (int64_t)a.I, 2) || !wg_maps(mg.a_sh, a.dgu_shared, a.T, 2 * (int64_t)a.Is, 2) ||
       !wg_maps(mg.b, a.x_sorted, R, a.H, 4) || !wg_maps(mg.b_sh, a.x, a.T, a.H, 4) ||
-      !map_f32_tile(&mg.out, a.dw_gate_up, (int64_t)a.E * 2 * a.I, a.H) ||
+      !map_f32_tile(&mg.out, a.dw_gate_up, nl * 2 * a.I, a.H) ||
       !map_f32_tile(&mg.out_sh, a.dws_gate_up, 2 * (int64_t)a.Is, a.H))
     return cudaErrorInvalidValue;
   WgParams p = {};
   p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k; p.I = a.I; p.Is = a.Is;
   p.offsets = a.offsets;
   p.status = status;
+  p.e0 = eb;
   // down: M = H, N = I
   p.tm_r = a.H / 128; p.tn_r = a.I / 256; p.tm_s = a.H / 128; p.tn_s = a.Is / 256;
-  p.total = p.tm_s * p.tn_s + a.E * p.tm_r * p.tn_r;
+  p.total = p.tm_s * p.tn_s + (ee - eb) * p.tm_r * p.tn_r;
   cudaError_t e = launch_wgrad<WGRAD_DOWN>(md, p, stream);
   if (e != cudaSuccess) return e;
   // gate_up: M = 2I, N = H
   p.tm_r = 2 * a.I / 128; p.tn_r = a.H / 256; p.tm_s = 2 * a.Is / 128; p.tn_s = a.H / 256;
-  p.total = p.tm_s * p.tn_s + a.E * p.tm_r * p.tn_r;
+  p.total = p.tm_s * p.tn_s + (ee - eb) * p.tm_r * p.tn_r;
   return launch_wgrad<WGRAD_GATE_UP>(mg, p, stream);
 }
 

@@ -114,11 +114,20 @@ struct BwArgs {
   void *x_sorted;               // [T*k, H] dtype, sorted order: x of the route's token (tensor-core path)
   float *dlogit;                // [T, k]
   float *dz;                    // [T]
+  // Expert partition: only experts [e_begin, e_end) run their dgrad and
+  // wgrad; w_gate_up, w_down, dw_gate_up, dw_down hold those experts only
+  // (expert e at index e - e_begin).  e_end < 0 means E.
+  int e_begin = 0, e_end = -1;
+  int yr_sorted = 0;            // y_routed rows in sorted order (route r at row route_pos[r])
 };
 size_t backward_scratch_bytes(int dtype, int T, int k, int E, int H, int I, int Is);
 // The backward (dtype 0 = float, 1 = bf16): the four expert GEMMs on the
 // tensor cores for bf16 when backward_tc_supported, else on CUDA cores.
-cudaError_t launch_backward(int dtype, const BwArgs &a, void *scratch, int *status, cudaStream_t stream);
+// phase bit 1: everything up to the routed input gradients dxr (own experts'
+// rows only) and the weight gradients; bit 2: dx from all dxr rows.
+enum { BWD_PHASE_EXPERTS = 1, BWD_PHASE_DX = 2, BWD_PHASE_ALL = 3 };
+cudaError_t launch_backward(int dtype, const BwArgs &a, void *scratch, int *status, cudaStream_t stream,
+                            int phase = BWD_PHASE_ALL);
 
 // ---- grad_tc.cu (bf16 tensor-core backward GEMMs) ----
 bool backward_tc_supported(int H, int I, int Is);
