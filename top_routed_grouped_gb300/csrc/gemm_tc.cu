@@ -39,6 +39,8 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdlib>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -160,6 +162,70 @@ __device__ inline bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *a
   int ok = 0;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status) ? 1 : 0;
   return __shfl_sync(FULL_MASK, ok, 0) != 0;
+}
+
+// Gate_up epilogue of one 32-column chunk (columns c0..c0+31 = rows of the
+// item) of one M tile: v holds this lane's 32 accumulator values; the warp's
+// 32 TMEM lanes are 16 gate rows then the 16 up rows of features fcol..+15.
+// Writes h (and, if guout, the [g | u] rows) through the warp's staging
+// buffer `stg` (2560 bytes).
+__device__ __forceinline__ void gate_up_epi_chunk(const float (&v)[32], int fcol, int c0, const Item &im, int Iseg,
+                                                  __nv_bfloat16 *hout, __nv_bfloat16 *guout, uint8_t *stg, int lane) {
+  // The h and the g/u staging share the warp's buffer, one after the other.
+  uint32_t *stg_h = (uint32_t *)stg;              // [32 cols][12 words] (8 used: 16 bf16)
+  __nv_bfloat16 *stg_gu = (__nv_bfloat16 *)stg;  // [32 cols][40] (32 used)
+  const int fl = lane & 15;
+  const int cbase = lane < 16 ? 0 : 16;
+  const bool odd = lane & 1;
+  // Lane i < 16 holds gate g of feature i, lane i + 16 the up value u of
+  // the same feature, for columns c0..c0+31.  One exchange gives lane i
+  // the u of columns 0-15 and lane i + 16 the g of columns 16-31, so
+  // both halves compute h for 16 columns each.
+  float hv[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float send = lane < 16 ? v[16 + j] : v[j];
+    const float recv = __shfl_xor_sync(FULL_MASK, send, 16);
+    const float g = lane < 16 ? v[j] : recv;
+    const float u = lane < 16 ? recv : v[16 + j];
+    hv[j] = __fdividef(g, 1.0f + __expf(-g)) * u;
+  }
+  // Pack features (2m, 2m+1) of a column into one bf16x2 word: for the
+  // column pair (j, j+1) the even lane writes column j, the odd lane
+  // column j+1, after swapping one value with its neighbour.
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const float x = __shfl_xor_sync(FULL_MASK, odd ? hv[j] : hv[j + 1], 1);
+    const __nv_bfloat162 w2 = odd ? __floats2bfloat162_rn(x, hv[j + 1]) : __floats2bfloat162_rn(hv[j], x);
+    stg_h[(cbase + j + (odd ? 1 : 0)) * 12 + (fl >> 1)] = *reinterpret_cast<const uint32_t *>(&w2);
+  }
+  __syncwarp();
+  // Two lanes per column row: 16 rows x 32 contiguous bytes per store instruction.
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = (lane >> 1) + 16 * i, cc = lane & 1;
+    if (c0 + r < im.rows) {
+      const int64_t row = im.row0 + c0 + r;
+      *(uint4 *)(hout + row * Iseg + fcol + cc * 8) = *(const uint4 *)(stg_h + r * 12 + cc * 4);
+    }
+  }
+  __syncwarp();
+  if (guout) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) stg_gu[j * 40 + lane] = __float2bfloat16_rn(v[j]);
+    __syncwarp();
+    if (c0 + lane < im.rows) {
+      const int64_t row = im.row0 + c0 + lane;
+      const uint4 *sg = (const uint4 *)(stg_gu + lane * 40);
+      uint4 *dg = (uint4 *)(guout + row * 2 * Iseg + fcol);
+      uint4 *du = (uint4 *)(guout + row * 2 * Iseg + Iseg + fcol);
+      dg[0] = sg[0];
+      dg[1] = sg[1];
+      du[0] = sg[2];
+      du[1] = sg[3];
+    }
+    __syncwarp();
+  }
 }
 
 template <int MODE>
@@ -322,70 +388,13 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const int Iseg = sh ? p.Is : p.I;
         __nv_bfloat16 *hout = sh ? p.h_shared : p.h_routed;
         __nv_bfloat16 *guout = sh ? p.gu_shared : p.gu_routed;
-        // The h and the g/u staging share the warp's buffer, one after the other.
-        uint32_t *stg_h = (uint32_t *)stg;              // [32 cols][12 words] (8 used: 16 bf16)
-        __nv_bfloat16 *stg_gu = (__nv_bfloat16 *)stg;  // [32 cols][40] (32 used)
-        const int fl = lane & 15;
-        const int cbase = lane < 16 ? 0 : 16;
-        const bool odd = lane & 1;
         for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
           float vt[MT][32];
           if (MT == 2) tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[MT - 1]);
           else tmem_ld32(tq + c0, vt[0]);
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const float(&v)[32] = vt[mt];
-            const int fcol = (im.f * MT + mt) * 64 + 16 * q;  // first feature of this warp's 16
-            // Lane i < 16 holds gate g of feature i, lane i + 16 the up value u of
-            // the same feature, for columns c0..c0+31.  One exchange gives lane i
-            // the u of columns 0-15 and lane i + 16 the g of columns 16-31, so
-            // both halves compute h for 16 columns each.
-            float hv[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float send = lane < 16 ? v[16 + j] : v[j];
-              const float recv = __shfl_xor_sync(FULL_MASK, send, 16);
-              const float g = lane < 16 ? v[j] : recv;
-              const float u = lane < 16 ? recv : v[16 + j];
-              hv[j] = __fdividef(g, 1.0f + __expf(-g)) * u;
-            }
-            // Pack features (2m, 2m+1) of a column into one bf16x2 word: for the
-            // column pair (j, j+1) the even lane writes column j, the odd lane
-            // column j+1, after swapping one value with its neighbour.
-#pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-              const float x = __shfl_xor_sync(FULL_MASK, odd ? hv[j] : hv[j + 1], 1);
-              const __nv_bfloat162 w2 = odd ? __floats2bfloat162_rn(x, hv[j + 1]) : __floats2bfloat162_rn(hv[j], x);
-              stg_h[(cbase + j + (odd ? 1 : 0)) * 12 + (fl >> 1)] = *reinterpret_cast<const uint32_t *>(&w2);
-            }
-            __syncwarp();
-            // Two lanes per column row: 16 rows x 32 contiguous bytes per store instruction.
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int r = (lane >> 1) + 16 * i, cc = lane & 1;
-              if (c0 + r < im.rows) {
-                const int64_t row = im.row0 + c0 + r;
-                *(uint4 *)(hout + row * Iseg + fcol + cc * 8) = *(const uint4 *)(stg_h + r * 12 + cc * 4);
-              }
-            }
-            __syncwarp();
-            if (guout) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) stg_gu[j * 40 + lane] = __float2bfloat16_rn(v[j]);
-              __syncwarp();
-              if (c0 + lane < im.rows) {
-                const int64_t row = im.row0 + c0 + lane;
-                const uint4 *sg = (const uint4 *)(stg_gu + lane * 40);
-                uint4 *dg = (uint4 *)(guout + row * 2 * Iseg + fcol);
-                uint4 *du = (uint4 *)(guout + row * 2 * Iseg + Iseg + fcol);
-                dg[0] = sg[0];
-                dg[1] = sg[1];
-                du[0] = sg[2];
-                du[1] = sg[3];
-              }
-              __syncwarp();
-            }
-          }
+          for (int mt = 0; mt < MT; ++mt)
+            gate_up_epi_chunk(vt[mt], (im.f * MT + mt) * 64 + 16 * q, c0, im, Iseg, hout, guout, stg, lane);
         }
       } else {
         const bool sh = im.seg == p.E;
@@ -469,6 +478,246 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, TC_TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// gate_up + SwiGLU on CTA pairs (cta_group::2).
+//
+// The item is the same as tc_gemm_kernel<TC_GATE_UP>'s: 128 features (two M
+// tiles of 64 gate + 64 up rows) x up to 256 rows of one segment.  The two
+// CTAs of a cluster run it as one M = 256 MMA: CTA r holds M tile 2f + r of
+// the weights and gathers rows [r n/2, (r + 1) n/2) of the item's x rows, so
+// each gathered row is fetched once per item and each CTA's accumulator is
+// 128 lanes x n columns.  That leaves room for two accumulator buffers, so
+// an item's epilogue overlaps the next item's mainloop.  A stage holds
+// PR_KSUB K blocks of 64: per block 16 KB of weights + 16 KB of rows per CTA
+// (fewer, larger stages: one handshake per 128 K for the single MMA thread
+// that drives both SMs).
+//
+// Synchronisation: the even CTA's MMA thread waits on its full[s]: one
+// arrival by the even CTA's producer, which expects the bytes of both CTAs'
+// weight tiles and gathered rows; every copy of both CTAs is a TMA load
+// (weights by tile, rows by gather4) completing on that barrier.  MMA
+// completion is committed to empty[s] / tfull[b] / mma_done in both CTAs at
+// once; the epilogue warps of both CTAs arrive on the even CTA's tempty[b].
+// ---------------------------------------------------------------------------
+constexpr int PR_KSUB = 2;    // K blocks of 64 per stage
+constexpr int PR_STAGES = 3;  // stage ring depth
+constexpr int PR_EPI_WARPS = 8, PR_EPI_BYTES = 2560;
+constexpr int PR_A_BYTES = TC_TILE_A_BYTES, PR_B_BYTES = 128 * 128;  // one K block
+constexpr int PR_STAGE_BYTES = PR_KSUB * (PR_A_BYTES + PR_B_BYTES);
+constexpr int PR_GATHER_FIRST = TC_EPI_FIRST + PR_EPI_WARPS;
+constexpr int PR_THREADS = 32 * (PR_GATHER_FIRST + TC_GATHER_WARPS);
+constexpr int PR_SMEM_BYTES = 1024 + PR_STAGES * PR_STAGE_BYTES + PR_EPI_WARPS * PR_EPI_BYTES + 512;
+static_assert(PR_SMEM_BYTES <= 232448, "pair kernel shared memory");
+
+__global__ void __launch_bounds__(PR_THREADS, 1)
+tc_gate_up_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // Stage s: K block j's weight tile at sa(s, j), its rows at sb(s, j).
+  auto sa = [&](int s, int j) { return base + s * PR_STAGE_BYTES + j * PR_A_BYTES; };
+  auto sb = [&](int s, int j) { return base + s * PR_STAGE_BYTES + PR_KSUB * PR_A_BYTES + j * PR_B_BYTES; };
+  uint8_t *epi = base + PR_STAGES * PR_STAGE_BYTES;
+  uint64_t *bars = (uint64_t *)(epi + PR_EPI_WARPS * PR_EPI_BYTES);
+  uint64_t *full = bars, *empty = full + PR_STAGES;
+  uint64_t *tfull = empty + PR_STAGES, *tempty = tfull + 2, *mma_done = tempty + 2;
+  uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
+  volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PR_STAGES; ++s) {
+      mbar_init(&full[s], 1);  // used in the even CTA
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * PR_EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&maps.a);
+    prefetch_tmap(&maps.a_sh);
+  }
+  cluster_sync();  // both CTAs' barriers exist before either touches the other's
+  if (warp == 1) tmem_alloc_pair(tmem_slot, TC_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_launch();
+  griddep_wait();
+  const int total = __ldg(p.item_start + p.E + 1);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (weights)
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_phase = 0;
+      bool ok = true;
+      for (int it = cid; it < total && ok; it += ncl) {
+        const Item im = decode_item<TC_GATE_UP>(it, p);
+        const bool sh = im.seg == p.E;
+        // 4 groups of 16 features: 16 gate rows then 16 up rows each (this CTA's M tile).
+        const int c3 = (im.f * 2 + (int)rank) * 4, c4 = sh ? 0 : im.seg - p.e0;
+        const CUtensorMap *am = sh ? &maps.a_sh : &maps.a;
+        for (int ks = 0; ks < im.nk / PR_KSUB; ++ks) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (leader) {
+            // Both CTAs' weight tiles and gathered rows (n/2 each) complete on this barrier.
+            mbar_arrive_expect_tx(&full[stage], PR_KSUB * (2 * PR_A_BYTES + (uint32_t)im.n * 128));
+#pragma unroll
+            for (int j = 0; j < PR_KSUB; ++j)
+              tma_load_5d(sa(stage, j), am, &full[stage], (ks * PR_KSUB + j) * 64, 0, 0, c3, c4, pol_w);
+          } else {
+            const uint32_t bar = mapa_shared(&full[stage], 0);
+#pragma unroll
+            for (int j = 0; j < PR_KSUB; ++j)
+              tma_load_5d_pair(sa(stage, j), am, bar, (ks * PR_KSUB + j) * 64, 0, 0, c3, c4, pol_w);
+          }
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == PR_STAGES) stage = 0, phase ^= 1;
+        }
+      }
+      if (!ok && leader) {
+        // The stages in flight (both CTAs' copies complete here) land before the pair exits.
+        volatile int never = 0;
+        for (int s = 0; s < PR_STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1, &never, nullptr, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (leader) {
+        // -------------------------------------------------------- MMA issuer (both CTAs' tensor memory)
+        int stage = 0;
+        uint32_t phase = 0, cnt = 0;
+        bool ok = true;
+        for (int it = cid; it < total && ok; it += ncl) {
+          const Item im = decode_item<TC_GATE_UP>(it, p);
+          const int b = cnt & 1;
+          if (!mbar_wait_cluster(&tempty[b], ((cnt >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+          tc_fence_after();
+          const uint32_t idesc = idesc_bf16_f32(256, im.n);
+          for (int ks = 0; ks < im.nk / PR_KSUB; ++ks) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int j = 0; j < PR_KSUB; ++j) {
+              const uint64_t ad = smem_desc_sw128(smem_u32(sa(stage, j)));
+              const uint64_t bd = smem_desc_sw128(smem_u32(sb(stage, j)));
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)  // K = 16 per MMA: +32 bytes = +2 in the descriptor address field
+                mma_bf16_pair(tmem + b * 256, ad + 2 * kk, bd + 2 * kk, idesc, (ks | j | kk) != 0);
+            }
+            mma_commit_pair(&empty[stage]);
+            if (++stage == PR_STAGES) stage = 0, phase ^= 1;
+          }
+          if (!ok) break;
+          mma_commit_pair(&tfull[b]);
+          ++cnt;
+        }
+        mma_commit_pair(mma_done);
+      }
+      // Every pair MMA has finished (it wrote both CTAs' tensor memory) before TMEM is released.
+      volatile int never = 0;
+      mbar_wait(mma_done, 0, &never, p.status);
+    }
+    __syncwarp();
+  } else if (warp < PR_GATHER_FIRST) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    constexpr int CSTEP = 32 * (PR_EPI_WARPS / 4);
+    const int cfirst = 32 * ((warp - TC_EPI_FIRST) >> 2);
+    uint8_t *stg = epi + (warp - TC_EPI_FIRST) * PR_EPI_BYTES;
+    const uint32_t tempty_leader0 = mapa_shared(&tempty[0], 0);
+    uint32_t cnt = 0;
+    for (int it = cid; it < total; it += ncl) {
+      const Item im = decode_item<TC_GATE_UP>(it, p);
+      const int b = cnt & 1;
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait(&tfull[b], (cnt >> 1) & 1, abort_flag, p.status) ? 1 : 0;
+      if (!__shfl_sync(FULL_MASK, ok, 0)) break;
+      tc_fence_after();
+      const bool sh = im.seg == p.E;
+      const int Iseg = sh ? p.Is : p.I;
+      __nv_bfloat16 *hout = sh ? p.h_shared : p.h_routed;
+      __nv_bfloat16 *guout = sh ? p.gu_shared : p.gu_routed;
+      const uint32_t tq = tmem + b * 256 + ((uint32_t)(q * 32) << 16);
+      const int fcol = (im.f * 2 + (int)rank) * 64 + 16 * q;
+      for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
+        float v[32];
+        tmem_ld32(tq + c0, v);
+        gate_up_epi_chunk(v, fcol, c0, im, Iseg, hout, guout, stg, lane);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tempty[b]);
+        else mbar_arrive_remote(tempty_leader0 + (uint32_t)(b * sizeof(uint64_t)));
+      }
+      ++cnt;
+    }
+  } else {
+    // ------------------------------------------------------------ row gather (TMA gather4)
+    // This CTA's rows of the item: [rank n/2, rank n/2 + n/2) ∩ [0, rows),
+    // row i at line i of a K block's B tile (the 128-byte swizzle), four rows
+    // per copy; quad qd = g + 8 lane (lanes 0-3) of warp g.  The bytes of
+    // both CTAs complete on the even CTA's full[s].  Lines past the item's
+    // rows read token 0: their accumulator columns are never read.
+    const int g = warp - PR_GATHER_FIRST;
+    const uint64_t pol_x = policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int it = cid; it < total && ok; it += ncl) {
+      const Item im = decode_item<TC_GATE_UP>(it, p);
+      const bool sh = im.seg == p.E;
+      const int half = im.n >> 1, hbase = (int)rank * half;
+      const int hrows = max(0, min(half, im.rows - hbase));
+      const int qd = g + 8 * lane;
+      const bool mine = lane < 4 && 4 * qd < half;
+      int t4[4] = {0, 0, 0, 0};
+      if (mine) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = 4 * qd + j;
+          if (r < hrows) {
+            const int64_t row = im.row0 + hbase + r;
+            t4[j] = sh ? (int)row : __ldg(p.sorted_route + row) / p.k;
+          }
+        }
+      }
+      for (int ks = 0; ks < im.nk / PR_KSUB; ++ks) {
+        int w = 0;
+        if (lane == 0) w = mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status) ? 1 : 0;
+        if (!__shfl_sync(FULL_MASK, w, 0)) { ok = false; break; }
+        if (mine) {
+          const uint32_t bar = mapa_shared(&full[stage], 0);
+#pragma unroll
+          for (int j = 0; j < PR_KSUB; ++j)
+            tma_gather4_pair(sb(stage, j) + qd * 512, &maps.b[0], bar, (ks * PR_KSUB + j) * 64, t4[0], t4[1], t4[2],
+                             t4[3], pol_x);
+        }
+        if (++stage == PR_STAGES) stage = 0, phase ^= 1;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no remote arrival, copy or commit targets this CTA any more
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, TC_TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -792,6 +1041,68 @@ static cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cu
   return launch_pdl(tc_gemm_kernel<MODE>, dim3(grid), dim3(tc_threads<MODE>()), TC_SMEM_BYTES, stream, maps, p);
 }
 
+// Clusters of two gate_up pair CTAs that fit on the device at once (0: the
+// pair kernel cannot run here).  Queried once per device.
+static int pair_clusters() {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int sms = device_sms();
+  if (ensure_smem((const void *)tc_gate_up_pair_kernel, PR_SMEM_BYTES) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  int &c = cache[dev & 63];
+  if (c == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * sms);
+    cfg.blockDim = dim3(PR_THREADS);
+    cfg.dynamicSmemBytes = PR_SMEM_BYTES;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void *)tc_gate_up_pair_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    c = n > 0 ? n : -1;
+  }
+  return c > 0 ? c : 0;
+}
+
+static bool use_gate_up_pair() {
+  const char *e = getenv("MOE_GATE_UP_PAIR");
+  if (e && e[0] == '0') return false;
+  return pair_clusters() > 0;
+}
+
+static cudaError_t launch_gate_up_pair(const TcMaps &maps, const TcParams &p, cudaStream_t stream) {
+  const int nc = pair_clusters();
+  if (nc <= 0) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * nc);
+  cfg.blockDim = dim3(PR_THREADS);
+  cfg.dynamicSmemBytes = PR_SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, tc_gate_up_pair_kernel, maps, p);
+}
+
 size_t router_tc_scratch_bytes(int E, int H) { return (size_t)E * 3 * H * 2; }
 
 cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const float *wr, const float *bias,
@@ -897,7 +1208,17 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   const int grid = device_sms();
   p.item_start = start_gu;
   p.items = items_gu;
-  cudaError_t e = launch_tc<TC_GATE_UP>(mg, p, grid, stream);
+  cudaError_t e;
+  if (use_gate_up_pair() && a.H % (64 * PR_KSUB) == 0) {
+    // One M tile (4 groups of 16 features) per CTA of the pair.
+    // x rows for the odd CTA's gather4 copies: a one-row box.
+    if (!map_gate_up(&mg.a, a.w_gate_up, std::max(n_local, 1), a.I, a.H, 4) ||
+        !map_gate_up(&mg.a_sh, a.ws_gate_up, 1, a.Is, a.H, 4) || !map_2d(&mg.b[0], a.x, a.T, a.H, 1))
+      return cudaErrorInvalidValue;
+    e = launch_gate_up_pair(mg, p, stream);
+  } else {
+    e = launch_tc<TC_GATE_UP>(mg, p, grid, stream);
+  }
   if (e != cudaSuccess) return e;
   p.item_start = start_dn;
   p.items = items_dn;

@@ -254,5 +254,110 @@ __device__ inline void mma_commit(uint64_t *bar) {
                : "memory");
 }
 
+
+// ---------------------------------------------------------------- CTA pairs
+// A cluster of two CTAs on two SMs runs one M = 256 MMA (cta_group::2): the
+// even CTA of the pair issues it, each CTA holds its half of A (128 rows) and
+// of B (N / 2 rows) at the same shared-memory offsets, and each CTA's tensor
+// memory receives its 128 rows of D.  Every tcgen05 instruction of such a
+// kernel uses cta_group::2.
+__device__ inline uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// All threads of both CTAs; orders the mbarrier initialisation (and, at the
+// end, every remote access) across the pair.
+__device__ inline void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ inline uint32_t mapa_shared(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// Arrive on a barrier of another CTA of the cluster (address from mapa_shared).
+__device__ inline void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ inline bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait for barriers that threads or tensor-core commits of the peer CTA
+// arrive on (cluster-scope acquire).
+__device__ inline bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status,
+                                         uint64_t timeout_ns = WAIT_TIMEOUT_NS) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        record_status(status, STATUS_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+// TMA loads into this CTA's shared memory whose completion (bytes) is
+// counted on a barrier of either CTA of the pair (`bar_cluster` from
+// mapa_shared): the odd CTA's operand halves complete on the even CTA's
+// stage barrier.
+__device__ inline void tma_load_5d_pair(void *dst, const CUtensorMap *m, uint32_t bar_cluster, int c0, int c1, int c2,
+                                        int c3, int c4, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar_cluster), "l"(policy)
+      : "memory");
+}
+__device__ inline void tma_gather4_pair(void *dst, const CUtensorMap *m, uint32_t bar_cluster, int c0, int r0, int r1,
+                                        int r2, int r3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::"
+      "cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar_cluster), "l"(policy)
+      : "memory");
+}
+// One warp of each CTA of the pair, together.
+__device__ inline void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ inline void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D (+)= A * B^T over the pair, M = 256, issued by one thread of the even CTA.
+__device__ inline void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the barrier at this offset in both CTAs of the pair when the
+// pair MMAs this thread issued so far have completed.
+__device__ inline void mma_commit_pair(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
 }  // namespace umma
 }  // namespace moe
