@@ -228,6 +228,36 @@ __device__ __forceinline__ void gate_up_epi_chunk(const float (&v)[32], int fcol
   }
 }
 
+// Down epilogue of one 32-column chunk (columns c0..c0+31 = rows of the
+// item): v holds this lane's 32 accumulator values, lane = output feature
+// ocol + lane; `dst` (lane j: the destination row of column c0 + j) comes
+// from the caller.  Writes bf16 rows of yout [*, H] through the warp's
+// staging buffer `stg` (2048 bytes).
+__device__ __forceinline__ void down_epi_chunk(const float (&v)[32], int ocol, int c0, int dst, const Item &im,
+                                               __nv_bfloat16 *yout, int H, uint8_t *stg, int lane) {
+  // [32 cols][16 words]: two consecutive rows span all 32 banks, so the
+  // pair writes and the quarter-warp 16-byte reads are conflict-free.
+  uint32_t *stg_y = (uint32_t *)stg;
+  const bool odd = lane & 1;
+  // Pack features (2m, 2m+1) of a column into one bf16x2 word (see gate_up_epi_chunk).
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const float x = __shfl_xor_sync(FULL_MASK, odd ? v[j] : v[j + 1], 1);
+    const __nv_bfloat162 w2 = odd ? __floats2bfloat162_rn(x, v[j + 1]) : __floats2bfloat162_rn(v[j], x);
+    stg_y[(j + (odd ? 1 : 0)) * 16 + (lane >> 1)] = *reinterpret_cast<const uint32_t *>(&w2);
+  }
+  __syncwarp();
+  // Four lanes per column row: 8 rows x 64 contiguous bytes per store instruction.
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = (lane >> 2) + 8 * i, cc = lane & 3;
+    const int drow = __shfl_sync(FULL_MASK, dst, r);
+    if (c0 + r < im.rows)
+      *(uint4 *)(yout + (int64_t)drow * H + ocol + cc * 8) = *(const uint4 *)(stg_y + r * 16 + cc * 4);
+  }
+  __syncwarp();
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(tc_threads<MODE>(), 1)
 tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
@@ -398,11 +428,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
       } else {
         const bool sh = im.seg == p.E;
-        // [32 cols][16 words]: two consecutive rows span all 32 banks, so the
-        // pair writes and the quarter-warp 16-byte reads are conflict-free.
-        uint32_t *stg_y = (uint32_t *)stg;
         __nv_bfloat16 *yout = sh ? p.y_shared : p.y_routed;
-        const bool odd = lane & 1;
         for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
           // Destination row of column c0 + lane, fetched before the accumulator loads.
           int dst = 0;
@@ -412,27 +438,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           if (MT == 2) tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[MT - 1]);
           else tmem_ld32(tq + c0, vt[0]);
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const int ocol = (im.f * MT + mt) * 128 + q * 32;  // first output feature of this warp's 32
-            // Pack features (2m, 2m+1) of a column into one bf16x2 word (see the gate_up epilogue).
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const float x = __shfl_xor_sync(FULL_MASK, odd ? vt[mt][j] : vt[mt][j + 1], 1);
-              const __nv_bfloat162 w2 =
-                  odd ? __floats2bfloat162_rn(x, vt[mt][j + 1]) : __floats2bfloat162_rn(vt[mt][j], x);
-              stg_y[(j + (odd ? 1 : 0)) * 16 + (lane >> 1)] = *reinterpret_cast<const uint32_t *>(&w2);
-            }
-            __syncwarp();
-            // Four lanes per column row: 8 rows x 64 contiguous bytes per store instruction.
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int r = (lane >> 2) + 8 * i, cc = lane & 3;
-              const int drow = __shfl_sync(FULL_MASK, dst, r);
-              if (c0 + r < im.rows)
-                *(uint4 *)(yout + (int64_t)drow * p.H + ocol + cc * 8) = *(const uint4 *)(stg_y + r * 16 + cc * 4);
-            }
-            __syncwarp();
-          }
+          for (int mt = 0; mt < MT; ++mt)
+            down_epi_chunk(vt[mt], (im.f * MT + mt) * 128 + q * 32, c0, dst, im, yout, p.H, stg, lane);
         }
       }
       tc_fence_before();
@@ -481,45 +488,67 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// gate_up + SwiGLU on CTA pairs (cta_group::2).
+// The grouped GEMMs on CTA pairs (cta_group::2).
 //
-// The item is the same as tc_gemm_kernel<TC_GATE_UP>'s: 128 features (two M
-// tiles of 64 gate + 64 up rows) x up to 256 rows of one segment.  The two
-// CTAs of a cluster run it as one M = 256 MMA: CTA r holds M tile 2f + r of
-// the weights and gathers rows [r n/2, (r + 1) n/2) of the item's x rows, so
-// each gathered row is fetched once per item and each CTA's accumulator is
-// 128 lanes x n columns.  That leaves room for two accumulator buffers, so
-// an item's epilogue overlaps the next item's mainloop.  A stage holds
-// PR_KSUB K blocks of 64: per block 16 KB of weights + 16 KB of rows per CTA
-// (fewer, larger stages: one handshake per 128 K for the single MMA thread
-// that drives both SMs).
+// An item is two M tiles (gate_up: 64 gate + 64 up rows each, i.e. 128
+// features; down: 128 outputs each) x up to 256 rows of one segment.  The
+// two CTAs of a cluster run it as one M = 256 MMA: CTA r holds M tile 2f + r
+// of the weights and rows [r n/2, (r + 1) n/2) of the item's rows (gate_up:
+// x rows gathered by TMA gather4; down: consecutive h rows by tile boxes),
+// so each row is fetched once per item and each CTA's accumulator is 128
+// lanes x n columns.  That leaves room for two accumulator buffers, so an
+// item's epilogue overlaps the next item's mainloop.  A stage holds PR_KSUB
+// K blocks of 64: per block 16 KB of weights + 16 KB of rows per CTA (fewer,
+// larger stages: one handshake per 128 K for the single MMA thread that
+// drives both SMs).
 //
 // Synchronisation: the even CTA's MMA thread waits on its full[s]: one
 // arrival by the even CTA's producer, which expects the bytes of both CTAs'
-// weight tiles and gathered rows; every copy of both CTAs is a TMA load
-// (weights by tile, rows by gather4) completing on that barrier.  MMA
-// completion is committed to empty[s] / tfull[b] / mma_done in both CTAs at
-// once; the epilogue warps of both CTAs arrive on the even CTA's tempty[b].
+// weight tiles and rows; every copy of both CTAs is a TMA load completing on
+// that barrier.  MMA completion is committed to empty[s] / tfull[b] /
+// mma_done in both CTAs at once; the epilogue warps of both CTAs arrive on
+// the even CTA's tempty[b].
 // ---------------------------------------------------------------------------
 constexpr int PR_KSUB = 2;    // K blocks of 64 per stage
 constexpr int PR_STAGES = 3;  // stage ring depth
-constexpr int PR_EPI_WARPS = 8, PR_EPI_BYTES = 2560;
 constexpr int PR_A_BYTES = TC_TILE_A_BYTES, PR_B_BYTES = 128 * 128;  // one K block
 constexpr int PR_STAGE_BYTES = PR_KSUB * (PR_A_BYTES + PR_B_BYTES);
-constexpr int PR_GATHER_FIRST = TC_EPI_FIRST + PR_EPI_WARPS;
-constexpr int PR_THREADS = 32 * (PR_GATHER_FIRST + TC_GATHER_WARPS);
-constexpr int PR_SMEM_BYTES = 1024 + PR_STAGES * PR_STAGE_BYTES + PR_EPI_WARPS * PR_EPI_BYTES + 512;
-static_assert(PR_SMEM_BYTES <= 232448, "pair kernel shared memory");
+// Per mode: epilogue warps and staging bytes per warp; rows of an item are
+// padded to a multiple of NROUND (each CTA's half a multiple of 8 for the
+// gate_up gather4 quads, of 16 for the down tile boxes).
+template <int MODE>
+struct PrCfg;
+template <>
+struct PrCfg<TC_GATE_UP> {
+  static constexpr int EPI_WARPS = 8, EPI_BYTES = 2560, NROUND = 16, GATHER_WARPS = TC_GATHER_WARPS;
+};
+template <>
+struct PrCfg<TC_DOWN> {
+  static constexpr int EPI_WARPS = 16, EPI_BYTES = 2048, NROUND = 32, GATHER_WARPS = 0;
+};
+template <int MODE>
+constexpr int pr_threads() {
+  return 32 * (TC_EPI_FIRST + PrCfg<MODE>::EPI_WARPS + PrCfg<MODE>::GATHER_WARPS);
+}
+template <int MODE>
+constexpr int pr_smem_bytes() {
+  return 1024 + PR_STAGES * PR_STAGE_BYTES + PrCfg<MODE>::EPI_WARPS * PrCfg<MODE>::EPI_BYTES + 512;
+}
+static_assert(pr_smem_bytes<TC_GATE_UP>() <= 232448 && pr_smem_bytes<TC_DOWN>() <= 232448, "pair shared memory");
 
-__global__ void __launch_bounds__(PR_THREADS, 1)
-tc_gate_up_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+template <int MODE>
+__global__ void __launch_bounds__(pr_threads<MODE>(), 1)
+tc_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+  constexpr int EPI_WARPS = PrCfg<MODE>::EPI_WARPS, EPI_BYTES = PrCfg<MODE>::EPI_BYTES;
+  constexpr int NROUND = PrCfg<MODE>::NROUND;
+  constexpr int GATHER_FIRST = TC_EPI_FIRST + EPI_WARPS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   // Stage s: K block j's weight tile at sa(s, j), its rows at sb(s, j).
   auto sa = [&](int s, int j) { return base + s * PR_STAGE_BYTES + j * PR_A_BYTES; };
   auto sb = [&](int s, int j) { return base + s * PR_STAGE_BYTES + PR_KSUB * PR_A_BYTES + j * PR_B_BYTES; };
   uint8_t *epi = base + PR_STAGES * PR_STAGE_BYTES;
-  uint64_t *bars = (uint64_t *)(epi + PR_EPI_WARPS * PR_EPI_BYTES);
+  uint64_t *bars = (uint64_t *)(epi + EPI_WARPS * EPI_BYTES);
   uint64_t *full = bars, *empty = full + PR_STAGES;
   uint64_t *tfull = empty + PR_STAGES, *tempty = tfull + 2, *mma_done = tempty + 2;
   uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
@@ -529,6 +558,12 @@ tc_gate_up_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  // The item with its rows padded for the pair (each CTA takes n / 2 of them).
+  auto item = [&](int it) {
+    Item im = decode_item<MODE>(it, p);
+    im.n = (int)round_up(im.rows, NROUND);
+    return im;
+  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < PR_STAGES; ++s) {
       mbar_init(&full[s], 1);  // used in the even CTA
@@ -536,7 +571,7 @@ tc_gate_up_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 2 * PR_EPI_WARPS);
+      mbar_init(&tempty[b], 2 * EPI_WARPS);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -557,31 +592,46 @@ tc_gate_up_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   const int total = __ldg(p.item_start + p.E + 1);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (weights)
+    // ------------------------------------------------------------ TMA producer
+    // Weights (both modes) and, for DOWN, this CTA's half of the item's h
+    // rows (consecutive in sorted order) as power-of-two boxes.
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      const uint32_t full0 = mapa_shared(&full[0], 0);
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_phase = 0;
       bool ok = true;
       for (int it = cid; it < total && ok; it += ncl) {
-        const Item im = decode_item<TC_GATE_UP>(it, p);
+        const Item im = item(it);
         const bool sh = im.seg == p.E;
-        // 4 groups of 16 features: 16 gate rows then 16 up rows each (this CTA's M tile).
-        const int c3 = (im.f * 2 + (int)rank) * 4, c4 = sh ? 0 : im.seg - p.e0;
+        const int mtile = im.f * 2 + (int)rank;  // this CTA's M tile (64 gate/up features or 128 outputs)
         const CUtensorMap *am = sh ? &maps.a_sh : &maps.a;
+        const int half = im.n >> 1;
         for (int ks = 0; ks < im.nk / PR_KSUB; ++ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
-          if (leader) {
-            // Both CTAs' weight tiles and gathered rows (n/2 each) complete on this barrier.
-            mbar_arrive_expect_tx(&full[stage], PR_KSUB * (2 * PR_A_BYTES + (uint32_t)im.n * 128));
+          // Both CTAs' weight tiles and rows (n / 2 each) complete on the even CTA's barrier.
+          if (leader) mbar_arrive_expect_tx(&full[stage], PR_KSUB * (2 * PR_A_BYTES + (uint32_t)im.n * 128));
+          const uint32_t bar = full0 + (uint32_t)(stage * sizeof(uint64_t));
 #pragma unroll
-            for (int j = 0; j < PR_KSUB; ++j)
-              tma_load_5d(sa(stage, j), am, &full[stage], (ks * PR_KSUB + j) * 64, 0, 0, c3, c4, pol_w);
-          } else {
-            const uint32_t bar = mapa_shared(&full[stage], 0);
+          for (int j = 0; j < PR_KSUB; ++j) {
+            const int kx = (ks * PR_KSUB + j) * 64;
+            if (MODE == TC_GATE_UP) {
+              // 4 groups of 16 features: 16 gate rows then 16 up rows each.
+              tma_load_5d_pair(sa(stage, j), am, bar, kx, 0, 0, mtile * 4, sh ? 0 : im.seg - p.e0, pol_w);
+            } else {
+              tma_load_2d_pair(sa(stage, j), am, bar, kx, (sh ? 0 : (im.seg - p.e0) * p.H) + mtile * 128, pol_w);
+              const CUtensorMap *bm = sh ? maps.b_sh : maps.b;
+              const int r0 = (int)im.row0 + (int)rank * half;
+              int r = 0;
 #pragma unroll
-            for (int j = 0; j < PR_KSUB; ++j)
-              tma_load_5d_pair(sa(stage, j), am, bar, (ks * PR_KSUB + j) * 64, 0, 0, c3, c4, pol_w);
+              for (int h = 1; h < 5; ++h) {  // boxes of 128 .. 16 rows
+                const int box = 256 >> h;
+                while (half - r >= box) {
+                  tma_load_2d_pair(sb(stage, j) + r * 128, &bm[h], bar, kx, r0 + r, pol_x);
+                  r += box;
+                }
+              }
+            }
           }
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -604,7 +654,7 @@ tc_gate_up_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         uint32_t phase = 0, cnt = 0;
         bool ok = true;
         for (int it = cid; it < total && ok; it += ncl) {
-          const Item im = decode_item<TC_GATE_UP>(it, p);
+          const Item im = item(it);
           const int b = cnt & 1;
           if (!mbar_wait_cluster(&tempty[b], ((cnt >> 1) & 1) ^ 1, abort_flag, p.status)) break;
           tc_fence_after();
@@ -634,31 +684,43 @@ tc_gate_up_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       mbar_wait(mma_done, 0, &never, p.status);
     }
     __syncwarp();
-  } else if (warp < PR_GATHER_FIRST) {
+  } else if (warp < GATHER_FIRST) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
-    constexpr int CSTEP = 32 * (PR_EPI_WARPS / 4);
+    constexpr int CSTEP = 32 * (EPI_WARPS / 4);
     const int cfirst = 32 * ((warp - TC_EPI_FIRST) >> 2);
-    uint8_t *stg = epi + (warp - TC_EPI_FIRST) * PR_EPI_BYTES;
+    uint8_t *stg = epi + (warp - TC_EPI_FIRST) * EPI_BYTES;
     const uint32_t tempty_leader0 = mapa_shared(&tempty[0], 0);
     uint32_t cnt = 0;
     for (int it = cid; it < total; it += ncl) {
-      const Item im = decode_item<TC_GATE_UP>(it, p);
+      const Item im = item(it);
       const int b = cnt & 1;
       int ok = 0;
       if (lane == 0) ok = mbar_wait(&tfull[b], (cnt >> 1) & 1, abort_flag, p.status) ? 1 : 0;
       if (!__shfl_sync(FULL_MASK, ok, 0)) break;
       tc_fence_after();
       const bool sh = im.seg == p.E;
-      const int Iseg = sh ? p.Is : p.I;
-      __nv_bfloat16 *hout = sh ? p.h_shared : p.h_routed;
-      __nv_bfloat16 *guout = sh ? p.gu_shared : p.gu_routed;
       const uint32_t tq = tmem + b * 256 + ((uint32_t)(q * 32) << 16);
-      const int fcol = (im.f * 2 + (int)rank) * 64 + 16 * q;
-      for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
-        float v[32];
-        tmem_ld32(tq + c0, v);
-        gate_up_epi_chunk(v, fcol, c0, im, Iseg, hout, guout, stg, lane);
+      const int mtile = im.f * 2 + (int)rank;
+      if (MODE == TC_GATE_UP) {
+        const int Iseg = sh ? p.Is : p.I;
+        __nv_bfloat16 *hout = sh ? p.h_shared : p.h_routed;
+        __nv_bfloat16 *guout = sh ? p.gu_shared : p.gu_routed;
+        for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
+          float v[32];
+          tmem_ld32(tq + c0, v);
+          gate_up_epi_chunk(v, mtile * 64 + 16 * q, c0, im, Iseg, hout, guout, stg, lane);
+        }
+      } else {
+        __nv_bfloat16 *yout = sh ? p.y_shared : p.y_routed;
+        for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
+          int dst = 0;
+          if (c0 + lane < im.rows)
+            dst = (sh || p.y_sorted) ? (int)(im.row0 + c0 + lane) : __ldg(p.sorted_route + im.row0 + c0 + lane);
+          float v[32];
+          tmem_ld32(tq + c0, v);
+          down_epi_chunk(v, mtile * 128 + q * 32, c0, dst, im, yout, p.H, stg, lane);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -668,20 +730,21 @@ tc_gate_up_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       }
       ++cnt;
     }
-  } else {
+  } else if (MODE == TC_GATE_UP) {
     // ------------------------------------------------------------ row gather (TMA gather4)
     // This CTA's rows of the item: [rank n/2, rank n/2 + n/2) ∩ [0, rows),
     // row i at line i of a K block's B tile (the 128-byte swizzle), four rows
     // per copy; quad qd = g + 8 lane (lanes 0-3) of warp g.  The bytes of
     // both CTAs complete on the even CTA's full[s].  Lines past the item's
     // rows read token 0: their accumulator columns are never read.
-    const int g = warp - PR_GATHER_FIRST;
+    const int g = warp - GATHER_FIRST;
     const uint64_t pol_x = policy_evict_last();
+    const uint32_t full0 = mapa_shared(&full[0], 0);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int it = cid; it < total && ok; it += ncl) {
-      const Item im = decode_item<TC_GATE_UP>(it, p);
+      const Item im = item(it);
       const bool sh = im.seg == p.E;
       const int half = im.n >> 1, hbase = (int)rank * half;
       const int hrows = max(0, min(half, im.rows - hbase));
@@ -703,7 +766,7 @@ tc_gate_up_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         if (lane == 0) w = mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status) ? 1 : 0;
         if (!__shfl_sync(FULL_MASK, w, 0)) { ok = false; break; }
         if (mine) {
-          const uint32_t bar = mapa_shared(&full[stage], 0);
+          const uint32_t bar = full0 + (uint32_t)(stage * sizeof(uint64_t));
 #pragma unroll
           for (int j = 0; j < PR_KSUB; ++j)
             tma_gather4_pair(sb(stage, j) + qd * 512, &maps.b[0], bar, (ks * PR_KSUB + j) * 64, t4[0], t4[1], t4[2],
@@ -1041,15 +1104,16 @@ static cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cu
   return launch_pdl(tc_gemm_kernel<MODE>, dim3(grid), dim3(tc_threads<MODE>()), TC_SMEM_BYTES, stream, maps, p);
 }
 
-// Clusters of two gate_up pair CTAs that fit on the device at once (0: the
-// pair kernel cannot run here).  Queried once per device.
+// Clusters of two pair CTAs of `MODE` that fit on the device at once (0:
+// the pair kernel cannot run here).  Queried once per device.
+template <int MODE>
 static int pair_clusters() {
   static std::mutex mu;
   static int cache[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   const int sms = device_sms();
-  if (ensure_smem((const void *)tc_gate_up_pair_kernel, PR_SMEM_BYTES) != cudaSuccess) {
+  if (ensure_smem((const void *)tc_pair_kernel<MODE>, pr_smem_bytes<MODE>()) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1058,8 +1122,8 @@ static int pair_clusters() {
   if (c == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * sms);
-    cfg.blockDim = dim3(PR_THREADS);
-    cfg.dynamicSmemBytes = PR_SMEM_BYTES;
+    cfg.blockDim = dim3(pr_threads<MODE>());
+    cfg.dynamicSmemBytes = pr_smem_bytes<MODE>();
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
@@ -1068,7 +1132,7 @@ static int pair_clusters() {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (const void *)tc_gate_up_pair_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, (const void *)tc_pair_kernel<MODE>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -1077,19 +1141,26 @@ static int pair_clusters() {
   return c > 0 ? c : 0;
 }
 
-static bool use_gate_up_pair() {
-  const char *e = getenv("MOE_GATE_UP_PAIR");
-  if (e && e[0] == '0') return false;
-  return pair_clusters() > 0;
+// Whether the grouped GEMM of `MODE` runs on CTA pairs.  MOE_TC_PAIR (a
+// diagnostic switch for comparing the two forms): "0" neither, "1" gate_up
+// only, "2" down only; unset: both wherever the shapes and the device allow.
+template <int MODE>
+static bool use_pair(const FfnArgs &a) {
+  const char *e = getenv("MOE_TC_PAIR");
+  if (e && (e[0] == '0' || (e[0] == '1' && MODE != TC_GATE_UP) || (e[0] == '2' && MODE != TC_DOWN))) return false;
+  const bool shapes = MODE == TC_GATE_UP ? a.H % (64 * PR_KSUB) == 0
+                                         : a.H % 256 == 0 && a.I % (64 * PR_KSUB) == 0 && a.Is % (64 * PR_KSUB) == 0;
+  return shapes && pair_clusters<MODE>() > 0;
 }
 
-static cudaError_t launch_gate_up_pair(const TcMaps &maps, const TcParams &p, cudaStream_t stream) {
-  const int nc = pair_clusters();
+template <int MODE>
+static cudaError_t launch_pair(const TcMaps &maps, const TcParams &p, cudaStream_t stream) {
+  const int nc = pair_clusters<MODE>();
   if (nc <= 0) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * nc);
-  cfg.blockDim = dim3(PR_THREADS);
-  cfg.dynamicSmemBytes = PR_SMEM_BYTES;
+  cfg.blockDim = dim3(pr_threads<MODE>());
+  cfg.dynamicSmemBytes = pr_smem_bytes<MODE>();
   cfg.stream = stream;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1100,7 +1171,7 @@ static cudaError_t launch_gate_up_pair(const TcMaps &maps, const TcParams &p, cu
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, tc_gate_up_pair_kernel, maps, p);
+  return cudaLaunchKernelEx(&cfg, tc_pair_kernel<MODE>, maps, p);
 }
 
 size_t router_tc_scratch_bytes(int E, int H) { return (size_t)E * 3 * H * 2; }
@@ -1179,7 +1250,9 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   int4 *items_gu = (int4 *)(w + 2 * starts);
   int4 *items_dn = (int4 *)(w + 2 * starts + round256((size_t)mi_gu * 16));
   const int eb = a.e_begin, ee = a.e_end < 0 ? a.E : a.e_end, n_local = ee - eb;
-  cudaError_t e0 = launch_item_tables(a.E, a.T, a.I / GU_FEAT, a.Is / GU_FEAT, a.H / DN_ROWS, a.H / DN_ROWS, a.offsets,
+  const bool gu_pair = use_pair<TC_GATE_UP>(a), dn_pair = use_pair<TC_DOWN>(a);
+  const int dn_rows = dn_pair ? 256 : DN_ROWS;  // outputs per down item (a pair item is two M tiles)
+  cudaError_t e0 = launch_item_tables(a.E, a.T, a.I / GU_FEAT, a.Is / GU_FEAT, a.H / dn_rows, a.H / dn_rows, a.offsets,
                                       start_gu, start_dn, items_gu, items_dn, mi_gu, mi_dn, stream, eb, ee,
                                       a.with_shared);
   if (e0 != cudaSuccess) return e0;
@@ -1209,20 +1282,20 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   p.item_start = start_gu;
   p.items = items_gu;
   cudaError_t e;
-  if (use_gate_up_pair() && a.H % (64 * PR_KSUB) == 0) {
-    // One M tile (4 groups of 16 features) per CTA of the pair.
-    // x rows for the odd CTA's gather4 copies: a one-row box.
+  if (gu_pair) {
+    // One M tile (4 groups of 16 features) per CTA of the pair; x rows for
+    // the gather4 copies through a one-row box.
     if (!map_gate_up(&mg.a, a.w_gate_up, std::max(n_local, 1), a.I, a.H, 4) ||
         !map_gate_up(&mg.a_sh, a.ws_gate_up, 1, a.Is, a.H, 4) || !map_2d(&mg.b[0], a.x, a.T, a.H, 1))
       return cudaErrorInvalidValue;
-    e = launch_gate_up_pair(mg, p, stream);
+    e = launch_pair<TC_GATE_UP>(mg, p, stream);
   } else {
     e = launch_tc<TC_GATE_UP>(mg, p, grid, stream);
   }
   if (e != cudaSuccess) return e;
   p.item_start = start_dn;
   p.items = items_dn;
-  return launch_tc<TC_DOWN>(md, p, grid, stream);
+  return dn_pair ? launch_pair<TC_DOWN>(md, p, stream) : launch_tc<TC_DOWN>(md, p, grid, stream);
 }
 
 }  // namespace moe

@@ -322,6 +322,14 @@ __device__ inline void tma_load_5d_pair(void *dst, const CUtensorMap *m, uint32_
       "l"(m), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar_cluster), "l"(policy)
       : "memory");
 }
+__device__ inline void tma_load_2d_pair(void *dst, const CUtensorMap *m, uint32_t bar_cluster, int c0, int c1,
+                                        uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(c0), "r"(c1), "r"(bar_cluster), "l"(policy)
+      : "memory");
+}
 __device__ inline void tma_gather4_pair(void *dst, const CUtensorMap *m, uint32_t bar_cluster, int c0, int r0, int r1,
                                         int r2, int r3, uint64_t policy) {
   asm volatile(
