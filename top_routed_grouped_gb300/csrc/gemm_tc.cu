@@ -656,7 +656,7 @@ tc_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         for (int it = cid; it < total && ok; it += ncl) {
           const Item im = item(it);
           const int b = cnt & 1;
-          if (!mbar_wait_cluster(&tempty[b], ((cnt >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+          if (!mbar_wait(&tempty[b], ((cnt >> 1) & 1) ^ 1, abort_flag, p.status)) break;
           tc_fence_after();
           const uint32_t idesc = idesc_bf16_f32(256, im.n);
           for (int ks = 0; ks < im.nk / PR_KSUB; ++ks) {

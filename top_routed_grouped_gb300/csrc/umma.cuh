@@ -277,38 +277,12 @@ __device__ inline uint32_t mapa_shared(const void *p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
 }
-// Arrive on a barrier of another CTA of the cluster (address from mapa_shared).
+// Arrive on a barrier of another CTA of the cluster (address from
+// mapa_shared).  CTA-scope release: what the arrival publishes to the other
+// CTA is tensor-memory state, ordered by the tcgen05 fences around it, not
+// generic memory.
 __device__ inline void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ inline bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// mbar_wait for barriers that threads or tensor-core commits of the peer CTA
-// arrive on (cluster-scope acquire).
-__device__ inline bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status,
-                                         uint64_t timeout_ns = WAIT_TIMEOUT_NS) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 63) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > timeout_ns) {
-        *abort_flag = 1;
-        record_status(status, STATUS_WAIT_TIMEOUT);
-        return false;
-      }
-    }
-  }
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // TMA loads into this CTA's shared memory whose completion (bytes) is
 // counted on a barrier of either CTA of the pair (`bar_cluster` from
