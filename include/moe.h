@@ -23,6 +23,7 @@
  *                    shared row, one rounding to the output type
  *   moe_backward     all gradients, reduced in fixed orders
  *   moe_backward_ep  one rank's part of moe_backward under an expert partition
+ *   moe_grouped_ffn_etp, moe_etp_reduce  the grouped FFN with I split across ranks
  *   moe_forward      the four forward calls in sequence, intermediates in the
  *                    caller's workspace
  *
@@ -294,6 +295,52 @@ int moe_grouped_ffn_ep(const moe_dims_t *d, int32_t e_begin, int32_t e_end, int3
  */
 int moe_combine_sorted(const moe_dims_t *d, const void *y_sorted, const int32_t *route_pos, const void *y_shared,
                        const float *topk_w, const float *shared_sig, void *y, void *stream);
+
+/*
+ * moe_grouped_ffn_etp -- moe_grouped_ffn for one rank of an expert-tensor-
+ * parallel (ETP) split of the intermediate dimension.  RL-Kernel PR #557
+ * "What", bullet "Fail closed" (EP 1 runs the experts expert-tensor-parallel
+ * over 4 ranks) and the embedded #503 commit message, bullet "TP4 block"
+ * (every expert on every rank, partial results reduced across ranks); the
+ * reduction here is a byte-copy gather plus a fixed-order local sum, as PR
+ * #557 "What" does for the EP exchange: rank r holds, for every expert, the gate and up rows of its
+ * feature slice [i0, i1) of I and the matching columns of W_down (and a
+ * slice of the shared expert's Is).  Since Yr = sum over features i of
+ * h_i W_down[:, i], its down projection is a partial sum of every routed and
+ * shared row.
+ *
+ *   d               the layer's dims with I and Is replaced by the rank's
+ *                   slice widths (bf16: multiples of 128)
+ *   w_gate_up [E, 2 I_r, H]: rows 0..I_r-1 = gate rows i0..i1-1, then the up
+ *                   rows i0..i1-1; w_down [E, H, I_r] = W_down[:, :, i0:i1];
+ *                   ws_gate_up / ws_down the same for the shared expert
+ *   yr_partial [T*k, H] float, route order; ys_partial [T, H] float: this
+ *                   rank's partial sums, the FP32 accumulators unrounded
+ *   saved           as moe_grouped_ffn, with the slice's widths
+ * Errors as moe_grouped_ffn.  Workspace: GROUPED_FFN for `d`.
+ */
+int moe_grouped_ffn_etp(const moe_dims_t *d, const void *x, const int32_t *expert_offsets,
+                        const int32_t *sorted_route, const void *w_gate_up, const void *w_down, const void *ws_gate_up,
+                        const void *ws_down, float *yr_partial, float *ys_partial, const moe_saved_t *saved, void *ws,
+                        size_t ws_bytes, void *stream);
+
+/*
+ * moe_etp_reduce -- the routed and shared rows from the ranks' partial sums:
+ * y_routed = dtype(((p_0 + p_1) + ...) + p_{n-1}), summed in FP32 in rank
+ * order with one rounding (same for y_shared), after every rank gathered all
+ * partials (a byte copy).  The result depends on the number of ranks (the
+ * rounding order does) but not on T, on the exchange, or on which rank
+ * reduces; with one rank it equals moe_grouped_ffn's rows bit for bit.
+ *
+ *   d               the layer's dims (full I, Is)
+ *   n_parts         1..16
+ *   yr_parts, ys_parts  HOST arrays of n_parts device pointers to the float
+ *                   partials ([T*k, H] and [T, H]), in rank order
+ *   y_routed [T*k, H], y_shared [T, H] dtype out (feed moe_combine)
+ * No workspace.
+ */
+int moe_etp_reduce(const moe_dims_t *d, int32_t n_parts, const float *const *yr_parts, const float *const *ys_parts,
+                   void *y_routed, void *y_shared, void *stream);
 
 /* Everything moe_forward reads and writes. */
 typedef struct moe_fwd_args {

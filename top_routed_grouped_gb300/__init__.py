@@ -26,7 +26,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
 EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_permute", "moe_grouped_ffn",
             "moe_combine", "moe_forward", "moe_backward", "moe_device_status", "moe_permute_noalloc",
             "moe_route_replay", "moe_grouped_ffn_ep", "moe_combine_sorted", "moe_router_logits",
-            "moe_backward_ep")
+            "moe_backward_ep", "moe_grouped_ffn_etp", "moe_etp_reduce")
 
 _vp = ctypes.c_void_p
 
@@ -90,6 +90,9 @@ def lib() -> ctypes.CDLL:
                 "moe_grouped_ffn_ep": ([D, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32] + [_vp] * 9 +
                                        [ctypes.POINTER(Saved), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_combine_sorted": ([D] + [_vp] * 6 + [_vp], ctypes.c_int),
+                "moe_grouped_ffn_etp": ([D] + [_vp] * 9 + [ctypes.POINTER(Saved), _vp, ctypes.c_size_t, _vp],
+                                        ctypes.c_int),
+                "moe_etp_reduce": ([D, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
                 "moe_forward": ([D, ctypes.POINTER(FwdArgs), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_backward": ([D, ctypes.POINTER(BwdArgs), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_backward_ep": ([D, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(BwdArgs), _vp,
@@ -210,6 +213,28 @@ def moe_grouped_ffn_ep(d, e_begin, e_end, with_shared, x, expert_offsets, sorted
         ctypes.byref(d), int(e_begin), int(e_end), int(with_shared), _p(x), _p(expert_offsets), _p(sorted_route),
         _p(w_gate_up), _p(w_down), _p(ws_gate_up), _p(ws_down), _p(y_sorted), _p(y_shared), ctypes.byref(sv), _p(ws),
         0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def moe_grouped_ffn_etp(d, x, expert_offsets, sorted_route, w_gate_up, w_down, ws_gate_up, ws_down, yr_partial,
+                        ys_partial, saved, ws, stream=None):
+    """One rank's part of the expert-tensor-parallel grouped FFN (see moe.h):
+    ``d`` carries the rank's slice widths; float partial rows out."""
+    sv = _saved(saved)
+    _check("moe_grouped_ffn_etp", lib().moe_grouped_ffn_etp(
+        ctypes.byref(d), _p(x), _p(expert_offsets), _p(sorted_route), _p(w_gate_up), _p(w_down), _p(ws_gate_up),
+        _p(ws_down), _p(yr_partial), _p(ys_partial), ctypes.byref(sv), _p(ws), 0 if ws is None else ws.numel(),
+        _stream(stream)))
+
+
+def moe_etp_reduce(d, yr_parts, ys_parts, y_routed, y_shared, stream=None):
+    """Rank-ordered FP32 sum of the partials, one rounding (see moe.h)."""
+    n = len(yr_parts)
+    if n != len(ys_parts):
+        raise ValueError("one routed and one shared partial per rank")
+    arr_r = (ctypes.c_void_p * max(n, 1))(*[_p(t) for t in yr_parts])
+    arr_s = (ctypes.c_void_p * max(n, 1))(*[_p(t) for t in ys_parts])
+    _check("moe_etp_reduce", lib().moe_etp_reduce(ctypes.byref(d), n, arr_r, arr_s, _p(y_routed), _p(y_shared),
+                                                  _stream(stream)))
 
 
 def moe_combine_sorted(d, y_sorted, route_pos, y_shared, topk_w, shared_sig, y, stream=None):

@@ -300,6 +300,55 @@ MOE_API int moe_grouped_ffn(const moe_dims_t *d, const void *x, const int32_t *e
   return cuda_status(launch_ffn_tc(a, sc.tiles, device_status_ptr(), (cudaStream_t)stream));
 }
 
+MOE_API int moe_grouped_ffn_etp(const moe_dims_t *d, const void *x, const int32_t *expert_offsets,
+                                const int32_t *sorted_route, const void *w_gate_up, const void *w_down,
+                                const void *ws_gate_up, const void *ws_down, float *yr_partial, float *ys_partial,
+                                const moe_saved_t *saved, void *ws, size_t ws_bytes, void *stream) {
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  const int64_t T = d->T, R = T * d->k;
+  if (!buf_ok(x, T * d->H) || !buf_ok(expert_offsets, 1) || !buf_ok(sorted_route, R) || !buf_ok(w_gate_up, 1) ||
+      !buf_ok(w_down, 1) || !buf_ok(ws_gate_up, 1) || !buf_ok(ws_down, 1) || !buf_ok(yr_partial, R * d->H) ||
+      !buf_ok(ys_partial, T * d->H) || !opt_ok(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (saved && (!opt_ok(saved->gu) || !opt_ok(saved->h) || !opt_ok(saved->gu_shared) || !opt_ok(saved->h_shared)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_size(d, MOE_OP_GROUPED_FFN)) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  Carver c(ws);
+  FfnScratch sc = ffn_ws(d, c);
+  FfnArgs a;
+  a.T = d->T; a.H = d->H; a.E = d->E; a.k = d->k; a.I = d->I; a.Is = d->Is;
+  a.x = x; a.offsets = expert_offsets; a.sorted_route = sorted_route;
+  a.w_gate_up = w_gate_up; a.w_down = w_down; a.ws_gate_up = ws_gate_up; a.ws_down = ws_down;
+  a.y_routed = yr_partial; a.y_shared = ys_partial;
+  a.y_f32 = 1;
+  a.h_routed = (saved && saved->h) ? saved->h : sc.h_routed;
+  a.h_shared = (saved && saved->h_shared) ? saved->h_shared : sc.h_shared;
+  a.gu_routed = saved ? saved->gu : nullptr;
+  a.gu_shared = saved ? saved->gu_shared : nullptr;
+  // The FP32 path's rows are float already: the partial sums are its outputs.
+  if (d->dtype == MOE_F32) return cuda_status(launch_ffn_simt(a, sc.tiles, (cudaStream_t)stream));
+  return cuda_status(launch_ffn_tc(a, sc.tiles, device_status_ptr(), (cudaStream_t)stream));
+}
+
+MOE_API int moe_etp_reduce(const moe_dims_t *d, int32_t n_parts, const float *const *yr_parts,
+                           const float *const *ys_parts, void *y_routed, void *y_shared, void *stream) {
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (n_parts < 1 || n_parts > ETP_MAX_PARTS || !yr_parts || !ys_parts) return MOE_ERR_INVALID_ARG;
+  const int64_t T = d->T, R = T * d->k;
+  for (int q = 0; q < n_parts; ++q)
+    if (!buf_ok(yr_parts[q], R * d->H) || !buf_ok(ys_parts[q], T * d->H)) return MOE_ERR_INVALID_ARG;
+  if (!buf_ok(y_routed, R * d->H) || !buf_ok(y_shared, T * d->H)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  const int dtype = d->dtype == MOE_F32 ? 0 : 1;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_etp_reduce(dtype, n_parts, yr_parts, R * d->H, y_routed, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_etp_reduce(dtype, n_parts, ys_parts, T * d->H, y_shared, s));
+}
+
 MOE_API int moe_grouped_ffn_ep(const moe_dims_t *d, int32_t e_begin, int32_t e_end, int32_t with_shared,
                                const void *x, const int32_t *expert_offsets, const int32_t *sorted_route,
                                const void *w_gate_up, const void *w_down, const void *ws_gate_up, const void *ws_down,

@@ -113,6 +113,7 @@ struct TcParams {
   int rt_splits;            // ROUTER: bf16 terms of the weight used (3: exact; 1: weight rounded to bf16)
   int e0;                   // first expert of the weight arrays (expert partition)
   int y_sorted;             // DOWN: routed rows in sorted order
+  int y_f32;                // DOWN: float rows, the accumulators unrounded
   const int32_t *offsets;
   const int32_t *sorted_route;
   const int32_t *item_start;  // [E+2] prefix of items per segment
@@ -256,6 +257,17 @@ __device__ __forceinline__ void down_epi_chunk(const float (&v)[32], int ocol, i
       *(uint4 *)(yout + (int64_t)drow * H + ocol + cc * 8) = *(const uint4 *)(stg_y + r * 16 + cc * 4);
   }
   __syncwarp();
+}
+
+// The same chunk written as float rows without rounding: lane = output
+// feature, so each of the 32 stores (one per column) is one 128-byte row segment.
+__device__ __forceinline__ void down_epi_chunk_f32(const float (&v)[32], int ocol, int c0, int dst, const Item &im,
+                                                   float *yout, int H, int lane) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int drow = __shfl_sync(FULL_MASK, dst, j);
+    if (c0 + j < im.rows) yout[(int64_t)drow * H + ocol + lane] = v[j];
+  }
 }
 
 template <int MODE>
@@ -438,8 +450,11 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           if (MT == 2) tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[MT - 1]);
           else tmem_ld32(tq + c0, vt[0]);
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-            down_epi_chunk(vt[mt], (im.f * MT + mt) * 128 + q * 32, c0, dst, im, yout, p.H, stg, lane);
+          for (int mt = 0; mt < MT; ++mt) {
+            const int ocol = (im.f * MT + mt) * 128 + q * 32;
+            if (p.y_f32) down_epi_chunk_f32(vt[mt], ocol, c0, dst, im, (float *)(void *)yout, p.H, lane);
+            else down_epi_chunk(vt[mt], ocol, c0, dst, im, yout, p.H, stg, lane);
+          }
         }
       }
       tc_fence_before();
@@ -719,7 +734,8 @@ tc_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             dst = (sh || p.y_sorted) ? (int)(im.row0 + c0 + lane) : __ldg(p.sorted_route + im.row0 + c0 + lane);
           float v[32];
           tmem_ld32(tq + c0, v);
-          down_epi_chunk(v, mtile * 128 + q * 32, c0, dst, im, yout, p.H, stg, lane);
+          if (p.y_f32) down_epi_chunk_f32(v, mtile * 128 + q * 32, c0, dst, im, (float *)(void *)yout, p.H, lane);
+          else down_epi_chunk(v, mtile * 128 + q * 32, c0, dst, im, yout, p.H, stg, lane);
         }
       }
       tc_fence_before();
@@ -1277,6 +1293,7 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   p.y_shared = (__nv_bfloat16 *)a.y_shared;
   p.e0 = eb;
   p.y_sorted = a.y_sorted;
+  p.y_f32 = a.y_f32;
   p.status = status;
   const int grid = device_sms();
   p.item_start = start_gu;

@@ -59,10 +59,21 @@ struct FfnArgs {
   // and, if with_shared, the shared expert; y_sorted: routed rows written in
   // sorted order (row j) instead of route order (row sorted_route[j]).
   int e_begin = 0, e_end = -1, with_shared = 1, y_sorted = 0;
+  // bf16 path: y_routed / y_shared are float buffers receiving the FP32
+  // accumulators unrounded (a partial sum over a slice of I, for the
+  // expert-tensor-parallel reduction).
+  int y_f32 = 0;
 };
 size_t ffn_simt_scratch_bytes(int E);
 // The MOE_F32 grouped FFN on CUDA cores (all buffers float).
 cudaError_t launch_ffn_simt(const FfnArgs &a, void *scratch, cudaStream_t stream);
+
+// ---- etp.cu ----
+constexpr int ETP_MAX_PARTS = 16;
+// out[i] = cast(((parts[0][i] + parts[1][i]) + ...) + parts[n-1][i]) for
+// i < count (FP32 sums in part order, one rounding to `dtype`).
+cudaError_t launch_etp_reduce(int dtype, int n, const float *const *parts, int64_t count, void *out,
+                              cudaStream_t stream);
 
 // ---- gemm_tc.cu (bf16 tensor-core path) ----
 size_t router_tc_scratch_bytes(int E, int H);
