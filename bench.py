@@ -9,6 +9,8 @@ the expert weights (3.2 GB) exceed L2, so no flush is needed between steps.
 Prints ONE JSON line (rank 0).  Keys beyond the basic contract:
   e2e          same metric through moe_forward with pinned host buffers and
                the host<->device copies of x and y inside the timed region
+               (copies on their own streams, two alternating buffers, so a
+               step's copies overlap its neighbours' compute)
   roofline     the dominant operation (moe_grouped_ffn) against measured HBM
   layer_roofline  the whole step against max(bytes/HBM, FLOPs/tensor peak)
   cpu_baseline the FP64 oracle on the host cores, on a bounded token sample
@@ -390,30 +392,57 @@ def main():
         raise RuntimeError("a kernel recorded a failed device-side check during the timed region")
 
     # ---- end to end: pinned host x -> device, moe_forward, y -> pinned host ----
+    # Every step copies its x in and its y out through pinned host memory.
+    # As a serving loop runs it, the copies go on their own streams into two
+    # alternating device buffers, so step i's copies overlap the compute of
+    # steps i - 1 and i + 1; the timed region spans the first copy in to the
+    # last copy out.
     x_host = cpu["x"].pin_memory()
-    y_host = torch.empty(T, H, dtype=dt).pin_memory()
-    x_dev = torch.empty_like(dev["x"])
+    y_host = [torch.empty(T, H, dtype=dt).pin_memory() for _ in range(2)]
+    x_buf = [torch.empty_like(dev["x"]) for _ in range(2)]
+    y_buf = [torch.empty_like(o["y"]) for _ in range(2)]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
     fws = moe.workspace(d, "forward")
-    fargs = {"x": x_dev, "w_router": dev["w_router"], "router_bias": dev["router_bias"],
-             "w_shared_gate": dev["w_shared_gate"], "w_gate_up": dev["w_gate_up"], "w_down": dev["w_down"],
-             "ws_gate_up": dev["ws_gate_up"], "ws_down": dev["ws_down"], "y": o["y"]}
+    fargs = [{"x": x_buf[b], "w_router": dev["w_router"], "router_bias": dev["router_bias"],
+              "w_shared_gate": dev["w_shared_gate"], "w_gate_up": dev["w_gate_up"], "w_down": dev["w_down"],
+              "ws_gate_up": dev["ws_gate_up"], "ws_down": dev["ws_down"], "y": y_buf[b]} for b in range(2)]
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    x_ready, x_free, y_ready, y_free = ([ev() for _ in range(2)] for _ in range(4))
+    for b in range(2):  # both buffers start free
+        x_free[b].record(stream)
+        y_free[b].record(stream)
 
-    def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_forward(d, fargs, fws, stream)
-        y_host.copy_(o["y"], non_blocking=True)
+    def e2e_step(i):
+        b = i & 1
+        h2d.wait_event(x_free[b])
+        with torch.cuda.stream(h2d):
+            x_buf[b].copy_(x_host, non_blocking=True)
+        x_ready[b].record(h2d)
+        stream.wait_event(x_ready[b])
+        stream.wait_event(y_free[b])
+        moe.moe_forward(d, fargs[b], fws, stream)
+        x_free[b].record(stream)
+        y_ready[b].record(stream)
+        d2h.wait_event(y_ready[b])
+        with torch.cuda.stream(d2h):
+            y_host[b].copy_(y_buf[b], non_blocking=True)
+        y_free[b].record(d2h)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    for i in range(args.warmup):
+        e2e_step(i)
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    h2d.wait_event(e0)
+    for i in range(args.steps):
+        e2e_step(i)
+    stream.wait_stream(d2h)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    if not torch.equal(y_buf[0], o["y"]):
+        raise RuntimeError("the end-to-end forward differs from the device-timed forward")
 
     peaks, peak_src = load_peaks()
     lb = layer_bytes_flops(T, H, E, k, Iw, Is, active)
