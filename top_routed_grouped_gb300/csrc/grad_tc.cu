@@ -26,9 +26,10 @@
 // rows past the segment's end in its last K block are zeroed in shared
 // memory before the MMAs read them, x rows are gathered by eight warps with
 // cp.async (zero-filled past the end).  Two TMEM accumulators alternate, so
-// the epilogue of one tile overlaps the MMAs of the next; the epilogue
-// stages 32 x 32 FP32 sub-tiles in shared memory and writes them with TMA
-// stores.  Empty segments get zero tiles (every output is written).
+// the epilogue of one tile overlaps the MMAs of the next; each epilogue warp
+// copies its whole share of an accumulator into registers and releases it at
+// once, then stages 32 x 32 FP32 sub-tiles in shared memory and writes them
+// with TMA stores.  Empty segments get zero tiles (every output is written).
 //
 // Every output element is reduced over K in one fixed order (K blocks of
 // 64, four K = 16 MMAs each); the tiling decides where a value is written,
@@ -327,16 +328,18 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
 // A stage holds one K block of both operands: A = 2 blocks (128 M) and B = 4
 // blocks (256 N) of 64 MN elements, each block hb K lines of 128 bytes, where
 // hb (64, 32 or 16) is the smallest box height that covers the rows left in
-// the segment; lines past the segment's end (at most 15 per block) are
-// zeroed before the MMAs read them.
-// WG_EPI_WARPS epilogue warps, WG_EPI_WARPS / 4 per TMEM lane quarter, each
+// the segment; the lines past the segment's end that the K = 16 MMAs read
+// (at most 15 per block) are zeroed by a dedicated warp before the stage is
+// released to the MMA thread.
+// WG_EPI_WARPS epilogue warps (warps 2..), WG_EPI_WARPS / 4 per TMEM lane quarter, each
 // draining WG_COLS of the 256 accumulator columns through WG_NSTG staging tiles.
 constexpr int WG_STAGES = 3, WG_EPI_WARPS = 8, WG_NSTG = 2;
 constexpr int WG_COLS = 1024 / WG_EPI_WARPS;
 constexpr int WG_A_BYTES = 2 * 8192;  // 128 M x 64 K lines, MN-major
 constexpr int WG_B_BYTES = 4 * 8192;  // 256 N x 64 K lines, MN-major
 constexpr int WG_STG_BYTES = 4096;    // one 32 x 32 FP32 store tile
-constexpr int WG_THREADS = 32 * (GT_EPI_FIRST + WG_EPI_WARPS);
+constexpr int WG_TAIL_WARP = GT_EPI_FIRST + WG_EPI_WARPS;  // zeroes segment tails, then releases the stage
+constexpr int WG_THREADS = 32 * (WG_TAIL_WARP + 1);
 constexpr int WG_SMEM = 1024 + WG_STAGES * (WG_A_BYTES + WG_B_BYTES) + (WG_NSTG * WG_EPI_WARPS + 1) * WG_STG_BYTES + 256;
 static_assert(WG_SMEM <= 232448, "wgrad shared memory");
 
@@ -401,7 +404,8 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
   uint64_t *bars = (uint64_t *)(zero_tile + WG_STG_BYTES);
   uint64_t *full = bars, *empty = bars + WG_STAGES;
   uint64_t *tfull = bars + 2 * WG_STAGES, *tempty = tfull + 2, *mma_done = tempty + 2;
-  uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
+  uint64_t *ready = mma_done + 1;  // stage s landed and its tail lines are zero
+  uint32_t *tmem_slot = (uint32_t *)(ready + WG_STAGES);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -411,6 +415,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
     for (int s = 0; s < WG_STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&ready[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -440,8 +445,10 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_phase = 0;
       bool ok = true;
+      WgItem nxt = wg_item(blockIdx.x, p);
       for (int it = blockIdx.x; it < p.total && ok; it += gridDim.x) {
-        const WgItem im = wg_item(it, p);
+        const WgItem im = nxt;
+        if (it + (int)gridDim.x < p.total) nxt = wg_item(it + gridDim.x, p);  // loads overlap this item
         const bool sh = im.seg == p.E;
         for (int kb = 0; kb < im.nk; ++kb) {
           const int hi = wg_box(min(64, im.rows - kb * 64));
@@ -464,58 +471,78 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (whole warp: tail zeroing)
-    int stage = 0;
-    uint32_t phase = 0, cnt = 0;
-    bool ok = true;
-    const uint32_t idesc = idesc_bf16_f32(128, 256) | IDESC_A_MN | IDESC_B_MN;
-    for (int it = blockIdx.x; it < p.total && ok; it += gridDim.x) {
-      const WgItem im = wg_item(it, p);
-      if (im.rows == 0) continue;
-      const int b = cnt & 1;
-      if (!gt_warp_wait(&tempty[b], ((cnt >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-      tc_fence_after();
-      for (int kb = 0; kb < im.nk; ++kb) {
-        if (!gt_warp_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
-        const int valid = min(64, im.rows - kb * 64);
-        const int hb = 64 >> wg_box(valid);  // lines per block in this stage
-        if (valid < hb) {
-          // Lines [valid, hb) of each block hold rows of the next segment (or
-          // TMA zero fill): clear them in both operands (6 blocks).
-          const int lines = hb - valid;
-          for (int i = lane; i < 6 * lines * 8; i += 32) {
-            const int blk = i / (lines * 8), rem = i % (lines * 8);
-            uint8_t *blk_base = blk < 2 ? sa + stage * WG_A_BYTES + blk * hb * 128
-                                        : sb + stage * WG_B_BYTES + (blk - 2) * hb * 128;
-            ((uint4 *)(blk_base + valid * 128))[rem] = make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, cnt = 0;
+      bool ok = true;
+      const uint32_t idesc = idesc_bf16_f32(128, 256) | IDESC_A_MN | IDESC_B_MN;
+      WgItem nxt = wg_item(blockIdx.x, p);
+      for (int it = blockIdx.x; it < p.total && ok; it += gridDim.x) {
+        const WgItem im = nxt;
+        if (it + (int)gridDim.x < p.total) nxt = wg_item(it + gridDim.x, p);
+        if (im.rows == 0) continue;
+        const int b = cnt & 1;
+        if (!mbar_wait(&tempty[b], ((cnt >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < im.nk; ++kb) {
+          if (!mbar_wait(&ready[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t lbo = (uint32_t)hb * 128;  // stride between 64-element MN blocks
+          const int valid = min(64, im.rows - kb * 64);
+          const uint32_t lbo = (uint32_t)(64 >> wg_box(valid)) * 128;  // stride between 64-element MN blocks
           const uint64_t ad = smem_desc_mn_sw128(smem_u32(sa + stage * WG_A_BYTES), lbo);
           const uint64_t bd = smem_desc_mn_sw128(smem_u32(sb + stage * WG_B_BYTES), lbo);
           const int nkk = (valid + 15) >> 4;
           for (int kk = 0; kk < nkk; ++kk)
             mma_bf16(tmem + b * 256, ad + 128 * kk, bd + 128 * kk, idesc, (kb | kk) != 0);
           mma_commit(&empty[stage]);
+          if (++stage == WG_STAGES) stage = 0, phase ^= 1;
         }
-        __syncwarp();
-        if (++stage == WG_STAGES) stage = 0, phase ^= 1;
+        if (!ok) break;
+        mma_commit(&tfull[b]);
+        ++cnt;
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(&tfull[b]);
-      __syncwarp();
-      ++cnt;
-    }
-    if (lane == 0) {
       mma_commit(mma_done);
       volatile int never = 0;
       mbar_wait(mma_done, 0, &never, p.status);
     }
     __syncwarp();
+  } else if (warp == WG_TAIL_WARP) {
+    // ------------------------------------------------------------ stage tails
+    // In a segment's last K block, lines [valid, 16 nkk) of each block hold
+    // rows of the next segment (or TMA zero fill) and the K = 16 MMAs read
+    // them: clear them in both operands (6 blocks, at most 15 lines each;
+    // lane = 16-byte chunk (lane % 8) of every 4th line), then release the
+    // stage to the MMA thread.
+    int stage = 0;
+    uint32_t phase = 0;
+    WgItem nxt = wg_item(blockIdx.x, p);
+    for (int it = blockIdx.x; it < p.total; it += gridDim.x) {
+      const WgItem im = nxt;
+      if (it + (int)gridDim.x < p.total) nxt = wg_item(it + gridDim.x, p);
+      if (im.rows == 0) continue;
+      bool ok = true;
+      for (int kb = 0; kb < im.nk; ++kb) {
+        if (!gt_warp_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+        const int valid = min(64, im.rows - kb * 64);
+        const int hb = 64 >> wg_box(valid);  // lines per block in this stage
+        const int lines = 16 * ((valid + 15) >> 4) - valid;
+        if (lines > 0) {
+#pragma unroll
+          for (int blk = 0; blk < 6; ++blk) {
+            uint8_t *blk_base = blk < 2 ? sa + stage * WG_A_BYTES + blk * hb * 128
+                                        : sb + stage * WG_B_BYTES + (blk - 2) * hb * 128;
+            for (int l = lane >> 3; l < lines; l += 4)
+              ((uint4 *)(blk_base + (valid + l) * 128))[lane & 7] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ready[stage]);
+        if (++stage == WG_STAGES) stage = 0, phase ^= 1;
+      }
+      if (!ok) break;
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     // Warp (q, part): TMEM lanes 32q.. (output rows), columns [WG_COLS part, +WG_COLS).
@@ -523,8 +550,10 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
     uint8_t *stg0 = stg_all + (warp - GT_EPI_FIRST) * WG_NSTG * WG_STG_BYTES;
     uint32_t cnt = 0, sbuf = 0;
     const int Mr = MODE == WGRAD_DOWN ? p.H : 2 * p.I;  // output rows per routed expert
+    WgItem nxt = wg_item(blockIdx.x, p);
     for (int it = blockIdx.x; it < p.total; it += gridDim.x) {
-      const WgItem im = wg_item(it, p);
+      const WgItem im = nxt;
+      if (it + (int)gridDim.x < p.total) nxt = wg_item(it + gridDim.x, p);
       const bool sh = im.seg == p.E;
       const CUtensorMap *om = sh ? &maps.out_sh : &maps.out;
       const int mrow = (sh ? 0 : (im.seg - p.e0) * Mr) + im.mt * 128 + q * 32;
@@ -541,10 +570,17 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
       if (!gt_warp_wait(&tfull[b], (cnt >> 1) & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t tb = tmem + b * 256 + ((uint32_t)(q * 32) << 16) + half * WG_COLS;
-#pragma unroll 1
-      for (int cc = 0; cc < WG_COLS / 32; ++cc) {
-        float v[32];
-        tmem_ld32(tb + cc * 32, v);
+      // The warp's whole share of the accumulator into registers, then the
+      // buffer goes back to the MMA thread before any store is staged.
+      constexpr int NCH = WG_COLS / 32;
+      float v[NCH][32];
+#pragma unroll
+      for (int cc = 0; cc < NCH; cc += 2) tmem_ld32x2(tb + cc * 32, tb + (cc + 1) * 32, v[cc], v[cc + 1]);
+      tc_fence_before();
+      mbar_arrive(&tempty[b]);
+      ++cnt;
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) {
         uint8_t *stg = stg0 + sbuf * WG_STG_BYTES;
         if (lane == 0) bulk_wait_read<WG_NSTG - 1>();  // the last store from this buffer has read it
         __syncwarp();
@@ -552,7 +588,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           *(float4 *)(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              make_float4(v[cc][4 * j], v[cc][4 * j + 1], v[cc][4 * j + 2], v[cc][4 * j + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -561,9 +597,6 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
         }
         if (++sbuf == WG_NSTG) sbuf = 0;
       }
-      tc_fence_before();
-      mbar_arrive(&tempty[b]);
-      ++cnt;
     }
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
