@@ -339,6 +339,8 @@ constexpr int WG_A_BYTES = 2 * 8192;  // 128 M x 64 K lines, MN-major
 constexpr int WG_B_BYTES = 4 * 8192;  // 256 N x 64 K lines, MN-major
 constexpr int WG_STG_BYTES = 4096;    // one 32 x 32 FP32 store tile
 constexpr int WG_TAIL_WARP = GT_EPI_FIRST + WG_EPI_WARPS;  // zeroes segment tails, then releases the stage
+// Zero lines copied over a stage's segment tail (at most 15 lines of 128 bytes).
+__device__ __align__(128) uint4 g_zero_lines[15 * 8];
 constexpr int WG_THREADS = 32 * (WG_TAIL_WARP + 1);
 constexpr int WG_SMEM = 1024 + WG_STAGES * (WG_A_BYTES + WG_B_BYTES) + (WG_NSTG * WG_EPI_WARPS + 1) * WG_STG_BYTES + 256;
 static_assert(WG_SMEM <= 232448, "wgrad shared memory");
@@ -511,38 +513,47 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
     // ------------------------------------------------------------ stage tails
     // In a segment's last K block, lines [valid, 16 nkk) of each block hold
     // rows of the next segment (or TMA zero fill) and the K = 16 MMAs read
-    // them: clear them in both operands (6 blocks, at most 15 lines each;
-    // lane = 16-byte chunk (lane % 8) of every 4th line), then release the
-    // stage to the MMA thread.
-    int stage = 0;
-    uint32_t phase = 0;
-    WgItem nxt = wg_item(blockIdx.x, p);
-    for (int it = blockIdx.x; it < p.total; it += gridDim.x) {
-      const WgItem im = nxt;
-      if (it + (int)gridDim.x < p.total) nxt = wg_item(it + gridDim.x, p);
-      if (im.rows == 0) continue;
+    // them: once the stage has landed, bulk copies from a zero buffer
+    // overwrite them in both operands (6 blocks, at most 15 lines each; an
+    // async-proxy write like the stage's own, so no proxy fence), completing
+    // on ready[s]; other stages are released at once.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_phase = 0;  // stages with zero copies in flight
       bool ok = true;
-      for (int kb = 0; kb < im.nk; ++kb) {
-        if (!gt_warp_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
-        const int valid = min(64, im.rows - kb * 64);
-        const int hb = 64 >> wg_box(valid);  // lines per block in this stage
-        const int lines = 16 * ((valid + 15) >> 4) - valid;
-        if (lines > 0) {
+      WgItem nxt = wg_item(blockIdx.x, p);
+      for (int it = blockIdx.x; it < p.total && ok; it += gridDim.x) {
+        const WgItem im = nxt;
+        if (it + (int)gridDim.x < p.total) nxt = wg_item(it + gridDim.x, p);
+        for (int kb = 0; kb < im.nk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          const int valid = min(64, im.rows - kb * 64);
+          const int hb = 64 >> wg_box(valid);  // lines per block in this stage
+          const uint32_t bytes = (uint32_t)(16 * ((valid + 15) >> 4) - valid) * 128;
+          if (bytes) {
+            mbar_arrive_expect_tx(&ready[stage], 6 * bytes);
 #pragma unroll
-          for (int blk = 0; blk < 6; ++blk) {
-            uint8_t *blk_base = blk < 2 ? sa + stage * WG_A_BYTES + blk * hb * 128
-                                        : sb + stage * WG_B_BYTES + (blk - 2) * hb * 128;
-            for (int l = lane >> 3; l < lines; l += 4)
-              ((uint4 *)(blk_base + (valid + l) * 128))[lane & 7] = make_uint4(0, 0, 0, 0);
+            for (int blk = 0; blk < 6; ++blk) {
+              uint8_t *blk_base = blk < 2 ? sa + stage * WG_A_BYTES + blk * hb * 128
+                                          : sb + stage * WG_B_BYTES + (blk - 2) * hb * 128;
+              bulk_load(blk_base + valid * 128, g_zero_lines, bytes, &ready[stage]);
+            }
+            issued |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          } else {
+            mbar_arrive(&ready[stage]);
           }
-          fence_proxy_async_smem();
+          if (++stage == WG_STAGES) stage = 0, phase ^= 1;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ready[stage]);
-        if (++stage == WG_STAGES) stage = 0, phase ^= 1;
       }
-      if (!ok) break;
+      if (!ok) {
+        // The zero copies in flight land before the CTA exits.
+        volatile int never = 0;
+        for (int s = 0; s < WG_STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(&ready[s], (issued_phase >> s) & 1, &never, nullptr, 100000000ull);
+      }
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     // Warp (q, part): TMEM lanes 32q.. (output rows), columns [WG_COLS part, +WG_COLS).

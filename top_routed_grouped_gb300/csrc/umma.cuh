@@ -122,6 +122,15 @@ __device__ inline void tma_gather4(void *dst, const CUtensorMap *m, uint64_t *ba
       : "memory");
 }
 
+// Plain bulk copy global -> shared (no tensor map): `bytes` (a multiple of
+// 16, both addresses 16-byte aligned) complete on `bar`.
+__device__ inline void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // Tile store shared -> global through a tensor map (bulk-group completion).
 __device__ inline void tma_store_2d(const CUtensorMap *m, const void *src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(m), "r"(c0),
