@@ -334,10 +334,11 @@ __global__ void __launch_bounds__(256)
 router_gate_partial_kernel(BwArgs a, const int32_t *__restrict__ chunk_start, float *__restrict__ partial) {
   griddep_launch();
   griddep_wait();
+  constexpr int VN = Vec16<TE>::N;  // columns per thread (16 bytes of x)
   __shared__ int64_t srow[RG_CHUNK];  // element offset of each row's x
   __shared__ float scoef[RG_CHUNK];
   const int total = chunk_start[a.E + 1];
-  const int h = blockIdx.y * 256 + threadIdx.x;
+  const int h = (blockIdx.y * 256 + threadIdx.x) * VN;
   const TE *x = (const TE *)a.x;
   for (int c = blockIdx.x; c < total; c += gridDim.x) {
     const BwTile tr = bw_decode(c, a.E, a.T, chunk_start, a.offsets, RG_CHUNK);
@@ -356,10 +357,20 @@ router_gate_partial_kernel(BwArgs a, const int32_t *__restrict__ chunk_start, fl
     }
     __syncthreads();
     if (h >= a.H) continue;
-    float acc = 0.f;
-#pragma unroll 16
-    for (int i = 0; i < n; ++i) acc = fmaf(scoef[i], Elem<TE>::load(x + srow[i] + h), acc);
-    partial[(int64_t)c * a.H + h] = acc;
+    float acc[VN];
+#pragma unroll
+    for (int v = 0; v < VN; ++v) acc[v] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < n; ++i) {
+      float xv[VN];
+      Vec16<TE>::load(x + srow[i] + h, xv);
+      const float cf = scoef[i];
+#pragma unroll
+      for (int v = 0; v < VN; ++v) acc[v] = fmaf(cf, xv[v], acc[v]);
+    }
+    float *dst = partial + (int64_t)c * a.H + h;
+#pragma unroll
+    for (int v = 0; v < VN; v += 4) *(float4 *)(dst + v) = make_float4(acc[v], acc[v + 1], acc[v + 2], acc[v + 3]);
   }
 }
 
@@ -575,8 +586,8 @@ static cudaError_t run_backward(const BwArgs &a, void *scratch, int *status, cud
     MOE_TRY(launch_build_tiles(a.E, a.T, RG_CHUNK, a.offsets, chunk_start, stream));
     const int64_t mc = max_chunks(a.T, a.k, a.E);
     MOE_TRY(launch_pdl(router_gate_partial_kernel<TE>,
-                       dim3((unsigned)std::min<int64_t>(mc, 65535), (unsigned)ceil_div(a.H, 256)), dim3(256), 0,
-                       stream, a, cs, partial));
+                       dim3((unsigned)std::min<int64_t>(mc, 65535), (unsigned)ceil_div(a.H, 256 * Vec16<TE>::N)),
+                       dim3(256), 0, stream, a, cs, partial));
     MOE_TRY(launch_pdl(router_gate_reduce_kernel, dim3((unsigned)ceil_div(a.H, 256), a.E + 1), dim3(256), 0, stream,
                        a, cs, pc));
   }
