@@ -146,8 +146,8 @@ class ClockSampler:
 # DRAM bytes (read + write) of one moe_grouped_ffn call (gate_up + down) at
 # bf16_t8192, from `ncu --set full` (profiles/grouped_ffn_bf16_t8192.md), valid
 # only for the kernel sources it was taken on (hash below); otherwise null.
-FFN_TRAFFIC = {"sources": "ce37ea7481c85a3b", "workload": "bf16_t8192",
-               "bytes": 2_197_897_000 + 66_834_944 + 1_187_027_000 + 320_964_352}
+FFN_TRAFFIC = {"sources": "aab2be53bfb0e80e", "workload": "bf16_t8192",
+               "bytes": 2_197_745_000 + 66_823_424 + 1_187_120_000 + 321_282_816}
 
 
 def kernel_sources_hash() -> str:
