@@ -146,15 +146,22 @@ class ClockSampler:
 # DRAM bytes (read + write) of one moe_grouped_ffn call (gate_up + down) at
 # bf16_t8192, from `ncu --set full` (profiles/grouped_ffn_bf16_t8192.md), valid
 # only for the kernel sources it was taken on (hash below); otherwise null.
-FFN_TRAFFIC = {"sources": "aab2be53bfb0e80e", "workload": "bf16_t8192",
+FFN_TRAFFIC = {"sources": "b3c26e1015e1fcdb", "workload": "bf16_t8192",
                "bytes": 2_197_745_000 + 66_823_424 + 1_187_120_000 + 321_282_816}
 
 
 def kernel_sources_hash() -> str:
+    """Hash of the grouped-FFN kernel sources with comments and white space
+    removed: changes when the code changes, not when a comment does."""
     import hashlib
+    import re
     csrc = os.path.join(ROOT, "top_routed_grouped_gb300", "csrc")
-    per = [hashlib.sha256(open(os.path.join(csrc, n), "rb").read()).hexdigest()
-           for n in ("gemm_tc.cu", "umma.cuh", "common.cuh")]
+    per = []
+    for n in ("gemm_tc.cu", "umma.cuh", "common.cuh"):
+        src = open(os.path.join(csrc, n)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        per.append(hashlib.sha256("".join(src.split()).encode()).hexdigest())
     return hashlib.sha256("".join(per).encode()).hexdigest()[:16]
 
 

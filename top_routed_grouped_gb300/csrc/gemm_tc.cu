@@ -19,9 +19,12 @@
 //            j of expert e's segment; the x rows are gathered by eight warps
 //            with 16-byte cp.async into the swizzled operand layout; epilogue
 //            h = silu(g) * u.
-//   DOWN     D[o, j] = W_dn[e][o] . h[j] for 256 output features (two M
-//            tiles); epilogue writes row j to y_routed[sorted_route[j]] (or
-//            y_shared).
+//   DOWN     D[o, j] = W_dn[e][o] . h[j] for 128 output features (one M
+//            tile, two accumulator buffers); epilogue writes row j to
+//            y_routed[sorted_route[j]] (or y_shared).
+// GATE_UP and DOWN also run on CTA pairs (tc_pair_kernel below, the form
+// used wherever the device and the shapes allow): the same items, one
+// M = 256 MMA over two SMs.
 // The weights are the M operand (128-row tiles) and the tokens the N <= 256 operand,
 // so a short expert segment costs at most 15 padded columns.  Every output
 // element is accumulated over K in a fixed order (K blocks of 64, four

@@ -1,9 +1,10 @@
 // Inline-PTX wrappers for the sm_103a tensor-core path: mbarriers (with
 // bounded waits), TMA tile / gather4 loads, tensor memory (TMEM) allocation
 // and loads, and tcgen05.mma with its shared-memory and instruction
-// descriptors, TMA tile stores.  Only the operand formats the MoE kernels
-// use are covered: bf16 A and B, K-major or MN-major, 128-byte swizzle,
-// FP32 accumulator, M = 128.
+// descriptors, TMA tile stores, and the CTA-pair (cta_group::2) forms.
+// Only the operand formats the MoE kernels use are covered: bf16 A and B,
+// K-major or MN-major, 128-byte swizzle, FP32 accumulator, M = 128 (one SM)
+// or 256 (a pair of SMs).
 #pragma once
 
 #include <cuda.h>
