@@ -18,6 +18,9 @@ Prints ONE JSON line (rank 0).  Keys beyond the basic contract:
   fwd_bwd      forward (activations saved) + backward at T=4096
                (bf16_t4096_fwdbwd) through moe_forward / moe_backward, with
                its own layer roofline (forward and backward bytes and FLOPs)
+  step_ms      p10 / p50 / p90 of the per-step times (also in fwd_bwd)
+  extra_forward  the forward at T=1024 and at T=16384 with Zipf-skewed
+               routing (same layer), reported beside the headline
 
 --impl reference times the oracle itself (the reference arm) on the host.
 Multi-GPU (torchrun): every rank runs its own replica of the workload
@@ -57,6 +60,26 @@ def host_cores() -> int:
         return len(os.sched_getaffinity(0))
     except AttributeError:  # pragma: no cover
         return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the oracle timing record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def percentiles(vals) -> dict:
+    """p10 / p50 / p90 of per-step times in ms."""
+    v = sorted(vals)
+    pick = lambda q: v[min(len(v) - 1, int(round(q * (len(v) - 1))))]  # noqa: E731
+    return {"p10": pick(0.1), "p50": pick(0.5), "p90": pick(0.9), "n": len(v)}
 
 
 def max_over_ranks(value: float, world: int) -> float:
@@ -244,11 +267,52 @@ def fwd_bwd_bench(cfg, dev_w, steps: int, warmup: int, world: int, peaks: dict) 
     t_roof = roof(fb) + roof(bb)
     return {"workload": cfg.name, "T": T, "value": T * world / (ms * 1e-3), "unit": "tokens/s",
             "ms_per_step": ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "steps": steps, "warmup": warmup,
+            "step_ms": percentiles([e[0].elapsed_time(e[2]) for e in evs]),
             "api": "moe_forward (activations saved) + moe_backward",
             "gpu_launches_per_step": 24,
             "layer_roofline": {"fwd_bytes": fb["bytes"], "fwd_flops": fb["flops"], "bwd_bytes": bb["bytes"],
                                "bwd_flops": bb["flops"], "roofline_ms": t_roof, "frac": t_roof / ms,
                                "bwd_roofline_ms": roof(bb), "bwd_frac": roof(bb) / bwd_ms}}
+
+
+def extra_forward(name: str, dev_w: dict, steps: int, warmup: int, peaks: dict) -> dict:
+    """The forward at another configuration of the same layer (reported beside
+    the headline, not instead of it): per-step times through moe_forward
+    (consecutive step starts, inputs resident), tokens/s at the median and
+    the layer-roofline fraction."""
+    import torch
+    import top_routed_grouped_gb300 as moe
+    from top_routed_grouped_gb300 import inputs as I
+    cfg = I.CONFIGS[name]
+    T, H, E, k, Iw, Is = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.Is
+    # The weights of every configuration of this layer are the same draw; x and the bias are per configuration.
+    dv = dict(dev_w, x=I.normal((T, H), 0, I._STREAM["x"], 1.0, cfg.torch_dtype).cuda(),
+              router_bias=I.zipf_bias(E).cuda() if cfg.zipf else None)
+    d = moe.make_dims(T, H, E, k, Iw, Is, cfg.torch_dtype)
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    fargs = {n: dv[n] for n in ("x", "w_router", "router_bias", "w_shared_gate", "w_gate_up", "w_down",
+                                "ws_gate_up", "ws_down")}
+    fargs.update(y=torch.empty(T, H, dtype=cfg.torch_dtype, device="cuda"), expert_offsets=off)
+    fws = moe.workspace(d, "forward")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        moe.moe_forward(d, fargs, fws, stream)
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    for i in range(steps):
+        evs[i].record(stream)
+        moe.moe_forward(d, fargs, fws, stream)
+    evs[steps].record(stream)
+    torch.cuda.synchronize()
+    if moe.moe_device_status(reset=True) != 0:
+        raise RuntimeError(f"a kernel recorded a failed device-side check ({name})")
+    pc = percentiles([evs[i].elapsed_time(evs[i + 1]) for i in range(steps)])
+    active = int((off[1:] - off[:-1] > 0).sum().item())
+    lb = layer_bytes_flops(T, H, E, k, Iw, Is, active)
+    roof = max(lb["bytes"] / (float(peaks["hbm_gbs"]) * 1e9), lb["flops"] / (float(peaks["bf16_tflops"]) * 1e12))
+    return {"workload": name, "T": T, "active_experts": active, "step_ms": pc,
+            "tokens_per_s": T / (pc["p50"] * 1e-3), "layer_roofline_ms": roof * 1e3,
+            "layer_roofline_frac": roof * 1e3 / pc["p50"], "api": "moe_forward"}
 
 
 def cpu_oracle_baseline(cfg, x_cpu, W_cpu, bias, budget_s: float = 12.0, max_tokens: int = 4096) -> dict:
@@ -272,7 +336,7 @@ def cpu_oracle_baseline(cfg, x_cpu, W_cpu, bias, budget_s: float = 12.0, max_tok
         done += xs.shape[0]
         assert np.isfinite(r["y"]).all()
     return {"value": done / elapsed, "unit": "tokens/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
-            "kind": "oracle", "sample": f"first {done} tokens of {cfg.name} (FP64 route + experts + combine), "
+            "cpu_model": cpu_model(), "kind": "oracle", "sample": f"first {done} tokens of {cfg.name} (FP64 route + experts + combine), "
                                         f"{elapsed:.1f} s of oracle time"}
 
 
@@ -313,6 +377,8 @@ def main():
     ap.add_argument("--workload", default="bf16_t8192")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fwd-bwd", action="store_true", help="skip the forward+backward measurement")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the forward at the 1024-token and 16384-token Zipf configurations")
     ap.add_argument("--fwd-bwd-workload", default="bf16_t4096_fwdbwd",
                     help="workload of the forward+backward measurement (same layer shape as --workload)")
     args = ap.parse_args()
@@ -480,6 +546,7 @@ def main():
                            "frac": t_roof_ms / ms, "peak_hbm_gbs": hbm, "peak_bf16_tflops": peaks["bf16_tflops"],
                            "peak_source": peak_src},
         "clocks": clk,
+        "step_ms": percentiles([evs[i][0].elapsed_time(evs[i + 1][0]) for i in range(args.steps - 1)]),
     }
     if not args.no_fwd_bwd and cfg.dtype == "bf16":
         del o, ws, fws
@@ -487,6 +554,8 @@ def main():
         fb_cfg = I.CONFIGS[args.fwd_bwd_workload]
         assert (fb_cfg.H, fb_cfg.E, fb_cfg.I, fb_cfg.Is) == (H, E, Iw, Is), "fwd+bwd workload must share the layer"
         line["fwd_bwd"] = fwd_bwd_bench(fb_cfg, dev, args.steps, args.warmup, world, peaks)
+    if world == 1 and not args.no_extra and cfg.name == "bf16_t8192":
+        line["extra_forward"] = [extra_forward(n, dev, 50, 5, peaks) for n in ("bf16_t1024", "bf16_t16384_zipf")]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         W = {kk: v for kk, v in cpu.items() if kk not in ("x", "dy", "router_bias")}
         line["cpu_baseline"] = cpu_oracle_baseline(cfg, cpu["x"], W, cpu["router_bias"])
