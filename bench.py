@@ -315,9 +315,12 @@ def extra_forward(name: str, dev_w: dict, steps: int, warmup: int, peaks: dict) 
             "layer_roofline_frac": roof * 1e3 / pc["p50"], "api": "moe_forward"}
 
 
-def cpu_oracle_baseline(cfg, x_cpu, W_cpu, bias, budget_s: float = 12.0, max_tokens: int = 4096) -> dict:
+def cpu_oracle_baseline(cfg, x_cpu, W_cpu, bias, budget_s: float = 20.0, max_tokens: int | None = None) -> dict:
     """Time the FP64 oracle (routing + experts + combine) on the first tokens
-    of the workload, in blocks of 32 tokens until `budget_s` has elapsed."""
+    of the workload (all of them by default), in blocks of 32 tokens until
+    `budget_s` has elapsed."""
+    if max_tokens is None:
+        max_tokens = cfg.T
     os.environ.setdefault("OMP_NUM_THREADS", str(host_cores()))
     import numpy as np
     import oracle
