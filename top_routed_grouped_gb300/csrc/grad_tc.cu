@@ -29,7 +29,8 @@
 // the epilogue of one tile overlaps the MMAs of the next; each epilogue warp
 // copies its whole share of an accumulator into registers and releases it at
 // once, then stages 32 x 32 FP32 sub-tiles in shared memory and writes them
-// with TMA stores.  Empty segments get zero tiles (every output is written).
+// with TMA stores (L2 evict-first).  Empty segments get zero tiles (every
+// output is written).
 //
 // Every output element is reduced over K in one fixed order (K blocks of
 // 64, four K = 16 MMAs each); the tiling decides where a value is written,
@@ -339,6 +340,14 @@ constexpr int WG_A_BYTES = 2 * 8192;  // 128 M x 64 K lines, MN-major
 constexpr int WG_B_BYTES = 4 * 8192;  // 256 N x 64 K lines, MN-major
 constexpr int WG_STG_BYTES = 4096;    // one 32 x 32 FP32 store tile
 constexpr int WG_TAIL_WARP = GT_EPI_FIRST + WG_EPI_WARPS;  // zeroes segment tails, then releases the stage
+// TMA tile store with an L2 cache policy (the weight gradients are written
+// once and not read again by this layer: evict-first keeps the operand rows
+// that the next tiles re-read in L2).
+__device__ inline void tma_store_2d_hint(const CUtensorMap *m, const void *src, int c0, int c1, uint64_t pol) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(m),
+               "r"(c0), "r"(c1), "r"(smem_u32(src)), "l"(pol)
+               : "memory");
+}
 // Zero lines copied over a stage's segment tail (at most 15 lines of 128 bytes).
 __device__ __align__(128) uint4 g_zero_lines[15 * 8];
 constexpr int WG_THREADS = 32 * (WG_TAIL_WARP + 1);
@@ -561,6 +570,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
     uint8_t *stg0 = stg_all + (warp - GT_EPI_FIRST) * WG_NSTG * WG_STG_BYTES;
     uint32_t cnt = 0, sbuf = 0;
     const int Mr = MODE == WGRAD_DOWN ? p.H : 2 * p.I;  // output rows per routed expert
+    const uint64_t pol_out = policy_evict_first();  // gradient stores
     WgItem nxt = wg_item(blockIdx.x, p);
     for (int it = blockIdx.x; it < p.total; it += gridDim.x) {
       const WgItem im = nxt;
@@ -603,7 +613,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(om, stg, ncol + cc * 32, mrow);
+          tma_store_2d_hint(om, stg, ncol + cc * 32, mrow, pol_out);
           bulk_commit();
         }
         if (++sbuf == WG_NSTG) sbuf = 0;
