@@ -42,9 +42,9 @@ sys.path.insert(0, ROOT)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "MoE layer tokens/sec (fwd, fwd+bwd) on 1 GB300; % of layer roofline"
 # Kernels one forward step launches: router weight split, router, top-k/gate;
-# permute count, chunk scan, expert scan, scatter; item tables (2), gate_up,
-# down; combine.
-LAUNCHES_PER_STEP = 12
+# the permute (one launch on a cluster of sixteen CTAs); item tables (2),
+# gate_up, down; combine.
+LAUNCHES_PER_STEP = 9
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -269,7 +269,10 @@ def fwd_bwd_bench(cfg, dev_w, steps: int, warmup: int, world: int, peaks: dict) 
             "ms_per_step": ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "steps": steps, "warmup": warmup,
             "step_ms": percentiles([e[0].elapsed_time(e[2]) for e in evs]),
             "api": "moe_forward (activations saved) + moe_backward",
-            "gpu_launches_per_step": 24,
+            # moe_forward: split, router, top-k, permute + item tables, gate_up, down, combine (7);
+            # moe_backward: combine bwd, item tables (2), down dgrad, gate_up dgrad, x gather,
+            # down wgrad, gate_up wgrad, tile table, router/gate partial sums and reduction, dx (12)
+            "gpu_launches_per_step": 19,
             "layer_roofline": {"fwd_bytes": fb["bytes"], "fwd_flops": fb["flops"], "bwd_bytes": bb["bytes"],
                                "bwd_flops": bb["flops"], "roofline_ms": t_roof, "frac": t_roof / ms,
                                "bwd_roofline_ms": roof(bb), "bwd_frac": roof(bb) / bwd_ms}}

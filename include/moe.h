@@ -188,7 +188,10 @@ int moe_route_replay(const moe_dims_t *d, const void *x, const float *w_router, 
  *
  * Integer only, no atomics on positions; the result equals a sequential
  * counting sort bit for bit.  An id outside [0, E) is skipped and recorded in
- * the device status word (moe_device_status).  Workspace: PERMUTE.
+ * the device status word (moe_device_status).  Workspace: PERMUTE.  Up to
+ * 2^20 routes, on devices that run clusters of sixteen CTAs, the sort is one
+ * launch that leaves the workspace untouched; otherwise it runs as four
+ * kernels over the workspace.  Both forms give the same result.
  */
 int moe_permute(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_offsets,
                 int32_t *sorted_route, int32_t *route_pos, void *ws, size_t ws_bytes, void *stream);
@@ -372,7 +375,10 @@ typedef struct moe_fwd_args {
 } moe_fwd_args_t;
 
 /* moe_forward -- moe_route, moe_permute, moe_grouped_ffn, moe_combine on one
- * stream.  Workspace: FORWARD (covers every optional output left NULL). */
+ * stream.  Workspace: FORWARD (covers every optional output left NULL).
+ * Same results as the four calls, bit for bit; where the permute runs as one
+ * launch (see moe_permute) and dtype is MOE_BF16, that launch also writes
+ * the grouped FFN's work lists. */
 int moe_forward(const moe_dims_t *d, const moe_fwd_args_t *a, void *ws, size_t ws_bytes, void *stream);
 
 /* Everything moe_backward reads and writes. */

@@ -175,15 +175,63 @@ def test_permute_bad_ids_reported_on_device():
     assert moe.moe_device_status(reset=True) == 0
 
 
+def check_permute(ids, E):
+    out = moe.permute(torch.as_tensor(ids, device="cuda"), E)
+    off, srt, pos = oracle.permute(ids, E)
+    np.testing.assert_array_equal(out["expert_offsets"].cpu().numpy(), off)
+    np.testing.assert_array_equal(out["sorted_route"].cpu().numpy(), srt)
+    np.testing.assert_array_equal(out["route_pos"].cpu().numpy(), pos)
+
+
 def test_permute_matches_oracle_random_ids():
+    """Distinct ids per token (uniform ids with repeats for the largest case).
+    Up to 2^20 routes the sort is one launch on a cluster of eight CTAs;
+    110,000 x 10 routes take the four-kernel sort."""
     rng = np.random.default_rng(0)
-    for T, E, k in [(1, 512, 10), (999, 512, 10), (5000, 64, 8), (70, 1024, 16)]:
-        ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
-        out = moe.permute(torch.as_tensor(ids, device="cuda"), E)
-        off, srt, pos = oracle.permute(ids, E)
-        np.testing.assert_array_equal(out["expert_offsets"].cpu().numpy(), off)
-        np.testing.assert_array_equal(out["sorted_route"].cpu().numpy(), srt)
-        np.testing.assert_array_equal(out["route_pos"].cpu().numpy(), pos)
+    for T, E, k in [(1, 512, 10), (999, 512, 10), (5000, 64, 8), (70, 1024, 16), (8192, 512, 10)]:
+        ids = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+        check_permute(ids, E)
+    check_permute(rng.integers(0, 512, size=(110_000, 10), dtype=np.int32), 512)
+
+
+def test_permute_skewed_ids_with_repeats():
+    """The counting sort does not need distinct ids: heavily skewed ids with
+    repeats inside a token, every chunk and warp boundary crossed by equal
+    ids, an expert count that is not a multiple of 32, routes not a multiple
+    of 32."""
+    rng = np.random.default_rng(1)
+    for T, E, k in [(4096, 16, 4), (333, 7, 3), (20_000, 1000, 10), (1, 1, 1), (3, 1024, 16)]:
+        p = 1.0 / np.arange(1, E + 1) ** 1.5
+        ids = rng.choice(E, size=(T, k), p=p / p.sum()).astype(np.int32)
+        check_permute(ids, E)
+    check_permute(np.zeros((5000, 8), np.int32), 512)  # every route to expert 0
+
+
+@pytest.mark.parametrize("T,zipf", [(333, False), (1024, False), (4096, True)])
+def test_forward_equals_step_by_step_calls(T, zipf):
+    """moe_forward (the one-launch sort also writes the grouped GEMMs' item
+    tables) equals moe_route, moe_permute, moe_grouped_ffn (which builds its
+    own tables) and moe_combine called one by one, bit for bit."""
+    W = to_dev(full_weights())
+    x = full_x(T).cuda()
+    bias = I.zipf_bias(512).cuda() if zipf else None
+    ref = moe.forward(x, W["w_router"], W["w_shared_gate"], W["w_gate_up"], W["w_down"], W["ws_gate_up"],
+                      W["ws_down"], 10, router_bias=bias)
+    r = moe.route(x, W["w_router"], W["w_shared_gate"], 10, router_bias=bias)
+    pm = moe.permute(r["topk_ids"], 512)
+    d = moe.dims_of(x, W["w_router"], W["w_gate_up"], W["ws_gate_up"], 10)
+    yr = torch.empty(T * 10, 2048, dtype=x.dtype, device="cuda")
+    ys = torch.empty(T, 2048, dtype=x.dtype, device="cuda")
+    moe.moe_grouped_ffn(d, x, pm["expert_offsets"], pm["sorted_route"], W["w_gate_up"], W["w_down"],
+                        W["ws_gate_up"], W["ws_down"], yr, ys, {}, moe.workspace(d, "grouped_ffn"))
+    y = torch.empty(T, 2048, dtype=x.dtype, device="cuda")
+    moe.moe_combine(d, yr, ys, r["topk_w"], r["shared_sig"], y)
+    for key in ("expert_offsets", "sorted_route", "route_pos"):
+        assert torch.equal(pm[key], ref[key]), key
+    assert torch.equal(bits(yr), bits(ref["y_routed"]))
+    assert torch.equal(bits(ys), bits(ref["y_shared"]))
+    assert torch.equal(bits(y), bits(ref["y"]))
+    assert moe.moe_device_status(reset=True) == 0
 
 
 def test_api_errors_on_device_buffers():

@@ -257,8 +257,8 @@ MOE_API int moe_route_replay(const moe_dims_t *d, const void *x, const float *w_
   return cuda_status(e);
 }
 
-MOE_API int moe_permute(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_offsets,
-                        int32_t *sorted_route, int32_t *route_pos, void *ws, size_t ws_bytes, void *stream) {
+static int permute_check(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_offsets,
+                         int32_t *sorted_route, int32_t *route_pos, void *ws, size_t ws_bytes) {
   int st = check_dims(d);
   if (st != MOE_OK) return st;
   const int64_t R = (int64_t)d->T * d->k;
@@ -266,14 +266,29 @@ MOE_API int moe_permute(const moe_dims_t *d, const int32_t *topk_ids, int32_t *e
       !opt_ok(ws))
     return MOE_ERR_INVALID_ARG;
   if (ws_bytes < ws_size(d, MOE_OP_PERMUTE)) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+// The sort runs as one launch where the cluster it needs fits (it uses no
+// workspace then), else as four kernels over the workspace; same result.
+MOE_API int moe_permute(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_offsets,
+                        int32_t *sorted_route, int32_t *route_pos, void *ws, size_t ws_bytes, void *stream) {
+  int st = permute_check(d, topk_ids, expert_offsets, sorted_route, route_pos, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  const int64_t R = (int64_t)d->T * d->k;
+  if (permute_cluster_ok(R, d->E))
+    return cuda_status(launch_permute_cluster(R, d->E, topk_ids, expert_offsets, sorted_route, route_pos,
+                                              device_status_ptr(), (cudaStream_t)stream));
   return cuda_status(launch_permute(R, d->E, topk_ids, expert_offsets, sorted_route, route_pos, ws, device_status_ptr(),
                                     (cudaStream_t)stream));
 }
 
-MOE_API int moe_grouped_ffn(const moe_dims_t *d, const void *x, const int32_t *expert_offsets,
-                            const int32_t *sorted_route, const void *w_gate_up, const void *w_down,
-                            const void *ws_gate_up, const void *ws_down, void *y_routed, void *y_shared,
-                            const moe_saved_t *saved, void *ws, size_t ws_bytes, void *stream) {
+// Checks the arguments of moe_grouped_ffn and fills `a` and `sc` (MOE_OK), or
+// returns the error.
+static int grouped_ffn_prepare(const moe_dims_t *d, const void *x, const int32_t *expert_offsets,
+                               const int32_t *sorted_route, const void *w_gate_up, const void *w_down,
+                               const void *ws_gate_up, const void *ws_down, void *y_routed, void *y_shared,
+                               const moe_saved_t *saved, void *ws, size_t ws_bytes, FfnArgs *a, FfnScratch *sc) {
   int st = check_dims(d);
   if (st != MOE_OK) return st;
   const int64_t T = d->T, R = T * d->k;
@@ -284,20 +299,35 @@ MOE_API int moe_grouped_ffn(const moe_dims_t *d, const void *x, const int32_t *e
   if (saved && (!opt_ok(saved->gu) || !opt_ok(saved->h) || !opt_ok(saved->gu_shared) || !opt_ok(saved->h_shared)))
     return MOE_ERR_INVALID_ARG;
   if (ws_bytes < ws_size(d, MOE_OP_GROUPED_FFN)) return MOE_ERR_WORKSPACE;
-  if (T == 0) return MOE_OK;
   Carver c(ws);
-  FfnScratch sc = ffn_ws(d, c);
-  FfnArgs a;
-  a.T = d->T; a.H = d->H; a.E = d->E; a.k = d->k; a.I = d->I; a.Is = d->Is;
-  a.x = x; a.offsets = expert_offsets; a.sorted_route = sorted_route;
-  a.w_gate_up = w_gate_up; a.w_down = w_down; a.ws_gate_up = ws_gate_up; a.ws_down = ws_down;
-  a.y_routed = y_routed; a.y_shared = y_shared;
-  a.h_routed = (saved && saved->h) ? saved->h : sc.h_routed;
-  a.h_shared = (saved && saved->h_shared) ? saved->h_shared : sc.h_shared;
-  a.gu_routed = saved ? saved->gu : nullptr;
-  a.gu_shared = saved ? saved->gu_shared : nullptr;
+  *sc = ffn_ws(d, c);
+  a->T = d->T; a->H = d->H; a->E = d->E; a->k = d->k; a->I = d->I; a->Is = d->Is;
+  a->x = x; a->offsets = expert_offsets; a->sorted_route = sorted_route;
+  a->w_gate_up = w_gate_up; a->w_down = w_down; a->ws_gate_up = ws_gate_up; a->ws_down = ws_down;
+  a->y_routed = y_routed; a->y_shared = y_shared;
+  a->h_routed = (saved && saved->h) ? saved->h : sc->h_routed;
+  a->h_shared = (saved && saved->h_shared) ? saved->h_shared : sc->h_shared;
+  a->gu_routed = saved ? saved->gu : nullptr;
+  a->gu_shared = saved ? saved->gu_shared : nullptr;
+  return MOE_OK;
+}
+
+static int grouped_ffn_run(const moe_dims_t *d, const FfnArgs &a, const FfnScratch &sc, void *stream) {
+  if (d->T == 0) return MOE_OK;
   if (d->dtype == MOE_F32) return cuda_status(launch_ffn_simt(a, sc.tiles, (cudaStream_t)stream));
   return cuda_status(launch_ffn_tc(a, sc.tiles, device_status_ptr(), (cudaStream_t)stream));
+}
+
+MOE_API int moe_grouped_ffn(const moe_dims_t *d, const void *x, const int32_t *expert_offsets,
+                            const int32_t *sorted_route, const void *w_gate_up, const void *w_down,
+                            const void *ws_gate_up, const void *ws_down, void *y_routed, void *y_shared,
+                            const moe_saved_t *saved, void *ws, size_t ws_bytes, void *stream) {
+  FfnArgs a;
+  FfnScratch sc;
+  int st = grouped_ffn_prepare(d, x, expert_offsets, sorted_route, w_gate_up, w_down, ws_gate_up, ws_down, y_routed,
+                               y_shared, saved, ws, ws_bytes, &a, &sc);
+  if (st != MOE_OK) return st;
+  return grouped_ffn_run(d, a, sc, stream);
 }
 
 MOE_API int moe_grouped_ffn_etp(const moe_dims_t *d, const void *x, const int32_t *expert_offsets,
@@ -444,10 +474,27 @@ MOE_API int moe_forward(const moe_dims_t *d, const moe_fwd_args_t *a, void *ws, 
                    s.inner_bytes, stream);
     if (st != MOE_OK) return st;
   }
-  st = moe_permute(d, ids, off, srt, pos, s.inner, s.inner_bytes, stream);
+  // Permute and grouped FFN.  On the bf16 path with the one-launch sort, that
+  // launch also writes the FFN's item tables into its scratch (the sort
+  // itself uses none), so the FFN starts with its GEMMs.
+  st = permute_check(d, ids, off, srt, pos, s.inner, s.inner_bytes);
   if (st != MOE_OK) return st;
-  st = moe_grouped_ffn(d, a->x, off, srt, a->w_gate_up, a->w_down, a->ws_gate_up, a->ws_down, yr, ys, &a->saved,
-                       s.inner, s.inner_bytes, stream);
+  FfnArgs fa;
+  FfnScratch fs;
+  st = grouped_ffn_prepare(d, a->x, off, srt, a->w_gate_up, a->w_down, a->ws_gate_up, a->ws_down, yr, ys, &a->saved,
+                           s.inner, s.inner_bytes, &fa, &fs);
+  if (st != MOE_OK) return st;
+  const int64_t R = T * d->k;
+  PermuteItems items;
+  if (d->dtype == MOE_BF16 && T > 0 && permute_cluster_ok(R, d->E) && ffn_tc_item_tables(fa, fs.tiles, &items)) {
+    st = cuda_status(launch_permute_cluster(R, d->E, ids, off, srt, pos, device_status_ptr(), (cudaStream_t)stream,
+                                            &items));
+    fa.items_ready = 1;
+  } else {
+    st = moe_permute(d, ids, off, srt, pos, s.inner, s.inner_bytes, stream);
+  }
+  if (st != MOE_OK) return st;
+  st = grouped_ffn_run(d, fa, fs, stream);
   if (st != MOE_OK) return st;
   return moe_combine(d, yr, ys, w, sig, a->y, stream);
 }

@@ -1256,6 +1256,32 @@ size_t ffn_tc_scratch_bytes(int T, int k, int E, int H, int I, int Is) {
          round256((size_t)max_items(T, k, E, H / DN_ROWS, H / DN_ROWS) * 16);
 }
 
+// Where launch_ffn_tc keeps its item tables in `scratch` and how many items
+// each row tile of a segment gives (false: the call needs tables that the
+// one-launch sort does not build, i.e. an expert range or no shared expert).
+bool ffn_tc_item_tables(const FfnArgs &a, void *scratch, PermuteItems *it) {
+  if (a.e_begin != 0 || (a.e_end >= 0 && a.e_end != a.E) || !a.with_shared) return false;
+  const size_t starts = round256((size_t)(a.E + 2) * 4);
+  constexpr int GU_FEAT = 64 * TcCfg<TC_GATE_UP>::MT;
+  constexpr int DN_ROWS = 128 * TcCfg<TC_DOWN>::MT;
+  const int mi_gu = (int)max_items(a.T, a.k, a.E, a.I / GU_FEAT, a.Is / GU_FEAT);
+  const int mi_dn = (int)max_items(a.T, a.k, a.E, a.H / DN_ROWS, a.H / DN_ROWS);
+  const int dn_rows = use_pair<TC_DOWN>(a) ? 256 : DN_ROWS;
+  uint8_t *w = (uint8_t *)scratch;
+  it->T = a.T;
+  it->nf_a_r = a.I / GU_FEAT;
+  it->nf_a_s = a.Is / GU_FEAT;
+  it->nf_b_r = a.H / dn_rows;
+  it->nf_b_s = a.H / dn_rows;
+  it->max_a = mi_gu;
+  it->max_b = mi_dn;
+  it->start_a = (int32_t *)w;
+  it->start_b = (int32_t *)(w + starts);
+  it->items_a = (int4 *)(w + 2 * starts);
+  it->items_b = (int4 *)(w + 2 * starts + round256((size_t)mi_gu * 16));
+  return true;
+}
+
 cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
   const size_t starts = round256((size_t)(a.E + 2) * 4);
@@ -1271,10 +1297,12 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
   const int eb = a.e_begin, ee = a.e_end < 0 ? a.E : a.e_end, n_local = ee - eb;
   const bool gu_pair = use_pair<TC_GATE_UP>(a), dn_pair = use_pair<TC_DOWN>(a);
   const int dn_rows = dn_pair ? 256 : DN_ROWS;  // outputs per down item (a pair item is two M tiles)
-  cudaError_t e0 = launch_item_tables(a.E, a.T, a.I / GU_FEAT, a.Is / GU_FEAT, a.H / dn_rows, a.H / dn_rows, a.offsets,
-                                      start_gu, start_dn, items_gu, items_dn, mi_gu, mi_dn, stream, eb, ee,
-                                      a.with_shared);
-  if (e0 != cudaSuccess) return e0;
+  if (!a.items_ready) {
+    cudaError_t e0 = launch_item_tables(a.E, a.T, a.I / GU_FEAT, a.Is / GU_FEAT, a.H / dn_rows, a.H / dn_rows,
+                                        a.offsets, start_gu, start_dn, items_gu, items_dn, mi_gu, mi_dn, stream, eb, ee,
+                                        a.with_shared);
+    if (e0 != cudaSuccess) return e0;
+  }
   const int64_t R = (int64_t)a.T * a.k;
   TcMaps mg, md;
   if (!map_gate_up(&mg.a, a.w_gate_up, std::max(n_local, 1), a.I, a.H, 4 * TcCfg<TC_GATE_UP>::MT) ||

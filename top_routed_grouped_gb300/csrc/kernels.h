@@ -37,6 +37,22 @@ size_t permute_scratch_bytes(int64_t R, int E, int chunk = PERMUTE_CHUNK_SMALL);
 cudaError_t launch_permute(int64_t R, int E, const int32_t *ids, int32_t *offsets, int32_t *sorted_route,
                            int32_t *route_pos, void *scratch, int *status, cudaStream_t stream,
                            int chunk = PERMUTE_CHUNK_SMALL);
+// Item tables of the two forward grouped GEMMs, written by the one-launch
+// sort below when it is given them (the layout launch_ffn_tc reads).
+struct PermuteItems {
+  int T, nf_a_r, nf_a_s, nf_b_r, nf_b_s, max_a, max_b;
+  int32_t *start_a, *start_b;
+  int4 *items_a, *items_b;
+};
+// ---- permute_cluster.cu ----
+// The same stable counting sort in one launch (a cluster of sixteen CTAs, no
+// scratch) for R <= 2^20 routes and E <= 1024 on devices where that cluster
+// fits; with `items`, also the grouped GEMMs' item tables of all E experts
+// and the shared expert.
+bool permute_cluster_ok(int64_t R, int E);
+cudaError_t launch_permute_cluster(int64_t R, int E, const int32_t *ids, int32_t *offsets, int32_t *sorted_route,
+                                   int32_t *route_pos, int *status, cudaStream_t stream,
+                                   const PermuteItems *items = nullptr);
 // tile_start[s] for s in [0, E+1]: prefix of ceil(n_s / bn) over the E routed
 // segments (n_s from offsets) and the shared segment (n_E = T); only routed
 // segments in [e_begin, e_end) (e_end < 0: E) and, if with_shared, the shared
@@ -63,6 +79,9 @@ struct FfnArgs {
   // accumulators unrounded (a partial sum over a slice of I, for the
   // expert-tensor-parallel reduction).
   int y_f32 = 0;
+  // bf16 path: the item tables are already in the scratch (written by the
+  // one-launch sort from ffn_tc_item_tables' description).
+  int items_ready = 0;
 };
 size_t ffn_simt_scratch_bytes(int E);
 // The MOE_F32 grouped FFN on CUDA cores (all buffers float).
@@ -85,6 +104,9 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
 size_t ffn_tc_scratch_bytes(int T, int k, int E, int H, int I, int Is);
 // gate_up + SwiGLU and down as two persistent tcgen05 grouped GEMMs (scratch: ffn_tc_scratch_bytes).
 cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStream_t stream);
+// The item tables of launch_ffn_tc for `a` in `scratch`, for the one-launch
+// sort to write (false where that sort cannot build them).
+bool ffn_tc_item_tables(const FfnArgs &a, void *scratch, PermuteItems *it);
 // Item tables of two grouped GEMMs over the same segments: per segment,
 // ceil(n_s / 256) token tiles times nf_*_r (routed) or nf_*_s (shared) M-tile
 // pairs; items = int4 (segment, pair, first row, rows).
