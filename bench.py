@@ -167,10 +167,11 @@ class ClockSampler:
 
 
 # DRAM bytes (read + write) of one moe_grouped_ffn call (gate_up + down) at
-# bf16_t8192, from `ncu --set full` (profiles/grouped_ffn_bf16_t8192.md), valid
-# only for the kernel sources it was taken on (hash below); otherwise null.
-FFN_TRAFFIC = {"sources": "b3c26e1015e1fcdb", "workload": "bf16_t8192",
-               "bytes": 2_197_745_000 + 66_823_424 + 1_187_120_000 + 321_282_816}
+# bf16_t8192, from an ncu capture of the two kernels' dram__bytes counters
+# (profiles/forward_kernels_counters_bf16_t8192.md), valid only for the kernel
+# sources it was taken on (hash below); otherwise null.
+FFN_TRAFFIC = {"sources": "0de4bcb767c0a8d3", "workload": "bf16_t8192",
+               "bytes": 2_197_890_816 + 63_752_192 + 1_187_873_536 + 317_864_960}
 
 
 def kernel_sources_hash() -> str:
