@@ -67,15 +67,18 @@ __device__ inline bool gt_warp_wait(uint64_t *bar, uint32_t parity, volatile int
 // accumulators of up to 256 columns fill TMEM (drained between items); MT = 1:
 // two accumulator buffers alternate, so the epilogue of one item overlaps the
 // mainloop of the next.
-constexpr int DG_EPI_WARPS = 8, DG_EPI_BYTES = 4096;
+constexpr int DG_EPI_BYTES = 4096;
 constexpr int DG_B_BYTES = 256 * 128;  // up to 256 rows x 64 K
-constexpr int DG_THREADS = 32 * (GT_EPI_FIRST + DG_EPI_WARPS);
 template <int MT>
 struct DgCfg {
   static constexpr int A_BYTES = MT * 2 * 8192;  // 2 MT blocks of 64 features x 64 K lines
-  static constexpr int STAGES = MT == 1 ? 4 : 3;
+  // The down dgrad's epilogue (the SwiGLU backward, with the saved g and u
+  // loaded per 32 x 32 tile) paces it: 16 epilogue warps, one stage fewer.
+  static constexpr int EPI_WARPS = MT == 1 ? 16 : 8;
+  static constexpr int THREADS = 32 * (GT_EPI_FIRST + EPI_WARPS);
+  static constexpr int STAGES = 3;
   static constexpr int NBUF = MT == 1 ? 2 : 1;
-  static constexpr int SMEM = 1024 + STAGES * (A_BYTES + DG_B_BYTES) + DG_EPI_WARPS * DG_EPI_BYTES + 256;
+  static constexpr int SMEM = 1024 + STAGES * (A_BYTES + DG_B_BYTES) + EPI_WARPS * DG_EPI_BYTES + 256;
   static_assert(SMEM <= 232448, "dgrad shared memory");
   static_assert(NBUF * MT * 256 <= 512, "TMEM columns");
 };
@@ -118,9 +121,10 @@ __device__ inline DgItem dg_item(int it, const DgParams &p) {
 }
 
 template <int MODE, int MT>
-__global__ void __launch_bounds__(DG_THREADS, 1)
+__global__ void __launch_bounds__(DgCfg<MT>::THREADS, 1)
 tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
   constexpr int DG_STAGES = DgCfg<MT>::STAGES, DG_A_BYTES = DgCfg<MT>::A_BYTES, NBUF = DgCfg<MT>::NBUF;
+  constexpr int DG_EPI_WARPS = DgCfg<MT>::EPI_WARPS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sa = base;
@@ -249,10 +253,18 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
       if (!gt_warp_wait(&tfull[b], (cnt / NBUF) & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t tq = tmem + b * MT * 256 + ((uint32_t)(q * 32) << 16);
+      bool released = false;
       for (int c0 = cfirst; c0 < im.n; c0 += CSTEP) {
         float vt[MT][32];
         if (MT == 2) tmem_ld32x2(tq + c0, tq + 256 + c0, vt[0], vt[MT - 1]);
         else tmem_ld32(tq + c0, vt[0]);
+        if (c0 + CSTEP >= im.n) {
+          // The warp's last accumulator columns are in registers: the buffer
+          // goes back to the MMA thread before the epilogue math.
+          tc_fence_before();
+          mbar_arrive(&tempty[b]);
+          released = true;
+        }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const int f0 = im.f * 128 * MT + mt * 128 + q * 32;  // first feature of this warp's 32
@@ -312,8 +324,10 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&tempty[b]);
+      if (!released) {
+        tc_fence_before();
+        mbar_arrive(&tempty[b]);
+      }
       ++cnt;
     }
   }
@@ -660,7 +674,7 @@ template <int MODE, int MT>
 static cudaError_t launch_dgrad(const DgMaps &m, const DgParams &p, int grid, cudaStream_t stream) {
   cudaError_t e = ensure_smem((const void *)tc_dgrad_kernel<MODE, MT>, DgCfg<MT>::SMEM);
   if (e != cudaSuccess) return e;
-  return launch_pdl(tc_dgrad_kernel<MODE, MT>, dim3(grid), dim3(DG_THREADS), DgCfg<MT>::SMEM, stream, m, p);
+  return launch_pdl(tc_dgrad_kernel<MODE, MT>, dim3(grid), dim3(DgCfg<MT>::THREADS), DgCfg<MT>::SMEM, stream, m, p);
 }
 
 cudaError_t launch_dgrad_tc(const BwArgs &a, void *scratch, int *status, cudaStream_t stream) {
