@@ -170,8 +170,8 @@ class ClockSampler:
 # bf16_t8192, from an ncu capture of the two kernels' dram__bytes counters
 # (profiles/forward_kernels_counters_bf16_t8192.md), valid only for the kernel
 # sources it was taken on (hash below); otherwise null.
-FFN_TRAFFIC = {"sources": "0de4bcb767c0a8d3", "workload": "bf16_t8192",
-               "bytes": 2_197_890_816 + 63_752_192 + 1_187_873_536 + 317_864_960}
+FFN_TRAFFIC = {"sources": "0d80e7544c1ac023", "workload": "bf16_t8192",
+               "bytes": 2_197_428_224 + 64_002_304 + 1_185_130_496 + 318_316_288}
 
 
 def kernel_sources_hash() -> str:

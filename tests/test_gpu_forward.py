@@ -251,20 +251,22 @@ def test_api_errors_on_device_buffers():
     assert e.value.status == -3
 
 
-@pytest.mark.parametrize("T", [300, 2048])
+@pytest.mark.parametrize("T", [37, 300, 2048, 8192])
 def test_pair_and_single_sm_gemms_agree_bitwise(T, monkeypatch):
-    """The grouped GEMMs on CTA pairs (two SMs per M = 256 MMA) and on single
-    SMs give the same bits: each output is one MMA chain over K in the same
-    order either way (training activations included)."""
+    """The router and the grouped GEMMs on CTA pairs (two SMs per M = 256
+    MMA) and on single SMs give the same bits: each output is one MMA chain
+    over K in the same order either way (router logits, routes and training
+    activations included)."""
     W = to_dev(full_weights())
     d = dict(W, x=full_x(T).cuda())
     args = [d[n] for n in ("w_router", "w_shared_gate", "w_gate_up", "w_down", "ws_gate_up", "ws_down")]
     outs = {}
     for mode in ("0", "3"):
         monkeypatch.setenv("MOE_TC_PAIR", mode)
-        outs[mode] = moe.forward(d["x"], *args, 10, save_for_backward=True)
+        outs[mode] = moe.forward(d["x"], *args, 10, save_for_backward=True, want_logits=True)
     monkeypatch.delenv("MOE_TC_PAIR")
-    for key in ("y", "y_routed", "y_shared"):
+    assert torch.equal(outs["0"]["topk_ids"], outs["3"]["topk_ids"])
+    for key in ("logits", "topk_w", "shared_sig", "y", "y_routed", "y_shared"):
         assert torch.equal(bits(outs["0"][key]), bits(outs["3"][key])), key
     for key in ("gu", "h", "gu_shared", "h_shared"):
         assert torch.equal(bits(outs["0"]["saved"][key]), bits(outs["3"]["saved"][key])), key

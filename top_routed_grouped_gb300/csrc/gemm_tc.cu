@@ -1000,6 +1000,210 @@ tc_router_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Router logits on CTA pairs (tcgen05.mma.cta_group::2, M = 256): a pair
+// item is 256 experts (128 per CTA: its M tile of each split weight) x up to
+// 256 tokens (each CTA loads half of the token rows; the even CTA's one MMA
+// thread drives both tensor cores).  A stage holds one K block of 64 hidden
+// units: per CTA the three split-weight tiles (48 KB) and its half of the x
+// rows (up to 16 KB), so three stages fit where the single-SM router holds
+// two.  The K chunks, their order and the FP32 sums of the epilogue are the
+// single-SM router's, so every logit is the same MMA chain and the same sum:
+// the two kernels give equal logits bit for bit.
+// ---------------------------------------------------------------------------
+constexpr int RP_STAGES = 3, RP_NROUND = 32;
+constexpr int RP_B_BYTES = 128 * 128;  // this CTA's half of up to 256 token rows x 64 bf16
+constexpr int RP_STAGE_BYTES = RT_A_BYTES + RP_B_BYTES;
+constexpr int RP_SMEM = 1024 + RP_STAGES * RP_STAGE_BYTES + 512;
+static_assert(RP_SMEM <= 232448, "pair router shared memory");
+
+__global__ void __launch_bounds__(RT_THREADS, 1)
+tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  auto sa = [&](int s) { return base + s * RP_STAGE_BYTES; };
+  auto sb = [&](int s) { return base + s * RP_STAGE_BYTES + RT_A_BYTES; };
+  uint64_t *bars = (uint64_t *)(base + RP_STAGES * RP_STAGE_BYTES);
+  uint64_t *full = bars, *empty = full + RP_STAGES;
+  uint64_t *tfull = empty + RP_STAGES, *tempty = tfull + 2, *mma_done = tempty + 2;
+  uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
+  volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RP_STAGES; ++s) {
+      mbar_init(&full[s], 1);  // used in the even CTA
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * RT_EPI_WARPS);  // used in the even CTA: one arrival per epilogue warp of the pair
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&maps.a);
+  cluster_sync();  // both CTAs' barriers exist before either touches the other's
+  if (warp == 1) tmem_alloc_pair(tmem_slot, TC_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_launch();
+  griddep_wait();
+  const int total = p.n_items, nkh = p.H / 64;
+  // Item it: experts [256 (it / rt_ntile), +256) (this CTA's 128 from 256 f + 128 rank),
+  // tokens [rt_rpt (it % rt_ntile), +rt_rpt), rows padded to RP_NROUND (each CTA loads n / 2).
+  auto item = [&](int it) {
+    const int nt = it % p.rt_ntile;
+    RtItem r;
+    r.f = it / p.rt_ntile;
+    r.row0 = (int64_t)nt * p.rt_rpt;
+    r.rows = min(p.rt_rpt, p.T - nt * p.rt_rpt);
+    r.n = (int)round_up(r.rows, RP_NROUND);
+    return r;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();  // split weights and x are read by many CTAs
+      const uint32_t full0 = mapa_shared(&full[0], 0);
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_phase = 0;
+      bool ok = true;
+      for (int it = cid; it < total && ok; it += ncl) {
+        const RtItem im = item(it);
+        const int erow = im.f * 256 + (int)rank * 128;
+        const int half = im.n >> 1;
+        const int64_t r0 = im.row0 + (int64_t)rank * half;
+        for (int j = 0; j < nkh; ++j) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          // Both CTAs' weight tiles and rows complete on the even CTA's barrier.
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * p.rt_splits * TC_TILE_A_BYTES + (uint32_t)im.n * 128);
+          const uint32_t bar = full0 + (uint32_t)(stage * sizeof(uint64_t));
+          for (int sp = 0; sp < p.rt_splits; ++sp)
+            tma_load_2d_pair(sa(stage) + sp * TC_TILE_A_BYTES, &maps.a, bar, sp * p.H + j * 64, erow, pol);
+          int r = 0;
+#pragma unroll
+          for (int h = 1; h < 5; ++h) {  // boxes of 128 .. 16 rows
+            const int box = 256 >> h;
+            while (half - r >= box) {
+              tma_load_2d_pair(sb(stage) + r * 128, &maps.b[h], bar, j * 64, (int)(r0 + r), pol);
+              r += box;
+            }
+          }
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == RP_STAGES) stage = 0, phase ^= 1;
+        }
+      }
+      if (!ok && leader) {
+        // The stages in flight (both CTAs' copies complete here) land before the pair exits.
+        volatile int never = 0;
+        for (int s = 0; s < RP_STAGES; ++s)
+          if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1, &never, nullptr, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (leader) {
+        // -------------------------------------------------------- MMA issuer (both CTAs' tensor memory)
+        int stage = 0;
+        uint32_t phase = 0, uses = 0;  // uses: bit b = parity of the uses of TMEM buffer b
+        bool ok = true;
+        for (int it = cid; it < total && ok; it += ncl) {
+          const RtItem im = item(it);
+          const uint32_t idesc = idesc_bf16_f32(256, im.n);
+          for (int c = 0; c < RT_CHUNKS && ok; ++c) {
+            const int b = c & 1;
+            if (!mbar_wait(&tempty[b], ((uses >> b) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d = tmem + b * 256;
+            const int j0 = c * nkh / RT_CHUNKS, j1 = (c + 1) * nkh / RT_CHUNKS;
+            for (int j = j0; j < j1; ++j) {
+              if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t bd = smem_desc_sw128(smem_u32(sb(stage)));
+              for (int sp = 0; sp < p.rt_splits; ++sp) {
+                const uint64_t ad = smem_desc_sw128(smem_u32(sa(stage) + sp * TC_TILE_A_BYTES));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_bf16_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, (j != j0 || sp != 0 || kk != 0) ? 1u : 0u);
+              }
+              mma_commit_pair(&empty[stage]);
+              if (++stage == RP_STAGES) stage = 0, phase ^= 1;
+            }
+            if (!ok) break;
+            mma_commit_pair(&tfull[b]);
+            uses ^= 1u << b;
+          }
+        }
+        mma_commit_pair(mma_done);
+      }
+      // Every pair MMA has finished (it wrote both CTAs' tensor memory) before TMEM is released.
+      volatile int never = 0;
+      mbar_wait(mma_done, 0, &never, p.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    // Warp (q, hq): TMEM lane quarter q (experts), columns [128 hq, 128 hq + 128).
+    const int q = warp & 3, hq = (warp - TC_EPI_FIRST) >> 2;
+    const uint32_t tempty_leader0 = mapa_shared(&tempty[0], 0);
+    uint32_t uses = 0;
+    bool ok = true;
+    for (int it = cid; it < total && ok; it += ncl) {
+      const RtItem im = item(it);
+      float acc[128];
+#pragma unroll
+      for (int c = 0; c < RT_CHUNKS; ++c) {
+        const int b = c & 1;
+        if (!warp_wait(&tfull[b], (uses >> b) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tb = tmem + b * 256 + ((uint32_t)(q * 32) << 16) + hq * 128;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          if (hq * 128 + cc * 32 < im.n) {
+            float v[32];
+            tmem_ld32(tb + cc * 32, v);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) acc[cc * 32 + jj] = c == 0 ? v[jj] : acc[cc * 32 + jj] + v[jj];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(&tempty[b]);
+          else mbar_arrive_remote(tempty_leader0 + (uint32_t)(b * sizeof(uint64_t)));
+        }
+        uses ^= 1u << b;
+      }
+      if (!ok) break;
+      const int e = im.f * 256 + (int)rank * 128 + q * 32 + lane;
+      const float bias = (p.bias && e < p.E) ? __ldg(p.bias + e) : 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int col = hq * 128 + cc * 32 + jj;
+          if (col < im.rows && e < p.E)
+            p.logits[(im.row0 + col) * p.E + e] = p.bias ? acc[cc * 32 + jj] + bias : acc[cc * 32 + jj];
+        }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no remote arrival, copy or commit targets this CTA any more
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, TC_TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
 // Exact three-way bf16 split of the FP32 router weight: Wr3[e] = [W1 | W2 | W3]
 // with W1 = rn(w), W2 = rn(w - W1), W3 = rn(w - W1 - W2).  Each residual is
 // exact in FP32 and holds at most 16 then 8 significant bits, so W3 captures
@@ -1195,6 +1399,41 @@ static cudaError_t launch_pair(const TcMaps &maps, const TcParams &p, cudaStream
 
 size_t router_tc_scratch_bytes(int E, int H) { return (size_t)E * 3 * H * 2; }
 
+// Clusters of two pair-router CTAs that fit on the device at once (0: the
+// pair form cannot run here).  Queried once per device.
+static int router_pair_clusters() {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (ensure_smem((const void *)tc_router_pair_kernel, RP_SMEM) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  int &c = cache[dev & 63];
+  if (c == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * device_sms());
+    cfg.blockDim = dim3(RT_THREADS);
+    cfg.dynamicSmemBytes = RP_SMEM;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void *)tc_router_pair_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    c = n > 0 ? n : -1;
+  }
+  return c > 0 ? c : 0;
+}
+
 cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const float *wr, const float *bias,
                                     float *logits, void *scratch, int *status, cudaStream_t stream, int splits) {
   if (splits != 1 && splits != 3) return cudaErrorInvalidValue;
@@ -1211,14 +1450,41 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
   TcParams p = {};
   p.T = T; p.H = H; p.E = E;
   p.rt_splits = splits;
+  p.bias = bias;
+  p.logits = logits;
+  p.status = status;
+  // The pair form (two 128-expert tiles per pair item) wherever E is a multiple
+  // of 256 and the device runs it; MOE_TC_PAIR=0 (the diagnostic switch of the
+  // grouped GEMMs) selects the single-SM form for comparison.
+  const char *env = getenv("MOE_TC_PAIR");
+  const int npc = (E % 256 == 0 && !(env && env[0] == '0')) ? router_pair_clusters() : 0;
+  if (npc > 0) {
+    const int ptiles = E / 256;
+    const int want = std::max<int>((int)ceil_div(T, RT_NMAX), std::min<int>(npc / ptiles, (int)ceil_div(T, RP_NROUND)));
+    p.rt_rpt = (int)round_up(ceil_div(T, want), RP_NROUND);
+    p.rt_ntile = (int)ceil_div(T, p.rt_rpt);
+    p.n_items = ptiles * p.rt_ntile;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * std::min(p.n_items, npc));
+    cfg.blockDim = dim3(RT_THREADS);
+    cfg.dynamicSmemBytes = RP_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, tc_router_pair_kernel, m, p);
+  }
   const int etiles = (int)ceil_div(E, 128), sms = device_sms();
   const int want = std::max<int>((int)ceil_div(T, RT_NMAX), std::min<int>(sms / etiles, (int)ceil_div(T, 16)));
   p.rt_rpt = (int)round_up(ceil_div(T, want), 16);
   p.rt_ntile = (int)ceil_div(T, p.rt_rpt);
   p.n_items = etiles * p.rt_ntile;
-  p.bias = bias;
-  p.logits = logits;
-  p.status = status;
   e = ensure_smem((const void *)tc_router_kernel, TC_SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int grid = std::min(p.n_items, sms);
