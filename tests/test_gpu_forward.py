@@ -185,7 +185,7 @@ def check_permute(ids, E):
 
 def test_permute_matches_oracle_random_ids():
     """Distinct ids per token (uniform ids with repeats for the largest case).
-    Up to 2^20 routes the sort is one launch on a cluster of eight CTAs;
+    Up to 2^20 routes the sort is one launch on a cluster of sixteen CTAs;
     110,000 x 10 routes take the four-kernel sort."""
     rng = np.random.default_rng(0)
     for T, E, k in [(1, 512, 10), (999, 512, 10), (5000, 64, 8), (70, 1024, 16), (8192, 512, 10)]:

@@ -24,7 +24,8 @@
 //            y_routed[sorted_route[j]] (or y_shared).
 // GATE_UP and DOWN also run on CTA pairs (tc_pair_kernel below, the form
 // used wherever the device and the shapes allow): the same items, one
-// M = 256 MMA over two SMs.
+// M = 256 MMA over two SMs.  So does the router (tc_router_pair_kernel, two
+// 128-expert tiles per pair item, where E is a multiple of 256).
 // The weights are the M operand (128-row tiles) and the tokens the N <= 256 operand,
 // so a short expert segment costs at most 15 padded columns.  Every output
 // element is accumulated over K in a fixed order (K blocks of 64, four
