@@ -54,3 +54,31 @@ def test_reference_arm_runs_on_rank_zero_only():
                         "--workload", "tiny_f32"], env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_roofline_denominators_match_the_buffers():
+    """The layer roofline's algorithmic bytes are the sizes of the buffers the
+    layer touches once: every expert weight (all 512 experts are active at
+    T=8192), the shared expert, the FP32 router weight and the shared gate, x
+    read and y written; the backward adds a gradient buffer per weight in FP32
+    and reads dy, writes dx.  FLOPs are 2 M N K per GEMM: per route a gate/up
+    product (M = 2I, K = H) and a down product (M = H, K = I), per token the
+    same with the shared expert's Is; the backward runs twice that."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from top_routed_grouped_gb300 import inputs as I
+    cfg = I.CONFIGS["bf16_t8192"]
+    T, H, E, k, Iw, Is = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.Is
+    w = I.make_inputs(cfg, T=1)
+    names = ("w_gate_up", "w_down", "ws_gate_up", "ws_down", "w_router", "w_shared_gate")
+    weight_bytes = sum(w[n].numel() * w[n].element_size() for n in names)
+    act = T * H * 2  # one bf16 [T, H] tensor
+    fwd = bench.layer_bytes_flops(T, H, E, k, Iw, Is, E)
+    assert fwd["bytes"] == weight_bytes + 2 * act
+    gemm = lambda m, n, kk: 2 * m * n * kk
+    flops = T * k * (gemm(2 * Iw, 1, H) + gemm(H, 1, Iw)) + T * (gemm(2 * Is, 1, H) + gemm(H, 1, Is))
+    assert fwd["flops"] == flops
+    bwd = bench.bwd_bytes_flops(T, H, E, k, Iw, Is)
+    grad_bytes = sum(w[n].numel() * 4 for n in names)
+    assert bwd["bytes"] == weight_bytes + grad_bytes + 3 * act
+    assert bwd["flops"] == 2 * flops
