@@ -167,9 +167,11 @@ class ClockSampler:
 
 
 # DRAM bytes (read + write) of one moe_grouped_ffn call (gate_up + down) at
-# bf16_t8192, from an ncu capture of the two kernels' dram__bytes counters
-# (profiles/forward_kernels_counters_bf16_t8192.md), valid only for the kernel
-# sources it was taken on (hash below); otherwise null.
+# bf16_t8192, from an ncu capture of the two kernels' dram__bytes_read.sum and
+# dram__bytes_write.sum counters (second forward step of
+# `bench.py --steps 3 --warmup 3 --no-cpu-baseline --no-fwd-bwd --no-extra`),
+# valid only for the kernel sources it was taken on (hash below); otherwise
+# null.
 FFN_TRAFFIC = {"sources": "0d80e7544c1ac023", "workload": "bf16_t8192",
                "bytes": 2_197_428_224 + 64_002_304 + 1_185_130_496 + 318_316_288}
 
