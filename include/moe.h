@@ -204,21 +204,25 @@ int moe_permute(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_of
  * plugin hosted by another runtime that owns the device memory pool and
  * hands out only input and output buffers, or a latency-critical loop that
  * must not call cudaMalloc because it can synchronise the device.  The
- * arguments and results are those of moe_permute (bit-identical outputs);
- * the kernels' scratch lives in a fixed array of
+ * arguments, their checks and the results are those of moe_permute
+ * (bit-identical outputs).  Up to 2^20 routes, where the device runs the
+ * one-launch cluster sort, no scratch is used at all; above that the
+ * four-kernel sort keeps its scratch in a fixed array of
  * MOE_PERMUTE_NOALLOC_SCRATCH_BYTES in the library's own device memory,
  * held by every GPU that loads the library until the process exits.  No
  * cudaMalloc, cudaFree or other allocating routine is called.
  *
- * Limit: the scratch needs (ceil(T*k / 512) * E + E) * 4 bytes; larger
- * sizes return MOE_ERR_UNSUPPORTED before any GPU work (with E = 512: up to
- * 1,047,552 routes, e.g. T = 104,755 tokens at k = 10).
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call uses the same array: calls that can
- * overlap on the GPU (different streams, no ordering between them) race and
- * must be serialised by the caller.  Each call writes every scratch word it
- * reads, so nothing is carried over from the previous call.
+ * Limit (four-kernel sort): the scratch needs (ceil(T*k / 128) * E + E) * 4
+ * bytes, or (ceil(T*k / 512) * E + E) * 4 bytes with the larger chunks it
+ * takes when the first does not fit; larger sizes return
+ * MOE_ERR_UNSUPPORTED before any GPU work (E = 64: up to 8,388,096 routes;
+ * E = 512: every size above 2^20 routes is refused).
+ * The first call on a device that needs the array looks up its device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  Every call uses the same array: calls that
+ * can overlap on the GPU (different streams, no ordering between them) race
+ * and must be serialised by the caller.  Each call writes every scratch word
+ * it reads, so nothing is carried over from the previous call.
  */
 #define MOE_PERMUTE_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 int moe_permute_noalloc(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_offsets,

@@ -257,14 +257,23 @@ MOE_API int moe_route_replay(const moe_dims_t *d, const void *x, const float *w_
   return cuda_status(e);
 }
 
-static int permute_check(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_offsets,
-                         int32_t *sorted_route, int32_t *route_pos, void *ws, size_t ws_bytes) {
+// The checks of the permutation's dims and buffers (shared by moe_permute and
+// moe_permute_noalloc; the workspace is checked by moe_permute alone).
+int moe::permute_args_check(const moe_dims_t *d, const int32_t *topk_ids, const int32_t *expert_offsets,
+                            const int32_t *sorted_route, const int32_t *route_pos) {
   int st = check_dims(d);
   if (st != MOE_OK) return st;
   const int64_t R = (int64_t)d->T * d->k;
-  if (!buf_ok(topk_ids, R) || !buf_ok(expert_offsets, 1) || !buf_ok(sorted_route, R) || !buf_ok(route_pos, R) ||
-      !opt_ok(ws))
+  if (!buf_ok(topk_ids, R) || !buf_ok(expert_offsets, 1) || !buf_ok(sorted_route, R) || !buf_ok(route_pos, R))
     return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+static int permute_check(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_offsets,
+                         int32_t *sorted_route, int32_t *route_pos, void *ws, size_t ws_bytes) {
+  int st = permute_args_check(d, topk_ids, expert_offsets, sorted_route, route_pos);
+  if (st != MOE_OK) return st;
+  if (!opt_ok(ws)) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < ws_size(d, MOE_OP_PERMUTE)) return MOE_ERR_WORKSPACE;
   return MOE_OK;
 }

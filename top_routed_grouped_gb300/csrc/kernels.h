@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/moe.h"
+
 namespace moe {
 
 // ---- route.cu ----
@@ -27,6 +29,10 @@ cudaError_t launch_replay_gate(int dtype, int T, int H, int E, int k, const floa
 // ---- api.cu ----
 // Device address of the status word on the current device (nullptr on error).
 int *device_status_ptr();
+// Checks of moe_permute's dims and buffers, without the workspace (MOE_OK or
+// the error status).
+int permute_args_check(const moe_dims_t *d, const int32_t *topk_ids, const int32_t *expert_offsets,
+                       const int32_t *sorted_route, const int32_t *route_pos);
 
 // ---- permute.cu ----
 // Routes per warp of the count and scatter kernels: 128 by default (more

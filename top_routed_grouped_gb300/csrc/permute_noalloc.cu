@@ -5,9 +5,11 @@
 // buffers: a custom operator or plugin hosted by another runtime that owns
 // the whole device memory pool, or a latency-critical loop that must not call
 // cudaMalloc because it can synchronise the device.  They cannot provide the
-// workspace moe_permute needs.  This entry point runs the same permutation
-// kernels with their scratch (the per-chunk expert histogram and the expert
-// totals) in a fixed-size array in the library's own device memory.
+// workspace moe_permute needs.  This entry point runs the same permutation:
+// as the one-launch cluster sort where that runs (it needs no scratch), else
+// as the four-kernel sort with its scratch (the per-chunk expert histogram
+// and the expert totals) in a fixed-size array in the library's own device
+// memory.
 //
 // The array below is a file-scope __device__ object: every GPU that loads the
 // library holds MOE_PERMUTE_NOALLOC_SCRATCH_BYTES of it until the process
@@ -48,15 +50,16 @@ using namespace moe;
 
 MOE_API int moe_permute_noalloc(const moe_dims_t *d, const int32_t *topk_ids, int32_t *expert_offsets,
                                 int32_t *sorted_route, int32_t *route_pos, void *stream) {
-  if (!d) return MOE_ERR_INVALID_ARG;
-  if (d->T < 0 || d->E <= 0 || d->k <= 0 || d->k > d->E || d->k > 16) return MOE_ERR_INVALID_ARG;
-  if (d->E > 1024 || (int64_t)d->T * d->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  // The same argument checks as moe_permute (dims and buffers; there is no workspace).
+  int st = permute_args_check(d, topk_ids, expert_offsets, sorted_route, route_pos);
+  if (st != MOE_OK) return st;
   const int64_t R = (int64_t)d->T * d->k;
-  auto ok = [](const void *p, int64_t n) { return n == 0 || (p != nullptr && ((uintptr_t)p & 15) == 0); };
-  if (!ok(topk_ids, R) || !ok(expert_offsets, 1) || !ok(sorted_route, R) || !ok(route_pos, R))
-    return MOE_ERR_INVALID_ARG;
-  // The default chunk where its scratch fits the fixed array, else the large
-  // chunk (same result); sizes that fit neither are refused before any GPU work.
+  if (permute_cluster_ok(R, d->E))  // the one-launch sort keeps its counts in shared memory: no scratch at all
+    return launch_permute_cluster(R, d->E, topk_ids, expert_offsets, sorted_route, route_pos, device_status_ptr(),
+                                  (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  // The four-kernel sort over the fixed array: the default chunk where its
+  // scratch fits, else the large chunk (same result); sizes that fit neither
+  // are refused before any GPU work.
   int chunk = PERMUTE_CHUNK_SMALL;
   if (permute_scratch_bytes(R, d->E, chunk) > MOE_PERMUTE_NOALLOC_SCRATCH_BYTES) chunk = PERMUTE_CHUNK_LARGE;
   if (permute_scratch_bytes(R, d->E, chunk) > MOE_PERMUTE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
