@@ -100,26 +100,71 @@ def barrier(world: int) -> None:
         dist.barrier()
 
 
-class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during a region.
+class _Nvml:
+    """Read-only NVML queries through ctypes (the driver's libnvidia-ml):
+    current and maximum SM clock, clock-event reasons and power draw."""
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
 
-    A reader thread timestamps each sample; start() returns once the first
-    sample has arrived, and only samples taken between begin() and end()
-    count."""
+    def __init__(self, index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_sm = self._clock(self.lib.nvmlDeviceGetMaxClockInfo)
+
+    def _clock(self, fn) -> int | None:
+        v = self.ct.c_uint(0)
+        return int(v.value) if fn(self.h, self.ct.c_int(1), self.ct.byref(v)) == 0 else None  # 1 = SM clock
+
+    def sample(self) -> tuple:
+        r = self.ct.c_ulonglong(0)
+        reasons = int(r.value) if self.reasons_fn(self.h, self.ct.byref(r)) == 0 else 0
+        mw = self.ct.c_uint(0)
+        power = mw.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.h, self.ct.byref(mw)) == 0 else None
+        return self._clock(self.lib.nvmlDeviceGetClockInfo), self.max_sm, reasons, power
+
+
+class ClockSampler:
+    """SM clock and throttle reasons during a region.
+
+    Preferred source: NVML polled every millisecond from a thread (read-only
+    queries), so that a region of a few milliseconds still gets samples;
+    fallback: nvidia-smi every 50 ms.  start() returns once sampling runs,
+    and only samples taken between begin() and end() count."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index: int, period_ms: int = 50):
-        self.idx, self.period = gpu_index, period_ms
+    def __init__(self, gpu_index: int, period_ms: int = 50, nvml_period_s: float = 0.001):
+        self.idx, self.period, self.nvml_period = gpu_index, period_ms, nvml_period_s
         self.proc, self.lines, self.t0, self.t1 = None, [], None, None
+        self.nvml, self.samples, self.stop_flag, self.thread = None, [], False, None
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append((time.perf_counter(), line))
 
+    def _poll(self):
+        while not self.stop_flag:
+            self.samples.append((time.perf_counter(), self.nvml.sample()))
+            time.sleep(self.nvml_period)
+
     def start(self):
         import threading
+        try:
+            self.nvml = _Nvml(self.idx)
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
+        except (OSError, AttributeError):
+            self.nvml = None
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", str(self.period)],
@@ -138,32 +183,50 @@ class ClockSampler:
     def end(self):
         self.t1 = time.perf_counter()
 
+    def _inside(self, ts) -> bool:
+        return self.t0 is None or self.t0 <= ts <= (self.t1 or ts)
+
     def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ts, line in list(self.lines):
-            if self.t0 is not None and not (self.t0 <= ts <= (self.t1 or ts)):
-                continue
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 8:
-                continue
+        sm, mx, reasons, power = [], [], set(), []
+        if self.nvml is not None:
+            self.stop_flag = True
+            self.thread.join(timeout=5)
+            for ts, (clk, cmax, bits, pw) in list(self.samples):
+                if not self._inside(ts) or clk is None:
+                    continue
+                sm.append(float(clk))
+                if cmax is not None:
+                    mx.append(float(cmax))
+                if pw is not None:
+                    power.append(pw)
+                reasons.update(n for b, n in _Nvml.REASONS.items() if bits & b)
+            src = "nvml, 1 ms"
+        elif self.proc is not None:
+            self.proc.terminate()
             try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            for ts, line in list(self.lines):
+                if not self._inside(ts):
+                    continue
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 8:
+                    continue
+                try:
+                    sm.append(float(f[0]))
+                    mx.append(float(f[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(self.NAMES, f[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+            src = f"nvidia-smi, {self.period} ms"
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": src,
+                "power_w_max": max(power) if power else None}
 
 
 # DRAM bytes (read + write) of one moe_grouped_ffn call (gate_up + down) at
@@ -321,10 +384,18 @@ def extra_forward(name: str, dev_w: dict, steps: int, warmup: int, peaks: dict) 
             "layer_roofline_frac": roof * 1e3 / pc["p50"], "api": "moe_forward"}
 
 
-def cpu_oracle_baseline(cfg, x_cpu, W_cpu, bias, budget_s: float = 20.0, max_tokens: int | None = None) -> dict:
+def widen(W_cpu: dict) -> dict:
+    """The weights widened to float64 once (exact), as the oracle reads them."""
+    import torch
+    return {k: v.to(torch.float64).numpy() for k, v in W_cpu.items()}
+
+
+def cpu_oracle_baseline(cfg, x_cpu, W_cpu, bias, budget_s: float = 20.0, max_tokens: int | None = None,
+                        f64: dict | None = None) -> dict:
     """Time the FP64 oracle (routing + experts + combine) on the first tokens
     of the workload (all of them by default), in blocks of 32 tokens until
-    `budget_s` has elapsed."""
+    `budget_s` has elapsed.  `f64`: the weights already widened (else widened
+    here, outside the timed blocks)."""
     if max_tokens is None:
         max_tokens = cfg.T
     os.environ.setdefault("OMP_NUM_THREADS", str(host_cores()))
@@ -332,7 +403,8 @@ def cpu_oracle_baseline(cfg, x_cpu, W_cpu, bias, budget_s: float = 20.0, max_tok
     import oracle
     import torch
 
-    f64 = {k: v.to(torch.float64).numpy() for k, v in W_cpu.items()}
+    if f64 is None:
+        f64 = widen(W_cpu)
     b64 = None if bias is None else bias.to(torch.float64).numpy()
     oracle.build()
     done, elapsed = 0, 0.0
@@ -345,33 +417,58 @@ def cpu_oracle_baseline(cfg, x_cpu, W_cpu, bias, budget_s: float = 20.0, max_tok
         done += xs.shape[0]
         assert np.isfinite(r["y"]).all()
     return {"value": done / elapsed, "unit": "tokens/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
-            "cpu_model": cpu_model(), "kind": "oracle", "sample": f"first {done} tokens of {cfg.name} (FP64 route + experts + combine), "
-                                        f"{elapsed:.1f} s of oracle time"}
+            "cpu_model": cpu_model(), "kind": "oracle", "tokens": done, "oracle_s": elapsed,
+            "sample": f"first {done} tokens of {cfg.name} (FP64 route + experts + combine), "
+                      f"{elapsed:.1f} s of oracle time"}
+
+
+def workload_config(cfg, active: int, world: int) -> dict:
+    """The `config` object of both arms' lines (same keys and values)."""
+    es = 2 if cfg.dtype == "bf16" else 4
+    wb = cfg.E * 3 * cfg.H * cfg.I * es
+    l2 = (f"no flush: expert weights ({wb / 1e9:.1f} GB) exceed the 129 MB L2" if wb > 129e6 else
+          f"expert weights ({wb / 1e6:.1f} MB) fit in L2; no flush")
+    return {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "Is": cfg.Is,
+            "step": "forward", "active_experts": active, "l2": l2, "parallelism": f"replicas x{world}"}
 
 
 def run_reference(args, cfg, rank: int) -> None:
-    """Reference arm: the oracle, as it stands, on the host cores."""
+    """Reference arm: the oracle, as it stands, on the host cores.  A step is
+    a bounded sample of the workload (the first tokens, as many as the
+    oracle finishes in a few seconds); value = tokens / oracle time over all
+    steps, ms_per_step = the measured time of one such step."""
     if rank != 0:
         return
-    import torch
+    import numpy as np
+    import oracle
     from top_routed_grouped_gb300 import inputs as I
     d = I.make_inputs(cfg)
     W = {k: v for k, v in d.items() if k not in ("x", "dy", "router_bias")}
+    # active experts of the whole workload, from the oracle's own routing
+    ids = oracle.topk_select(oracle.router_logits(d["x"], W["w_router"], d["router_bias"]), cfg.k)
+    active = int((np.bincount(ids.reshape(-1), minlength=cfg.E) > 0).sum())
     budget = max(2.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
+    f64 = widen(W)
     for _ in range(args.warmup):
-        cpu_oracle_baseline(cfg, d["x"], W, d["router_bias"], budget_s=0.5, max_tokens=32)
-    vals = []
+        cpu_oracle_baseline(cfg, d["x"], W, d["router_bias"], budget_s=0.5, max_tokens=32, f64=f64)
+    tokens, secs, per_step = 0, 0.0, []
     cb = None
     for _ in range(args.steps):
-        cb = cpu_oracle_baseline(cfg, d["x"], W, d["router_bias"], budget_s=budget)
-        vals.append(cb["value"])
-    v = statistics.median(vals)
-    cb["value"] = v
+        t0 = time.perf_counter()
+        cb = cpu_oracle_baseline(cfg, d["x"], W, d["router_bias"], budget_s=budget, f64=f64)
+        per_step.append(time.perf_counter() - t0)
+        tokens += cb["tokens"]
+        secs += cb["oracle_s"]
+    v = tokens / secs
+    cb = dict(cb, value=v, sample=f"{args.steps} steps, each the first {tokens // args.steps} tokens of "
+                                  f"{cfg.name} (FP64 route + experts + combine, {budget:.1f} s budget per step)")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * cfg.T / v,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * statistics.mean(per_step),
+            "tokens_per_step": tokens // args.steps,
+            "ms_per_workload_scaled": {"value": 1000.0 * cfg.T / v, "note": f"scaled: the oracle's rate applied to "
+                                       f"all {cfg.T} tokens of the workload, not measured"},
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I,
-                       "Is": cfg.Is, "step": "forward"},
+            "config": workload_config(cfg, active, args.gpus),
             "cpu_baseline": cb, "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                                         "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -539,9 +636,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) weights)",
-        "config": {"workload": cfg.name, "T": T, "H": H, "E": E, "k": k, "I": Iw, "Is": Is, "step": "forward",
-                   "active_experts": active, "l2": "no flush: expert weights (3.2 GB) exceed the 129 MB L2",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(cfg, active, world),
         "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2, "api": "moe_forward"},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,

@@ -13,7 +13,12 @@ weights in FP64 on that ordered set.
 """
 from __future__ import annotations
 
+import ctypes
 import functools
+import os
+import re
+import threading
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import torch
@@ -25,6 +30,49 @@ TIE_GAP = 1e-4
 BF16_MAX_ABS = 2e-2
 BF16_REL_L2 = 5e-3
 F32_MAX_ABS = 1e-4
+
+# Every value comparison of the session: (tensor, precision, max_abs, scale,
+# rel_l2, elements), printed as a per-tensor summary at the end of the run.
+RECORDS: list[tuple] = []
+_rec_lock = threading.Lock()
+
+
+def record(what: str, kind: str, max_abs: float, scale: float, rel: float, n: int) -> None:
+    name = re.split(r"[\s\[(,]", what.strip(), maxsplit=1)[0] or what
+    with _rec_lock:
+        RECORDS.append((name, kind, max_abs, scale, rel, n))
+
+
+def summary_lines() -> list[str]:
+    """Worst case per (tensor, precision) over the session's comparisons."""
+    worst: dict = {}
+    for name, kind, m, s, r, n in RECORDS:
+        key = (kind, name)
+        w = worst.setdefault(key, [0.0, 1.0, 0.0, 0, 0])
+        if m / s >= w[0] / w[1]:
+            w[0], w[1] = m, s
+        w[2] = max(w[2], r)
+        w[3] += n
+        w[4] += 1
+    lines = [f"{'tensor':<15}{'dtype':<6}{'max_abs':>10}{'scale':>8}{'rel_l2':>10}{'elements':>12}{'checks':>7}"]
+    for (kind, name), (m, s, r, n, c) in sorted(worst.items()):
+        lines.append(f"{name:<15}{kind:<6}{m:>10.2e}{s:>8.3g}{r:>10.2e}{n:>12d}{c:>7d}")
+    return lines
+
+
+def _omp_one_thread() -> None:
+    """Limit the calling thread's OpenMP regions to one thread (the oracle's
+    per-token calls then run side by side in a thread pool)."""
+    try:
+        ctypes.CDLL("libgomp.so.1").omp_set_num_threads(1)
+    except OSError:  # pragma: no cover
+        pass
+
+
+def _pool_map(fn, items):
+    n = max(1, min(16, len(os.sched_getaffinity(0))))
+    with ThreadPoolExecutor(n, initializer=_omp_one_thread) as ex:
+        return list(ex.map(fn, items))
 
 
 @functools.lru_cache(maxsize=None)
@@ -73,22 +121,37 @@ def oracle_routes(x, w_router, bias, k: int, gpu_logits: np.ndarray):
 
 def oracle_rows(x_rows, ids_rows, w_rows, sig_rows, W: dict, want_rows=False):
     """Oracle forward of a few tokens at full size, one token at a time with
-    only its k experts widened to float64 (the experts are remapped to 0..k-1)."""
-    ys, yrs, yss = [], [], []
-    for t in range(x_rows.shape[0]):
+    only its k experts widened to float64 (the experts are remapped to 0..k-1);
+    the tokens run side by side in a thread pool."""
+    def one(t):
         e = torch.as_tensor(np.asarray(ids_rows[t], dtype=np.int64))
         wgu = W["w_gate_up"].index_select(0, e.to(W["w_gate_up"].device)).cpu()
         wdn = W["w_down"].index_select(0, e.to(W["w_down"].device)).cpu()
         local = np.arange(len(e), dtype=np.int32)[None, :]
-        r = oracle.moe_forward(x_rows[t:t + 1], local, np.asarray(w_rows[t:t + 1]), np.asarray(sig_rows[t:t + 1]),
-                               wgu, wdn, W["ws_gate_up"].cpu(), W["ws_down"].cpu(), want_rows=want_rows)
-        if want_rows:
-            ys.append(r[0]); yrs.append(r[1]); yss.append(r[2])
-        else:
-            ys.append(r)
+        return oracle.moe_forward(x_rows[t:t + 1], local, np.asarray(w_rows[t:t + 1]), np.asarray(sig_rows[t:t + 1]),
+                                  wgu, wdn, W["ws_gate_up"].cpu(), W["ws_down"].cpu(), want_rows=want_rows)
+    res = _pool_map(one, range(x_rows.shape[0]))
     if want_rows:
-        return np.concatenate(ys), np.concatenate(yrs), np.concatenate(yss)
-    return np.concatenate(ys)
+        return tuple(np.concatenate([r[i] for r in res]) for i in range(3))
+    return np.concatenate(res)
+
+
+def oracle_segment_rows(x_tokens, w_gate_up_e, w_down_e):
+    """Oracle rows of one expert on the given token rows (its whole segment):
+    the layer with that one expert, weight 1, and no shared expert."""
+    n, H = x_tokens.shape
+    ids = np.zeros((n, 1), np.int32)
+    _, yr, _ = oracle.moe_forward(x_tokens, ids, np.ones((n, 1)), np.zeros(n), w_gate_up_e[None], w_down_e[None],
+                                  np.zeros((0, H)), np.zeros((H, 0)), want_rows=True)
+    return yr
+
+
+def oracle_shared_rows(x_tokens, ws_gate_up, ws_down):
+    """Oracle rows of the shared expert on the given token rows (no routes)."""
+    n, H = x_tokens.shape
+    _, _, ys = oracle.moe_forward(x_tokens, np.zeros((n, 0), np.int32), np.zeros((n, 0)), np.ones(n),
+                                  np.zeros((1, 0, H)), np.zeros((1, H, 0)), ws_gate_up, ws_down, want_rows=True)
+    return ys
 
 
 def err_stats(got, ref) -> tuple[float, float]:
@@ -102,12 +165,14 @@ def err_stats(got, ref) -> tuple[float, float]:
 
 def assert_bf16_close(got, ref, what=""):
     m, r = err_stats(got, ref)
+    record(what, "bf16", m, 1.0, r, int(np.asarray(ref).size))
     assert m <= BF16_MAX_ABS and r <= BF16_REL_L2, f"{what}: max_abs={m:.3e} rel_l2={r:.3e}"
     return m, r
 
 
 def assert_f32_close(got, ref, what=""):
     m, r = err_stats(got, ref)
+    record(what, "f32", m, 1.0, r, int(np.asarray(ref).size))
     assert m <= F32_MAX_ABS, f"{what}: max_abs={m:.3e}"
     return m, r
 
@@ -134,6 +199,7 @@ def grad_scale(ref) -> float:
 def assert_grad_close(got, ref, what="", f32=False):
     m, r = err_stats(got, ref)
     s = grad_scale(ref)
+    record(what, "f32" if f32 else "bf16", m, s, r, int(np.asarray(ref).size))
     if f32:
         assert m <= F32_MAX_ABS * s, f"{what}: max_abs={m:.3e} scale={s:.3g}"
     else:
@@ -144,23 +210,22 @@ def assert_grad_close(got, ref, what="", f32=False):
 
 def oracle_bwd_rows(x_rows, ids_rows, w_rows, sig_rows, dy_rows, W: dict):
     """Oracle per-token backward (dx, dw, dlogit, dsig) of a few tokens at full
-    size, one token at a time with only its k experts widened to float64.
-    Local ids keep the ascending order of the global ids, so the oracle's
-    ascending-expert sum of the routed input gradients is unchanged."""
-    out = [[], [], [], []]
-    for t in range(x_rows.shape[0]):
+    size, one token at a time with only its k experts widened to float64;
+    the tokens run side by side in a thread pool.  Local ids keep the
+    ascending order of the global ids, so the oracle's ascending-expert sum
+    of the routed input gradients is unchanged."""
+    def one(t):
         e = np.asarray(ids_rows[t], dtype=np.int64)
         srt = np.sort(e)
         local = np.searchsorted(srt, e).astype(np.int32)[None, :]
         idx = torch.as_tensor(srt)
-        g = lambda name: W[name].index_select(0, idx.to(W[name].device)).cpu()
-        r = oracle.backward_tokens(x_rows[t:t + 1], local, np.asarray(w_rows[t:t + 1]),
-                                   np.asarray(sig_rows[t:t + 1]), g("w_router"), W["w_shared_gate"].cpu(),
-                                   g("w_gate_up"), g("w_down"), W["ws_gate_up"].cpu(), W["ws_down"].cpu(),
-                                   dy_rows[t:t + 1])
-        for i in range(4):
-            out[i].append(r[i])
-    return tuple(np.concatenate(o) for o in out)
+        g = lambda name: W[name].index_select(0, idx.to(W[name].device)).cpu()  # noqa: E731
+        return oracle.backward_tokens(x_rows[t:t + 1], local, np.asarray(w_rows[t:t + 1]),
+                                      np.asarray(sig_rows[t:t + 1]), g("w_router"), W["w_shared_gate"].cpu(),
+                                      g("w_gate_up"), g("w_down"), W["ws_gate_up"].cpu(), W["ws_down"].cpu(),
+                                      dy_rows[t:t + 1])
+    res = _pool_map(one, range(x_rows.shape[0]))
+    return tuple(np.concatenate([r[i] for r in res]) for i in range(4))
 
 
 def small_layer(T, H, E, k, I_, Is, seed=11):

@@ -25,3 +25,18 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Per-tensor worst errors of every value comparison against the FP64
+    oracle in this run (max_abs with the scale its bar is taken relative
+    to, and rel-L2), so the figures behind the tolerances are on record."""
+    try:
+        import _util
+    except ImportError:  # pragma: no cover
+        return
+    if not _util.RECORDS:
+        return
+    terminalreporter.write_sep("-", "errors against the FP64 oracle (worst per tensor)")
+    for line in _util.summary_lines():
+        terminalreporter.write_line(line)

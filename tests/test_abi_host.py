@@ -107,3 +107,16 @@ def test_permute_small_workspace(L):
     p = ctypes.c_void_p(16)
     need = moe.moe_workspace_size(d, "permute")
     assert L.moe_permute(ctypes.byref(d), p, p, p, p, p, need - 256, None) == -3
+
+
+def test_moe_layer_parameters_on_cpu():
+    """MoELayer's parameters follow the library's layout (no GPU needed to
+    construct it on the CPU)."""
+    import torch
+    import top_routed_grouped_gb300 as moe
+    m = moe.MoELayer(256, 16, 4, 128, 128, dtype=torch.bfloat16, device="cpu")
+    shapes = {n: (tuple(p.shape), p.dtype) for n, p in m.named_parameters()}
+    assert shapes == {"w_router": ((16, 256), torch.float32), "w_shared_gate": ((256,), torch.bfloat16),
+                      "w_gate_up": ((16, 256, 256), torch.bfloat16), "w_down": ((16, 256, 128), torch.bfloat16),
+                      "ws_gate_up": ((256, 256), torch.bfloat16), "ws_down": ((256, 128), torch.bfloat16)}
+    assert m.top_k == 4 and m.router_bias is None

@@ -100,10 +100,12 @@ def test_bf16_small_batches_full_parity(T):
 
 
 def test_bf16_t4096_sampled():
-    """The forward+backward workload at full size: sampled tokens against the
-    per-token oracle, sampled experts' weight gradients, and the router and
-    gate weight gradients against the oracle's reduction of the GPU's
-    (separately checked) logit and gate gradients."""
+    """The forward+backward workload at full size: the input, logit and gate
+    gradients of 512 tokens (every token of the largest and of the smallest
+    expert segment, the rest drawn at random) against the per-token oracle,
+    the weight gradients of the largest, smallest and two more experts, and
+    the router and gate weight gradients against the oracle's reduction of
+    the GPU's (separately checked) logit and gate gradients."""
     W = full_weights()
     T = 4096
     x, dy = full_x(T), full_dy(T)
@@ -111,7 +113,12 @@ def test_bf16_t4096_sampled():
     f, g = fwd_bwd(d, dy.cuda(), 10)
     ids, w, sig = checked_routes(f, x, W, None, 10)
     rng = np.random.default_rng(5)
-    sample = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 14, replace=False)]))
+    loads = np.bincount(ids.reshape(-1), minlength=512)
+    seg_tokens = np.flatnonzero((ids == int(np.argmax(loads))).any(1) | (ids == int(np.argmin(loads))).any(1))
+    rest = np.setdiff1d(np.arange(T), seg_tokens)
+    sample = np.unique(np.concatenate([[0, T - 1], seg_tokens,
+                                       rng.choice(rest, 510 - len(seg_tokens), replace=False)]))
+    assert len(sample) >= 500
     dx, dw, dl, ds = oracle_bwd_rows(x[sample], ids[sample], w[sample], sig[sample], dy[sample], W)
     st = torch.as_tensor(sample, device="cuda")
     assert_grad_close(g["dx"][st], dx, "dx sampled")
@@ -124,7 +131,6 @@ def test_bf16_t4096_sampled():
     dwr, dwsg = oracle.backward_router(x, ids, gdl, np.full(T, 0.5), 4.0 * gdz, 512)
     assert_grad_close(g["dw_router"], dwr, "dw_router")
     assert_grad_close(g["dw_shared_gate"], dwsg, "dw_shared_gate")
-    loads = np.bincount(ids.reshape(-1), minlength=512)
     for e in sorted({int(np.argmax(loads)), int(np.argmin(loads)), 0, 511}):
         dwgu, dwdn = oracle.backward_expert_weights(x, ids, w, dy, W["w_gate_up"], W["w_down"], e, e + 1)
         assert_grad_close(g["dw_gate_up"][e:e + 1], dwgu, f"dw_gate_up[{e}] ({loads[e]} routes)")

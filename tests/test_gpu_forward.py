@@ -15,7 +15,7 @@ from top_routed_grouped_gb300 import build
 from top_routed_grouped_gb300 import inputs as I
 
 from _util import (assert_bf16_close, assert_f32_close, bits, full_weights, full_x, oracle_routes, oracle_rows,
-                   to_dev)
+                   oracle_segment_rows, oracle_shared_rows, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -81,9 +81,29 @@ def test_bf16_small_batches_full_parity(T):
     assert_bf16_close(out["y"], y, "y")
 
 
+def pick_segments(off, T, k, zipf):
+    """Expert segments to compare whole: the largest, the smallest non-empty,
+    one whose length leaves a ragged tail in its last 256-row pair item, and
+    (skewed routing) the largest two spanning several pair items besides it."""
+    n = off[1:] - off[:-1]
+    nz = np.flatnonzero(n > 0)
+    order = nz[np.argsort(n[nz], kind="stable")]
+    pick = [int(order[-1]), int(order[0])]
+    ragged = [int(e) for e in order[::-1] if n[e] % 32 not in (0, 16) and int(e) not in pick]
+    pick += ragged[:1]
+    if zipf:
+        multi = [int(e) for e in order[::-1] if n[e] > 256 and int(e) not in pick]
+        pick += multi[:2]
+        pick += [e for e in ragged if n[e] > 256 and e not in pick][:1]
+    return pick
+
+
 @pytest.mark.parametrize("T,zipf", [(1024, False), (8192, False), (16384, True)])
-def test_bf16_full_size_sampled(T, zipf):
-    """Full workload sizes: routes and permutation of every token, values of sampled tokens."""
+def test_bf16_full_size(T, zipf):
+    """Full workload sizes: routes and permutation of every token; values of
+    sampled tokens; at T >= 8192 also the unweighted rows of whole expert
+    segments (the largest, the smallest, ragged tails, segments over several
+    256-row pair items) and 512 shared-expert rows, element by element."""
     W = full_weights()
     x = full_x(16384)[:T].clone()
     bias = I.zipf_bias(512) if zipf else None
@@ -101,6 +121,21 @@ def test_bf16_full_size_sampled(T, zipf):
         loads = np.bincount(out["topk_ids"].cpu().numpy().reshape(-1), minlength=512)
         assert int((loads == 0).sum()) == ref["empty_experts"]
         assert abs(int(loads.max()) - ref["max_load"]) <= 2
+    if T < 8192:
+        return
+    off = out["expert_offsets"].cpu().numpy()
+    srt = out["sorted_route"].cpu().numpy()
+    segs = pick_segments(off, T, 10, zipf)
+    if zipf:
+        assert max(off[e + 1] - off[e] for e in segs) > 6000
+    for e in segs:
+        routes = srt[off[e]:off[e + 1]]
+        yr = oracle_segment_rows(x[torch.as_tensor(routes // 10)], W["w_gate_up"][e], W["w_down"][e])
+        assert_bf16_close(out["y_routed"][torch.as_tensor(routes, device="cuda", dtype=torch.int64)], yr,
+                          f"y_routed segment e={e} ({len(routes)} rows)")
+    rows = np.unique(np.concatenate([rng.choice(T, 510, replace=False), [0, T - 1]]))
+    ys = oracle_shared_rows(x[torch.as_tensor(rows)], W["ws_gate_up"], W["ws_down"])
+    assert_bf16_close(out["y_shared"][torch.as_tensor(rows, device="cuda")], ys, f"y_shared {len(rows)} rows")
 
 
 def test_batch_invariance_bits():
@@ -251,23 +286,27 @@ def test_api_errors_on_device_buffers():
     assert e.value.status == -3
 
 
-@pytest.mark.parametrize("T", [37, 300, 2048, 8192])
-def test_pair_and_single_sm_gemms_agree_bitwise(T, monkeypatch):
+def test_pair_and_single_sm_gemms_agree_bitwise(tmp_path):
     """The router and the grouped GEMMs on CTA pairs (two SMs per M = 256
     MMA) and on single SMs give the same bits: each output is one MMA chain
     over K in the same order either way (router logits, routes and training
-    activations included)."""
-    W = to_dev(full_weights())
-    d = dict(W, x=full_x(T).cuda())
-    args = [d[n] for n in ("w_router", "w_shared_gate", "w_gate_up", "w_down", "ws_gate_up", "ws_down")]
-    outs = {}
-    for mode in ("0", "3"):
-        monkeypatch.setenv("MOE_TC_PAIR", mode)
-        outs[mode] = moe.forward(d["x"], *args, 10, save_for_backward=True, want_logits=True)
-    monkeypatch.delenv("MOE_TC_PAIR")
-    assert torch.equal(outs["0"]["topk_ids"], outs["3"]["topk_ids"])
-    for key in ("logits", "topk_w", "shared_sig", "y", "y_routed", "y_shared"):
-        assert torch.equal(bits(outs["0"][key]), bits(outs["3"][key])), key
-    for key in ("gu", "h", "gu_shared", "h_shared"):
-        assert torch.equal(bits(outs["0"]["saved"][key]), bits(outs["3"]["saved"][key])), key
-    assert moe.moe_device_status(reset=True) == 0
+    activations included).  The library reads its form switch (MOE_TC_PAIR)
+    once per process, so the single-SM forms run in a child process."""
+    import os
+    import subprocess
+    import sys
+    from _forms_child import KEYS, SAVED, run
+    if "MOE_TC_PAIR" in os.environ:
+        pytest.skip("this process runs a forced GEMM form")
+    Ts = (37, 300, 2048, 8192)
+    out = tmp_path / "single_sm.pt"
+    env = dict(os.environ, MOE_TC_PAIR="0")
+    child = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_forms_child.py")
+    subprocess.run([sys.executable, child, str(out)] + [str(T) for T in Ts], env=env, check=True, timeout=900)
+    single = torch.load(out)
+    for T in Ts:
+        pair = run(T)
+        for key in KEYS:
+            assert torch.equal(bits(pair[key]), bits(single[T][key])), (T, key)
+        for key in SAVED:
+            assert torch.equal(bits(pair["saved_" + key]), bits(single[T]["saved_" + key])), (T, key)

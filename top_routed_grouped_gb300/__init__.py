@@ -9,6 +9,9 @@ lower-case helpers (``route``, ``permute``, ``grouped_ffn``, ``combine``,
 
 There is no fallback: if the library is missing, ``lib()`` raises.  Build it
 with ``python -m top_routed_grouped_gb300.build`` (or ``__graft_entry__.build()``).
+
+``MoELayer`` / ``MoEFunction`` (``layer.py``): the layer as a torch module
+whose autograd Function calls ``moe_forward`` and ``moe_backward``.
 """
 from __future__ import annotations
 
@@ -347,9 +350,10 @@ def permute(topk_ids, E: int, stream=None):
 
 
 def forward(x, w_router, w_shared_gate, w_gate_up, w_down, ws_gate_up, ws_down, k: int, router_bias=None,
-            save_for_backward: bool = False, want_logits: bool = False, replay_ids=None, stream=None):
+            save_for_backward: bool = False, want_logits: bool = False, replay_ids=None, stream=None, ws=None):
     """Full layer forward through ``moe_forward``.  Returns a dict with ``y`` and every intermediate.
-    ``replay_ids`` [T,k] int32: route with these experts instead of the top-k (router replay)."""
+    ``replay_ids`` [T,k] int32: route with these experts instead of the top-k (router replay).
+    ``ws``: a caller-owned workspace (allocated here when None)."""
     import torch
     T, H = x.shape
     d = dims_of(x, w_router, w_gate_up, ws_gate_up, k)
@@ -374,7 +378,7 @@ def forward(x, w_router, w_shared_gate, w_gate_up, w_down, ws_gate_up, ws_down, 
                         "h_shared": torch.empty(T, Is, dtype=dt, device=dev)}
     args = dict(out, x=x, w_router=w_router, router_bias=router_bias, w_shared_gate=w_shared_gate,
                 w_gate_up=w_gate_up, w_down=w_down, ws_gate_up=ws_gate_up, ws_down=ws_down, replay_ids=replay_ids)
-    moe_forward(d, args, workspace(d, "forward", dev), stream)
+    moe_forward(d, args, workspace(d, "forward", dev) if ws is None else ws, stream)
     return out
 
 
@@ -404,3 +408,12 @@ def backward(fwd: dict, dy, x, w_router, w_shared_gate, w_gate_up, w_down, ws_ga
                                        "route_pos", "y_routed", "y_shared")})
     moe_backward(d, args, workspace(d, "backward", dev) if ws is None else ws, stream)
     return out
+
+
+def __getattr__(name):
+    # The torch module lives in layer.py (imported on first use, so that this
+    # binding itself does not import torch at load time).
+    if name in ("MoELayer", "MoEFunction"):
+        from . import layer
+        return getattr(layer, name)
+    raise AttributeError(name)

@@ -1365,13 +1365,24 @@ static int pair_clusters() {
   return c > 0 ? c : 0;
 }
 
-// Whether the grouped GEMM of `MODE` runs on CTA pairs.  MOE_TC_PAIR (a
-// diagnostic switch for comparing the two forms): "0" neither, "1" gate_up
-// only, "2" down only; unset: both wherever the shapes and the device allow.
+// MOE_TC_PAIR, a diagnostic switch for comparing the CTA-pair and single-SM
+// forms, read once per process at the first launch: "0" no pair form (router
+// and both grouped GEMMs on single SMs), "1" the gate_up pair only, "2" the
+// down pair only; unset (-1): every pair form wherever the shapes and the
+// device allow.
+static int pair_override() {
+  static const int mode = [] {
+    const char *e = getenv("MOE_TC_PAIR");
+    return (e && e[0] >= '0' && e[0] <= '2') ? e[0] - '0' : -1;
+  }();
+  return mode;
+}
+
+// Whether the grouped GEMM of `MODE` runs on CTA pairs.
 template <int MODE>
 static bool use_pair(const FfnArgs &a) {
-  const char *e = getenv("MOE_TC_PAIR");
-  if (e && (e[0] == '0' || (e[0] == '1' && MODE != TC_GATE_UP) || (e[0] == '2' && MODE != TC_DOWN))) return false;
+  const int m = pair_override();
+  if (m == 0 || (m == 1 && MODE != TC_GATE_UP) || (m == 2 && MODE != TC_DOWN)) return false;
   const bool shapes = MODE == TC_GATE_UP ? a.H % (64 * PR_KSUB) == 0
                                          : a.H % 256 == 0 && a.I % (64 * PR_KSUB) == 0 && a.Is % (64 * PR_KSUB) == 0;
   return shapes && pair_clusters<MODE>() > 0;
@@ -1457,8 +1468,7 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
   // The pair form (two 128-expert tiles per pair item) wherever E is a multiple
   // of 256 and the device runs it; MOE_TC_PAIR=0 (the diagnostic switch of the
   // grouped GEMMs) selects the single-SM form for comparison.
-  const char *env = getenv("MOE_TC_PAIR");
-  const int npc = (E % 256 == 0 && !(env && env[0] == '0')) ? router_pair_clusters() : 0;
+  const int npc = (E % 256 == 0 && pair_override() != 0) ? router_pair_clusters() : 0;
   if (npc > 0) {
     const int ptiles = E / 256;
     const int want = std::max<int>((int)ceil_div(T, RT_NMAX), std::min<int>(npc / ptiles, (int)ceil_div(T, RP_NROUND)));

@@ -22,6 +22,9 @@ bf16_t4096_fwdbwd      4096    2048  512  10  512  512  bf16   forward + backwar
 bf16_e64_t512          512     2048  64   10  512  512  bf16   small profiling case:
                                                                80 routes per expert
                                                                as at T=4096, ~1 GB
+bf16_smoke             300     256   256  4   256  512  bf16   smallest shape on every
+                                                               tensor-core kernel
+                                                               (forward and backward)
 =====================  ======  ====  ===  ==  ===  ===  =====  ====================
 
 Distributions: x ~ N(0,1); every weight ~ N(0, 0.02) (the router weight is
@@ -84,6 +87,7 @@ CONFIGS = {
     "bf16_t16384_zipf": MoEConfig("bf16_t16384_zipf", 16384, 2048, 512, 10, 512, 512, "bf16", zipf=True),
     "bf16_t4096_fwdbwd": MoEConfig("bf16_t4096_fwdbwd", 4096, 2048, 512, 10, 512, 512, "bf16", backward=True),
     "bf16_e64_t512": MoEConfig("bf16_e64_t512", 512, 2048, 64, 10, 512, 512, "bf16", backward=True),
+    "bf16_smoke": MoEConfig("bf16_smoke", 300, 256, 256, 4, 256, 512, "bf16", backward=True),
 }
 
 
