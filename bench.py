@@ -2,7 +2,8 @@
 
 One step = one forward of the layer over one batch of T tokens (router,
 top-k and gate, dispatch permute, grouped SwiGLU experts with the shared
-expert, ordered combine) through the C ABI, inputs resident in HBM.  The
+expert, ordered combine) through the C ABI's moe_forward, inputs resident in
+HBM.  The
 default workload is bf16_t8192 (T=8192, H=2048, 512 experts top-10, I=Is=512);
 the expert weights (3.2 GB) exceed L2, so no flush is needed between steps.
 
@@ -11,7 +12,9 @@ Prints ONE JSON line (rank 0).  Keys beyond the basic contract:
                the host<->device copies of x and y inside the timed region
                (copies on their own streams, two alternating buffers, so a
                step's copies overlap its neighbours' compute)
-  roofline     the dominant operation (moe_grouped_ffn) against measured HBM
+  roofline     the dominant operation (moe_grouped_ffn) against measured HBM,
+               its launches timed by CUDA events in a second loop of K steps
+               that calls the four steps one by one (step_by_step)
   layer_roofline  the whole step against max(bytes/HBM, FLOPs/tensor peak)
   cpu_baseline the FP64 oracle on the host cores, on a bounded token sample
   clocks       nvidia-smi samples taken during the timed region
@@ -21,6 +24,9 @@ Prints ONE JSON line (rank 0).  Keys beyond the basic contract:
   step_ms      p10 / p50 / p90 of the per-step times (also in fwd_bwd)
   extra_forward  the forward at T=1024 and at T=16384 with Zipf-skewed
                routing (same layer), reported beside the headline
+  etp_slice    one expert-tensor-parallel rank's grouped FFN (128-feature
+               slices) at T=8192: two kernels with h through HBM against
+               the fused kernel that keeps h in shared memory
 
 --impl reference times the oracle itself (the reference arm) on the host.
 Multi-GPU (torchrun): every rank runs its own replica of the workload
@@ -41,10 +47,13 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "MoE layer tokens/sec (fwd, fwd+bwd) on 1 GB300; % of layer roofline"
-# Kernels one forward step launches: router weight split, router, top-k/gate;
-# the permute (one launch on a cluster of sixteen CTAs); item tables (2),
-# gate_up, down; combine.
-LAUNCHES_PER_STEP = 9
+# Kernels one forward step (moe_forward) launches: router weight split,
+# router, top-k/gate; the permute (one launch on a cluster of sixteen CTAs,
+# which also writes the grouped GEMMs' item tables); gate_up, down; combine.
+LAUNCHES_PER_STEP = 7
+# The same forward as four separate calls: moe_grouped_ffn builds its own
+# item tables (2 more launches).
+LAUNCHES_PER_STEP_BY_STEP = 9
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -390,6 +399,59 @@ def widen(W_cpu: dict) -> dict:
     return {k: v.to(torch.float64).numpy() for k, v in W_cpu.items()}
 
 
+def etp_slice_bench(dev_w: dict, steps: int, warmup: int, T: int = 8192, world: int = 4) -> dict:
+    """One expert-tensor-parallel rank's FFN (rank 0 of `world`, 128-feature
+    slices of I and Is) at T tokens: the two grouped GEMMs with h through
+    device memory (moe_grouped_ffn_etp) against the fused form that keeps h
+    in shared memory (moe_grouped_ffn_etp_fused), CUDA events, same inputs
+    and routes; the partial rows must agree bit for bit."""
+    import torch
+    import top_routed_grouped_gb300 as moe
+    from top_routed_grouped_gb300 import etp
+    from top_routed_grouped_gb300 import inputs as I
+    E, H, k = dev_w["w_router"].shape[0], dev_w["w_router"].shape[1], 10
+    I_full, Is_full = dev_w["w_down"].shape[-1], dev_w["ws_down"].shape[-1]
+    x = I.normal((T, H), 0, I._STREAM["x"], 1.0, torch.bfloat16).cuda()
+    r = moe.route(x, dev_w["w_router"], dev_w["w_shared_gate"], k)
+    pm = moe.permute(r["topk_ids"], E)
+    rng, rng_sh = etp.feature_ranges(I_full, world)[0], etp.feature_ranges(Is_full, world)[0]
+    wg, wd, wsg, wsd = etp.rank_weights(dev_w["w_gate_up"], dev_w["w_down"], dev_w["ws_gate_up"], dev_w["ws_down"],
+                                        rng, rng_sh)
+    d = moe.make_dims(T, H, E, k, rng[1] - rng[0], rng_sh[1] - rng_sh[0], torch.bfloat16)
+    ws = moe.workspace(d, "grouped_ffn")
+    outs = {}
+    res = {"workload": f"rank 0 of {world}: I and Is slices of {rng[1] - rng[0]} features, T={T}, k={k}, E={E}",
+           "api": "moe_grouped_ffn_etp vs moe_grouped_ffn_etp_fused"}
+    for name, fused in (("two_kernels", False), ("fused", True)):
+        pr = torch.empty(T * k, H, dtype=torch.float32, device="cuda")
+        ps = torch.empty(T, H, dtype=torch.float32, device="cuda")
+
+        def call():
+            if fused:
+                moe.moe_grouped_ffn_etp_fused(d, x, pm["expert_offsets"], pm["sorted_route"], wg, wd, wsg, wsd, pr,
+                                              ps, ws)
+            else:
+                moe.moe_grouped_ffn_etp(d, x, pm["expert_offsets"], pm["sorted_route"], wg, wd, wsg, wsd, pr, ps,
+                                        None, ws)
+        for _ in range(warmup):
+            call()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        stream = torch.cuda.current_stream()
+        for i in range(steps):
+            evs[i].record(stream)
+            call()
+        evs[steps].record(stream)
+        torch.cuda.synchronize()
+        res[name + "_ms"] = percentiles([evs[i].elapsed_time(evs[i + 1]) for i in range(steps)])["p50"]
+        outs[name] = (pr, ps)
+    if moe.moe_device_status(reset=True) != 0:
+        raise RuntimeError("a kernel recorded a failed device-side check (ETP slice)")
+    res["bitwise_equal"] = bool(torch.equal(outs["fused"][0], outs["two_kernels"][0]) and
+                                torch.equal(outs["fused"][1], outs["two_kernels"][1]))
+    res["fused_gain"] = 1.0 - res["fused_ms"] / res["two_kernels_ms"]
+    return res
+
+
 def cpu_oracle_baseline(cfg, x_cpu, W_cpu, bias, budget_s: float = 20.0, max_tokens: int | None = None,
                         f64: dict | None = None) -> dict:
     """Time the FP64 oracle (routing + experts + combine) on the first tokens
@@ -530,16 +592,28 @@ def main():
     ws = torch.empty(max(moe.moe_workspace_size(d, op) for op in ("route", "permute", "grouped_ffn")),
                      dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
+    fws = moe.workspace(d, "forward")
+    f_out = {"x": dev["x"], "w_router": dev["w_router"], "router_bias": dev["router_bias"],
+             "w_shared_gate": dev["w_shared_gate"], "w_gate_up": dev["w_gate_up"], "w_down": dev["w_down"],
+             "ws_gate_up": dev["ws_gate_up"], "ws_down": dev["ws_down"], "y": o["y"], "topk_ids": o["ids"],
+             "topk_w": o["w"], "shared_sig": o["sig"], "expert_offsets": o["off"], "sorted_route": o["srt"],
+             "route_pos": o["pos"], "y_routed": o["yr"], "y_shared": o["ys"]}
 
-    def step(ev=None):
-        if ev: ev[0].record(stream)
+    def step():
+        """One layer forward: moe_forward (router weight split, router, top-k
+        and gate, permute with the item tables, gate_up, down, combine)."""
+        moe.moe_forward(d, f_out, fws, stream)
+
+    def step_by_step(ev):
+        """The same forward as the four calls one by one, with events around
+        moe_grouped_ffn (the dominant operation's launches)."""
         moe.moe_route(d, dev["x"], dev["w_router"], dev["router_bias"], dev["w_shared_gate"], o["ids"], o["w"],
                       o["sig"], None, ws, stream)
         moe.moe_permute(d, o["ids"], o["off"], o["srt"], o["pos"], ws, stream)
-        if ev: ev[1].record(stream)
+        ev[0].record(stream)
         moe.moe_grouped_ffn(d, dev["x"], o["off"], o["srt"], dev["w_gate_up"], dev["w_down"], dev["ws_gate_up"],
                             dev["ws_down"], o["yr"], o["ys"], None, ws, stream)
-        if ev: ev[2].record(stream)
+        ev[1].record(stream)
         moe.moe_combine(d, o["yr"], o["ys"], o["w"], o["sig"], o["y"], stream)
 
     for _ in range(args.warmup):
@@ -548,27 +622,42 @@ def main():
     moe.moe_device_status(reset=True)
     active = int((o["off"][1:] - o["off"][:-1] > 0).sum().item())
 
-    # ---- device-timed region ----
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- device-timed region: K forward steps through moe_forward ----
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
     clocks.begin()
-    start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
-    end.record(stream)
+        evs[i].record(stream)
+        step()
+    evs[args.steps].record(stream)
     torch.cuda.synchronize()
     clocks.end()
     clk = clocks.stop()
     barrier(world)
-    ms_local = start.elapsed_time(end) / args.steps
-    ffn_ms = statistics.mean(evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps))
+    ms_local = evs[0].elapsed_time(evs[args.steps]) / args.steps
     ms = max_over_ranks(ms_local, world)
     if moe.moe_device_status(reset=True) != 0:
         raise RuntimeError("a kernel recorded a failed device-side check during the timed region")
+    y_ref = o["y"].clone()
+
+    # ---- the dominant operation: K steps of the step-by-step calls, events around moe_grouped_ffn ----
+    for _ in range(args.warmup):
+        step_by_step([torch.cuda.Event(enable_timing=True) for _ in range(2)])
+    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s0.record(stream)
+    for i in range(args.steps):
+        step_by_step(fevs[i])
+    s1.record(stream)
+    torch.cuda.synchronize()
+    ffn_ms = statistics.mean(fevs[i][0].elapsed_time(fevs[i][1]) for i in range(args.steps))
+    sbs_ms = s0.elapsed_time(s1) / args.steps
+    if not torch.equal(o["y"], y_ref):
+        raise RuntimeError("the step-by-step forward differs from moe_forward")
 
     # ---- end to end: pinned host x -> device, moe_forward, y -> pinned host ----
     # Every step copies its x in and its y out through pinned host memory.
@@ -581,7 +670,6 @@ def main():
     x_buf = [torch.empty_like(dev["x"]) for _ in range(2)]
     y_buf = [torch.empty_like(o["y"]) for _ in range(2)]
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
-    fws = moe.workspace(d, "forward")
     fargs = [{"x": x_buf[b], "w_router": dev["w_router"], "router_bias": dev["router_bias"],
               "w_shared_gate": dev["w_shared_gate"], "w_gate_up": dev["w_gate_up"], "w_down": dev["w_down"],
               "ws_gate_up": dev["ws_gate_up"], "ws_down": dev["ws_down"], "y": y_buf[b]} for b in range(2)]
@@ -620,7 +708,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
-    if not torch.equal(y_buf[0], o["y"]):
+    if not torch.equal(y_buf[0], y_ref):
         raise RuntimeError("the end-to-end forward differs from the device-timed forward")
 
     peaks, peak_src = load_peaks()
@@ -650,7 +738,10 @@ def main():
                            "frac": t_roof_ms / ms, "peak_hbm_gbs": hbm, "peak_bf16_tflops": peaks["bf16_tflops"],
                            "peak_source": peak_src},
         "clocks": clk,
-        "step_ms": percentiles([evs[i][0].elapsed_time(evs[i + 1][0]) for i in range(args.steps - 1)]),
+        "step_ms": percentiles([evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]),
+        "step_by_step": {"ms_per_step": sbs_ms, "api": "moe_route, moe_permute, moe_grouped_ffn, moe_combine",
+                         "launches_per_step": LAUNCHES_PER_STEP_BY_STEP,
+                         "note": "the timed loop of the roofline's moe_grouped_ffn launches"},
     }
     if not args.no_fwd_bwd and cfg.dtype == "bf16":
         del o, ws, fws
@@ -660,6 +751,7 @@ def main():
         line["fwd_bwd"] = fwd_bwd_bench(fb_cfg, dev, args.steps, args.warmup, world, peaks)
     if world == 1 and not args.no_extra and cfg.name == "bf16_t8192":
         line["extra_forward"] = [extra_forward(n, dev, 50, 5, peaks) for n in ("bf16_t1024", "bf16_t16384_zipf")]
+        line["etp_slice"] = etp_slice_bench(dev, 50, 5)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         W = {kk: v for kk, v in cpu.items() if kk not in ("x", "dy", "router_bias")}
         line["cpu_baseline"] = cpu_oracle_baseline(cfg, cpu["x"], W, cpu["router_bias"])

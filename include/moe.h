@@ -24,6 +24,7 @@
  *   moe_backward     all gradients, reduced in fixed orders
  *   moe_backward_ep  one rank's part of moe_backward under an expert partition
  *   moe_grouped_ffn_etp, moe_etp_reduce  the grouped FFN with I split across ranks
+ *   moe_grouped_ffn_etp_fused  one rank's slice with gate_up and down fused (h on chip)
  *   moe_forward      the four forward calls in sequence, intermediates in the
  *                    caller's workspace
  *
@@ -330,6 +331,32 @@ int moe_grouped_ffn_etp(const moe_dims_t *d, const void *x, const int32_t *exper
                         const int32_t *sorted_route, const void *w_gate_up, const void *w_down, const void *ws_gate_up,
                         const void *ws_down, float *yr_partial, float *ys_partial, const moe_saved_t *saved, void *ws,
                         size_t ws_bytes, void *stream);
+
+/*
+ * moe_grouped_ffn_etp_fused -- moe_grouped_ffn_etp for a 128-feature slice
+ * with the two projections fused: the intermediate h of a tile of rows stays
+ * in shared memory between the gate_up and the down GEMM instead of going
+ * through device memory.  Same passages as moe_grouped_ffn_etp (#503 commit
+ * message, bullet "TP4 block": every expert on every rank; "Experts":
+ * per-route gate_up and down projections).
+ * The partial rows equal moe_grouped_ffn_etp's bit for bit (the same
+ * roundings, every output one MMA chain over K in the same order).
+ *
+ *   d               as moe_grouped_ffn_etp; bf16 only, with I = Is = 128 (one
+ *                   rank's slice, e.g. I = 512 over four ranks) and H a
+ *                   multiple of 128; other shapes return MOE_ERR_UNSUPPORTED
+ *   x, expert_offsets, sorted_route, the weight slices, yr_partial,
+ *   ys_partial      as moe_grouped_ffn_etp (no saved activations: h is never
+ *                   written out, so a training step saves it with
+ *                   moe_grouped_ffn_etp instead)
+ *   ws              at least moe_workspace_size(d, MOE_OP_GROUPED_FFN) bytes
+ * Errors: MOE_ERR_INVALID_ARG for a NULL or misaligned buffer,
+ * MOE_ERR_WORKSPACE for a short workspace; nothing is launched then.
+ */
+int moe_grouped_ffn_etp_fused(const moe_dims_t *d, const void *x, const int32_t *expert_offsets,
+                              const int32_t *sorted_route, const void *w_gate_up, const void *w_down,
+                              const void *ws_gate_up, const void *ws_down, float *yr_partial, float *ys_partial,
+                              void *ws, size_t ws_bytes, void *stream);
 
 /*
  * moe_etp_reduce -- the routed and shared rows from the ranks' partial sums:

@@ -116,3 +116,68 @@ def test_reduce_rejects_bad_part_counts():
         parts = [torch.zeros(1, 4, device="cuda") for _ in range(n)]
         with pytest.raises(moe.MoEError):
             moe.moe_etp_reduce(dims, parts, parts, y, y)
+
+
+def rank_partials(d, k, rng, rng_sh, bias=None, fused=False):
+    """One rank's FP32 partial rows through moe_grouped_ffn_etp(_fused)."""
+    x = d["x"]
+    T, H = x.shape
+    E = d["w_router"].shape[0]
+    r = moe.route(x, d["w_router"], d["w_shared_gate"], k, router_bias=bias)
+    pm = moe.permute(r["topk_ids"], E)
+    wg, wd, wsg, wsd = etp.rank_weights(d["w_gate_up"], d["w_down"], d["ws_gate_up"], d["ws_down"], rng, rng_sh)
+    dims = moe.make_dims(T, H, E, k, rng[1] - rng[0], rng_sh[1] - rng_sh[0], x.dtype)
+    pr = torch.full((T * k, H), float("nan"), device="cuda")
+    ps = torch.full((T, H), float("nan"), device="cuda")
+    ws = moe.workspace(dims, "grouped_ffn")
+    if fused:
+        moe.moe_grouped_ffn_etp_fused(dims, x, pm["expert_offsets"], pm["sorted_route"], wg, wd, wsg, wsd, pr, ps, ws)
+    else:
+        moe.moe_grouped_ffn_etp(dims, x, pm["expert_offsets"], pm["sorted_route"], wg, wd, wsg, wsd, pr, ps, None, ws)
+    return pr, ps
+
+
+@pytest.mark.parametrize("T,zipf", [(37, False), (1024, False), (8192, False), (4096, True)])
+def test_fused_slice_equals_two_kernel_slice(T, zipf):
+    """The fused gate_up -> down of a 128-feature slice (h kept in shared
+    memory) gives the two-kernel path's FP32 partial rows bit for bit, for
+    every rank of a four-way split: ragged row tiles (T = 37), one item per
+    expert (T = 1024), about 160 rows per expert (T = 8192), and long skewed
+    segments of many 128-row items (Zipf routing)."""
+    W = to_dev(full_weights())
+    d = dict(W, x=full_x(T).cuda())
+    bias = I.zipf_bias(512).cuda() if zipf else None
+    ranges, ranges_sh = etp.feature_ranges(512, 4), etp.feature_ranges(512, 4)
+    for rank, (rng, rng_sh) in enumerate(zip(ranges, ranges_sh)):
+        ref_r, ref_s = rank_partials(d, 10, rng, rng_sh, bias)
+        got_r, got_s = rank_partials(d, 10, rng, rng_sh, bias, fused=True)
+        assert torch.equal(bits(got_r), bits(ref_r)), f"rank {rank}: routed partials"
+        assert torch.equal(bits(got_s), bits(ref_s)), f"rank {rank}: shared partials"
+    assert moe.moe_device_status(reset=True) == 0
+
+
+def test_fused_split_matches_oracle():
+    W = full_weights()
+    T = 1024
+    x = full_x(T)
+    d = to_dev(dict(W, x=x))
+    out = etp.forward_simulated(d["x"], *[d[n] for n in WKEYS], 10, 4, fused=True)
+    assert moe.moe_device_status(reset=True) == 0
+    ref = run(d, 10, 4)
+    for key in ("y", "y_routed", "y_shared"):
+        assert torch.equal(bits(out[key]), bits(ref[key])), key
+    r = out["route"]
+    sample = np.array([0, 1, 2, 100, 511, 777, 1023])
+    st = torch.as_tensor(sample, device="cuda")
+    ids = r["topk_ids"].cpu().numpy()[sample]
+    w = r["topk_w"].double().cpu().numpy()[sample]
+    sig = r["shared_sig"].double().cpu().numpy()[sample]
+    assert_bf16_close(out["y"][st], oracle_rows(x[sample], ids, w, sig, W), "y, 4 ranks (fused slices)")
+
+
+def test_fused_rejects_other_slice_widths():
+    W = to_dev(full_weights())
+    d = dict(W, x=full_x(64).cuda())
+    with pytest.raises(moe.MoEError) as e:  # two ranks: 256-feature slices
+        rank_partials(d, 10, (0, 256), (0, 256), fused=True)
+    assert e.value.status == -2

@@ -29,7 +29,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3:
 EXPORTED = ("moe_workspace_size", "moe_status_string", "moe_route", "moe_permute", "moe_grouped_ffn",
             "moe_combine", "moe_forward", "moe_backward", "moe_device_status", "moe_permute_noalloc",
             "moe_route_replay", "moe_grouped_ffn_ep", "moe_combine_sorted", "moe_router_logits",
-            "moe_backward_ep", "moe_grouped_ffn_etp", "moe_etp_reduce")
+            "moe_backward_ep", "moe_grouped_ffn_etp", "moe_etp_reduce", "moe_grouped_ffn_etp_fused")
 
 _vp = ctypes.c_void_p
 
@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
                 "moe_grouped_ffn_etp": ([D] + [_vp] * 9 + [ctypes.POINTER(Saved), _vp, ctypes.c_size_t, _vp],
                                         ctypes.c_int),
                 "moe_etp_reduce": ([D, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
+                "moe_grouped_ffn_etp_fused": ([D] + [_vp] * 9 + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_forward": ([D, ctypes.POINTER(FwdArgs), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_backward": ([D, ctypes.POINTER(BwdArgs), _vp, ctypes.c_size_t, _vp], ctypes.c_int),
                 "moe_backward_ep": ([D, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(BwdArgs), _vp,
@@ -227,6 +228,15 @@ def moe_grouped_ffn_etp(d, x, expert_offsets, sorted_route, w_gate_up, w_down, w
         ctypes.byref(d), _p(x), _p(expert_offsets), _p(sorted_route), _p(w_gate_up), _p(w_down), _p(ws_gate_up),
         _p(ws_down), _p(yr_partial), _p(ys_partial), ctypes.byref(sv), _p(ws), 0 if ws is None else ws.numel(),
         _stream(stream)))
+
+
+def moe_grouped_ffn_etp_fused(d, x, expert_offsets, sorted_route, w_gate_up, w_down, ws_gate_up, ws_down,
+                              yr_partial, ys_partial, ws, stream=None):
+    """moe_grouped_ffn_etp for a 128-feature slice with gate_up and down fused
+    (h kept on chip; no saved activations), same partial rows bit for bit."""
+    _check("moe_grouped_ffn_etp_fused", lib().moe_grouped_ffn_etp_fused(
+        ctypes.byref(d), _p(x), _p(expert_offsets), _p(sorted_route), _p(w_gate_up), _p(w_down), _p(ws_gate_up),
+        _p(ws_down), _p(yr_partial), _p(ys_partial), _p(ws), 0 if ws is None else ws.numel(), _stream(stream)))
 
 
 def moe_etp_reduce(d, yr_parts, ys_parts, y_routed, y_shared, stream=None):

@@ -371,6 +371,30 @@ MOE_API int moe_grouped_ffn_etp(const moe_dims_t *d, const void *x, const int32_
   return cuda_status(launch_ffn_tc(a, sc.tiles, device_status_ptr(), (cudaStream_t)stream));
 }
 
+MOE_API int moe_grouped_ffn_etp_fused(const moe_dims_t *d, const void *x, const int32_t *expert_offsets,
+                                      const int32_t *sorted_route, const void *w_gate_up, const void *w_down,
+                                      const void *ws_gate_up, const void *ws_down, float *yr_partial, float *ys_partial,
+                                      void *ws, size_t ws_bytes, void *stream) {
+  int st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->dtype != MOE_BF16 || !etp_fused_supported(d->H, d->I, d->Is)) return MOE_ERR_UNSUPPORTED;
+  const int64_t T = d->T, R = T * d->k;
+  if (!buf_ok(x, T * d->H) || !buf_ok(expert_offsets, 1) || !buf_ok(sorted_route, R) || !buf_ok(w_gate_up, 1) ||
+      !buf_ok(w_down, 1) || !buf_ok(ws_gate_up, 1) || !buf_ok(ws_down, 1) || !buf_ok(yr_partial, R * d->H) ||
+      !buf_ok(ys_partial, T * d->H) || !opt_ok(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_size(d, MOE_OP_GROUPED_FFN) || ws_bytes < etp_fused_scratch_bytes(d->T, d->k, d->E))
+    return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  FfnArgs a;
+  a.T = d->T; a.H = d->H; a.E = d->E; a.k = d->k; a.I = d->I; a.Is = d->Is;
+  a.x = x; a.offsets = expert_offsets; a.sorted_route = sorted_route;
+  a.w_gate_up = w_gate_up; a.w_down = w_down; a.ws_gate_up = ws_gate_up; a.ws_down = ws_down;
+  a.y_routed = yr_partial; a.y_shared = ys_partial;
+  a.y_f32 = 1;
+  return cuda_status(launch_etp_fused(a, ws, device_status_ptr(), (cudaStream_t)stream));
+}
+
 MOE_API int moe_etp_reduce(const moe_dims_t *d, int32_t n_parts, const float *const *yr_parts,
                            const float *const *ys_parts, void *y_routed, void *y_shared, void *stream) {
   int st = check_dims(d);

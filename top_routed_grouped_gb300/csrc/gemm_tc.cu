@@ -1243,18 +1243,18 @@ __global__ void split_router_weight_kernel(int64_t n4, int H, const float4 *__re
 }
 
 // Item tables of two grouped GEMMs over the same segments, one block of 1024
-// threads.  start_x[s] = sum_{s' < s} ceil(n_s' / 256) * nf_s' (nf_*_r for the
-// routed segments, nf_*_s for the shared segment n_E = T); items[it] =
-// (segment, M-tile pair, first row, rows): the rows of a segment are cut into
-// ceil(n / 256) tiles of equal size rounded up to 16, a cut that depends only
-// on the segment's own length.  One block forms the prefixes; the expansion
+// threads.  start_x[s] = sum_{s' < s} ceil(n_s' / tile) * nf_s' (nf_*_r for
+// the routed segments, nf_*_s for the shared segment n_E = T; tile = 256 rows
+// for the grouped GEMMs); items[it] = (segment, M-tile pair, first row, rows):
+// the rows of a segment are cut into ceil(n / tile) tiles of equal size
+// rounded up to 16, a cut that depends only on the segment's own length.  One block forms the prefixes; the expansion
 // runs one warp per segment.
 constexpr int IT_MAX_E = 1024;
 
 __global__ void __launch_bounds__(1024)
 item_tables_kernel(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s, const int32_t *__restrict__ offsets,
                    int32_t *__restrict__ start_a, int32_t *__restrict__ start_b, int e_begin, int e_end,
-                   int with_shared) {
+                   int with_shared, int tile) {
   griddep_launch();
   griddep_wait();
   __shared__ int32_t s_off[IT_MAX_E + 1], s_a[IT_MAX_E + 2], s_b[IT_MAX_E + 2];
@@ -1266,8 +1266,8 @@ item_tables_kernel(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s,
   for (int base = 0; base <= E; base += 1024) {
     const int s = base + threadIdx.x;
     int32_t v = 0;
-    if (s < E) v = (s >= e_begin && s < e_end) ? (int32_t)ceil_div(s_off[s + 1] - s_off[s], 256) : 0;
-    else if (s == E) v = with_shared ? (int32_t)ceil_div(T, 256) : 0;
+    if (s < E) v = (s >= e_begin && s < e_end) ? (int32_t)ceil_div(s_off[s + 1] - s_off[s], tile) : 0;
+    else if (s == E) v = with_shared ? (int32_t)ceil_div(T, tile) : 0;
     buf[threadIdx.x] = v;
     __syncthreads();
     for (int d = 1; d < 1024; d <<= 1) {
@@ -1299,7 +1299,7 @@ item_tables_kernel(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s,
 __global__ void __launch_bounds__(256)
 item_expand_kernel(int E, int T, const int32_t *__restrict__ offsets, const int32_t *__restrict__ start_a,
                    const int32_t *__restrict__ start_b, int4 *__restrict__ items_a, int4 *__restrict__ items_b,
-                   int max_a, int max_b) {
+                   int max_a, int max_b, int tile) {
   griddep_launch();
   griddep_wait();
   const int sg = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
@@ -1308,7 +1308,7 @@ item_expand_kernel(int E, int T, const int32_t *__restrict__ offsets, const int3
   const int n_s = sg == E ? T : __ldg(offsets + sg + 1) - base;
   if (n_s == 0 || __ldg(start_a + sg + 1) == __ldg(start_a + sg) && __ldg(start_b + sg + 1) == __ldg(start_b + sg))
     return;  // empty, or outside the expert range
-  const int ntile = (n_s + 255) >> 8;
+  const int ntile = (n_s + tile - 1) / tile;
   const int rpt = ((n_s + ntile - 1) / ntile + 15) & ~15;
   const int a0 = __ldg(start_a + sg), na = __ldg(start_a + sg + 1) - a0;
   const int b0 = __ldg(start_b + sg), nb = __ldg(start_b + sg + 1) - b0;
@@ -1513,14 +1513,15 @@ static int64_t max_items(int T, int k, int E, int nf_routed, int nf_shared) {
 
 cudaError_t launch_item_tables(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s, const int32_t *offsets,
                                int32_t *start_a, int32_t *start_b, int4 *items_a, int4 *items_b, int max_a,
-                               int max_b, cudaStream_t stream, int e_begin, int e_end, int with_shared) {
-  if (E > IT_MAX_E) return cudaErrorInvalidValue;
+                               int max_b, cudaStream_t stream, int e_begin, int e_end, int with_shared, int tile) {
+  if (E > IT_MAX_E || tile < 16 || tile > 256 || tile % 16) return cudaErrorInvalidValue;
   if (e_end < 0) e_end = E;
   cudaError_t e = launch_pdl(item_tables_kernel, dim3(1), dim3(1024), 0, stream, E, T, nf_a_r, nf_a_s, nf_b_r, nf_b_s,
-                             offsets, start_a, start_b, e_begin, e_end, with_shared);
+                             offsets, start_a, start_b, e_begin, e_end, with_shared, tile);
   if (e != cudaSuccess) return e;
   return launch_pdl(item_expand_kernel, dim3((unsigned)ceil_div((int64_t)(E + 1) * 32, 256)), dim3(256), 0, stream, E,
-                    T, offsets, (const int32_t *)start_a, (const int32_t *)start_b, items_a, items_b, max_a, max_b);
+                    T, offsets, (const int32_t *)start_a, (const int32_t *)start_b, items_a, items_b, max_a, max_b,
+                    tile);
 }
 
 static size_t round256(size_t b) { return (b + 255) / 256 * 256; }

@@ -18,15 +18,14 @@
 // layout (one 3-D TMA box per stage: 4 blocks of 64 features x 64 K rows);
 // the gradient rows are the K-major N operand (TMA row boxes).
 //
-// Weight gradients (persistent kernel tc_wgrad_kernel, items = a 128 x 256
+// Weight gradients (persistent kernel tc_wgrad_kernel, items = a 128 x 128
 // output tile of one segment, K = the segment's rows in ascending order):
 //   WGRAD_DOWN     dWdn[e][h, i] = sum_j dYr[j, h] h[j, i]
 //   WGRAD_GATE_UP  dWgu[e][f, h] = sum_j dGU[j, f] x[tok(j), h]
 // Both operands are MN-major (a row j of the activations is one K line);
 // rows past the segment's end in its last K block are zeroed in shared
-// memory before the MMAs read them, x rows are gathered by eight warps with
-// cp.async (zero-filled past the end).  Two TMEM accumulators alternate, so
-// the epilogue of one tile overlaps the MMAs of the next; each epilogue warp
+// memory before the MMAs read them.  Four TMEM accumulators rotate, so
+// the epilogue of one tile overlaps the MMAs of the next ones; each epilogue warp
 // copies its whole share of an accumulator into registers and releases it at
 // once, then stages 32 x 32 FP32 sub-tiles in shared memory and writes them
 // with TMA stores (L2 evict-first).  Empty segments get zero tiles (every
@@ -340,18 +339,25 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
 // ===========================================================================
 // Weight gradients
 // ===========================================================================
-// A stage holds one K block of both operands: A = 2 blocks (128 M) and B = 4
-// blocks (256 N) of 64 MN elements, each block hb K lines of 128 bytes, where
+// A stage holds one K block of both operands: A = 2 blocks (128 M) and B =
+// WG_NBLK blocks (WG_N) of 64 MN elements, each block hb K lines of 128 bytes, where
 // hb (64, 32 or 16) is the smallest box height that covers the rows left in
 // the segment; the lines past the segment's end that the K = 16 MMAs read
 // (at most 15 per block) are zeroed by a dedicated warp before the stage is
 // released to the MMA thread.
 // WG_EPI_WARPS epilogue warps (warps 2..), WG_EPI_WARPS / 4 per TMEM lane quarter, each
-// draining WG_COLS of the 256 accumulator columns through WG_NSTG staging tiles.
-constexpr int WG_STAGES = 3, WG_EPI_WARPS = 8, WG_NSTG = 2;
-constexpr int WG_COLS = 1024 / WG_EPI_WARPS;
-constexpr int WG_A_BYTES = 2 * 8192;  // 128 M x 64 K lines, MN-major
-constexpr int WG_B_BYTES = 4 * 8192;  // 256 N x 64 K lines, MN-major
+// draining WG_COLS of the WG_N accumulator columns through WG_NSTG staging tiles.
+// WG_N output columns per tile (256 or 128): TMEM holds 512 / WG_N accumulators.
+// 128 x 128 tiles with four operand stages: the gradient store stream paces
+// these kernels, and the smaller stages let the loads run further ahead of
+// it (T=4096 backward 2.08 -> 2.02 ms against 128 x 256 tiles with three
+// stages; three stages with three staging tiles per warp, five stages with
+// one, and sixteen epilogue warps were all slower).
+constexpr int WG_N = 128, WG_STAGES = 4, WG_EPI_WARPS = 8, WG_NSTG = 2;
+constexpr int WG_NBUF = 512 / WG_N, WG_NBLK = WG_N / 64;
+constexpr int WG_COLS = 4 * WG_N / WG_EPI_WARPS;
+constexpr int WG_A_BYTES = 2 * 8192;        // 128 M x 64 K lines, MN-major
+constexpr int WG_B_BYTES = WG_NBLK * 8192;  // WG_N N x 64 K lines, MN-major
 constexpr int WG_STG_BYTES = 4096;    // one 32 x 32 FP32 store tile
 constexpr int WG_TAIL_WARP = GT_EPI_FIRST + WG_EPI_WARPS;  // zeroes segment tails, then releases the stage
 // TMA tile store with an L2 cache policy (the weight gradients are written
@@ -370,7 +376,7 @@ static_assert(WG_SMEM <= 232448, "wgrad shared memory");
 
 struct WgMaps {
   CUtensorMap a[3], a_sh[3];  // A^T operand rows, boxes (64, hb, 2) for hb = 64, 32, 16
-  CUtensorMap b[3], b_sh[3];  // B^T operand rows, boxes (64, hb, 4)
+  CUtensorMap b[3], b_sh[3];  // B^T operand rows, boxes (64, hb, WG_NBLK)
   CUtensorMap out, out_sh;    // FP32 gradients, 32 x 32 boxes
 };
 
@@ -428,7 +434,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
   uint8_t *zero_tile = stg_all + WG_NSTG * WG_EPI_WARPS * WG_STG_BYTES;
   uint64_t *bars = (uint64_t *)(zero_tile + WG_STG_BYTES);
   uint64_t *full = bars, *empty = bars + WG_STAGES;
-  uint64_t *tfull = bars + 2 * WG_STAGES, *tempty = tfull + 2, *mma_done = tempty + 2;
+  uint64_t *tfull = bars + 2 * WG_STAGES, *tempty = tfull + WG_NBUF, *mma_done = tempty + WG_NBUF;
   uint64_t *ready = mma_done + 1;  // stage s landed and its tail lines are zero
   uint32_t *tmem_slot = (uint32_t *)(ready + WG_STAGES);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
@@ -442,7 +448,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
       mbar_init(&empty[s], 1);
       mbar_init(&ready[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < WG_NBUF; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 32 * WG_EPI_WARPS);
     }
@@ -482,7 +488,8 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
           mbar_arrive_expect_tx(&full[stage], bytes);
           const int row = (int)im.r0 + kb * 64;
           tma_load_3d(sa + stage * WG_A_BYTES, sh ? &maps.a_sh[hi] : &maps.a[hi], &full[stage], 0, row, im.mt * 2, pol);
-          tma_load_3d(sb + stage * WG_B_BYTES, sh ? &maps.b_sh[hi] : &maps.b[hi], &full[stage], 0, row, im.nt * 4, pol);
+          tma_load_3d(sb + stage * WG_B_BYTES, sh ? &maps.b_sh[hi] : &maps.b[hi], &full[stage], 0, row, im.nt * WG_NBLK,
+                      pol);
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == WG_STAGES) stage = 0, phase ^= 1;
@@ -501,14 +508,14 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
       int stage = 0;
       uint32_t phase = 0, cnt = 0;
       bool ok = true;
-      const uint32_t idesc = idesc_bf16_f32(128, 256) | IDESC_A_MN | IDESC_B_MN;
+      const uint32_t idesc = idesc_bf16_f32(128, WG_N) | IDESC_A_MN | IDESC_B_MN;
       WgItem nxt = wg_item(blockIdx.x, p);
       for (int it = blockIdx.x; it < p.total && ok; it += gridDim.x) {
         const WgItem im = nxt;
         if (it + (int)gridDim.x < p.total) nxt = wg_item(it + gridDim.x, p);
         if (im.rows == 0) continue;
-        const int b = cnt & 1;
-        if (!mbar_wait(&tempty[b], ((cnt >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        const int b = cnt % WG_NBUF;
+        if (!mbar_wait(&tempty[b], ((cnt / WG_NBUF) & 1) ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         for (int kb = 0; kb < im.nk; ++kb) {
           if (!mbar_wait(&ready[stage], phase, abort_flag, p.status)) { ok = false; break; }
@@ -519,7 +526,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
           const uint64_t bd = smem_desc_mn_sw128(smem_u32(sb + stage * WG_B_BYTES), lbo);
           const int nkk = (valid + 15) >> 4;
           for (int kk = 0; kk < nkk; ++kk)
-            mma_bf16(tmem + b * 256, ad + 128 * kk, bd + 128 * kk, idesc, (kb | kk) != 0);
+            mma_bf16(tmem + b * WG_N, ad + 128 * kk, bd + 128 * kk, idesc, (kb | kk) != 0);
           mma_commit(&empty[stage]);
           if (++stage == WG_STAGES) stage = 0, phase ^= 1;
         }
@@ -554,9 +561,9 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
           const int hb = 64 >> wg_box(valid);  // lines per block in this stage
           const uint32_t bytes = (uint32_t)(16 * ((valid + 15) >> 4) - valid) * 128;
           if (bytes) {
-            mbar_arrive_expect_tx(&ready[stage], 6 * bytes);
+            mbar_arrive_expect_tx(&ready[stage], (2 + WG_NBLK) * bytes);
 #pragma unroll
-            for (int blk = 0; blk < 6; ++blk) {
+            for (int blk = 0; blk < 2 + WG_NBLK; ++blk) {
               uint8_t *blk_base = blk < 2 ? sa + stage * WG_A_BYTES + blk * hb * 128
                                           : sb + stage * WG_B_BYTES + (blk - 2) * hb * 128;
               bulk_load(blk_base + valid * 128, g_zero_lines, bytes, &ready[stage]);
@@ -592,7 +599,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
       const bool sh = im.seg == p.E;
       const CUtensorMap *om = sh ? &maps.out_sh : &maps.out;
       const int mrow = (sh ? 0 : (im.seg - p.e0) * Mr) + im.mt * 128 + q * 32;
-      const int ncol = im.nt * 256 + half * WG_COLS;
+      const int ncol = im.nt * WG_N + half * WG_COLS;
       if (im.rows == 0) {
         if (lane == 0) {
           for (int cc = 0; cc < WG_COLS / 32; ++cc) tma_store_2d(om, zero_tile, ncol + cc * 32, mrow);
@@ -601,10 +608,10 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
         __syncwarp();
         continue;
       }
-      const int b = cnt & 1;
-      if (!gt_warp_wait(&tfull[b], (cnt >> 1) & 1, abort_flag, p.status)) break;
+      const int b = cnt % WG_NBUF;
+      if (!gt_warp_wait(&tfull[b], (cnt / WG_NBUF) & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t tb = tmem + b * 256 + ((uint32_t)(q * 32) << 16) + half * WG_COLS;
+      const uint32_t tb = tmem + b * WG_N + ((uint32_t)(q * 32) << 16) + half * WG_COLS;
       // The warp's whole share of the accumulator into registers, then the
       // buffer goes back to the MMA thread before any store is staged.
       constexpr int NCH = WG_COLS / 32;
@@ -743,10 +750,10 @@ cudaError_t launch_wgrad_tc(const BwArgs &a, int *status, cudaStream_t stream) {
   if (e0 != cudaSuccess) return e0;
   WgMaps md, mg;
   if (!wg_maps(md.a, a.dyr, R, a.H, 2) || !wg_maps(md.a_sh, a.dys, a.T, a.H, 2) ||
-      !wg_maps(md.b, a.h_routed, R, a.I, 4) || !wg_maps(md.b_sh, a.h_shared, a.T, a.Is, 4) ||
+      !wg_maps(md.b, a.h_routed, R, a.I, WG_NBLK) || !wg_maps(md.b_sh, a.h_shared, a.T, a.Is, WG_NBLK) ||
       !map_f32_tile(&md.out, a.dw_down, nl * a.H, a.I) || !map_f32_tile(&md.out_sh, a.dws_down, a.H, a.Is) ||
       !wg_maps(mg.a, a.dgu_routed, R, 2 * (int64_t)a.I, 2) || !wg_maps(mg.a_sh, a.dgu_shared, a.T, 2 * (int64_t)a.Is, 2) ||
-      !wg_maps(mg.b, a.x_sorted, R, a.H, 4) || !wg_maps(mg.b_sh, a.x, a.T, a.H, 4) ||
+      !wg_maps(mg.b, a.x_sorted, R, a.H, WG_NBLK) || !wg_maps(mg.b_sh, a.x, a.T, a.H, WG_NBLK) ||
       !map_f32_tile(&mg.out, a.dw_gate_up, nl * 2 * a.I, a.H) ||
       !map_f32_tile(&mg.out_sh, a.dws_gate_up, 2 * (int64_t)a.Is, a.H))
     return cudaErrorInvalidValue;
@@ -756,12 +763,12 @@ cudaError_t launch_wgrad_tc(const BwArgs &a, int *status, cudaStream_t stream) {
   p.status = status;
   p.e0 = eb;
   // down: M = H, N = I
-  p.tm_r = a.H / 128; p.tn_r = a.I / 256; p.tm_s = a.H / 128; p.tn_s = a.Is / 256;
+  p.tm_r = a.H / 128; p.tn_r = a.I / WG_N; p.tm_s = a.H / 128; p.tn_s = a.Is / WG_N;
   p.total = p.tm_s * p.tn_s + (ee - eb) * p.tm_r * p.tn_r;
   cudaError_t e = launch_wgrad<WGRAD_DOWN>(md, p, stream);
   if (e != cudaSuccess) return e;
   // gate_up: M = 2I, N = H
-  p.tm_r = 2 * a.I / 128; p.tn_r = a.H / 256; p.tm_s = 2 * a.Is / 128; p.tn_s = a.H / 256;
+  p.tm_r = 2 * a.I / 128; p.tn_r = a.H / WG_N; p.tm_s = 2 * a.Is / 128; p.tn_s = a.H / WG_N;
   p.total = p.tm_s * p.tn_s + (ee - eb) * p.tm_r * p.tn_r;
   return launch_wgrad<WGRAD_GATE_UP>(mg, p, stream);
 }

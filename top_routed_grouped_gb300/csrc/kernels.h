@@ -100,6 +100,14 @@ constexpr int ETP_MAX_PARTS = 16;
 cudaError_t launch_etp_reduce(int dtype, int n, const float *const *parts, int64_t count, void *out,
                               cudaStream_t stream);
 
+// ---- etp_fused.cu ----
+// One ETP rank's 128-feature slice (I = Is = 128, bf16) with gate_up and down
+// in one kernel, h kept in shared memory; FP32 partial rows like the y_f32
+// path of launch_ffn_tc (scratch: etp_fused_scratch_bytes).
+bool etp_fused_supported(int H, int I, int Is);
+size_t etp_fused_scratch_bytes(int T, int k, int E);
+cudaError_t launch_etp_fused(const FfnArgs &a, void *scratch, int *status, cudaStream_t stream);
+
 // ---- gemm_tc.cu (bf16 tensor-core path) ----
 size_t router_tc_scratch_bytes(int E, int H);
 // Router logits via the exact three-way bf16 split of w_router (splits = 3), or
@@ -114,12 +122,14 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
 // sort to write (false where that sort cannot build them).
 bool ffn_tc_item_tables(const FfnArgs &a, void *scratch, PermuteItems *it);
 // Item tables of two grouped GEMMs over the same segments: per segment,
-// ceil(n_s / 256) token tiles times nf_*_r (routed) or nf_*_s (shared) M-tile
-// pairs; items = int4 (segment, pair, first row, rows).
+// ceil(n_s / tile) token tiles (tile = 256 rows unless given) times nf_*_r
+// (routed) or nf_*_s (shared) M-tile pairs; items = int4 (segment, pair,
+// first row, rows).
 int64_t tc_max_items(int T, int k, int E, int nf_routed, int nf_shared);
 cudaError_t launch_item_tables(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s, const int32_t *offsets,
                                int32_t *start_a, int32_t *start_b, int4 *items_a, int4 *items_b, int max_a,
-                               int max_b, cudaStream_t stream, int e_begin = 0, int e_end = -1, int with_shared = 1);
+                               int max_b, cudaStream_t stream, int e_begin = 0, int e_end = -1, int with_shared = 1,
+                               int tile = 256);
 
 // ---- combine.cu ----
 // route_pos != nullptr: y_routed rows are in sorted order (route r at row route_pos[r]).

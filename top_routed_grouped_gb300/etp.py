@@ -69,11 +69,12 @@ def rank_weights(w_gate_up, w_down, ws_gate_up, ws_down, rng, rng_sh):
 
 
 def forward_simulated(x, w_router, w_shared_gate, w_gate_up, w_down, ws_gate_up, ws_down, k: int, world: int,
-                      router_bias=None, stream=None):
+                      router_bias=None, stream=None, fused: bool = False):
     """The layer forward with I (and Is) split over `world` ranks, run on one
     GPU: replicated routing and permutation; per rank, its weight slices and
-    one moe_grouped_ffn_etp call (FP32 partials); the rank-ordered reduction;
-    the combine.  Returns dict(y, y_routed, y_shared, parts, ranges)."""
+    one moe_grouped_ffn_etp call (FP32 partials; ``fused``: the
+    moe_grouped_ffn_etp_fused form, for 128-feature slices); the rank-ordered
+    reduction; the combine.  Returns dict(y, y_routed, y_shared, parts, ranges)."""
     import torch
     T, H = x.shape
     E = w_router.shape[0]
@@ -88,8 +89,12 @@ def forward_simulated(x, w_router, w_shared_gate, w_gate_up, w_down, ws_gate_up,
         d = moe.make_dims(T, H, E, k, rng[1] - rng[0], rng_sh[1] - rng_sh[0], x.dtype)
         pr = torch.empty(T * k, H, dtype=torch.float32, device=x.device)
         ps = torch.empty(T, H, dtype=torch.float32, device=x.device)
-        moe.moe_grouped_ffn_etp(d, x, pm["expert_offsets"], pm["sorted_route"], wg, wd, wsg, wsd, pr, ps, None,
-                                moe.workspace(d, "grouped_ffn", x.device), stream)
+        if fused:
+            moe.moe_grouped_ffn_etp_fused(d, x, pm["expert_offsets"], pm["sorted_route"], wg, wd, wsg, wsd, pr, ps,
+                                          moe.workspace(d, "grouped_ffn", x.device), stream)
+        else:
+            moe.moe_grouped_ffn_etp(d, x, pm["expert_offsets"], pm["sorted_route"], wg, wd, wsg, wsd, pr, ps, None,
+                                    moe.workspace(d, "grouped_ffn", x.device), stream)
         parts_r.append(pr)
         parts_s.append(ps)
     d = moe.make_dims(T, H, E, k, I, Is, x.dtype)
