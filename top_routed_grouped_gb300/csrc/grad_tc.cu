@@ -348,12 +348,13 @@ tc_dgrad_kernel(const __grid_constant__ DgMaps maps, const DgParams p) {
 // WG_EPI_WARPS epilogue warps (warps 2..), WG_EPI_WARPS / 4 per TMEM lane quarter, each
 // draining WG_COLS of the WG_N accumulator columns through WG_NSTG staging tiles.
 // WG_N output columns per tile (256 or 128): TMEM holds 512 / WG_N accumulators.
-// 128 x 128 tiles with four operand stages: the gradient store stream paces
-// these kernels, and the smaller stages let the loads run further ahead of
-// it (T=4096 backward 2.08 -> 2.02 ms against 128 x 256 tiles with three
-// stages; three stages with three staging tiles per warp, five stages with
-// one, and sixteen epilogue warps were all slower).
-constexpr int WG_N = 128, WG_STAGES = 4, WG_EPI_WARPS = 8, WG_NSTG = 2;
+// 128 x 128 tiles with five operand stages: the gradient store stream paces
+// these kernels and stalls whenever an accumulator waits for its operands,
+// so the smaller stages let the loads run further ahead of it (T=4096
+// backward 2.08 ms with 128 x 256 tiles and three stages, 2.02 with 128 x 128
+// and four, 1.99 with five; more staging tiles per warp instead of stages,
+// or sixteen epilogue warps, were slower).
+constexpr int WG_N = 128, WG_STAGES = 5, WG_EPI_WARPS = 8, WG_NSTG = 2;
 constexpr int WG_NBUF = 512 / WG_N, WG_NBLK = WG_N / 64;
 constexpr int WG_COLS = 4 * WG_N / WG_EPI_WARPS;
 constexpr int WG_A_BYTES = 2 * 8192;        // 128 M x 64 K lines, MN-major
@@ -371,7 +372,7 @@ __device__ inline void tma_store_2d_hint(const CUtensorMap *m, const void *src, 
 // Zero lines copied over a stage's segment tail (at most 15 lines of 128 bytes).
 __device__ __align__(128) uint4 g_zero_lines[15 * 8];
 constexpr int WG_THREADS = 32 * (WG_TAIL_WARP + 1);
-constexpr int WG_SMEM = 1024 + WG_STAGES * (WG_A_BYTES + WG_B_BYTES) + (WG_NSTG * WG_EPI_WARPS + 1) * WG_STG_BYTES + 256;
+constexpr int WG_SMEM = 1024 + WG_STAGES * (WG_A_BYTES + WG_B_BYTES) + WG_NSTG * WG_EPI_WARPS * WG_STG_BYTES + 256;
 static_assert(WG_SMEM <= 232448, "wgrad shared memory");
 
 struct WgMaps {
@@ -431,8 +432,7 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
   uint8_t *sa = base;
   uint8_t *sb = sa + WG_STAGES * WG_A_BYTES;
   uint8_t *stg_all = sb + WG_STAGES * WG_B_BYTES;
-  uint8_t *zero_tile = stg_all + WG_NSTG * WG_EPI_WARPS * WG_STG_BYTES;
-  uint64_t *bars = (uint64_t *)(zero_tile + WG_STG_BYTES);
+  uint64_t *bars = (uint64_t *)(stg_all + WG_NSTG * WG_EPI_WARPS * WG_STG_BYTES);
   uint64_t *full = bars, *empty = bars + WG_STAGES;
   uint64_t *tfull = bars + 2 * WG_STAGES, *tempty = tfull + WG_NBUF, *mma_done = tempty + WG_NBUF;
   uint64_t *ready = mma_done + 1;  // stage s landed and its tail lines are zero
@@ -440,7 +440,6 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < WG_STG_BYTES / 16; i += blockDim.x) ((uint4 *)zero_tile)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (threadIdx.x == 0) {
     for (int s = 0; s < WG_STAGES; ++s) {
@@ -600,27 +599,26 @@ tc_wgrad_kernel(const __grid_constant__ WgMaps maps, const WgParams p) {
       const CUtensorMap *om = sh ? &maps.out_sh : &maps.out;
       const int mrow = (sh ? 0 : (im.seg - p.e0) * Mr) + im.mt * 128 + q * 32;
       const int ncol = im.nt * WG_N + half * WG_COLS;
-      if (im.rows == 0) {
-        if (lane == 0) {
-          for (int cc = 0; cc < WG_COLS / 32; ++cc) tma_store_2d(om, zero_tile, ncol + cc * 32, mrow);
-          bulk_commit();
-        }
-        __syncwarp();
-        continue;
-      }
-      const int b = cnt % WG_NBUF;
-      if (!gt_warp_wait(&tfull[b], (cnt / WG_NBUF) & 1, abort_flag, p.status)) break;
-      tc_fence_after();
-      const uint32_t tb = tmem + b * WG_N + ((uint32_t)(q * 32) << 16) + half * WG_COLS;
-      // The warp's whole share of the accumulator into registers, then the
-      // buffer goes back to the MMA thread before any store is staged.
       constexpr int NCH = WG_COLS / 32;
       float v[NCH][32];
+      if (im.rows == 0) {  // an empty segment's gradient tile is zero (no accumulator is used)
 #pragma unroll
-      for (int cc = 0; cc < NCH; cc += 2) tmem_ld32x2(tb + cc * 32, tb + (cc + 1) * 32, v[cc], v[cc + 1]);
-      tc_fence_before();
-      mbar_arrive(&tempty[b]);
-      ++cnt;
+        for (int cc = 0; cc < NCH; ++cc)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[cc][j] = 0.f;
+      } else {
+        const int b = cnt % WG_NBUF;
+        if (!gt_warp_wait(&tfull[b], (cnt / WG_NBUF) & 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t tb = tmem + b * WG_N + ((uint32_t)(q * 32) << 16) + half * WG_COLS;
+        // The warp's whole share of the accumulator into registers, then the
+        // buffer goes back to the MMA thread before any store is staged.
+#pragma unroll
+        for (int cc = 0; cc < NCH; cc += 2) tmem_ld32x2(tb + cc * 32, tb + (cc + 1) * 32, v[cc], v[cc + 1]);
+        tc_fence_before();
+        mbar_arrive(&tempty[b]);
+        ++cnt;
+      }
 #pragma unroll
       for (int cc = 0; cc < NCH; ++cc) {
         uint8_t *stg = stg0 + sbuf * WG_STG_BYTES;
