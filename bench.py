@@ -365,7 +365,7 @@ def extra_forward(name: str, dev_w: dict, steps: int, warmup: int, peaks: dict) 
     T, H, E, k, Iw, Is = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.Is
     # The weights of every configuration of this layer are the same draw; x and the bias are per configuration.
     dv = dict(dev_w, x=I.normal((T, H), 0, I._STREAM["x"], 1.0, cfg.torch_dtype).cuda(),
-              router_bias=I.zipf_bias(E).cuda() if cfg.zipf else None)
+              router_bias=I.zipf_bias(E, cfg.zipf_beta, n_empty=cfg.zipf_empty).cuda() if cfg.zipf else None)
     d = moe.make_dims(T, H, E, k, Iw, Is, cfg.torch_dtype)
     off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
     fargs = {n: dv[n] for n in ("x", "w_router", "router_bias", "w_shared_gate", "w_gate_up", "w_down",
@@ -549,6 +549,10 @@ def main():
                     help="skip the forward at the 1024-token and 16384-token Zipf configurations")
     ap.add_argument("--fwd-bwd-workload", default="bf16_t4096_fwdbwd",
                     help="workload of the forward+backward measurement (same layer shape as --workload)")
+    ap.add_argument("--etp-only", action="store_true",
+                    help="only the expert-tensor-parallel slice comparison (two kernels vs fused) on the layer of "
+                         "--workload at --etp-tokens tokens, printed as one JSON object (a profiling case)")
+    ap.add_argument("--etp-tokens", type=int, default=8192)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -569,6 +573,10 @@ def main():
     if rank == 0 or not B.up_to_date():
         B.build()
     torch.cuda.set_device(local)
+    if args.etp_only:
+        w = {k: v.cuda() for k, v in I.make_inputs(cfg, T=1).items() if k not in ("x", "dy", "router_bias")}
+        print(json.dumps({"etp_slice": etp_slice_bench(w, args.steps, args.warmup, T=args.etp_tokens)}), flush=True)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))

@@ -25,6 +25,11 @@ bf16_e64_t512          512     2048  64   10  512  512  bf16   small profiling c
 bf16_smoke             300     256   256  4   256  512  bf16   smallest shape on every
                                                                tensor-core kernel
                                                                (forward and backward)
+bf16_e64_zipf_t4096    4096    2048  64   10  512  512  bf16   small profiling case of
+                                                               long skewed segments:
+                                                               Zipf bias over 64 experts
+                                                               (8 empty, beta 0.3: the
+                                                               largest gets 2304 rows)
 =====================  ======  ====  ===  ==  ===  ===  =====  ====================
 
 Distributions: x ~ N(0,1); every weight ~ N(0, 0.02) (the router weight is
@@ -67,6 +72,8 @@ class MoEConfig:
     dtype: str  # "f32" or "bf16"
     zipf: bool = False
     backward: bool = False
+    zipf_beta: float = 0.3065471947193146  # ZIPF_BETA
+    zipf_empty: int = 64                   # ZIPF_EMPTY
 
     @property
     def R(self) -> int:
@@ -88,6 +95,8 @@ CONFIGS = {
     "bf16_t4096_fwdbwd": MoEConfig("bf16_t4096_fwdbwd", 4096, 2048, 512, 10, 512, 512, "bf16", backward=True),
     "bf16_e64_t512": MoEConfig("bf16_e64_t512", 512, 2048, 64, 10, 512, 512, "bf16", backward=True),
     "bf16_smoke": MoEConfig("bf16_smoke", 300, 256, 256, 4, 256, 512, "bf16", backward=True),
+    "bf16_e64_zipf_t4096": MoEConfig("bf16_e64_zipf_t4096", 4096, 2048, 64, 10, 512, 512, "bf16", zipf=True,
+                                     zipf_beta=0.3, zipf_empty=8),
 }
 
 
@@ -155,7 +164,8 @@ def make_inputs(cfg: MoEConfig, seed: int = 0, T: int | None = None, device: str
         "w_down": normal((E, H, I), seed, _STREAM["w_down"], WEIGHT_STD, dt),
         "ws_gate_up": normal((2 * Is, H), seed, _STREAM["ws_gate_up"], WEIGHT_STD, dt),
         "ws_down": normal((H, Is), seed, _STREAM["ws_down"], WEIGHT_STD, dt),
-        "router_bias": zipf_bias(E, ZIPF_BETA if beta is None else beta) if cfg.zipf else None,
+        "router_bias": zipf_bias(E, cfg.zipf_beta if beta is None else beta, n_empty=cfg.zipf_empty)
+        if cfg.zipf else None,
     }
     if with_dy or (with_dy is None and cfg.backward):
         d["dy"] = normal((T, H), 2, _STREAM["dy"], 1.0, dt)
