@@ -239,13 +239,15 @@ class ClockSampler:
 
 
 # DRAM bytes (read + write) of one moe_grouped_ffn call (gate_up + down) at
-# bf16_t8192, from an ncu capture of the two kernels' dram__bytes_read.sum and
-# dram__bytes_write.sum counters (second forward step of
-# `bench.py --steps 3 --warmup 3 --no-cpu-baseline --no-fwd-bwd --no-extra`),
-# valid only for the kernel sources it was taken on (hash below); otherwise
-# null.
-FFN_TRAFFIC = {"sources": "0d80e7544c1ac023", "workload": "bf16_t8192",
-               "bytes": 2_197_428_224 + 64_002_304 + 1_185_130_496 + 318_316_288}
+# bf16_t8192: dram__bytes_read.sum + dram__bytes_write.sum of the two kernels
+# in the fourth forward step of
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
+#       -k regex:tc_pair_kernel -s 6 -c 2 \
+#       python bench.py --steps 3 --warmup 3 --no-cpu-baseline --no-fwd-bwd --no-extra
+# (one pass per launch), valid only for the kernel sources it was taken on
+# (hash below); otherwise null.
+FFN_TRAFFIC = {"sources": "a4180031b0e64493", "workload": "bf16_t8192",
+               "bytes": 2_196_004_608 + 66_656_256 + 1_187_334_656 + 317_994_752}
 
 
 def kernel_sources_hash() -> str:
