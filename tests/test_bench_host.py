@@ -82,3 +82,34 @@ def test_roofline_denominators_match_the_buffers():
     grad_bytes = sum(w[n].numel() * 4 for n in names)
     assert bwd["bytes"] == weight_bytes + grad_bytes + 3 * act
     assert bwd["flops"] == 2 * flops
+
+
+def test_reference_arm_line_on_cpu():
+    """The reference arm (the FP64 oracle on the host cores) prints one JSON
+    line with the contract's keys: its cpu_baseline value is the line's
+    value, its e2e moves no bytes, and its config has the same keys as the
+    GPU arm's (workload_config)."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    from top_routed_grouped_gb300 import inputs as I
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "tiny_f32", "--steps", "2", "--warmup", "3"], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 3 and line["n_gpus"] == 1
+    assert line["value"] > 0 and line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    cfg = I.CONFIGS["tiny_f32"]
+    assert set(line["config"]) == set(bench.workload_config(cfg, cfg.E, 1))
+    assert line["config"]["workload"] == "tiny_f32" and line["config"]["T"] == cfg.T

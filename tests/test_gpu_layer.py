@@ -87,3 +87,51 @@ def test_module_dx_is_batch_invariant(layer):
             parts.append(dx)
         assert torch.equal(bits(torch.cat(parts)[inv]), bits(dx_full)), f"batch {b}"
     assert moe.moe_device_status(reset=True) == 0
+
+
+def test_micro_batches_forwarded_before_backward(layer):
+    """Gradient accumulation: two micro-batches of different sizes run their
+    forwards first (the second one regrows the layer's workspace pair), then
+    one backward over both.  The saved activations are per call, so the
+    gradients equal the sum of the two calls' moe_backward results, and dx of
+    each micro-batch equals its own moe_backward dx bit for bit."""
+    layer._ws = None
+    x1 = full_x(64).cuda().requires_grad_(True)
+    x2 = full_x(1024)[64:1024].cuda().requires_grad_(True)
+    dy1, dy2 = full_dy(64).cuda(), full_dy(1024)[64:1024].cuda()
+    y1 = layer(x1)
+    y2 = layer(x2)
+    grads = torch.autograd.grad([y1, y2], [x1, x2, *layer.weights()], grad_outputs=[dy1, dy2])
+    W = [w.detach() for w in layer.weights()]
+    g1 = moe.backward(moe.forward(x1.detach(), *W, 10, save_for_backward=True), dy1, x1.detach(), *W)
+    g2 = moe.backward(moe.forward(x2.detach(), *W, 10, save_for_backward=True), dy2, x2.detach(), *W)
+    assert torch.equal(bits(grads[0]), bits(g1["dx"]))
+    assert torch.equal(bits(grads[1]), bits(g2["dx"]))
+    for got, name, p in zip(grads[2:], ("dw_router", "dw_shared_gate", "dw_gate_up", "dw_down", "dws_gate_up",
+                                        "dws_down"), W):
+        # autograd sums the two per-call gradients after casting each to the parameter dtype
+        want = g1[name].to(p.dtype) + g2[name].to(p.dtype)
+        assert torch.equal(bits(got), bits(want)), name
+    assert moe.moe_device_status(reset=True) == 0
+
+
+def test_f32_module_matches_library():
+    """An FP32 module: the weight gradients reach the parameters unrounded,
+    equal to moe_backward's FP32 outputs bit for bit."""
+    build.build()
+    cfg = I.CONFIGS["tiny_f32"]
+    c = I.make_inputs(cfg, with_dy=True)
+    m = moe.MoELayer(cfg.H, cfg.E, cfg.k, cfg.I, cfg.Is, dtype=torch.float32, device="cuda")
+    with torch.no_grad():
+        for n in WKEYS:
+            getattr(m, n).copy_(c[n])
+    x = c["x"].cuda().requires_grad_(True)
+    dy = c["dy"].cuda()
+    grads = torch.autograd.grad(m(x), [x, *m.weights()], grad_outputs=dy)
+    W = [w.detach() for w in m.weights()]
+    g = moe.backward(moe.forward(x.detach(), *W, cfg.k, save_for_backward=True), dy, x.detach(), *W)
+    assert torch.equal(bits(grads[0]), bits(g["dx"]))
+    for got, name in zip(grads[1:], ("dw_router", "dw_shared_gate", "dw_gate_up", "dw_down", "dws_gate_up",
+                                     "dws_down")):
+        assert got.dtype == torch.float32 and torch.equal(bits(got), bits(g[name])), name
+    assert moe.moe_device_status(reset=True) == 0

@@ -27,8 +27,7 @@
 // (0 <= c <= n) runs, for each output tile t of H / 128: phase-1 K blocks
 // 2t and 2t+1 of item i_c (c < n), then phase-2 tile t of item i_{c-1}
 // (c >= 1).  So the tensor cores accumulate the next item's gate/up while
-// the epilogue drains the current item's FP32 tiles (the store stream paces
-// this kernel).  The phase-1 accumulator of round c is committed after the
+// the epilogue drains the current item's FP32 tiles.  The phase-1 accumulator of round c is committed after the
 // round's last phase-2 MMA, so when the epilogue sees it, no MMA reads the
 // previous item's h any more and it can be overwritten.
 //
@@ -37,8 +36,15 @@
 // Roles: warp 0 TMA producer (weight tiles), warp 1 TMEM allocator + MMA
 // issuer, EF_EPI_WARPS epilogue warps from warp 2 (EF_WPQ per TMEM lane
 // quarter, EF_CPW columns each), then one warp that gathers the token rows of
-// phase 1 with TMA gather4.  Every wait is
-// bounded (2 s), records the device status word and drains what is in flight.
+// phase 1 with TMA gather4; the weight tile of a stage completes on full[s]
+// (armed by the producer), its gathered rows on rows[s] (armed by the gather
+// warp), so each issuing warp can wait for its own copies.  Every wait is
+// bounded (2 s), records the device status word, and on a timeout each role
+// waits for its own copies in flight before the CTA releases TMEM and exits.
+// Measured slower than the two-kernel path (the bench's etp_slice entry):
+// one SM per 128-row item fetches the slice's gate/up rows twice as often as
+// the CTA-pair kernels, and the tensor pipe idles while phase 1's
+// accumulator is turned into h.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -148,14 +154,16 @@ etp_fused_kernel(const __grid_constant__ EfMaps maps, const EfParams p) {
   uint64_t *full = bars, *empty = full + EF_STAGES;
   uint64_t *t1full = empty + EF_STAGES, *t1empty = t1full + 1, *hfull = t1empty + 1;
   uint64_t *t2full = hfull + 1, *t2empty = t2full + 2, *mma_done = t2empty + 2;
-  uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
+  uint64_t *rows = mma_done + 1;  // [EF_STAGES]: a phase-1 stage's gathered rows landed
+  uint32_t *tmem_slot = (uint32_t *)(rows + EF_STAGES);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < EF_STAGES; ++s) {
-      mbar_init(&full[s], 1);  // the producer's expect-tx arrival; the gathered rows complete bytes on it
+      mbar_init(&full[s], 1);  // the producer's expect-tx arrival (weight tile bytes)
       mbar_init(&empty[s], 1);
+      mbar_init(&rows[s], 1);  // the gather warp's expect-tx arrival (row bytes), phase-1 uses only
     }
     mbar_init(t1full, 1);
     mbar_init(t1empty, 32 * EF_EPI_WARPS);
@@ -199,8 +207,7 @@ etp_fused_kernel(const __grid_constant__ EfMaps maps, const EfParams p) {
             const bool is_p1 = c < n_mine && j < 2;
             const EfItem im = is_p1 ? cur : prev;
             if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
-            // phase 1: the weight tile and the n gathered token rows of 128 bytes
-            mbar_arrive_expect_tx(&full[stage], EF_A_BYTES + (is_p1 ? (uint32_t)im.n * 128 : 0u));
+            mbar_arrive_expect_tx(&full[stage], EF_A_BYTES);
             const bool sh = im.seg == p.E;
             if (is_p1) {  // K block 2t + j of the slice's 256 gate/up rows
               tma_load_5d(sa(stage), sh ? &maps.gu_sh : &maps.gu, &full[stage], (2 * t + j) * 64, 0, 0, 0,
@@ -227,7 +234,7 @@ etp_fused_kernel(const __grid_constant__ EfMaps maps, const EfParams p) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0, cnt2 = 0;
+      uint32_t phase = 0, cnt2 = 0, rphase = 0;  // rphase bit s: parity of rows[s]'s next phase-1 use
       bool ok = true;
       for (int c = 0; c <= n_mine && ok; ++c) {
         const EfItem cur = c < n_mine ? item_of(c) : EfItem{}, prev = c > 0 ? item_of(c - 1) : EfItem{};
@@ -241,7 +248,9 @@ etp_fused_kernel(const __grid_constant__ EfMaps maps, const EfParams p) {
           if (c < n_mine) {
             for (int j = 0; j < 2 && ok; ++j) {
               const int kb = 2 * t + j;
-              if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+              if (!mbar_wait(&full[stage], phase, abort_flag, p.status) ||
+                  !mbar_wait(&rows[stage], (rphase >> stage) & 1, abort_flag, p.status)) { ok = false; break; }
+              rphase ^= 1u << stage;
               tc_fence_after();
               const uint64_t bd = smem_desc_sw128(smem_u32(sb(stage)));
 #pragma unroll
@@ -369,12 +378,12 @@ etp_fused_kernel(const __grid_constant__ EfMaps maps, const EfParams p) {
     // ------------------------------------------------------------ row gather (phase 1)
     // Lane qd copies rows 4 qd .. 4 qd + 3 of the item (one gather4 per
     // K block, landing as four consecutive 128-byte swizzled lines at 512 qd;
-    // the bytes complete on the stage's full barrier, whose expected count
-    // the producer set).  Rows past the item's end up to n read token 0:
+    // the bytes complete on the stage's rows barrier, armed here with the
+    // item's n x 128 bytes).  Rows past the item's end up to n read token 0:
     // their accumulator columns are never stored.
     const uint64_t pol_x = policy_evict_last();
     int stage = 0;
-    uint32_t phase = 0;
+    uint32_t phase = 0, rphase = 0, issued = 0, issued_rphase = 0;
     bool ok = true;
     for (int c = 0; c <= n_mine && ok; ++c) {
       const EfItem cur = c < n_mine ? item_of(c) : EfItem{};
@@ -395,13 +404,24 @@ etp_fused_kernel(const __grid_constant__ EfMaps maps, const EfParams p) {
         for (int j = 0; j < nst; ++j) {
           if (c < n_mine && j < 2) {
             if (!warp_wait_ef(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+            if (lane == 0) mbar_arrive_expect_tx(&rows[stage], (uint32_t)cur.n * 128);
+            __syncwarp();
             if (mine)
-              tma_gather4(sb(stage) + lane * 512, &maps.x, &full[stage], (2 * t + j) * 64, t4[0], t4[1], t4[2], t4[3],
+              tma_gather4(sb(stage) + lane * 512, &maps.x, &rows[stage], (2 * t + j) * 64, t4[0], t4[1], t4[2], t4[3],
                           pol_x);
+            issued |= 1u << stage;
+            issued_rphase = (issued_rphase & ~(1u << stage)) | (rphase & (1u << stage));
+            rphase ^= 1u << stage;
           }
           if (++stage == EF_STAGES) stage = 0, phase ^= 1;
         }
       }
+    }
+    if (!ok && lane == 0) {
+      // The row copies in flight land before the CTA exits.
+      volatile int never = 0;
+      for (int s2 = 0; s2 < EF_STAGES; ++s2)
+        if (issued & (1u << s2)) mbar_wait(&rows[s2], (issued_rphase >> s2) & 1, &never, nullptr, 100000000ull);
     }
     __syncwarp();
   }

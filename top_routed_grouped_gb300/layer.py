@@ -17,7 +17,11 @@ library's bf16 dx bit for bit.  The routes are held fixed in the backward
 
 Workspaces are caller-visible: pass ``ws_forward`` / ``ws_backward`` (uint8
 device tensors of at least ``moe_workspace_size`` bytes) to ``forward``, or
-let the layer keep one pair per token count in ``MoELayer.workspaces``.
+let the layer keep one pair, grown to the largest token count seen
+(``MoELayer.workspace``).  A workspace is scratch only: the tensors saved for
+the backward are allocated per call, so several forwards may run before
+their backwards (gradient accumulation) on the layer's one pair, in stream
+order.
 """
 from __future__ import annotations
 
@@ -97,21 +101,23 @@ class MoELayer(torch.nn.Module):
         self.ws_down = mk(H, Is)
         self.register_buffer("router_bias", None if router_bias is None else
                              router_bias.to(device=dev, dtype=torch.float32))
-        self.workspaces: dict = {}
+        self._ws: tuple[torch.Tensor, torch.Tensor] | None = None
         self.last_routes: dict = {}
 
     def weights(self):
         return tuple(getattr(self, n) for n in _WKEYS)
 
     def workspace(self, T: int) -> tuple[torch.Tensor, torch.Tensor]:
-        """The forward and backward workspaces for T tokens (kept per T)."""
-        if T not in self.workspaces:
-            d = dims_of(torch.empty(T, self.w_router.shape[1], dtype=self.w_gate_up.dtype, device="meta"),
-                        self.w_router, self.w_gate_up, self.ws_gate_up, self.top_k)
-            dev = self.w_router.device
-            self.workspaces[T] = tuple(torch.empty(max(moe_workspace_size(d, op), 256), dtype=torch.uint8, device=dev)
-                                       for op in ("forward", "backward"))
-        return self.workspaces[T]
+        """The forward and backward workspaces for T tokens: the layer's one
+        pair, reallocated only when T needs more bytes than it holds."""
+        d = dims_of(torch.empty(T, self.w_router.shape[1], dtype=self.w_gate_up.dtype, device="meta"),
+                    self.w_router, self.w_gate_up, self.ws_gate_up, self.top_k)
+        need = [max(moe_workspace_size(d, op), 256) for op in ("forward", "backward")]
+        if self._ws is None or any(w.numel() < n for w, n in zip(self._ws, need)):
+            old = (0, 0) if self._ws is None else tuple(w.numel() for w in self._ws)
+            self._ws = tuple(torch.empty(max(n, o), dtype=torch.uint8, device=self.w_router.device)
+                             for n, o in zip(need, old))
+        return self._ws
 
     def forward(self, x: torch.Tensor, ws_forward: torch.Tensor | None = None,
                 ws_backward: torch.Tensor | None = None) -> torch.Tensor:
