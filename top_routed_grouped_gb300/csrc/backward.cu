@@ -95,6 +95,140 @@ combine_bwd_kernel(int T, int H, int k, const TE *__restrict__ dy, const TE *__r
   }
 }
 
+// The same step with the row held in registers: for H = NCH * 32 * VN (each
+// lane owns NCH 16-byte chunks of a row) and k <= KMAX, dy is loaded once and
+// every chunk of a routed row is requested before its dot product starts,
+// so the loads of one row (and, as the unrolled slots allow, of the next)
+// are in flight together instead of one chunk at a time.  Every sum, product
+// and store is the one above in the same order: the results are identical.
+template <typename TE, int NCH, int KMAX>
+__global__ void __launch_bounds__(128)
+combine_bwd_rows_kernel(int T, int H, int k, const TE *__restrict__ dy, const TE *__restrict__ yr,
+                        const TE *__restrict__ ys, const float *__restrict__ w, const float *__restrict__ sig,
+                        const int32_t *__restrict__ route_pos, TE *__restrict__ dyr_sorted, TE *__restrict__ dys,
+                        float *__restrict__ dlogit, float *__restrict__ dz, int yr_sorted) {
+  griddep_launch();
+  griddep_wait();
+  constexpr int VN = Vec16<TE>::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  const TE *dyr = dy + t * H + lane * VN;
+  uint4 a[NCH];
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) a[i] = __ldg((const uint4 *)(dyr + i * 32 * VN));
+  float dws[KMAX];
+#pragma unroll
+  for (int s = 0; s < KMAX; ++s) {
+    dws[s] = 0.f;
+    if (s < k) {
+      const TE *row = yr + (yr_sorted ? (int64_t)__ldg(route_pos + t * k + s) : t * k + s) * H + lane * VN;
+      uint4 b[NCH];
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) b[i] = __ldg((const uint4 *)(row + i * 32 * VN));
+      float part = 0.f;
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        float av[VN], bv[VN];
+        Vec16<TE>::unpack(a[i], av);
+        Vec16<TE>::unpack(b[i], bv);
+#pragma unroll
+        for (int j = 0; j < VN; ++j) part = fmaf(av[j], bv[j], part);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(FULL_MASK, part, off);
+      dws[s] = part;
+    }
+  }
+  float ps = 0.f;
+  {
+    uint4 b[NCH];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) b[i] = __ldg((const uint4 *)(ys + t * H + lane * VN + i * 32 * VN));
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      float av[VN], bv[VN];
+      Vec16<TE>::unpack(a[i], av);
+      Vec16<TE>::unpack(b[i], bv);
+#pragma unroll
+      for (int j = 0; j < VN; ++j) ps = fmaf(av[j], bv[j], ps);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(FULL_MASK, ps, off);
+  // router Jacobian of the softmax over the selected set, slot order
+  float wv[KMAX];
+  float wdw = 0.f;
+#pragma unroll
+  for (int s = 0; s < KMAX; ++s) {
+    wv[s] = s < k ? __ldg(w + t * k + s) : 0.f;
+    if (s < k) wdw = fmaf(wv[s], dws[s], wdw);
+  }
+  if (lane < k) {
+    float dwl = 0.f, wl = 0.f;
+#pragma unroll
+    for (int s = 0; s < KMAX; ++s)
+      if (s == lane) dwl = dws[s], wl = wv[s];
+    dlogit[t * k + lane] = wl * (dwl - wdw);
+  }
+  const float g = __ldg(sig + t);
+  if (lane == 0) dz[t] = ps * g * (1.f - g);
+  // scaled rows
+  int pos[KMAX];
+#pragma unroll
+  for (int s = 0; s < KMAX; ++s) pos[s] = s < k ? __ldg(route_pos + t * k + s) : 0;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    const int h = lane * VN + i * 32 * VN;
+    float av[VN], o[VN];
+    Vec16<TE>::unpack(a[i], av);
+#pragma unroll
+    for (int s = 0; s < KMAX; ++s) {
+      if (s < k) {
+#pragma unroll
+        for (int j = 0; j < VN; ++j) o[j] = wv[s] * av[j];
+        Vec16<TE>::store(dyr_sorted + (int64_t)pos[s] * H + h, o);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < VN; ++j) o[j] = g * av[j];
+    Vec16<TE>::store(dys + t * H + h, o);
+  }
+}
+
+template <typename TE, int NCH>
+static cudaError_t launch_combine_bwd_rows(const BwArgs &a, cudaStream_t stream) {
+  const dim3 g((unsigned)ceil_div(a.T, 4)), b(128);
+  const TE *dy = (const TE *)a.dy, *yr = (const TE *)a.y_routed, *ys = (const TE *)a.y_shared;
+  TE *dyr = (TE *)a.dyr, *dys = (TE *)a.dys;
+  if (a.k <= 8)
+    return launch_pdl(combine_bwd_rows_kernel<TE, NCH, 8>, g, b, 0, stream, a.T, a.H, a.k, dy, yr, ys, a.topk_w,
+                      a.shared_sig, a.route_pos, dyr, dys, a.dlogit, a.dz, a.yr_sorted);
+  if (a.k <= 10)
+    return launch_pdl(combine_bwd_rows_kernel<TE, NCH, 10>, g, b, 0, stream, a.T, a.H, a.k, dy, yr, ys, a.topk_w,
+                      a.shared_sig, a.route_pos, dyr, dys, a.dlogit, a.dz, a.yr_sorted);
+  return launch_pdl(combine_bwd_rows_kernel<TE, NCH, 16>, g, b, 0, stream, a.T, a.H, a.k, dy, yr, ys, a.topk_w,
+                    a.shared_sig, a.route_pos, dyr, dys, a.dlogit, a.dz, a.yr_sorted);
+}
+
+// b1: the register form when H is 1, 2, 4 or 8 chunks of 16 bytes per lane, else the loop form.
+template <typename TE>
+static cudaError_t launch_combine_bwd(const BwArgs &a, cudaStream_t stream) {
+  constexpr int VN = Vec16<TE>::N;
+  if (a.H % (32 * VN) == 0) {
+    switch (a.H / (32 * VN)) {
+      case 1: return launch_combine_bwd_rows<TE, 1>(a, stream);
+      case 2: return launch_combine_bwd_rows<TE, 2>(a, stream);
+      case 4: return launch_combine_bwd_rows<TE, 4>(a, stream);
+      case 8: return launch_combine_bwd_rows<TE, 8>(a, stream);
+      default: break;
+    }
+  }
+  return launch_pdl(combine_bwd_kernel<TE>, dim3((unsigned)ceil_div(a.T, 8)), dim3(256), 0, stream, a.T, a.H, a.k,
+                    (const TE *)a.dy, (const TE *)a.y_routed, (const TE *)a.y_shared, a.topk_w, a.shared_sig,
+                    a.route_pos, (TE *)a.dyr, (TE *)a.dys, a.dlogit, a.dz, a.yr_sorted);
+}
+
 // ---------------------------------------------------------------- tiles
 // Segment s < E: sorted rows offsets[s]..offsets[s+1]; segment E: tokens 0..T.
 constexpr int BW_BM = 32;  // rows per tile of the row-parallel GEMMs
@@ -552,9 +686,7 @@ static cudaError_t run_backward(const BwArgs &a, void *scratch, int *status, cud
 #define MOE_TRY(x) \
   if ((err = (x)) != cudaSuccess) return err
   if (phase & BWD_PHASE_EXPERTS) {
-    MOE_TRY(launch_pdl(combine_bwd_kernel<TE>, dim3((unsigned)ceil_div(a.T, 8)), dim3(256), 0, stream, a.T, a.H, a.k,
-                       (const TE *)a.dy, (const TE *)a.y_routed, (const TE *)a.y_shared, a.topk_w, a.shared_sig,
-                       a.route_pos, (TE *)a.dyr, (TE *)a.dys, a.dlogit, a.dz, a.yr_sorted));
+    MOE_TRY(launch_combine_bwd<TE>(a, stream));
     const int Imax = a.I > a.Is ? a.I : a.Is;
     if (sizeof(TE) == 2 && backward_tc_supported(a.H, a.I, a.Is)) {
       MOE_TRY(launch_dgrad_tc(a, scratch, status, stream));

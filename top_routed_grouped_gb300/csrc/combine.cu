@@ -17,7 +17,9 @@ namespace moe {
 
 // SORTED: the routed rows are in sorted order and route r's row is
 // yr[route_pos[r]] (the expert-partitioned path); otherwise yr[r].
-template <typename TE, bool SORTED>
+// KMAX >= k: the routed chunks one thread keeps in flight (a template
+// parameter so that they live in registers).
+template <typename TE, bool SORTED, int KMAX>
 __global__ void __launch_bounds__(256)
 combine_kernel(int T, int H, int k, const TE *__restrict__ yr, const TE *__restrict__ ys,
                const float *__restrict__ w, const float *__restrict__ sig, TE *__restrict__ y,
@@ -30,42 +32,67 @@ combine_kernel(int T, int H, int k, const TE *__restrict__ yr, const TE *__restr
   if (gid >= (int64_t)T * vec_per_row) return;
   const int64_t t = gid / vec_per_row;
   const int h = (int)(gid % vec_per_row) * VN;
+  // All k routed chunks and the shared chunk are requested before the first
+  // multiply-add (k <= KMAX loads in flight per thread instead of one), then
+  // accumulated in slot order.
+  uint4 raw[KMAX];
+  float wv[KMAX];
+#pragma unroll
+  for (int s = 0; s < KMAX; ++s) {
+    if (s < k) {
+      const int64_t row = SORTED ? (int64_t)__ldg(route_pos + t * k + s) : t * k + s;
+      raw[s] = __ldg((const uint4 *)(yr + row * H + h));
+      wv[s] = __ldg(w + t * k + s);
+    }
+  }
+  const uint4 rs = __ldg((const uint4 *)(ys + t * H + h));
+  const float g = __ldg(sig + t);
   float acc[VN];
 #pragma unroll
   for (int j = 0; j < VN; ++j) acc[j] = 0.f;
-  for (int s = 0; s < k; ++s) {
-    const float ws = w[t * k + s];
-    float v[VN];
-    const int64_t row = SORTED ? (int64_t)__ldg(route_pos + t * k + s) : t * k + s;
-    Vec16<TE>::load(yr + row * H + h, v);
 #pragma unroll
-    for (int j = 0; j < VN; ++j) acc[j] = fmaf(ws, v[j], acc[j]);
+  for (int s = 0; s < KMAX; ++s) {
+    if (s < k) {
+      float v[VN];
+      Vec16<TE>::unpack(raw[s], v);
+#pragma unroll
+      for (int j = 0; j < VN; ++j) acc[j] = fmaf(wv[s], v[j], acc[j]);
+    }
   }
-  const float g = sig[t];
   float v[VN];
-  Vec16<TE>::load(ys + t * H + h, v);
+  Vec16<TE>::unpack(rs, v);
 #pragma unroll
   for (int j = 0; j < VN; ++j) acc[j] = fmaf(g, v[j], acc[j]);
   Vec16<TE>::store(y + t * H + h, acc);
 }
 
+template <typename TE, int KMAX>
+static cudaError_t launch_combine_k(dim3 g, int T, int H, int k, const TE *yr, const TE *ys, const float *w,
+                                   const float *sig, TE *y, cudaStream_t stream, const int32_t *route_pos) {
+  if (route_pos)
+    return launch_pdl(combine_kernel<TE, true, KMAX>, g, dim3(256), 0, stream, T, H, k, yr, ys, w, sig, y, route_pos);
+  return launch_pdl(combine_kernel<TE, false, KMAX>, g, dim3(256), 0, stream, T, H, k, yr, ys, w, sig, y, route_pos);
+}
+
+template <typename TE>
+static cudaError_t launch_combine_t(int T, int H, int k, const void *y_routed, const void *y_shared, const float *w,
+                                   const float *sig, void *y, cudaStream_t stream, const int32_t *route_pos) {
+  const int64_t n = (int64_t)T * (H / Vec16<TE>::N);
+  const dim3 g((unsigned)ceil_div(n, 256));
+  const TE *yr = (const TE *)y_routed, *ys = (const TE *)y_shared;
+  TE *yo = (TE *)y;
+  if (k <= 2) return launch_combine_k<TE, 2>(g, T, H, k, yr, ys, w, sig, yo, stream, route_pos);
+  if (k <= 4) return launch_combine_k<TE, 4>(g, T, H, k, yr, ys, w, sig, yo, stream, route_pos);
+  if (k <= 8) return launch_combine_k<TE, 8>(g, T, H, k, yr, ys, w, sig, yo, stream, route_pos);
+  if (k <= 10) return launch_combine_k<TE, 10>(g, T, H, k, yr, ys, w, sig, yo, stream, route_pos);
+  return launch_combine_k<TE, 16>(g, T, H, k, yr, ys, w, sig, yo, stream, route_pos);
+}
+
 cudaError_t launch_combine(int dtype, int T, int H, int k, const void *y_routed, const void *y_shared,
                            const float *w, const float *sig, void *y, cudaStream_t stream, const int32_t *route_pos) {
   if (T == 0) return cudaSuccess;
-  const int VN = dtype == 0 ? 4 : 8;
-  const int64_t n = (int64_t)T * (H / VN);
-  const dim3 g((unsigned)ceil_div(n, 256)), b(256);
-  if (dtype == 0) {
-    const float *yr = (const float *)y_routed, *ys = (const float *)y_shared;
-    if (route_pos) return launch_pdl(combine_kernel<float, true>, g, b, 0, stream, T, H, k, yr, ys, w, sig, (float *)y,
-                                     route_pos);
-    return launch_pdl(combine_kernel<float, false>, g, b, 0, stream, T, H, k, yr, ys, w, sig, (float *)y, route_pos);
-  }
-  const __nv_bfloat16 *yr = (const __nv_bfloat16 *)y_routed, *ys = (const __nv_bfloat16 *)y_shared;
-  if (route_pos) return launch_pdl(combine_kernel<__nv_bfloat16, true>, g, b, 0, stream, T, H, k, yr, ys, w, sig,
-                                   (__nv_bfloat16 *)y, route_pos);
-  return launch_pdl(combine_kernel<__nv_bfloat16, false>, g, b, 0, stream, T, H, k, yr, ys, w, sig,
-                    (__nv_bfloat16 *)y, route_pos);
+  if (dtype == 0) return launch_combine_t<float>(T, H, k, y_routed, y_shared, w, sig, y, stream, route_pos);
+  return launch_combine_t<__nv_bfloat16>(T, H, k, y_routed, y_shared, w, sig, y, stream, route_pos);
 }
 
 }  // namespace moe
