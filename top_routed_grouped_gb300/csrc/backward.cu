@@ -524,9 +524,12 @@ router_gate_reduce_kernel(BwArgs a, const int32_t *__restrict__ chunk_start, con
 // ---------------------------------------------------------------- b8
 // One warp per (token, 32 x 16-byte chunk of the row): the slots are ranked
 // by expert id (ids of a token are distinct), then each lane assembles one
-// 16-byte chunk.
+// 16-byte chunk.  Five blocks per SM (48 registers): the kernel is bound by
+// the latency of its row loads, and more resident warps keep more of them in
+// flight (T = 4096 backward: 102 us with three blocks per SM, 91-97 with
+// five, 104 with six, 117 with eight).
 template <typename TE>
-__global__ void __launch_bounds__(256) dx_kernel(BwArgs a) {
+__global__ void __launch_bounds__(256, 5) dx_kernel(BwArgs a) {
   griddep_launch();
   griddep_wait();
   constexpr int VN = Vec16<TE>::N;
