@@ -17,8 +17,8 @@ import top_routed_grouped_gb300 as moe
 from top_routed_grouped_gb300 import build
 from top_routed_grouped_gb300 import inputs as I
 
-from _util import (assert_grad_close, bits, full_dy, full_weights, full_x, oracle_bwd_rows, oracle_routes, small_layer,
-                   to_dev)
+from _util import (assert_bf16_close, assert_grad_close, bits, full_dy, full_weights, full_x, oracle_bwd_rows,
+                   oracle_routes, small_layer, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -241,4 +241,27 @@ def test_bf16_small_shapes_every_gradient(shape):
                 "dlogit"):
         assert_grad_close(g[key], ref[key], key)
     assert_grad_close(g["dz"], dz_of(ref["dsig"], sig), "dz")
+    assert moe.moe_device_status(reset=True) == 0
+
+
+@pytest.mark.parametrize("shape", [(120, 768, 32, 1, 128, 128), (90, 1024, 64, 7, 256, 256),
+                                   (64, 512, 32, 13, 128, 128)],
+                         ids=["H768-k1", "H1024-k7", "H512-k13"])
+def test_bf16_row_lengths_and_slot_counts(shape):
+    """y and the gradients that the combine and its backward produce, for
+    slot counts and row lengths the workloads do not reach: k = 1, 7 and 13
+    (the combine keeps up to 2, 8 and 16 routed chunks per thread in flight)
+    and rows of 768, 1024 and 512 features (the combine backward's loop form,
+    and its register form with 4 and 2 chunks per lane)."""
+    T, H, E, k, I_, Is = shape
+    c = small_layer(T, H, E, k, I_, Is, seed=23)
+    d = to_dev(c)
+    f, g = fwd_bwd(d, d["dy"], k)
+    ids, w, sig = checked_routes(f, c["x"], c, None, k)
+    y = oracle.moe_forward(c["x"], ids, w, sig, c["w_gate_up"], c["w_down"], c["ws_gate_up"], c["ws_down"])
+    assert_bf16_close(f["y"], y, f"y {shape}")
+    ref = oracle.layer_backward(c["x"], ids, w, sig, *[c[n] for n in WKEYS], c["dy"])
+    for key in ("dx", "dlogit", "dw_router", "dw_shared_gate"):
+        assert_grad_close(g[key], ref[key], f"{key} {shape}")
+    assert_grad_close(g["dz"], dz_of(ref["dsig"], sig), f"dz {shape}")
     assert moe.moe_device_status(reset=True) == 0
