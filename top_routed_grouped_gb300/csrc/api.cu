@@ -71,7 +71,7 @@ static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 // ---------------------------------------------------------------- sizes
 static void route_ws(const moe_dims_t *d, Carver &c) {
   c.take((size_t)d->T * d->E * sizeof(float));  // logits when the caller passes none
-  if (d->dtype == MOE_BF16) c.take(router_tc_scratch_bytes(d->E, d->H));  // split router weight
+  if (d->dtype == MOE_BF16) c.take(router_tc_scratch_bytes(d->T, d->E, d->H));  // split router weight
 }
 
 static void permute_ws(const moe_dims_t *d, Carver &c) {
@@ -202,7 +202,7 @@ MOE_API int moe_route(const moe_dims_t *d, const void *x, const float *w_router,
     e = launch_router_logits_simt(d->T, d->H, d->E, (const float *)x, w_router, router_bias, lg, s);
   else
     e = launch_router_logits_tc(d->T, d->H, d->E, x, w_router, router_bias, lg,
-                                c.take(router_tc_scratch_bytes(d->E, d->H)), device_status_ptr(), s);
+                                c.take(router_tc_scratch_bytes(d->T, d->E, d->H)), device_status_ptr(), s);
   if (e == cudaSuccess)
     e = launch_topk_gate(d->dtype, d->T, d->H, d->E, d->k, lg, x, w_shared_gate, topk_ids, topk_w, shared_sig, s);
   return cuda_status(e);
@@ -226,7 +226,7 @@ MOE_API int moe_router_logits(const moe_dims_t *d, const void *x, const float *w
   if (d->dtype == MOE_F32)
     return cuda_status(launch_router_logits_simt(d->T, d->H, d->E, (const float *)x, w_router, router_bias, logits, s));
   return cuda_status(launch_router_logits_tc(d->T, d->H, d->E, x, w_router, router_bias, logits,
-                                             c.take(router_tc_scratch_bytes(d->E, d->H)), device_status_ptr(), s,
+                                             c.take(router_tc_scratch_bytes(d->T, d->E, d->H)), device_status_ptr(), s,
                                              exact ? 3 : 1));
 }
 
@@ -250,7 +250,7 @@ MOE_API int moe_route_replay(const moe_dims_t *d, const void *x, const float *w_
     e = launch_router_logits_simt(d->T, d->H, d->E, (const float *)x, w_router, router_bias, lg, s);
   else
     e = launch_router_logits_tc(d->T, d->H, d->E, x, w_router, router_bias, lg,
-                                c.take(router_tc_scratch_bytes(d->E, d->H)), device_status_ptr(), s);
+                                c.take(router_tc_scratch_bytes(d->T, d->E, d->H)), device_status_ptr(), s);
   if (e == cudaSuccess)
     e = launch_replay_gate(d->dtype, d->T, d->H, d->E, d->k, lg, x, w_shared_gate, topk_ids, topk_w, shared_sig,
                            device_status_ptr(), s);

@@ -115,6 +115,8 @@ struct TcParams {
   int n_items;              // ROUTER: number of items (others: item_start[E+1])
   int rt_ntile, rt_rpt;     // ROUTER: token tiles and rows per tile
   int rt_splits;            // ROUTER: bf16 terms of the weight used (3: exact; 1: weight rounded to bf16)
+  int rt_kparts;            // ROUTER (pair form): RT_CHUNKS = one item per K chunk, partials to rt_partial; else 1
+  float *rt_partial;        // ROUTER: [RT_CHUNKS][T][E] per-chunk logit sums when rt_kparts == RT_CHUNKS
   int e0;                   // first expert of the weight arrays (expert partition)
   int y_sorted;             // DOWN: routed rows in sorted order
   int y_f32;                // DOWN: float rows, the accumulators unrounded
@@ -821,9 +823,10 @@ constexpr int RT_THREADS = 32 * (TC_EPI_FIRST + RT_EPI_WARPS);
 static_assert(RT_STAGES * (RT_A_BYTES + TC_B_BYTES) + 256 + 1024 <= TC_SMEM_BYTES, "router smem");
 
 struct RtItem {
-  int f;         // expert tile (128 experts)
+  int f;         // expert tile (128 experts; the pair form: 256)
   int64_t row0;  // first token
   int rows, n;
+  int kc;        // the pair form with split K: the one K chunk of the item
 };
 
 // Token tiles of rt_rpt rows (a multiple of 16, at most 256); the host picks
@@ -1058,15 +1061,22 @@ tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   const int total = p.n_items, nkh = p.H / 64;
   // Item it: experts [256 (it / rt_ntile), +256) (this CTA's 128 from 256 f + 128 rank),
   // tokens [rt_rpt (it % rt_ntile), +rt_rpt), rows padded to RP_NROUND (each CTA loads n / 2).
+  // With split K (kparts = RT_CHUNKS) item it computes only K chunk it % kparts.
+  const int kparts = p.rt_kparts > 1 ? p.rt_kparts : 1;
   auto item = [&](int it) {
-    const int nt = it % p.rt_ntile;
+    const int rest = it / kparts;
+    const int nt = rest % p.rt_ntile;
     RtItem r;
-    r.f = it / p.rt_ntile;
+    r.kc = it % kparts;
+    r.f = rest / p.rt_ntile;
     r.row0 = (int64_t)nt * p.rt_rpt;
     r.rows = min(p.rt_rpt, p.T - nt * p.rt_rpt);
     r.n = (int)round_up(r.rows, RP_NROUND);
     return r;
   };
+  // The chunks [c_begin, c_end) of an item.
+  auto c_begin = [&](const RtItem &im) { return kparts == 1 ? 0 : im.kc; };
+  auto c_end = [&](const RtItem &im) { return kparts == 1 ? RT_CHUNKS : im.kc + 1; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -1081,7 +1091,7 @@ tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const int erow = im.f * 256 + (int)rank * 128;
         const int half = im.n >> 1;
         const int64_t r0 = im.row0 + (int64_t)rank * half;
-        for (int j = 0; j < nkh; ++j) {
+        for (int j = c_begin(im) * nkh / RT_CHUNKS; j < c_end(im) * nkh / RT_CHUNKS; ++j) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           // Both CTAs' weight tiles and rows complete on the even CTA's barrier.
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * p.rt_splits * TC_TILE_A_BYTES + (uint32_t)im.n * 128);
@@ -1120,7 +1130,7 @@ tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         for (int it = cid; it < total && ok; it += ncl) {
           const RtItem im = item(it);
           const uint32_t idesc = idesc_bf16_f32(256, im.n);
-          for (int c = 0; c < RT_CHUNKS && ok; ++c) {
+          for (int c = c_begin(im); c < c_end(im) && ok; ++c) {
             const int b = c & 1;
             if (!mbar_wait(&tempty[b], ((uses >> b) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
             tc_fence_after();
@@ -1160,9 +1170,11 @@ tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     bool ok = true;
     for (int it = cid; it < total && ok; it += ncl) {
       const RtItem im = item(it);
+      const int cb = c_begin(im), ce = c_end(im);
       float acc[128];
 #pragma unroll
       for (int c = 0; c < RT_CHUNKS; ++c) {
+        if (c < cb || c >= ce) continue;
         const int b = c & 1;
         if (!warp_wait(&tfull[b], (uses >> b) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
@@ -1173,7 +1185,7 @@ tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             float v[32];
             tmem_ld32(tb + cc * 32, v);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) acc[cc * 32 + jj] = c == 0 ? v[jj] : acc[cc * 32 + jj] + v[jj];
+            for (int jj = 0; jj < 32; ++jj) acc[cc * 32 + jj] = c == cb ? v[jj] : acc[cc * 32 + jj] + v[jj];
           }
         }
         tc_fence_before();
@@ -1186,15 +1198,27 @@ tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       }
       if (!ok) break;
       const int e = im.f * 256 + (int)rank * 128 + q * 32 + lane;
-      const float bias = (p.bias && e < p.E) ? __ldg(p.bias + e) : 0.f;
+      if (kparts == 1) {
+        const float bias = (p.bias && e < p.E) ? __ldg(p.bias + e) : 0.f;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
+        for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int col = hq * 128 + cc * 32 + jj;
-          if (col < im.rows && e < p.E)
-            p.logits[(im.row0 + col) * p.E + e] = p.bias ? acc[cc * 32 + jj] + bias : acc[cc * 32 + jj];
-        }
+          for (int jj = 0; jj < 32; ++jj) {
+            const int col = hq * 128 + cc * 32 + jj;
+            if (col < im.rows && e < p.E)
+              p.logits[(im.row0 + col) * p.E + e] = p.bias ? acc[cc * 32 + jj] + bias : acc[cc * 32 + jj];
+          }
+      } else {
+        // This item's chunk sum, summed with the other chunks (in chunk order) by router_chunk_sum_kernel.
+        float *part = p.rt_partial + (size_t)im.kc * p.T * p.E;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int col = hq * 128 + cc * 32 + jj;
+            if (col < im.rows && e < p.E) part[(im.row0 + col) * p.E + e] = acc[cc * 32 + jj];
+          }
+      }
     }
   }
   tc_fence_before();
@@ -1202,6 +1226,38 @@ tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   cluster_sync();  // no remote arrival, copy or commit targets this CTA any more
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem, TC_TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// Router with split K (small batches): the pair router wrote the four chunk
+// sums of every logit separately; logit = ((part0 + part1) + part2) + part3
+// (+ bias), the additions and order of the epilogue that sums all four
+// chunks of an item itself, so a token's logits do not depend on which
+// form ran (that is, on T).  Four consecutive logits per thread (E % 256 == 0).
+__global__ void __launch_bounds__(256)
+router_chunk_sum_kernel(int64_t n, int E, const float *__restrict__ part, const float *__restrict__ bias,
+                        float *__restrict__ logits) {
+  griddep_launch();
+  griddep_wait();
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i >= n) return;
+  float4 a = __ldg((const float4 *)(part + i));
+#pragma unroll
+  for (int c = 1; c < RT_CHUNKS; ++c) {
+    const float4 b = __ldg((const float4 *)(part + c * n + i));
+    a.x = a.x + b.x;
+    a.y = a.y + b.y;
+    a.z = a.z + b.z;
+    a.w = a.w + b.w;
+  }
+  if (bias) {
+    const float4 g = __ldg((const float4 *)(bias + i % E));
+    a.x = a.x + g.x;
+    a.y = a.y + g.y;
+    a.z = a.z + g.z;
+    a.w = a.w + g.w;
+  }
+  *(float4 *)(logits + i) = a;
 }
 
 // ---------------------------------------------------------------------------
@@ -1409,7 +1465,16 @@ static cudaError_t launch_pair(const TcMaps &maps, const TcParams &p, cudaStream
   return cudaLaunchKernelEx(&cfg, tc_pair_kernel<MODE>, maps, p);
 }
 
-size_t router_tc_scratch_bytes(int E, int H) { return (size_t)E * 3 * H * 2; }
+// Split K for the pair router: a small batch (T * E / 256 <= 4096 token-tiles' worth)
+// has too few tokens per weight tile to use the tensor cores well, so each
+// of its items takes one K chunk; a rule on the shapes alone, so that the
+// workspace size does not depend on the device.
+bool router_split_k(int T, int E) { return T > 0 && E % 256 == 0 && (int64_t)T * (E / 256) <= 4096; }
+
+size_t router_tc_scratch_bytes(int T, int E, int H) {
+  const size_t wr3 = (size_t)round_up((int64_t)E * 3 * H * 2, 256);
+  return wr3 + (router_split_k(T, E) ? (size_t)RT_CHUNKS * T * E * sizeof(float) : 0);
+}
 
 // Clusters of two pair-router CTAs that fit on the device at once (0: the
 // pair form cannot run here).  Queried once per device.
@@ -1471,10 +1536,15 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
   const int npc = (E % 256 == 0 && pair_override() != 0) ? router_pair_clusters() : 0;
   if (npc > 0) {
     const int ptiles = E / 256;
-    const int want = std::max<int>((int)ceil_div(T, RT_NMAX), std::min<int>(npc / ptiles, (int)ceil_div(T, RP_NROUND)));
+    const bool split = router_split_k(T, E);
+    p.rt_kparts = split ? RT_CHUNKS : 1;
+    p.rt_partial = split ? (float *)((uint8_t *)scratch + round_up((int64_t)E * 3 * H * 2, 256)) : nullptr;
+    const int per_tile = ptiles * p.rt_kparts;  // items per token tile
+    const int want = std::max<int>((int)ceil_div(T, RT_NMAX),
+                                   std::min<int>(std::max(npc / per_tile, 1), (int)ceil_div(T, RP_NROUND)));
     p.rt_rpt = (int)round_up(ceil_div(T, want), RP_NROUND);
     p.rt_ntile = (int)ceil_div(T, p.rt_rpt);
-    p.n_items = ptiles * p.rt_ntile;
+    p.n_items = per_tile * p.rt_ntile;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * std::min(p.n_items, npc));
     cfg.blockDim = dim3(RT_THREADS);
@@ -1489,7 +1559,11 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
     at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, tc_router_pair_kernel, m, p);
+    e = cudaLaunchKernelEx(&cfg, tc_router_pair_kernel, m, p);
+    if (e != cudaSuccess || !split) return e;
+    const int64_t n = (int64_t)T * E;
+    return launch_pdl(router_chunk_sum_kernel, dim3((unsigned)ceil_div(n / 4, 256)), dim3(256), 0, stream, n, E,
+                      (const float *)p.rt_partial, bias, logits);
   }
   const int etiles = (int)ceil_div(E, 128), sms = device_sms();
   const int want = std::max<int>((int)ceil_div(T, RT_NMAX), std::min<int>(sms / etiles, (int)ceil_div(T, 16)));

@@ -109,7 +109,8 @@ size_t etp_fused_scratch_bytes(int T, int k, int E);
 cudaError_t launch_etp_fused(const FfnArgs &a, void *scratch, int *status, cudaStream_t stream);
 
 // ---- gemm_tc.cu (bf16 tensor-core path) ----
-size_t router_tc_scratch_bytes(int E, int H);
+size_t router_tc_scratch_bytes(int T, int E, int H);
+bool router_split_k(int T, int E);
 // Router logits via the exact three-way bf16 split of w_router (splits = 3), or
 // with the weight rounded once to bf16 (splits = 1, the BF16-router ablation)
 // (scratch: router_tc_scratch_bytes).
