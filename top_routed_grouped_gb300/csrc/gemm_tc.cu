@@ -1015,12 +1015,20 @@ tc_router_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
 // the two kernels give equal logits bit for bit.
 // ---------------------------------------------------------------------------
 constexpr int RP_STAGES = 3, RP_NROUND = 32;
+// Sixteen epilogue warps, 64 accumulator columns each: a warp keeps the
+// running chunk sums of its columns in registers (64 per thread) without
+// spilling them.  With eight warps (128 sums per thread, 168 registers at
+// three warps per SM sub-partition) part of the sums spilled to local
+// memory, which the small L1 left by 198 KB of shared memory serves from L2,
+// or from memory when L2 holds other data.
+constexpr int RP_EPI_WARPS = 16, RP_COLS = 4 * RT_NMAX / RP_EPI_WARPS;
+constexpr int RP_THREADS = 32 * (TC_EPI_FIRST + RP_EPI_WARPS);
 constexpr int RP_B_BYTES = 128 * 128;  // this CTA's half of up to 256 token rows x 64 bf16
 constexpr int RP_STAGE_BYTES = RT_A_BYTES + RP_B_BYTES;
 constexpr int RP_SMEM = 1024 + RP_STAGES * RP_STAGE_BYTES + 512;
 static_assert(RP_SMEM <= 232448, "pair router shared memory");
 
-__global__ void __launch_bounds__(RT_THREADS, 1)
+__global__ void __launch_bounds__(RP_THREADS, 1)
 tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -1043,7 +1051,7 @@ tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 2 * RT_EPI_WARPS);  // used in the even CTA: one arrival per epilogue warp of the pair
+      mbar_init(&tempty[b], 2 * RP_EPI_WARPS);  // used in the even CTA: one arrival per epilogue warp of the pair
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -1163,29 +1171,30 @@ tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    // Warp (q, hq): TMEM lane quarter q (experts), columns [128 hq, 128 hq + 128).
-    const int q = warp & 3, hq = (warp - TC_EPI_FIRST) >> 2;
+    // Warp (q, part): TMEM lane quarter q (experts), columns [RP_COLS part, RP_COLS part + RP_COLS).
+    const int q = warp & 3, part = (warp - TC_EPI_FIRST) >> 2;
+    constexpr int NCC = RP_COLS / 32;  // 32-column pieces of the stores (TMEM is read 16 columns at a time)
     const uint32_t tempty_leader0 = mapa_shared(&tempty[0], 0);
     uint32_t uses = 0;
     bool ok = true;
     for (int it = cid; it < total && ok; it += ncl) {
       const RtItem im = item(it);
       const int cb = c_begin(im), ce = c_end(im);
-      float acc[128];
+      float acc[RP_COLS];
 #pragma unroll
       for (int c = 0; c < RT_CHUNKS; ++c) {
         if (c < cb || c >= ce) continue;
         const int b = c & 1;
         if (!warp_wait(&tfull[b], (uses >> b) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tb = tmem + b * 256 + ((uint32_t)(q * 32) << 16) + hq * 128;
+        const uint32_t tb = tmem + b * 256 + ((uint32_t)(q * 32) << 16) + part * RP_COLS;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          if (hq * 128 + cc * 32 < im.n) {
-            float v[32];
-            tmem_ld32(tb + cc * 32, v);
+        for (int cc = 0; cc < RP_COLS / 16; ++cc) {
+          if (part * RP_COLS + cc * 16 < im.n) {
+            float v[16];
+            tmem_ld16(tb + cc * 16, v);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) acc[cc * 32 + jj] = c == cb ? v[jj] : acc[cc * 32 + jj] + v[jj];
+            for (int jj = 0; jj < 16; ++jj) acc[cc * 16 + jj] = c == cb ? v[jj] : acc[cc * 16 + jj] + v[jj];
           }
         }
         tc_fence_before();
@@ -1201,22 +1210,22 @@ tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       if (kparts == 1) {
         const float bias = (p.bias && e < p.E) ? __ldg(p.bias + e) : 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+        for (int cc = 0; cc < NCC; ++cc)
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
-            const int col = hq * 128 + cc * 32 + jj;
+            const int col = part * RP_COLS + cc * 32 + jj;
             if (col < im.rows && e < p.E)
               p.logits[(im.row0 + col) * p.E + e] = p.bias ? acc[cc * 32 + jj] + bias : acc[cc * 32 + jj];
           }
       } else {
         // This item's chunk sum, summed with the other chunks (in chunk order) by router_chunk_sum_kernel.
-        float *part = p.rt_partial + (size_t)im.kc * p.T * p.E;
+        float *plane = p.rt_partial + (size_t)im.kc * p.T * p.E;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+        for (int cc = 0; cc < NCC; ++cc)
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
-            const int col = hq * 128 + cc * 32 + jj;
-            if (col < im.rows && e < p.E) part[(im.row0 + col) * p.E + e] = acc[cc * 32 + jj];
+            const int col = part * RP_COLS + cc * 32 + jj;
+            if (col < im.rows && e < p.E) plane[(im.row0 + col) * p.E + e] = acc[cc * 32 + jj];
           }
       }
     }
@@ -1492,7 +1501,7 @@ static int router_pair_clusters() {
   if (c == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * device_sms());
-    cfg.blockDim = dim3(RT_THREADS);
+    cfg.blockDim = dim3(RP_THREADS);
     cfg.dynamicSmemBytes = RP_SMEM;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1547,7 +1556,7 @@ cudaError_t launch_router_logits_tc(int T, int H, int E, const void *x, const fl
     p.n_items = per_tile * p.rt_ntile;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * std::min(p.n_items, npc));
-    cfg.blockDim = dim3(RT_THREADS);
+    cfg.blockDim = dim3(RP_THREADS);
     cfg.dynamicSmemBytes = RP_SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute at[2];
