@@ -246,8 +246,8 @@ class ClockSampler:
 #       python bench.py --steps 3 --warmup 3 --no-cpu-baseline --no-fwd-bwd --no-extra
 # (one pass per launch), valid only for the kernel sources it was taken on
 # (hash below); otherwise null.
-FFN_TRAFFIC = {"sources": "a4180031b0e64493", "workload": "bf16_t8192",
-               "bytes": 2_196_004_608 + 66_656_256 + 1_187_334_656 + 317_994_752}
+FFN_TRAFFIC = {"sources": "cb80d43aa1efc387", "workload": "bf16_t8192",
+               "bytes": 2_196_788_480 + 66_760_192 + 1_184_815_616 + 317_869_568}
 
 
 def kernel_sources_hash() -> str:
