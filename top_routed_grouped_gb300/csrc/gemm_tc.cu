@@ -1012,7 +1012,9 @@ tc_router_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
 // rows (up to 16 KB), so three stages fit where the single-SM router holds
 // two.  The K chunks, their order and the FP32 sums of the epilogue are the
 // single-SM router's, so every logit is the same MMA chain and the same sum:
-// the two kernels give equal logits bit for bit.
+// the two kernels give equal logits bit for bit.  Small batches run with
+// split K: each item computes one chunk and writes its sum to a partial
+// plane, which router_chunk_sum_kernel adds in the same order.
 // ---------------------------------------------------------------------------
 constexpr int RP_STAGES = 3, RP_NROUND = 32;
 // Sixteen epilogue warps, 64 accumulator columns each: a warp keeps the
@@ -1067,9 +1069,10 @@ tc_router_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   griddep_launch();
   griddep_wait();
   const int total = p.n_items, nkh = p.H / 64;
-  // Item it: experts [256 (it / rt_ntile), +256) (this CTA's 128 from 256 f + 128 rank),
-  // tokens [rt_rpt (it % rt_ntile), +rt_rpt), rows padded to RP_NROUND (each CTA loads n / 2).
-  // With split K (kparts = RT_CHUNKS) item it computes only K chunk it % kparts.
+  // Item it, with q = it / kparts: experts [256 f, +256) for f = q / rt_ntile (this CTA's
+  // 128 from 256 f + 128 rank), tokens [rt_rpt (q % rt_ntile), +rt_rpt), rows padded to
+  // RP_NROUND (each CTA loads n / 2); with split K (kparts = RT_CHUNKS) only K chunk
+  // it % kparts, else all RT_CHUNKS chunks.
   const int kparts = p.rt_kparts > 1 ? p.rt_kparts : 1;
   auto item = [&](int it) {
     const int rest = it / kparts;
