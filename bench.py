@@ -47,10 +47,18 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "MoE layer tokens/sec (fwd, fwd+bwd) on 1 GB300; % of layer roofline"
-# Kernels one forward step (moe_forward) launches: router weight split,
-# router, top-k/gate; the permute (one launch on a cluster of sixteen CTAs,
-# which also writes the grouped GEMMs' item tables); gate_up, down; combine.
-LAUNCHES_PER_STEP = 7
+# Kernels one forward step (moe_forward, bf16) launches: router weight split,
+# router (and, for T * E / 256 <= 4096, the sum of its K-chunk planes),
+# top-k/gate; the permute (one launch on a cluster of sixteen CTAs, which also
+# writes the grouped GEMMs' item tables); gate_up, down; combine; above 4096
+# tokens the shared expert on the second stream: its item tables (two
+# launches), gate_up, down.
+
+
+def launches_per_forward(T: int, E: int) -> int:
+    return 7 + (1 if T * (E // 256) <= 4096 else 0) + (4 if T > 4096 else 0)
+
+
 # The same forward as four separate calls: moe_grouped_ffn builds its own
 # item tables (2 more launches).
 LAUNCHES_PER_STEP_BY_STEP = 9
@@ -346,10 +354,10 @@ def fwd_bwd_bench(cfg, dev_w, steps: int, warmup: int, world: int, peaks: dict) 
             "ms_per_step": ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "steps": steps, "warmup": warmup,
             "step_ms": percentiles([e[0].elapsed_time(e[2]) for e in evs]),
             "api": "moe_forward (activations saved) + moe_backward",
-            # moe_forward: split, router, top-k, permute + item tables, gate_up, down, combine (7);
-            # moe_backward: combine bwd, item tables (2), down dgrad, gate_up dgrad, x gather,
-            # down wgrad, gate_up wgrad, tile table, router/gate partial sums and reduction, dx (12)
-            "gpu_launches_per_step": 19,
+            # moe_forward (launches_per_forward); moe_backward: combine bwd, item tables (2), down
+            # dgrad, gate_up dgrad, x gather, down wgrad, gate_up wgrad, tile table, router/gate
+            # partial sums and reduction, dx (12)
+            "gpu_launches_per_step": launches_per_forward(T, E) + 12,
             "layer_roofline": {"fwd_bytes": fb["bytes"], "fwd_flops": fb["flops"], "bwd_bytes": bb["bytes"],
                                "bwd_flops": bb["flops"], "roofline_ms": t_roof, "frac": t_roof / ms,
                                "bwd_roofline_ms": roof(bb), "bwd_frac": roof(bb) / bwd_ms}}
@@ -737,7 +745,7 @@ def main():
         "config": workload_config(cfg, active, world),
         "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2, "api": "moe_forward"},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": launches_per_forward(T, E) * args.steps,
         "roofline": {"kernel": "moe_grouped_ffn (gate_up+SwiGLU, down)", "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": FFN_TRAFFIC["bytes"] if (kernel_sources_hash() == FFN_TRAFFIC["sources"] and

@@ -242,23 +242,28 @@ def test_permute_skewed_ids_with_repeats():
     check_permute(np.zeros((5000, 8), np.int32), 512)  # every route to expert 0
 
 
-@pytest.mark.parametrize("T,zipf", [(333, False), (1024, False), (4096, True)])
+@pytest.mark.parametrize("T,zipf", [(333, False), (1024, False), (4096, True), (6144, True), (8192, False)])
 def test_forward_equals_step_by_step_calls(T, zipf):
     """moe_forward (the one-launch sort also writes the grouped GEMMs' item
-    tables) equals moe_route, moe_permute, moe_grouped_ffn (which builds its
-    own tables) and moe_combine called one by one, bit for bit."""
+    tables; above 4096 tokens the shared expert's GEMMs run on a second
+    stream) equals moe_route, moe_permute, moe_grouped_ffn (which builds its
+    own tables, shared expert included) and moe_combine called one by one,
+    bit for bit."""
     W = to_dev(full_weights())
     x = full_x(T).cuda()
     bias = I.zipf_bias(512).cuda() if zipf else None
     ref = moe.forward(x, W["w_router"], W["w_shared_gate"], W["w_gate_up"], W["w_down"], W["ws_gate_up"],
-                      W["ws_down"], 10, router_bias=bias)
+                      W["ws_down"], 10, router_bias=bias, save_for_backward=True)
     r = moe.route(x, W["w_router"], W["w_shared_gate"], 10, router_bias=bias)
     pm = moe.permute(r["topk_ids"], 512)
     d = moe.dims_of(x, W["w_router"], W["w_gate_up"], W["ws_gate_up"], 10)
     yr = torch.empty(T * 10, 2048, dtype=x.dtype, device="cuda")
     ys = torch.empty(T, 2048, dtype=x.dtype, device="cuda")
+    saved = {n: torch.empty_like(v) for n, v in ref["saved"].items()}  # the training activations too
     moe.moe_grouped_ffn(d, x, pm["expert_offsets"], pm["sorted_route"], W["w_gate_up"], W["w_down"],
-                        W["ws_gate_up"], W["ws_down"], yr, ys, {}, moe.workspace(d, "grouped_ffn"))
+                        W["ws_gate_up"], W["ws_down"], yr, ys, saved, moe.workspace(d, "grouped_ffn"))
+    for key, v in saved.items():
+        assert torch.equal(bits(v), bits(ref["saved"][key])), key
     y = torch.empty(T, 2048, dtype=x.dtype, device="cuda")
     moe.moe_combine(d, yr, ys, r["topk_w"], r["shared_sig"], y)
     for key in ("expert_offsets", "sorted_route", "route_pos"):

@@ -98,6 +98,7 @@ struct FwdScratch {
   void *y_routed, *y_shared;
   void *inner;  // scratch shared by the four steps (they run one after another)
   size_t inner_bytes;
+  void *side_tiles, *side_h_shared;  // bf16: the shared expert's item tables and h (its own stream)
 };
 
 static FwdScratch fwd_ws(const moe_dims_t *d, Carver &c) {
@@ -120,8 +121,26 @@ static FwdScratch fwd_ws(const moe_dims_t *d, Carver &c) {
   if (f.off > inner) inner = f.off;
   s.inner_bytes = (size_t)round_up((int64_t)inner, 256);
   s.inner = c.take(s.inner_bytes);
+  s.side_tiles = s.side_h_shared = nullptr;
+  if (d->dtype == MOE_BF16) {
+    s.side_tiles = c.take(ffn_tc_scratch_bytes(d->T, d->k, d->E, d->H, d->I, d->Is));
+    s.side_h_shared = c.take((size_t)d->T * d->Is * esize(d));
+  }
   return s;
 }
+
+// The second stream of the shared expert (one per device, created once).
+static cudaStream_t side_stream() {
+  static std::mutex mu;
+  static cudaStream_t streams[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  cudaStream_t &s = streams[dev & 63];
+  if (!s && cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) s = nullptr;
+  return s;
+}
+
 
 struct BwdScratch {
   void *dyr, *dys, *dgu_routed, *dgu_shared;
@@ -479,7 +498,7 @@ MOE_API int moe_forward(const moe_dims_t *d, const moe_fwd_args_t *a, void *ws, 
   int st = check_dims(d);
   if (st != MOE_OK) return st;
   if (!a || !opt_ok(ws)) return MOE_ERR_INVALID_ARG;
-  const int64_t T = d->T;
+  const int64_t T = d->T, R = T * d->k;
   if (!buf_ok(a->x, T * d->H) || !buf_ok(a->y, T * d->H)) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < ws_size(d, MOE_OP_FORWARD)) return MOE_ERR_WORKSPACE;
   Carver c(ws);
@@ -492,42 +511,87 @@ MOE_API int moe_forward(const moe_dims_t *d, const moe_fwd_args_t *a, void *ws, 
   int32_t *pos = a->route_pos ? a->route_pos : s.route_pos;
   void *yr = a->y_routed ? a->y_routed : s.y_routed;
   void *ys = a->y_shared ? a->y_shared : s.y_shared;
-  if (a->replay_ids) {
-    if (!buf_ok(a->replay_ids, T * d->k)) return MOE_ERR_INVALID_ARG;
-    st = moe_route_replay(d, a->x, a->w_router, a->router_bias, a->w_shared_gate, a->replay_ids, w, sig, a->logits,
-                          s.inner, s.inner_bytes, stream);
-    if (st != MOE_OK) return st;
-    if (a->topk_ids && a->topk_ids != a->replay_ids && T > 0 &&
-        cudaMemcpyAsync(a->topk_ids, a->replay_ids, (size_t)T * d->k * sizeof(int32_t), cudaMemcpyDeviceToDevice,
-                        (cudaStream_t)stream) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    ids = (int32_t *)a->replay_ids;  // read only from here on
-  } else {
-    st = moe_route(d, a->x, a->w_router, a->router_bias, a->w_shared_gate, ids, w, sig, a->logits, s.inner,
-                   s.inner_bytes, stream);
-    if (st != MOE_OK) return st;
-  }
-  // Permute and grouped FFN.  On the bf16 path with the one-launch sort, that
-  // launch also writes the FFN's item tables into its scratch (the sort
-  // itself uses none), so the FFN starts with its GEMMs.
-  st = permute_check(d, ids, off, srt, pos, s.inner, s.inner_bytes);
+  if (a->replay_ids && !buf_ok(a->replay_ids, T * d->k)) return MOE_ERR_INVALID_ARG;
+  const int32_t *route_ids = a->replay_ids ? a->replay_ids : ids;
+  st = permute_check(d, route_ids, off, srt, pos, s.inner, s.inner_bytes);
   if (st != MOE_OK) return st;
   FfnArgs fa;
   FfnScratch fs;
   st = grouped_ffn_prepare(d, a->x, off, srt, a->w_gate_up, a->w_down, a->ws_gate_up, a->ws_down, yr, ys, &a->saved,
                            s.inner, s.inner_bytes, &fa, &fs);
   if (st != MOE_OK) return st;
-  const int64_t R = T * d->k;
+  cudaStream_t ms = (cudaStream_t)stream;
+  // On the bf16 path with the one-launch sort, the shared expert needs no
+  // routes: above 4096 tokens its GEMMs run on a second stream from the start
+  // of the call, while the routing kernels (which leave most SMs idle) run,
+  // and the combine waits for them.  Its rows and tables use their own
+  // scratch.  The routed GEMMs then take only the routed segments (the sort
+  // writes their tables); every output is the same MMA chain as in one
+  // launch.  Measured on one GB300, each form against the other in the same
+  // process: T = 8192 -7 µs, 16384 skewed -33 µs; T = 4096 and below the
+  // shared GEMMs take SMs from the shorter routing kernels (T = 2048: +7 µs).
+  const bool one_launch = d->dtype == MOE_BF16 && T > 0 && permute_cluster_ok(R, d->E);
+  cudaStream_t ss = (one_launch && T > 4096) ? side_stream() : nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  if (ss && (cudaEventCreateWithFlags(&ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+             cudaEventCreateWithFlags(&ev_join, cudaEventDisableTiming) != cudaSuccess)) {
+    if (ev_fork) cudaEventDestroy(ev_fork);
+    return MOE_ERR_CUDA;
+  }
+  if (ss) {
+    FfnArgs sa = fa;
+    sa.e_begin = 0;
+    sa.e_end = 0;  // no routed segment
+    sa.with_shared = 1;
+    sa.items_ready = 0;
+    if (!a->saved.h_shared) sa.h_shared = s.side_h_shared;
+    fa.with_shared = 0;
+    cudaError_t e = cudaEventRecord(ev_fork, ms);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ss, ev_fork, 0);
+    if (e == cudaSuccess) e = launch_ffn_tc(sa, s.side_tiles, device_status_ptr(), ss);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_join, ss);
+    if (e != cudaSuccess) {
+      cudaEventDestroy(ev_fork);
+      cudaEventDestroy(ev_join);
+      return MOE_ERR_CUDA;
+    }
+  }
+  // The rest runs on the caller's stream; whatever happens, it joins the
+  // second stream before returning.
+  auto join = [&](int status) {
+    if (!ss) return status;
+    const cudaError_t e = cudaStreamWaitEvent(ms, ev_join, 0);
+    cudaEventDestroy(ev_fork);
+    cudaEventDestroy(ev_join);
+    return (status == MOE_OK && e != cudaSuccess) ? MOE_ERR_CUDA : status;
+  };
+  if (a->replay_ids) {
+    st = moe_route_replay(d, a->x, a->w_router, a->router_bias, a->w_shared_gate, a->replay_ids, w, sig, a->logits,
+                          s.inner, s.inner_bytes, stream);
+    if (st != MOE_OK) return join(st);
+    if (a->topk_ids && a->topk_ids != a->replay_ids && T > 0 &&
+        cudaMemcpyAsync(a->topk_ids, a->replay_ids, (size_t)T * d->k * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                        ms) != cudaSuccess)
+      return join(MOE_ERR_CUDA);
+  } else {
+    st = moe_route(d, a->x, a->w_router, a->router_bias, a->w_shared_gate, ids, w, sig, a->logits, s.inner,
+                   s.inner_bytes, stream);
+    if (st != MOE_OK) return join(st);
+  }
+  // Permute and grouped FFN.  On the bf16 path with the one-launch sort, that
+  // launch also writes the FFN's item tables into its scratch (the sort
+  // itself uses none), so the FFN starts with its GEMMs.
   PermuteItems items;
-  if (d->dtype == MOE_BF16 && T > 0 && permute_cluster_ok(R, d->E) && ffn_tc_item_tables(fa, fs.tiles, &items)) {
-    st = cuda_status(launch_permute_cluster(R, d->E, ids, off, srt, pos, device_status_ptr(), (cudaStream_t)stream,
-                                            &items));
+  if (one_launch && ffn_tc_item_tables(fa, fs.tiles, &items)) {
+    st = cuda_status(launch_permute_cluster(R, d->E, route_ids, off, srt, pos, device_status_ptr(), ms, &items));
     fa.items_ready = 1;
   } else {
-    st = moe_permute(d, ids, off, srt, pos, s.inner, s.inner_bytes, stream);
+    st = moe_permute(d, route_ids, off, srt, pos, s.inner, s.inner_bytes, stream);
   }
-  if (st != MOE_OK) return st;
+  if (st != MOE_OK) return join(st);
   st = grouped_ffn_run(d, fa, fs, stream);
+  if (st != MOE_OK) return join(st);
+  st = join(MOE_OK);
   if (st != MOE_OK) return st;
   return moe_combine(d, yr, ys, w, sig, a->y, stream);
 }

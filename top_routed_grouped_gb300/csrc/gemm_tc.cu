@@ -1328,7 +1328,9 @@ item_tables_kernel(int E, int T, int nf_a_r, int nf_a_s, int nf_b_r, int nf_b_s,
   __shared__ int32_t s_off[IT_MAX_E + 1], s_a[IT_MAX_E + 2], s_b[IT_MAX_E + 2];
   __shared__ int32_t buf[1024];
   __shared__ int32_t carry;
-  for (int i = threadIdx.x; i <= E; i += 1024) s_off[i] = offsets[i];
+  // An empty expert range (the shared expert alone) reads no offsets: they
+  // may not exist yet when that table is built.
+  for (int i = threadIdx.x; i <= E; i += 1024) s_off[i] = e_begin < e_end ? offsets[i] : 0;
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   for (int base = 0; base <= E; base += 1024) {
@@ -1372,10 +1374,11 @@ item_expand_kernel(int E, int T, const int32_t *__restrict__ offsets, const int3
   griddep_wait();
   const int sg = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
   if (sg > E) return;
+  if (__ldg(start_a + sg + 1) == __ldg(start_a + sg) && __ldg(start_b + sg + 1) == __ldg(start_b + sg))
+    return;  // empty, or outside the expert range (its offsets are not read)
   const int base = sg == E ? 0 : __ldg(offsets + sg);
   const int n_s = sg == E ? T : __ldg(offsets + sg + 1) - base;
-  if (n_s == 0 || __ldg(start_a + sg + 1) == __ldg(start_a + sg) && __ldg(start_b + sg + 1) == __ldg(start_b + sg))
-    return;  // empty, or outside the expert range
+  if (n_s == 0) return;
   const int ntile = (n_s + tile - 1) / tile;
   const int rpt = ((n_s + ntile - 1) / ntile + 15) & ~15;
   const int a0 = __ldg(start_a + sg), na = __ldg(start_a + sg + 1) - a0;
@@ -1621,10 +1624,11 @@ size_t ffn_tc_scratch_bytes(int T, int k, int E, int H, int I, int Is) {
 }
 
 // Where launch_ffn_tc keeps its item tables in `scratch` and how many items
-// each row tile of a segment gives (false: the call needs tables that the
-// one-launch sort does not build, i.e. an expert range or no shared expert).
+// each row tile of a segment gives (none for the shared segment without
+// with_shared; false: the call needs tables that the one-launch sort does not
+// build, i.e. an expert range).
 bool ffn_tc_item_tables(const FfnArgs &a, void *scratch, PermuteItems *it) {
-  if (a.e_begin != 0 || (a.e_end >= 0 && a.e_end != a.E) || !a.with_shared) return false;
+  if (a.e_begin != 0 || (a.e_end >= 0 && a.e_end != a.E)) return false;
   const size_t starts = round256((size_t)(a.E + 2) * 4);
   constexpr int GU_FEAT = 64 * TcCfg<TC_GATE_UP>::MT;
   constexpr int DN_ROWS = 128 * TcCfg<TC_DOWN>::MT;
@@ -1634,9 +1638,9 @@ bool ffn_tc_item_tables(const FfnArgs &a, void *scratch, PermuteItems *it) {
   uint8_t *w = (uint8_t *)scratch;
   it->T = a.T;
   it->nf_a_r = a.I / GU_FEAT;
-  it->nf_a_s = a.Is / GU_FEAT;
+  it->nf_a_s = a.with_shared ? a.Is / GU_FEAT : 0;
   it->nf_b_r = a.H / dn_rows;
-  it->nf_b_s = a.H / dn_rows;
+  it->nf_b_s = a.with_shared ? a.H / dn_rows : 0;
   it->max_a = mi_gu;
   it->max_b = mi_dn;
   it->start_a = (int32_t *)w;
