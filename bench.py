@@ -50,13 +50,13 @@ METRIC = "MoE layer tokens/sec (fwd, fwd+bwd) on 1 GB300; % of layer roofline"
 # Kernels one forward step (moe_forward, bf16) launches: router weight split,
 # router (and, for T * E / 256 <= 4096, the sum of its K-chunk planes),
 # top-k/gate; the permute (one launch on a cluster of sixteen CTAs, which also
-# writes the grouped GEMMs' item tables); gate_up, down; combine; above 4096
+# writes the grouped GEMMs' item tables); gate_up, down; combine; above 2048
 # tokens the shared expert on the second stream: its item tables (two
 # launches), gate_up, down.
 
 
 def launches_per_forward(T: int, E: int) -> int:
-    return 7 + (1 if T * (E // 256) <= 4096 else 0) + (4 if T > 4096 else 0)
+    return 7 + (1 if T * (E // 256) <= 4096 else 0) + (4 if T > 2048 else 0)
 
 
 # The same forward as four separate calls: moe_grouped_ffn builds its own

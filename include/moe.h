@@ -409,11 +409,13 @@ typedef struct moe_fwd_args {
  * stream.  Workspace: FORWARD (covers every optional output left NULL).
  * Same results as the four calls, bit for bit; where the permute runs as one
  * launch (see moe_permute) and dtype is MOE_BF16, that launch also writes
- * the grouped FFN's work lists.  There, above 4096 tokens, the shared
+ * the grouped FFN's work lists.  There, above 2048 tokens, the shared
  * expert's GEMMs (they need no routes) run on a second stream of the library
  * (one per device, non-blocking) that starts from an event recorded on
- * `stream` at the call and is joined back into `stream` before the combine:
- * work on `stream` after the call sees every output, as with one stream.
+ * `stream` (after the router launch while the routed GEMMs average fewer
+ * than 256 routes per expert, at the call otherwise) and is joined back into
+ * `stream` before the combine: work on `stream` after the call sees every
+ * output, as with one stream.
  * Under CUDA graph capture of `stream` the second stream joins the capture
  * through those events; two threads capturing or running moe_forward on one
  * device at once share that stream (correct, but serialised there). */

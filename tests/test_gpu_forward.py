@@ -242,13 +242,15 @@ def test_permute_skewed_ids_with_repeats():
     check_permute(np.zeros((5000, 8), np.int32), 512)  # every route to expert 0
 
 
-@pytest.mark.parametrize("T,zipf", [(333, False), (1024, False), (4096, True), (6144, True), (8192, False)])
+@pytest.mark.parametrize("T,zipf", [(333, False), (1024, False), (4096, True), (6144, True), (8192, False),
+                                    (16384, True)])
 def test_forward_equals_step_by_step_calls(T, zipf):
     """moe_forward (the one-launch sort also writes the grouped GEMMs' item
-    tables; above 4096 tokens the shared expert's GEMMs run on a second
-    stream) equals moe_route, moe_permute, moe_grouped_ffn (which builds its
-    own tables, shared expert included) and moe_combine called one by one,
-    bit for bit."""
+    tables; above 2048 tokens the shared expert's GEMMs run on a second
+    stream, forked after the router launch below 256 routes per expert and
+    at the call from there on, i.e. T = 16384) equals moe_route,
+    moe_permute, moe_grouped_ffn (which builds its own tables, shared expert
+    included) and moe_combine called one by one, bit for bit."""
     W = to_dev(full_weights())
     x = full_x(T).cuda()
     bias = I.zipf_bias(512).cuda() if zipf else None

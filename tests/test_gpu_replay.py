@@ -127,3 +127,21 @@ def test_replay_invalid_ids_fail_closed(bad, code):
     assert torch.count_nonzero(w[3]) == 0
     others = torch.cat([w[:3], w[4:]])
     assert torch.allclose(others.sum(dim=1), torch.ones(T - 1), atol=1e-6)
+
+
+@pytest.mark.parametrize("T", [4096, 16384])
+def test_replayed_forward_with_second_stream_is_bitwise(T):
+    """Above 2048 tokens moe_forward runs the shared expert's GEMMs on a
+    second stream, forked after the router launch (T = 4096: 80 routes per
+    expert) or at the call (T = 16384: 320).  Replaying the call's own routes
+    takes the replay gate instead of top-k at the fork point and gives the
+    same rows and output bit for bit."""
+    W = to_dev(full_weights())
+    x = full_x(T).cuda()
+    args = [W[n] for n in WKEYS]
+    f = moe.forward(x, *args, 10)
+    g = moe.forward(x, *args, 10, replay_ids=f["topk_ids"].clone())
+    assert torch.equal(g["topk_ids"], f["topk_ids"])
+    for key in ("y_routed", "y_shared", "y"):
+        assert torch.equal(bits(g[key]), bits(f[key])), key
+    assert moe.moe_device_status(reset=True) == 0

@@ -201,14 +201,20 @@ MOE_API const char *moe_status_string(int status) {
   }
 }
 
-MOE_API int moe_route(const moe_dims_t *d, const void *x, const float *w_router, const float *router_bias,
-                      const void *w_shared_gate, int32_t *topk_ids, float *topk_w, float *shared_sig, float *logits,
-                      void *ws, size_t ws_bytes, void *stream) {
+// moe_route (replay == nullptr: top-k of the logits into topk_ids) and
+// moe_route_replay (the given ids, replay == topk_ids).  `after_router` runs
+// on the host between the router launch and the top-k (or replay gate)
+// launch; moe_forward forks its second stream there.
+template <class F>
+static int route_impl(const moe_dims_t *d, const void *x, const float *w_router, const float *router_bias,
+                      const void *w_shared_gate, const int32_t *replay, int32_t *topk_ids, float *topk_w,
+                      float *shared_sig, float *logits, void *ws, size_t ws_bytes, void *stream, F &&after_router) {
   int st = check_dims(d);
   if (st != MOE_OK) return st;
   const int64_t T = d->T, R = T * d->k;
+  const int32_t *ids_in = replay ? replay : topk_ids;
   if (!buf_ok(x, T * d->H) || !buf_ok(w_router, 1) || !opt_ok(router_bias) || !buf_ok(w_shared_gate, 1) ||
-      !buf_ok(topk_ids, R) || !buf_ok(topk_w, R) || !buf_ok(shared_sig, T) || !opt_ok(logits) || !opt_ok(ws))
+      !buf_ok(ids_in, R) || !buf_ok(topk_w, R) || !buf_ok(shared_sig, T) || !opt_ok(logits) || !opt_ok(ws))
     return MOE_ERR_INVALID_ARG;
   if (ws_bytes < ws_size(d, MOE_OP_ROUTE)) return MOE_ERR_WORKSPACE;
   if (T == 0) return MOE_OK;
@@ -222,9 +228,22 @@ MOE_API int moe_route(const moe_dims_t *d, const void *x, const float *w_router,
   else
     e = launch_router_logits_tc(d->T, d->H, d->E, x, w_router, router_bias, lg,
                                 c.take(router_tc_scratch_bytes(d->T, d->E, d->H)), device_status_ptr(), s);
-  if (e == cudaSuccess)
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  st = after_router();
+  if (st != MOE_OK) return st;
+  if (replay)
+    e = launch_replay_gate(d->dtype, d->T, d->H, d->E, d->k, lg, x, w_shared_gate, replay, topk_w, shared_sig,
+                           device_status_ptr(), s);
+  else
     e = launch_topk_gate(d->dtype, d->T, d->H, d->E, d->k, lg, x, w_shared_gate, topk_ids, topk_w, shared_sig, s);
   return cuda_status(e);
+}
+
+MOE_API int moe_route(const moe_dims_t *d, const void *x, const float *w_router, const float *router_bias,
+                      const void *w_shared_gate, int32_t *topk_ids, float *topk_w, float *shared_sig, float *logits,
+                      void *ws, size_t ws_bytes, void *stream) {
+  return route_impl(d, x, w_router, router_bias, w_shared_gate, nullptr, topk_ids, topk_w, shared_sig, logits, ws,
+                    ws_bytes, stream, [] { return (int)MOE_OK; });
 }
 
 MOE_API int moe_router_logits(const moe_dims_t *d, const void *x, const float *w_router, const float *router_bias,
@@ -252,28 +271,8 @@ MOE_API int moe_router_logits(const moe_dims_t *d, const void *x, const float *w
 MOE_API int moe_route_replay(const moe_dims_t *d, const void *x, const float *w_router, const float *router_bias,
                              const void *w_shared_gate, const int32_t *topk_ids, float *topk_w, float *shared_sig,
                              float *logits, void *ws, size_t ws_bytes, void *stream) {
-  int st = check_dims(d);
-  if (st != MOE_OK) return st;
-  const int64_t T = d->T, R = T * d->k;
-  if (!buf_ok(x, T * d->H) || !buf_ok(w_router, 1) || !opt_ok(router_bias) || !buf_ok(w_shared_gate, 1) ||
-      !buf_ok(topk_ids, R) || !buf_ok(topk_w, R) || !buf_ok(shared_sig, T) || !opt_ok(logits) || !opt_ok(ws))
-    return MOE_ERR_INVALID_ARG;
-  if (ws_bytes < ws_size(d, MOE_OP_ROUTE)) return MOE_ERR_WORKSPACE;
-  if (T == 0) return MOE_OK;
-  cudaStream_t s = (cudaStream_t)stream;
-  Carver c(ws);
-  float *lg = (float *)c.take((size_t)T * d->E * sizeof(float));
-  if (logits) lg = logits;
-  cudaError_t e;
-  if (d->dtype == MOE_F32)
-    e = launch_router_logits_simt(d->T, d->H, d->E, (const float *)x, w_router, router_bias, lg, s);
-  else
-    e = launch_router_logits_tc(d->T, d->H, d->E, x, w_router, router_bias, lg,
-                                c.take(router_tc_scratch_bytes(d->T, d->E, d->H)), device_status_ptr(), s);
-  if (e == cudaSuccess)
-    e = launch_replay_gate(d->dtype, d->T, d->H, d->E, d->k, lg, x, w_shared_gate, topk_ids, topk_w, shared_sig,
-                           device_status_ptr(), s);
-  return cuda_status(e);
+  return route_impl(d, x, w_router, router_bias, w_shared_gate, topk_ids, nullptr, topk_w, shared_sig, logits, ws,
+                    ws_bytes, stream, [] { return (int)MOE_OK; });
 }
 
 // The checks of the permutation's dims and buffers (shared by moe_permute and
@@ -522,23 +521,34 @@ MOE_API int moe_forward(const moe_dims_t *d, const moe_fwd_args_t *a, void *ws, 
   if (st != MOE_OK) return st;
   cudaStream_t ms = (cudaStream_t)stream;
   // On the bf16 path with the one-launch sort, the shared expert needs no
-  // routes: above 4096 tokens its GEMMs run on a second stream from the start
-  // of the call, while the routing kernels (which leave most SMs idle) run,
-  // and the combine waits for them.  Its rows and tables use their own
-  // scratch.  The routed GEMMs then take only the routed segments (the sort
-  // writes their tables); every output is the same MMA chain as in one
-  // launch.  Measured on one GB300, each form against the other in the same
-  // process: T = 8192 -7 µs, 16384 skewed -33 µs; T = 4096 and below the
-  // shared GEMMs take SMs from the shorter routing kernels (T = 2048: +7 µs).
+  // routes: above 2048 tokens its GEMMs run on a second stream, joined before
+  // the combine, with their own rows and tables in scratch.  The routed GEMMs
+  // then take only the routed segments (the sort writes their tables); every
+  // output is the same MMA chain as in one launch.  Where the routed GEMMs
+  // stream their weights (fewer than 256 routes per expert on average), the
+  // second stream forks after the router launch: the shared gate_up takes the
+  // SMs that top-k leaves and runs beside the permute and the start of the
+  // routed gate_up, the shared down beside the routed down.  With more routes
+  // per expert the routed GEMMs are bound by the tensor pipe themselves, and
+  // the fork comes first, so that both shared GEMMs run ahead of the router.
+  // Measured on one GB300, back-to-back calls, against the shared expert as
+  // items of the routed launches: T = 4096 -6 µs, 8192 -9 µs, 16384 skewed
+  // -37 µs; with the other fork point +7, +3 and +10 µs more; at T = 2048 the
+  // second stream would cost 8 µs.
   const bool one_launch = d->dtype == MOE_BF16 && T > 0 && permute_cluster_ok(R, d->E);
-  cudaStream_t ss = (one_launch && T > 4096) ? side_stream() : nullptr;
+  cudaStream_t ss = (one_launch && T > 2048) ? side_stream() : nullptr;
+  const bool fork_first = ss && T * d->k >= (int64_t)256 * d->E;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   if (ss && (cudaEventCreateWithFlags(&ev_fork, cudaEventDisableTiming) != cudaSuccess ||
              cudaEventCreateWithFlags(&ev_join, cudaEventDisableTiming) != cudaSuccess)) {
     if (ev_fork) cudaEventDestroy(ev_fork);
     return MOE_ERR_CUDA;
   }
-  if (ss) {
+  bool recorded = false;  // ev_join marks the end of the second stream's work
+  // The second stream waits for the work queued so far on the caller's
+  // stream (x is ready) and takes the shared expert.
+  auto fork = [&]() -> int {
+    if (!ss) return MOE_OK;
     FfnArgs sa = fa;
     sa.e_begin = 0;
     sa.e_end = 0;  // no routed segment
@@ -548,34 +558,33 @@ MOE_API int moe_forward(const moe_dims_t *d, const moe_fwd_args_t *a, void *ws, 
     fa.with_shared = 0;
     cudaError_t e = cudaEventRecord(ev_fork, ms);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ss, ev_fork, 0);
-    if (e == cudaSuccess) e = launch_ffn_tc(sa, s.side_tiles, device_status_ptr(), ss);
-    if (e == cudaSuccess) e = cudaEventRecord(ev_join, ss);
-    if (e != cudaSuccess) {
-      cudaEventDestroy(ev_fork);
-      cudaEventDestroy(ev_join);
-      return MOE_ERR_CUDA;
-    }
-  }
-  // The rest runs on the caller's stream; whatever happens, it joins the
-  // second stream before returning.
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_ffn_tc(sa, s.side_tiles, device_status_ptr(), ss);
+    recorded = cudaEventRecord(ev_join, ss) == cudaSuccess;  // also after a failed launch
+    return (e == cudaSuccess && recorded) ? MOE_OK : MOE_ERR_CUDA;
+  };
+  // Whatever happens after the fork, the caller's stream joins the second
+  // stream before returning.
   auto join = [&](int status) {
     if (!ss) return status;
-    const cudaError_t e = cudaStreamWaitEvent(ms, ev_join, 0);
+    const cudaError_t e = recorded ? cudaStreamWaitEvent(ms, ev_join, 0) : cudaSuccess;
     cudaEventDestroy(ev_fork);
     cudaEventDestroy(ev_join);
     return (status == MOE_OK && e != cudaSuccess) ? MOE_ERR_CUDA : status;
   };
+  auto fork_after_router = [&]() { return fork_first ? (int)MOE_OK : fork(); };
+  if (fork_first && (st = fork()) != MOE_OK) return join(st);
   if (a->replay_ids) {
-    st = moe_route_replay(d, a->x, a->w_router, a->router_bias, a->w_shared_gate, a->replay_ids, w, sig, a->logits,
-                          s.inner, s.inner_bytes, stream);
+    st = route_impl(d, a->x, a->w_router, a->router_bias, a->w_shared_gate, a->replay_ids, nullptr, w, sig,
+                    a->logits, s.inner, s.inner_bytes, stream, fork_after_router);
     if (st != MOE_OK) return join(st);
     if (a->topk_ids && a->topk_ids != a->replay_ids && T > 0 &&
         cudaMemcpyAsync(a->topk_ids, a->replay_ids, (size_t)T * d->k * sizeof(int32_t), cudaMemcpyDeviceToDevice,
                         ms) != cudaSuccess)
       return join(MOE_ERR_CUDA);
   } else {
-    st = moe_route(d, a->x, a->w_router, a->router_bias, a->w_shared_gate, ids, w, sig, a->logits, s.inner,
-                   s.inner_bytes, stream);
+    st = route_impl(d, a->x, a->w_router, a->router_bias, a->w_shared_gate, nullptr, ids, w, sig, a->logits, s.inner,
+                    s.inner_bytes, stream, fork_after_router);
     if (st != MOE_OK) return join(st);
   }
   // Permute and grouped FFN.  On the bf16 path with the one-launch sort, that

@@ -758,7 +758,11 @@ tc_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     // row i at line i of a K block's B tile (the 128-byte swizzle), four rows
     // per copy; quad qd = g + 8 lane (lanes 0-3) of warp g.  The bytes of
     // both CTAs complete on the even CTA's full[s].  Lines past the item's
-    // rows read token 0: their accumulator columns are never read.
+    // rows read token 0: their accumulator columns are never read.  The
+    // shared expert's rows are consecutive tokens: lane 0 of warp 0 copies
+    // the largest multiple of 16 of them as boxes of 128 .. 16 rows
+    // (maps.b_sh; lines past the last token are zero-filled), and the quads
+    // after it (at most one 8-row remainder) take gather4 copies as above.
     const int g = warp - GATHER_FIRST;
     const uint64_t pol_x = policy_evict_last();
     const uint32_t full0 = mapa_shared(&full[0], 0);
@@ -771,7 +775,9 @@ tc_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       const int half = im.n >> 1, hbase = (int)rank * half;
       const int hrows = max(0, min(half, im.rows - hbase));
       const int qd = g + 8 * lane;
-      const bool mine = lane < 4 && 4 * qd < half;
+      const int hbox = sh ? (half & ~15) : 0;  // rows copied as boxes
+      const bool mine = lane < 4 && 4 * qd >= hbox && 4 * qd < half;
+      const bool boxes = hbox > 0 && g == 0 && lane == 0;
       int t4[4] = {0, 0, 0, 0};
       if (mine) {
 #pragma unroll
@@ -793,6 +799,23 @@ tc_pair_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           for (int j = 0; j < PR_KSUB; ++j)
             tma_gather4_pair(sb(stage, j) + qd * 512, &maps.b[0], bar, (ks * PR_KSUB + j) * 64, t4[0], t4[1], t4[2],
                              t4[3], pol_x);
+        }
+        if (boxes) {
+          const uint32_t bar = full0 + (uint32_t)(stage * sizeof(uint64_t));
+          const int r0 = (int)im.row0 + hbase;
+#pragma unroll
+          for (int j = 0; j < PR_KSUB; ++j) {
+            const int kx = (ks * PR_KSUB + j) * 64;
+            int r = 0;
+#pragma unroll
+            for (int h = 1; h < 5; ++h) {  // boxes of 128 .. 16 rows
+              const int box = 256 >> h;
+              while (hbox - r >= box) {
+                tma_load_2d_pair(sb(stage, j) + r * 128, &maps.b_sh[h], bar, kx, r0 + r, pol_x);
+                r += box;
+              }
+            }
+          }
         }
         if (++stage == PR_STAGES) stage = 0, phase ^= 1;
       }
@@ -1702,7 +1725,8 @@ cudaError_t launch_ffn_tc(const FfnArgs &a, void *scratch, int *status, cudaStre
     // One M tile (4 groups of 16 features) per CTA of the pair; x rows for
     // the gather4 copies through a one-row box.
     if (!map_gate_up(&mg.a, a.w_gate_up, std::max(n_local, 1), a.I, a.H, 4) ||
-        !map_gate_up(&mg.a_sh, a.ws_gate_up, 1, a.Is, a.H, 4) || !map_2d(&mg.b[0], a.x, a.T, a.H, 1))
+        !map_gate_up(&mg.a_sh, a.ws_gate_up, 1, a.Is, a.H, 4) || !map_2d(&mg.b[0], a.x, a.T, a.H, 1) ||
+        (a.with_shared && !map_rows(mg.b_sh, a.x, a.T, a.H)))  // the shared expert's row boxes
       return cudaErrorInvalidValue;
     e = launch_pair<TC_GATE_UP>(mg, p, stream);
   } else {
