@@ -248,14 +248,16 @@ class ClockSampler:
 
 # DRAM bytes (read + write) of one moe_grouped_ffn call (gate_up + down) at
 # bf16_t8192: dram__bytes_read.sum + dram__bytes_write.sum of the two kernels
-# in the fourth forward step of
+# in the first timed step-by-step call (the launch pair that the roofline
+# times; the forward steps before it launch four pair GEMMs each, the shared
+# expert's on the second stream) of
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \
-#       -k regex:tc_pair_kernel -s 6 -c 2 \
+#       -k regex:tc_pair_kernel -s 30 -c 2 \
 #       python bench.py --steps 3 --warmup 3 --no-cpu-baseline --no-fwd-bwd --no-extra
 # (one pass per launch), valid only for the kernel sources it was taken on
 # (hash below); otherwise null.
-FFN_TRAFFIC = {"sources": "cb80d43aa1efc387", "workload": "bf16_t8192",
-               "bytes": 2_196_788_480 + 66_760_192 + 1_184_815_616 + 317_869_568}
+FFN_TRAFFIC = {"sources": "9c8829fd09602b61", "workload": "bf16_t8192",
+               "bytes": 2_197_893_120 + 66_823_680 + 1_187_426_048 + 317_621_248}
 
 
 def kernel_sources_hash() -> str:
