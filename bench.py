@@ -256,8 +256,8 @@ class ClockSampler:
 #       python bench.py --steps 3 --warmup 3 --no-cpu-baseline --no-fwd-bwd --no-extra
 # (one pass per launch), valid only for the kernel sources it was taken on
 # (hash below); otherwise null.
-FFN_TRAFFIC = {"sources": "9c8829fd09602b61", "workload": "bf16_t8192",
-               "bytes": 2_197_893_120 + 66_823_680 + 1_187_426_048 + 317_621_248}
+FFN_TRAFFIC = {"sources": "74736556d040a5f5", "workload": "bf16_t8192",
+               "bytes": 2_188_150_272 + 73_008_384 + 1_186_576_640 + 317_780_224}
 
 
 def kernel_sources_hash() -> str:
