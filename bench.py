@@ -548,6 +548,31 @@ def run_reference(args, cfg, rank: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+def route_only_bench(cfg, steps: int, warmup: int) -> dict:
+    """moe_route alone on the workload's x, router weight and gate: CUDA
+    events around `steps` back-to-back calls after `warmup` calls."""
+    import torch
+    import top_routed_grouped_gb300 as moe
+    from top_routed_grouped_gb300 import inputs as I
+    cpu = I.make_inputs(cfg)
+    x, wr, wsg = cpu["x"].cuda(), cpu["w_router"].cuda(), cpu["w_shared_gate"].cuda()
+    bias = cpu["router_bias"].cuda() if cpu.get("router_bias") is not None else None
+    for _ in range(warmup):
+        moe.route(x, wr, wsg, cfg.k, router_bias=bias)
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for _ in range(steps):
+        moe.route(x, wr, wsg, cfg.k, router_bias=bias)
+    e1.record(s)
+    torch.cuda.synchronize()
+    if moe.moe_device_status(reset=True) != 0:
+        raise RuntimeError("a kernel recorded a failed device-side check")
+    return {"workload": cfg.name, "T": cfg.T, "E": cfg.E, "k": cfg.k, "steps": steps,
+            "ms_per_call": e0.elapsed_time(e1) / max(steps, 1), "api": "moe_route"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -565,6 +590,10 @@ def main():
                     help="only the expert-tensor-parallel slice comparison (two kernels vs fused) on the layer of "
                          "--workload at --etp-tokens tokens, printed as one JSON object (a profiling case)")
     ap.add_argument("--etp-tokens", type=int, default=8192)
+    ap.add_argument("--route-only", action="store_true",
+                    help="only moe_route (router weight split, router, top-k and gate) on --workload, --steps "
+                         "back-to-back calls after --warmup, printed as one JSON object (a profiling case that "
+                         "holds x, the router weight and the logits only)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -588,6 +617,9 @@ def main():
     if args.etp_only:
         w = {k: v.cuda() for k, v in I.make_inputs(cfg, T=1).items() if k not in ("x", "dy", "router_bias")}
         print(json.dumps({"etp_slice": etp_slice_bench(w, args.steps, args.warmup, T=args.etp_tokens)}), flush=True)
+        return
+    if args.route_only:
+        print(json.dumps({"route_only": route_only_bench(cfg, args.steps, args.warmup)}), flush=True)
         return
     if world > 1:
         import torch.distributed as dist
