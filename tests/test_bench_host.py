@@ -113,3 +113,17 @@ def test_reference_arm_line_on_cpu():
     cfg = I.CONFIGS["tiny_f32"]
     assert set(line["config"]) == set(bench.workload_config(cfg, cfg.E, 1))
     assert line["config"]["workload"] == "tiny_f32" and line["config"]["T"] == cfg.T
+
+
+def test_launch_counts_follow_the_forward_structure():
+    """gpu_launches: seven launches on the caller's stream, the router's
+    chunk sum where T * E / 256 <= 4096, the shared expert's four on the
+    second stream above 2048 tokens (the ncu launch lists in profiles/ show
+    11 per forward at T = 8192 and at T = 4096, 23 per forward + backward)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.launches_per_forward(8192, 512) == 11
+    assert bench.launches_per_forward(4096, 512) == 11
+    assert bench.launches_per_forward(2048, 512) == 8
+    assert bench.launches_per_forward(1024, 512) == 8
+    assert bench.launches_per_forward(16384, 512) == 11
